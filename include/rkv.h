@@ -1,0 +1,188 @@
+/*
+ * rkv.h -- C ABI of the GB300 (sm_103a) two-stage compressed decode library.
+ *
+ * The library implements the decode hot path of RocketKV ("RocketKV:
+ * Accelerating Long-Context LLM Inference via Two-Stage KV Cache
+ * Compression", papercache digest of arXiv:2502.14051, section 方法细节):
+ *   stage 1  SnapKV eviction at the end of prefill (observation-window scores
+ *            summed over the GQA group, 1-D max-pool, top-k, compaction);
+ *   KT cache per-block elementwise Kmax / Kmin of the keys (HSA step 1);
+ *   stage 2  Hybrid Sparse Attention per decode step (Algorithm 1: top-k1
+ *            channels of sum|q|, sign-selected Kmax/Kmin block scores, top-k2
+ *            blocks, exact attention over the selected blocks);
+ *   MT       RocketKV-MT: the full cache is kept and stage 2 is restricted to
+ *            the stage-1 survivors plus decoded tokens.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller.  The
+ *     library never allocates or frees device memory and keeps no state
+ *     between calls (apart from a per-library device error word, see
+ *     rkv_read_device_flags).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument checks run on the host before any launch and
+ *     their status is returned synchronously; a failed launch returns
+ *     RKV_ERR_CUDA.  No C++ exception crosses the ABI.
+ *   - bf16 tensors hold IEEE bfloat16; fp32 outputs are IEEE float.
+ *   - Layouts are row-major with the last index fastest:
+ *       K, V (caches)   [B, Hkv, cap, D]         bf16
+ *       q (decode)      [B, Hq, D]               bf16
+ *       q_obs (window)  [B, Hq, W, D]            bf16
+ *       KT              [B, Hkv, 2, D, nblk_cap] bf16, index 0 = Kmax, 1 = Kmin
+ *       idx (MT)        [B, Hkv, idx_cap]        int32 physical cache rows
+ *     Query head h belongs to KV head h / (Hq / Hkv).
+ *   - Supported on the GPU: head_dim == 128, 1 <= Hq/Hkv <= 16, block size a
+ *     multiple of 8 in [8, 128].  Other shapes return RKV_ERR_UNSUPPORTED.
+ *   - Thread safety: entry points may be called from several host threads;
+ *     rkv_last_error() is per thread.
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RKV_OK = 0,
+  RKV_ERR_INVALID_ARG = 1,   /* a pointer, size or stride is invalid */
+  RKV_ERR_UNSUPPORTED = 2,   /* valid, but outside the shapes this library runs */
+  RKV_ERR_WORKSPACE = 3,     /* workspace pointer NULL or smaller than required */
+  RKV_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+  RKV_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (device flag) */
+} rkv_status;
+
+typedef struct {
+  int32_t batch;        /* B   */
+  int32_t n_q_heads;    /* Hq  */
+  int32_t n_kv_heads;   /* Hkv */
+  int32_t head_dim;     /* D   */
+} rkv_dims;
+
+/* Message describing the last non-OK status returned on this host thread. */
+const char* rkv_last_error(void);
+
+/* Library ABI version (incremented when a signature changes). */
+int32_t rkv_abi_version(void);
+
+/*
+ * Budget split.  [RocketKV digest, 方法细节: token budget definition; adaptive
+ * split factor r = min(0.2 + 0.06*log2(c), 0.8) with r kept in [0.2, 0.8]]
+ * c = S / t.  Stage 1 keeps B1 = floor(S / c^r) tokens, clamped to
+ * [min(W+1, S), S].  The token budget t is split evenly between HSA steps 2
+ * and 3, so step 3 reads k2 = max(1, floor((t/2)/blk)) blocks.
+ * r_override >= 0 replaces the adaptive r (the static-split ablation).
+ * Host only; no GPU work.  Output pointers must be non-NULL.
+ */
+rkv_status rkv_budget_split(int64_t S, int64_t t, int32_t blk, int32_t W, double r_override,
+                            double* r, int64_t* B1, int32_t* k2);
+
+/*
+ * Workspace bytes needed by rkv_snap_evict for these dims, prompt length S and
+ * window W (device memory, caller-allocated, 256-byte aligned).
+ */
+size_t rkv_snap_evict_workspace(rkv_dims d, int64_t S, int32_t W);
+
+/*
+ * Stage 1: SnapKV eviction.  [RocketKV digest, 方法细节: SnapKV in stage 1,
+ * GQA group-level token selection, pooling kernel size 63]
+ * For every (batch b, KV head h):
+ *   score[j] = sum over the group's query heads g and window rows w of
+ *              softmax_j(q_obs[b,g,w] . k[b,h,j] * scale), the softmax over
+ *              keys 0 .. S-W+w (causal), for prefix keys j < S-W;
+ *   pooled   = max-pool(score, kernel pool_kernel, stride 1, clipped ends);
+ *   keep     = [0, n_sink) + top-(B1-W-n_sink) of pooled over [n_sink, S-W)
+ *              (larger first, equal values: lower index first) + [S-W, S),
+ *              sorted ascending, B1 entries.
+ * If B1 >= S every token is kept.
+ * Arguments
+ *   q_obs      [B, Hq, W, D] bf16, window queries (the last W prompt tokens).
+ *   k, v       [B, Hkv, cap, D] bf16 prompt caches; rows [0, S) are read.
+ *   keep_idx   [B, Hkv, keep_ld] int32 output; entries [0, B1) of each row are
+ *              written (keep_ld >= B1; MT callers point it at their idx rows).
+ *   k_out,v_out[B, Hkv, out_cap, D] bf16 compacted caches (rows [0, B1)
+ *              written).  Both NULL = MT mask mode: only keep_idx is written.
+ *   pooled_out optional [B, Hkv, S-W] fp32 pooled scores (NULL = skip).
+ *   ws         workspace of rkv_snap_evict_workspace() bytes.
+ * k/v and k_out/v_out must not overlap.
+ */
+rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v,
+                          int64_t cap, int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1,
+                          float scale, int32_t* keep_idx, int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap,
+                          float* pooled_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * KT cache build.  [RocketKV digest, 方法细节: HSA step 1 -- tokens grouped
+ * into pages along the sequence, elementwise Kmax and Kmin per page stored
+ * aligned along the head dimension]
+ * For block j (tokens j*blk .. min(n, (j+1)*blk)-1) and channel c:
+ *   kt[b,h,0,c,j] = max of k[b,h,row(t),c],  kt[b,h,1,c,j] = min of the same,
+ * row(t) = t (idx == NULL) or idx[b,h,t] (MT candidate rows).
+ * Writes blocks [0, ceil(n/blk)); requires ceil(n/blk) <= nblk_cap, n <= cap.
+ */
+rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const int32_t* idx,
+                        int64_t idx_cap, int32_t blk, void* kt, int64_t nblk_cap, void* stream);
+
+/*
+ * Append one decoded token per (b, h) and update the KT cache.  [RocketKV
+ * digest, 方法细节: HSA step 1 -- the auxiliary storage is updated whenever a
+ * new key is generated]
+ *   k[b,h,row] = k_new[b,h], v[b,h,row] = v_new[b,h]   ([B, Hkv, D] bf16);
+ *   candidate n joins block n/blk: a new block starts from k_new, otherwise
+ *   Kmax = max(Kmax, k_new), Kmin = min(Kmin, k_new);
+ *   MT (idx != NULL): idx[b,h,n] = row.  Non-MT: pass row == n, idx = NULL.
+ * The caller's n becomes n+1 after the call.
+ */
+rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void* k, void* v, int64_t cap,
+                         int64_t n, int64_t row, int32_t* idx, int64_t idx_cap, void* kt,
+                         int64_t nblk_cap, int32_t blk, void* stream);
+
+/*
+ * Stage 2: one HSA decode step.  [RocketKV digest, 方法细节: HSA steps 2-3 and
+ * Algorithm 1]  For every (b, KV head h) with the group's queries q_g:
+ *   i1   = top-k1 channels of sum_g |q_g| (equal values: lower channel first);
+ *   qbar = sum_g q_g;  P[c] = Kmax[c] if qbar[c] >= 0 else Kmin[c];
+ *   s[j] = sum_{c in i1} qbar[c] * P[c, j] for blocks j < nblk = ceil(n/blk);
+ *   i2   = top-k2 blocks of s (equal: lower block first; all if k2 >= nblk);
+ *   out[b, g] = softmax(q_g . k_t * scale) weighted sum of v_t over the valid
+ *               tokens t < n of the blocks in i2 (fp32 output [B, Hq, D]).
+ * Arguments
+ *   k, v       [B, Hkv, cap, D] bf16 compacted caches, rows [0, n) valid.
+ *   kt         KT cache covering [0, n).
+ *   sel_blocks optional [B, Hkv, k2] int32: i2 ascending, -1 padded.
+ *   sel_channels optional [B, Hkv, k1] int32: i1 ascending.
+ * Requires 1 <= n <= cap, ceil(n/blk) <= nblk_cap, 1 <= k1 <= D, k2 >= 1,
+ * ceil(n/blk) <= 8192.  No workspace: split partials are combined on chip.
+ */
+rkv_status rkv_hsa_decode(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap, int64_t n,
+                          const void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
+                          float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+                          void* stream);
+
+/*
+ * RocketKV-MT decode step.  [RocketKV digest, 方法细节: RocketKV-MT -- all KV
+ * tokens stay in memory, stage 2 selects only among the stage-1 survivors
+ * plus newly generated tokens]
+ * Same as rkv_hsa_decode over the candidate sequence t = 0 .. n-1 whose key
+ * and value rows are k[b,h,idx[b,h,t]] and v[b,h,idx[b,h,t]] (full caches);
+ * kt must be built over that sequence (rkv_build_kt with the same idx).
+ */
+rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap,
+                             const int32_t* idx, int64_t idx_cap, int64_t n, const void* kt,
+                             int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
+                             float* out, int32_t* sel_blocks, int32_t* sel_channels, void* stream);
+
+/*
+ * Read and clear the library's device error word (synchronises the device).
+ * Bit 0: a bounded wait for an asynchronous copy gave up in some kernel.
+ * Returns RKV_ERR_TIMEOUT if any bit was set, RKV_OK otherwise.
+ */
+rkv_status rkv_read_device_flags(uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RKV_H */

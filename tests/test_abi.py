@@ -1,0 +1,109 @@
+"""CPU checks of the C-ABI library: it loads, exports every symbol that
+include/rkv.h declares, its host-side budget helper agrees with the oracle,
+and argument errors are reported before any GPU work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from two_stage_kv_gb300 import build, rkv
+from two_stage_kv_gb300.synth import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(rkv.LIB_PATH):
+        build.build()
+    return rkv.lib()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "rkv.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?(rkv_[a-z_0-9]+)\(", text, re.M)))
+
+
+def test_header_symbols_exported(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 9
+    assert sorted(rkv.EXPORTED) == syms
+    for s in syms:
+        assert hasattr(lib, s), s
+        assert ctypes.cast(getattr(lib, s), ctypes.c_void_p).value
+
+
+def test_abi_version(lib):
+    assert rkv.rkv_abi_version() == 1
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_budget_split_matches_oracle(lib, name):
+    wl = WORKLOADS[name]
+    for turn in range(wl.n_turns):
+        S = wl.turn_context(turn)
+        r, B1, k2 = rkv.rkv_budget_split(S, wl.t, wl.blk, wl.W)
+        ro, B1o, k2o = oracle.budget_split(S, wl.t, wl.blk, wl.W)
+        assert abs(r - ro) < 1e-12 and B1 == B1o and k2 == k2o
+
+
+def test_budget_split_override_and_errors(lib):
+    assert rkv.rkv_budget_split(32768, 1024, 16, 32, 0.3) == (0.3, *oracle.budget_split(32768, 1024, 16, 32, 0.3)[1:])
+    with pytest.raises(rkv.RkvError) as e:
+        rkv.rkv_budget_split(0, 1, 16)
+    assert e.value.status == 1
+
+
+D4 = (1, 32, 8, 128)
+
+
+@pytest.mark.parametrize("call,status", [
+    (lambda: rkv.rkv_hsa_decode((1, 32, 8, 64), 16, 16, 16, 100, 10, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 2),
+    (lambda: rkv.rkv_hsa_decode((1, 30, 8, 128), 16, 16, 16, 100, 10, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 0, 16, 16, 100, 10, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 0, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 101, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 12, 8, 4, 0.1, 16, stream=0), 2),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 3, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 16, 0, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 16, 129, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 16, 8, 0, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode(D4, 8, 16, 16, 100, 100, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_mt(D4, 16, 16, 16, 100, None, 0, 10, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict(D4, 16, 32, 16, 16, 100, 100, 64, 0, 50, 0.1, 16, 50, 16, 16, 50, None, 16,
+                                1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict(D4, 16, 32, 16, 16, 100, 100, 63, 0, 50, 0.1, 16, 50, 16, 16, 50, None, None,
+                                0, stream=0), 3),
+    (lambda: rkv.rkv_snap_evict(D4, 16, 32, 16, 16, 100, 100, 63, 0, 20, 0.1, 16, 20, 16, 16, 20, None, 256,
+                                1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict(D4, 16, 32, 16, 16, 100, 100, 63, 0, 50, 0.1, 16, 40, 16, 16, 50, None, 256,
+                                1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict(D4, 16, 32, 16, 16, 100, 100, 63, 0, 99, 0.1, 16, 99, 16, None, 99, None, 256,
+                                1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_build_kt(D4, 16, 10, 20, None, 0, 16, 16, 4, stream=0), 1),
+    (lambda: rkv.rkv_build_kt(D4, 16, 100, 100, None, 0, 16, 16, 6, stream=0), 1),
+    (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 11, None, 0, 16, 10, 16, stream=0), 1),
+    (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 160, 160, None, 0, 16, 10, 16, stream=0), 1),
+    (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 10, 16, 10, 16, 10, 16, stream=0), 1),
+])
+def test_invalid_arguments_rejected_on_host(lib, call, status):
+    with pytest.raises(rkv.RkvError) as e:
+        call()
+    assert e.value.status == status, str(e.value)
+    assert lib.rkv_last_error()
+
+
+def test_empty_batch_is_a_no_op(lib):
+    d0 = (0, 32, 8, 128)
+    rkv.rkv_hsa_decode(d0, None, None, None, 0, 0, None, 0, 16, 8, 4, 0.1, None, stream=0)
+    rkv.rkv_build_kt(d0, None, 0, 0, None, 0, 16, None, 0, stream=0)
+    rkv.rkv_append_kv(d0, None, None, None, None, 0, 0, 0, None, 0, None, 0, 16, stream=0)
+    rkv.rkv_snap_evict(d0, None, 32, None, None, 0, 0, 63, 0, 0, 0.1, None, 0, None, None, 0, None, None, 0, stream=0)
+
+
+def test_workspace_query(lib):
+    assert rkv.rkv_snap_evict_workspace((8, 32, 8, 128), 32768, 32) > 8 * 8 * (32768 - 32) * 4
+    assert rkv.rkv_snap_evict_workspace((8, 32, 8, 64), 32768, 32) == 0

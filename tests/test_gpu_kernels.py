@@ -1,0 +1,277 @@
+"""GPU parity of each entry point against the CPU oracle on small and ragged
+shapes (several tiles plus a partial tail), through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import ATOL_OUT, check_topk, max_abs, t2bits, t2f64
+from two_stage_kv_gb300 import rkv
+from two_stage_kv_gb300.synth import bf16_bits_to_f64, small_random
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _bf16(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+def _rand(seed, shape, scale=1.0):
+    b = small_random(seed, shape, scale)
+    return b, _bf16(b)
+
+
+# ----------------------------------------------------------------- KT cache --
+
+
+@pytest.mark.parametrize("n,blk,cap_extra", [(300, 16, 5), (64, 16, 0), (1, 16, 3), (1000, 32, 7), (77, 8, 1),
+                                              (129, 128, 0)])
+def test_build_kt_bit_exact(n, blk, cap_extra):
+    B, Hq, Hkv, D = 2, 8, 2, 128
+    cap = n + cap_extra
+    kb, k = _rand(11 + n, (B, Hkv, cap, D))
+    nblk = -(-n // blk)
+    kt = torch.full((B, Hkv, 2, D, nblk + 3), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt((B, Hq, Hkv, D), k, cap, n, None, 0, blk, kt, nblk + 3)
+    torch.cuda.synchronize()
+    got = t2f64(kt)
+    kf = bf16_bits_to_f64(kb)
+    for b in range(B):
+        for h in range(Hkv):
+            kmax, kmin = oracle.build_kt(kf[b, h], n, blk)
+            assert np.array_equal(got[b, h, 0, :, :nblk], kmax)
+            assert np.array_equal(got[b, h, 1, :, :nblk], kmin)
+    # blocks past nblk are untouched
+    assert torch.isnan(kt[..., nblk:].float()).all()
+
+
+def test_build_kt_mt_rows():
+    B, Hq, Hkv, D, full, n, blk = 1, 4, 2, 128, 500, 173, 16
+    kb, k = _rand(3, (B, Hkv, full, D))
+    rng = np.random.default_rng(5)
+    idx = np.stack([np.stack([np.sort(rng.choice(full, n, replace=False)) for _ in range(Hkv)])])
+    idx_t = torch.from_numpy(idx.astype(np.int32)).to(DEV)
+    nblk = -(-n // blk)
+    kt = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt((B, Hq, Hkv, D), k, full, n, idx_t, n, blk, kt, nblk)
+    got = t2f64(kt)
+    kf = bf16_bits_to_f64(kb)
+    for h in range(Hkv):
+        kmax, kmin = oracle.build_kt_mt(kf[0, h], idx[0, h], n, blk)
+        assert np.array_equal(got[0, h, 0], kmax) and np.array_equal(got[0, h, 1], kmin)
+
+
+def test_append_matches_rebuild():
+    B, Hq, Hkv, D, blk = 2, 8, 2, 128, 16
+    n0, steps = 45, 40
+    cap = n0 + steps
+    kb, k = _rand(21, (B, Hkv, cap, D))
+    vb, v = _rand(22, (B, Hkv, cap, D))
+    nb, knew = _rand(23, (steps, B, Hkv, D))
+    mb, vnew = _rand(24, (steps, B, Hkv, D))
+    nblk_cap = -(-cap // blk)
+    kt = torch.empty((B, Hkv, 2, D, nblk_cap), dtype=torch.bfloat16, device=DEV)
+    dims = (B, Hq, Hkv, D)
+    rkv.rkv_build_kt(dims, k, cap, n0, None, 0, blk, kt, nblk_cap)
+    for s in range(steps):
+        rkv.rkv_append_kv(dims, knew[s], vnew[s], k, v, cap, n0 + s, n0 + s, None, 0, kt, nblk_cap, blk)
+    torch.cuda.synchronize()
+    kexp = kb.copy()
+    vexp = vb.copy()
+    kexp[:, :, n0:] = nb.transpose(1, 2, 0, 3)
+    vexp[:, :, n0:] = mb.transpose(1, 2, 0, 3)
+    assert np.array_equal(t2bits(k), kexp) and np.array_equal(t2bits(v), vexp)
+    got = t2f64(kt)
+    for b in range(B):
+        for h in range(Hkv):
+            kmax, kmin = oracle.build_kt(bf16_bits_to_f64(kexp[b, h]), cap, blk)
+            assert np.array_equal(got[b, h, 0], kmax) and np.array_equal(got[b, h, 1], kmin)
+
+
+# --------------------------------------------------------------- HSA decode --
+
+
+def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=False, full_rows=None):
+    D = 128
+    G = Hq // Hkv
+    dims = (B, Hq, Hkv, D)
+    scale = 1 / math.sqrt(D)
+    rows = full_rows if mt else n + cap_extra
+    kb, k = _rand(seed, (B, Hkv, rows, D))
+    vb, v = _rand(seed + 1, (B, Hkv, rows, D))
+    qb, q = _rand(seed + 2, (B, Hq, D), q_scale)
+    kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
+    nblk = -(-n // blk)
+    kt = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
+    sc = torch.full((B, Hkv, k1), -7, dtype=torch.int32, device=DEV)
+    if mt:
+        rng = np.random.default_rng(seed)
+        idx = np.stack([np.stack([np.sort(rng.choice(rows, n, replace=False)) for _ in range(Hkv)])
+                        for _ in range(B)]).astype(np.int32)
+        idx_t = torch.from_numpy(idx).to(DEV)
+        rkv.rkv_build_kt(dims, k, rows, n, idx_t, n, blk, kt, nblk)
+        rkv.rkv_hsa_decode_mt(dims, q, k, v, rows, idx_t, n, n, kt, nblk, blk, k1, k2, scale, out, sb, sc)
+    else:
+        rkv.rkv_build_kt(dims, k, rows, n, None, 0, blk, kt, nblk)
+        rkv.rkv_hsa_decode(dims, q, k, v, rows, n, kt, nblk, blk, k1, k2, scale, out, sb, sc)
+    torch.cuda.synchronize()
+    out_h, sb_h, sc_h = out.cpu().numpy(), sb.cpu().numpy(), sc.cpu().numpy()
+    worst, exempt = 0.0, 0
+    for b in range(B):
+        for h in range(Hkv):
+            qg = qf[b, h * G:(h + 1) * G]
+            if mt:
+                rws = idx[b, h]
+                Kc, Vc = kf[b, h][rws], vf[b, h][rws]
+            else:
+                Kc, Vc = kf[b, h], vf[b, h]
+            kmax, kmin = oracle.build_kt(Kc, n, blk)
+            res = oracle.hsa_decode(qg, Kc, Vc, n, kmax, kmin, blk, k1, k2, scale)
+            assert sc_h[b, h].tolist() == res["i1"].tolist(), "channel set differs"
+            k2e = min(k2, nblk)
+            exempt += check_topk(sb_h[b, h, :k2e], res["s"], k2, "blocks")
+            assert np.all(sb_h[b, h, k2e:] == -1)
+            y = res["y"] if np.array_equal(sb_h[b, h, :k2e], res["i2"]) else \
+                oracle.attention_over_blocks(qg, Kc, Vc, n, sb_h[b, h, :k2e], blk, scale)
+            worst = max(worst, max_abs(out_h[b, h * G:(h + 1) * G], y))
+    assert worst <= ATOL_OUT, worst
+    return worst, exempt
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n,blk,k1,k2", [
+    (2, 32, 8, 300, 16, 32, 5),       # ragged tail, G = 4
+    (1, 8, 8, 517, 16, 16, 9),        # G = 1
+    (1, 64, 8, 1000, 32, 64, 11),     # G = 8, block 32
+    (1, 32, 2, 333, 8, 128, 40),      # G = 16, block 8, all channels
+    (2, 32, 8, 130, 16, 32, 64),      # k2 >= nblk: full attention
+    (1, 32, 8, 1, 16, 32, 4),         # a single token
+    (1, 32, 8, 4096, 128, 20, 3),     # block 128
+    (1, 32, 8, 20000, 16, 32, 300),   # many blocks, several rounds per CTA
+])
+def test_hsa_decode_parity(B, Hq, Hkv, n, blk, k1, k2):
+    _hsa_case(100 + n, B, Hq, Hkv, n, blk, k1, k2)
+
+
+def test_hsa_decode_peaked_attention():
+    # large queries make the softmax nearly one-hot: checks the P hi/lo split
+    _hsa_case(7, 1, 32, 8, 700, 16, 32, 8, q_scale=6.0)
+
+
+@pytest.mark.parametrize("n,blk,k2", [(250, 16, 6), (97, 8, 20), (600, 32, 4)])
+def test_hsa_decode_mt_parity(n, blk, k2):
+    _hsa_case(300 + n, 2, 32, 8, n, blk, 32, k2, mt=True, full_rows=3 * n + 11)
+
+
+def test_hsa_decode_mt_equals_compacted():
+    """MT over (full cache, idx) gives bit-identical results to the compacted path."""
+    B, Hq, Hkv, D, full, n, blk, k1, k2 = 2, 32, 8, 128, 900, 300, 16, 32, 7
+    dims = (B, Hq, Hkv, D)
+    kb, k = _rand(41, (B, Hkv, full, D))
+    vb, v = _rand(42, (B, Hkv, full, D))
+    _, q = _rand(43, (B, Hq, D))
+    rng = np.random.default_rng(44)
+    idx = np.stack([np.stack([np.sort(rng.choice(full, n, replace=False)) for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    idx_t = torch.from_numpy(idx).to(DEV)
+    kc = torch.stack([torch.stack([k[b, h, idx_t[b, h].long()] for h in range(Hkv)]) for b in range(B)]).contiguous()
+    vc = torch.stack([torch.stack([v[b, h, idx_t[b, h].long()] for h in range(Hkv)]) for b in range(B)]).contiguous()
+    nblk = -(-n // blk)
+    kt1 = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
+    kt2 = torch.empty_like(kt1)
+    rkv.rkv_build_kt(dims, k, full, n, idx_t, n, blk, kt1, nblk)
+    rkv.rkv_build_kt(dims, kc, n, n, None, 0, blk, kt2, nblk)
+    o1 = torch.empty(B, Hq, D, device=DEV)
+    o2 = torch.empty_like(o1)
+    s1 = torch.empty(B, Hkv, k2, dtype=torch.int32, device=DEV)
+    s2 = torch.empty_like(s1)
+    rkv.rkv_hsa_decode_mt(dims, q, k, v, full, idx_t, n, n, kt1, nblk, blk, k1, k2, 0.1, o1, s1, None)
+    rkv.rkv_hsa_decode(dims, q, kc, vc, n, n, kt2, nblk, blk, k1, k2, 0.1, o2, s2, None)
+    torch.cuda.synchronize()
+    assert torch.equal(kt1, kt2) and torch.equal(s1, s2) and torch.equal(o1, o2)
+
+
+def test_hsa_decode_deterministic():
+    B, Hq, Hkv, D, n, blk = 4, 32, 8, 128, 3000, 16
+    dims = (B, Hq, Hkv, D)
+    _, k = _rand(51, (B, Hkv, n, D))
+    _, v = _rand(52, (B, Hkv, n, D))
+    _, q = _rand(53, (B, Hq, D))
+    nblk = -(-n // blk)
+    kt = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt(dims, k, n, n, None, 0, blk, kt, nblk)
+    outs = []
+    for _ in range(3):
+        o = torch.empty(B, Hq, D, device=DEV)
+        rkv.rkv_hsa_decode(dims, q, k, v, n, n, kt, nblk, blk, 32, 32, 0.1, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+# ----------------------------------------------------------------- stage 1 --
+
+
+def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0, compact=True):
+    D = 128
+    G = Hq // Hkv
+    dims = (B, Hq, Hkv, D)
+    cap = S + cap_extra
+    scale = 1 / math.sqrt(D)
+    kb, k = _rand(seed, (B, Hkv, cap, D))
+    vb, v = _rand(seed + 1, (B, Hkv, cap, D))
+    qb, q = _rand(seed + 2, (B, Hq, W, D), q_scale)
+    keep = torch.full((B, Hkv, B1 + 2), -5, dtype=torch.int32, device=DEV)
+    ko = torch.empty((B, Hkv, B1 + 1, D), dtype=torch.bfloat16, device=DEV) if compact else None
+    vo = torch.empty_like(ko) if compact else None
+    L = max(S - W, 0)
+    pooled = torch.empty((B, Hkv, max(L, 1)), dtype=torch.float32, device=DEV)
+    ws_bytes = rkv.rkv_snap_evict_workspace(dims, S, W)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=DEV)
+    rkv.rkv_snap_evict(dims, q, W, k, v, cap, S, P, n_sink, B1, scale, keep, B1 + 2, ko, vo, B1 + 1,
+                       pooled, ws, ws_bytes)
+    torch.cuda.synchronize()
+    keep_h = keep.cpu().numpy()
+    kf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(qb)
+    exempt = 0
+    for b in range(B):
+        for h in range(Hkv):
+            ref, pooled_o = oracle.snap_keep(qf[b, h * G:(h + 1) * G], kf[b, h, :S], B1, W, P, scale, n_sink)
+            got = keep_h[b, h, :B1]
+            assert np.all(keep_h[b, h, B1:] == -5)
+            if B1 >= S or L == 0:
+                assert got.tolist() == list(range(S))
+                continue
+            # pooled scores (fp32 accumulation of probabilities)
+            pg = pooled[b, h, :L].cpu().numpy().astype(np.float64)
+            assert np.max(np.abs(pg - pooled_o) / np.maximum(np.abs(pooled_o), 1e-30)) < 2e-5
+            ns = min(n_sink, L)
+            assert got[:ns].tolist() == list(range(ns))
+            assert got[B1 - min(W, S):].tolist() == list(range(S - min(W, S), S))
+            exempt += check_topk(got[ns:B1 - min(W, S)] - ns, pooled_o[ns:], B1 - min(W, S) - ns, "keep")
+            if compact:
+                assert np.array_equal(t2bits(ko[b, h, :B1]), kb[b, h][got])
+                assert np.array_equal(t2bits(vo[b, h, :B1]), vb[b, h][got])
+    return exempt
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,W,P,B1,sink", [
+    (1, 32, 8, 4096, 32, 63, 1209, 0),      # the 4K workload's shape
+    (2, 32, 8, 5000, 32, 63, 700, 0),       # ragged S
+    (1, 64, 8, 3000, 32, 63, 500, 0),       # G * W = 256 rows (two row groups)
+    (1, 8, 8, 2100, 32, 7, 300, 4),         # G = 1, pool 7, sinks
+    (1, 24, 8, 1500, 32, 1, 100, 0),        # G = 3 (96 rows), no pooling
+    (1, 32, 8, 200, 32, 63, 200, 0),        # B1 == S: keep all
+    (1, 32, 8, 20, 32, 63, 20, 0),          # prompt shorter than the window
+    (1, 32, 8, 70000, 32, 63, 900, 0),      # long prompt, many chunks
+])
+def test_snap_evict_parity(B, Hq, Hkv, S, W, P, B1, sink):
+    _snap_case(500 + S, B, Hq, Hkv, S, W, P, B1, sink)
+
+
+def test_snap_evict_mask_mode_and_peaked():
+    _snap_case(9, 1, 32, 8, 3000, 32, 63, 400, compact=False, q_scale=4.0)

@@ -1,0 +1,277 @@
+// C ABI of the library (declared in include/rkv.h): host-side argument checks,
+// TMA descriptor encoding and kernel launches.  Every entry point validates its
+// arguments before any launch and returns a status; no exception escapes.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/rkv.h"
+#include "rkv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+rkv_status fail(rkv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+rkv_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(RKV_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rkv_status check_dims(const rkv_dims& d) {
+  if (d.batch < 0 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.head_dim < 1)
+    return fail(RKV_ERR_INVALID_ARG, "dims: batch=%d Hq=%d Hkv=%d D=%d", d.batch, d.n_q_heads, d.n_kv_heads,
+                d.head_dim);
+  if (d.n_q_heads % d.n_kv_heads != 0)
+    return fail(RKV_ERR_INVALID_ARG, "dims: Hq=%d is not a multiple of Hkv=%d", d.n_q_heads, d.n_kv_heads);
+  if (d.head_dim != rkv::HD_HOST)
+    return fail(RKV_ERR_UNSUPPORTED, "dims: head_dim=%d (only 128 is implemented)", d.head_dim);
+  if (d.n_q_heads / d.n_kv_heads > 16)
+    return fail(RKV_ERR_UNSUPPORTED, "dims: group size %d > 16", d.n_q_heads / d.n_kv_heads);
+  return RKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [pairs, cap, 128] bf16 cache: rows >= `rows` read as zero.
+// Box = 64 channels (128 bytes, 128-byte swizzle) x box_rows rows x 1 pair.
+rkv_status make_kv_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t cap, int64_t rows, int box_rows,
+                       const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {(cuuint64_t)rkv::HD_HOST, (cuuint64_t)rows, (cuuint64_t)pairs};
+  cuuint64_t strides[2] = {(cuuint64_t)rkv::HD_HOST * 2, (cuuint64_t)cap * rkv::HD_HOST * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+  return RKV_OK;
+}
+
+rkv_status hsa_common(const rkv_dims& d, const void* q, const void* k, const void* v, int64_t cap,
+                      const int32_t* idx, int64_t idx_cap, int64_t n, const void* kt, int64_t nblk_cap, int32_t blk,
+                      int32_t k1, int32_t k2, float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+                      void* stream, bool mt) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0) return RKV_OK;
+  if (!q || !k || !v || !kt || !out) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode: q/k/v must be 16-byte aligned");
+  if (mt && !idx) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: idx is NULL");
+  if (n < 1 || n > cap) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: n=%lld outside [1, cap=%lld]", (long long)n,
+                                    (long long)cap);
+  if (mt && n > idx_cap) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: n=%lld > idx_cap=%lld", (long long)n,
+                                     (long long)idx_cap);
+  if (blk < 8 || blk > 128 || blk % 8 != 0)
+    return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: block size %d (needs a multiple of 8 in [8,128])", blk);
+  const int64_t nblk = (n + blk - 1) / blk;
+  if (nblk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: ceil(n/blk)=%lld > nblk_cap=%lld",
+                                   (long long)nblk, (long long)nblk_cap);
+  if (nblk > 8192) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: %lld blocks > 8192", (long long)nblk);
+  if (k1 < 1 || k1 > rkv::HD_HOST) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: k1=%d outside [1,128]", k1);
+  if (k2 < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: k2=%d < 1", k2);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: bad scale");
+  if (cap >= (int64_t)1 << 31) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: cap >= 2^31");
+
+  rkv::HsaArgs a = {};
+  a.q = q; a.k = k; a.v = v; a.kt = kt; a.idx = idx; a.out = out;
+  a.sel_blocks = sel_blocks; a.sel_channels = sel_channels;
+  a.cap = cap; a.nblk_cap = nblk_cap; a.idx_cap = idx_cap;
+  a.n = (int32_t)n; a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
+  a.blk = blk; a.k1 = k1; a.k2 = k2;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  if (!rkv::hsa_plan(a)) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: shared memory plan does not fit");
+
+  CUtensorMap tmK, tmV;
+  std::memset(&tmK, 0, sizeof(tmK));
+  std::memset(&tmV, 0, sizeof(tmV));
+  const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
+  if (!mt) {
+    if ((s = make_kv_map(&tmK, k, pairs, cap, n, blk, "k")) != RKV_OK) return s;
+    if ((s = make_kv_map(&tmV, v, pairs, cap, n, blk, "v")) != RKV_OK) return s;
+  }
+  cudaError_t e = rkv::hsa_launch(a, &tmK, &tmV, mt, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "hsa_decode launch");
+  return RKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rkv_last_error(void) { return g_last_error.c_str(); }
+
+int32_t rkv_abi_version(void) { return 1; }
+
+rkv_status rkv_budget_split(int64_t S, int64_t t, int32_t blk, int32_t W, double r_override, double* r,
+                            int64_t* B1, int32_t* k2) {
+  if (!r || !B1 || !k2) return fail(RKV_ERR_INVALID_ARG, "budget_split: NULL output");
+  if (S < 1 || t < 1 || blk < 1 || W < 0) return fail(RKV_ERR_INVALID_ARG, "budget_split: S, t, blk >= 1 and W >= 0");
+  const double c = (double)S / (double)t;
+  double rr;
+  if (r_override >= 0.0) {
+    rr = r_override;
+  } else {
+    rr = std::fmin(0.2 + 0.06 * std::log2(c), 0.8);
+    rr = std::fmax(rr, 0.2);
+  }
+  int64_t b1 = (int64_t)std::floor((double)S * std::pow(c, -rr));
+  const int64_t lo = std::min<int64_t>((int64_t)W + 1, S);
+  b1 = std::max(lo, std::min(b1, S));
+  *r = rr;
+  *B1 = b1;
+  *k2 = (int32_t)std::max<int64_t>(1, (t / 2) / blk);
+  return RKV_OK;
+}
+
+size_t rkv_snap_evict_workspace(rkv_dims d, int64_t S, int32_t W) {
+  if (check_dims(d) != RKV_OK || S < 1 || W < 1) return 0;
+  const int64_t w = std::min<int64_t>(W, S);
+  return rkv::snap_workspace_bytes(d.batch, d.n_q_heads, d.n_kv_heads, S, (int32_t)w);
+}
+
+rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v, int64_t cap,
+                          int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1, float scale, int32_t* keep_idx,
+                          int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out, void* ws, size_t ws_bytes,
+                          void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0) return RKV_OK;
+  if (!q_obs || !k || !keep_idx) return fail(RKV_ERR_INVALID_ARG, "snap_evict: NULL q_obs, k or keep_idx");
+  if ((k_out == nullptr) != (v_out == nullptr))
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict: k_out and v_out must both be set or both be NULL");
+  if (k_out && !v) return fail(RKV_ERR_INVALID_ARG, "snap_evict: v is NULL but compaction was requested");
+  if (!aligned16(q_obs) || !aligned16(k) || (v && !aligned16(v)) || (k_out && (!aligned16(k_out) || !aligned16(v_out))))
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict: tensors must be 16-byte aligned");
+  if (W < 1) return fail(RKV_ERR_INVALID_ARG, "snap_evict: W=%d < 1", W);
+  if (S < 1 || S > cap) return fail(RKV_ERR_INVALID_ARG, "snap_evict: S=%lld outside [1, cap=%lld]", (long long)S,
+                                    (long long)cap);
+  if (cap >= (int64_t)1 << 31) return fail(RKV_ERR_UNSUPPORTED, "snap_evict: cap >= 2^31");
+  if (pool_kernel < 1 || pool_kernel % 2 == 0 || pool_kernel > 1025)
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict: pool kernel %d must be odd in [1, 1025]", pool_kernel);
+  if (n_sink < 0) return fail(RKV_ERR_INVALID_ARG, "snap_evict: n_sink < 0");
+  const int64_t w = std::min<int64_t>(W, S);
+  const int64_t L = S - w;
+  const int64_t sinks = std::min<int64_t>(n_sink, L);
+  const bool keep_all = B1 >= S || L <= 0;
+  if (keep_all && B1 != S)
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict: B1=%lld must equal S=%lld when nothing is evicted",
+                (long long)B1, (long long)S);
+  if (!keep_all && B1 < w + sinks)
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict: B1=%lld < window %lld + sinks %lld", (long long)B1, (long long)w,
+                (long long)sinks);
+  if (keep_ld < B1) return fail(RKV_ERR_INVALID_ARG, "snap_evict: keep_ld=%lld < B1", (long long)keep_ld);
+  if (k_out && out_cap < B1) return fail(RKV_ERR_INVALID_ARG, "snap_evict: out_cap=%lld < B1", (long long)out_cap);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "snap_evict: bad scale");
+  const size_t need = rkv::snap_workspace_bytes(d.batch, d.n_q_heads, d.n_kv_heads, S, (int32_t)w);
+  if (!keep_all && (ws == nullptr || ws_bytes < need))
+    return fail(RKV_ERR_WORKSPACE, "snap_evict: workspace %zu bytes < %zu required", ws_bytes, need);
+  if (!keep_all && (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict: workspace must be 256-byte aligned");
+
+  rkv::SnapArgs a = {};
+  a.q_obs = q_obs; a.k = k; a.v = v; a.cap = cap; a.S = S; a.out_cap = out_cap; a.B1 = B1;
+  a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
+  a.W = (int32_t)w; a.pool = pool_kernel; a.n_sink = (int32_t)sinks;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.keep = keep_idx; a.keep_ld = keep_ld; a.k_out = k_out; a.v_out = v_out; a.pooled_out = pooled_out;
+  a.ws = ws; a.ws_bytes = ws_bytes;
+  CUtensorMap tmK;
+  std::memset(&tmK, 0, sizeof(tmK));
+  if (!keep_all) {
+    if ((s = make_kv_map(&tmK, k, (int64_t)d.batch * d.n_kv_heads, cap, S, 64, "k")) != RKV_OK) return s;
+  }
+  cudaError_t e = rkv::snap_launch(a, &tmK, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "snap_evict launch");
+  return RKV_OK;
+}
+
+rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
+                        int32_t blk, void* kt, int64_t nblk_cap, void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0 || n == 0) return RKV_OK;
+  if (!k || !kt) return fail(RKV_ERR_INVALID_ARG, "build_kt: NULL k or kt");
+  if (!aligned16(k)) return fail(RKV_ERR_INVALID_ARG, "build_kt: k must be 16-byte aligned");
+  if (blk < 1) return fail(RKV_ERR_INVALID_ARG, "build_kt: blk < 1");
+  if (n < 0 || (!idx && n > cap) || (idx && n > idx_cap))
+    return fail(RKV_ERR_INVALID_ARG, "build_kt: n=%lld out of range", (long long)n);
+  if ((n + blk - 1) / blk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "build_kt: nblk_cap too small");
+  cudaError_t e = rkv::kt_build_launch(k, cap, n, idx, idx_cap, blk, kt, nblk_cap, d.batch * d.n_kv_heads,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "build_kt launch");
+  return RKV_OK;
+}
+
+rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
+                         int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
+                         void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0) return RKV_OK;
+  if (!k_new || !v_new || !k || !v || !kt) return fail(RKV_ERR_INVALID_ARG, "append_kv: NULL pointer");
+  if (blk < 1 || n < 0 || row < 0 || row >= cap) return fail(RKV_ERR_INVALID_ARG, "append_kv: bad n/row/blk");
+  if (!idx && row != n) return fail(RKV_ERR_INVALID_ARG, "append_kv: without idx the row must equal n");
+  if (idx && n >= idx_cap) return fail(RKV_ERR_INVALID_ARG, "append_kv: n >= idx_cap");
+  if (n / blk >= nblk_cap) return fail(RKV_ERR_INVALID_ARG, "append_kv: block %lld >= nblk_cap", (long long)(n / blk));
+  cudaError_t e = rkv::append_launch(k_new, v_new, k, v, cap, n, row, idx, idx_cap, kt, nblk_cap, blk,
+                                     d.batch * d.n_kv_heads, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append_kv launch");
+  return RKV_OK;
+}
+
+rkv_status rkv_hsa_decode(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap, int64_t n,
+                          const void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
+                          float* out, int32_t* sel_blocks, int32_t* sel_channels, void* stream) {
+  return hsa_common(d, q, k, v, cap, nullptr, 0, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks, sel_channels,
+                    stream, false);
+}
+
+rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap, const int32_t* idx,
+                             int64_t idx_cap, int64_t n, const void* kt, int64_t nblk_cap, int32_t blk, int32_t k1,
+                             int32_t k2, float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+                             void* stream) {
+  return hsa_common(d, q, k, v, cap, idx, idx_cap, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
+                    sel_channels, stream, true);
+}
+
+rkv_status rkv_read_device_flags(uint32_t* flags) {
+  if (!flags) return fail(RKV_ERR_INVALID_ARG, "read_device_flags: NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "read_device_flags");
+  *flags = rkv::hsa_take_device_error() | rkv::snap_take_device_error();
+  if (*flags) return fail(RKV_ERR_TIMEOUT, "device flags 0x%x: a bounded wait gave up", *flags);
+  return RKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Internal launch interfaces between the C-ABI layer (rkv_api.cu) and the
+// kernel translation units.  Host-side only; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rkv {
+
+constexpr int HD_HOST = 128;   // head dimension of the implemented path
+
+// ------------------------------------------------------------ HSA decode ---
+struct HsaArgs {
+  const void* q;        // [B, Hq, D] bf16
+  const void* k;        // [B, Hkv, cap, D] bf16
+  const void* v;
+  const void* kt;       // [B, Hkv, 2, D, nblk_cap] bf16
+  const int32_t* idx;   // MT candidate rows [B, Hkv, idx_cap] or nullptr
+  float* out;           // [B, Hq, D] fp32
+  int32_t* sel_blocks;  // [B, Hkv, k2] or nullptr
+  int32_t* sel_channels;  // [B, Hkv, k1] or nullptr
+  int64_t cap, nblk_cap, idx_cap;
+  int32_t n, B, Hq, Hkv, G, blk, k1, k2;
+  int32_t nblk;         // ceil(n / blk)
+  int32_t k2e;          // min(k2, nblk)
+  int32_t ns;           // CTAs per cluster (one cluster per (b, kv head))
+  int32_t chunk;        // selected blocks per CTA: ceil(k2e / ns)
+  int32_t slots_round;  // blocks staged in shared memory per round
+  float scale_log2;     // softmax scale * log2(e)
+  // dynamic shared-memory layout (bytes)
+  uint32_t off_scores, off_sel, off_part, off_recv, off_tiles, tile_half_bytes, smem_bytes;
+};
+
+// Computes ns/chunk/slots_round and the shared-memory layout.  Returns false if
+// the configuration does not fit on the device.
+bool hsa_plan(HsaArgs& a);
+cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV, bool mt,
+                       cudaStream_t st);
+
+// ------------------------------------------------------------ stage 1 -------
+struct SnapArgs {
+  const void* q_obs;    // [B, Hq, W, D]
+  const void* k;        // [B, Hkv, cap, D]
+  const void* v;
+  int64_t cap, S, out_cap, B1;
+  int32_t B, Hq, Hkv, G, W, pool, n_sink;
+  float scale_log2;
+  int32_t* keep;        // [B, Hkv, keep_ld]
+  int64_t keep_ld;
+  void* k_out;          // [B, Hkv, out_cap, D] or nullptr (mask mode)
+  void* v_out;
+  float* pooled_out;    // [B, Hkv, S-W] or nullptr
+  // workspace carve-up
+  void* ws;
+  size_t ws_bytes;
+};
+size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t W);
+cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, cudaStream_t st);
+
+// ------------------------------------------------------------ KT / append ---
+cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
+                            int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st);
+cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
+                          int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
+                          int32_t pairs, cudaStream_t st);
+
+// Device error words of each translation unit (read and cleared).
+unsigned int hsa_take_device_error();
+unsigned int snap_take_device_error();
+
+}  // namespace rkv

@@ -215,9 +215,15 @@ def needle_positions(wl: Workload, layer: int, b: int) -> np.ndarray:
     return np.sort(r.choice(wl.S - wl.W, size=wl.n_needles, replace=False))
 
 
+def needle_step(wl: Workload, i: int) -> int:
+    """Decode step whose query needle i answers (i mod steps)."""
+    return i % wl.steps
+
+
 def needle_directions(wl: Workload, layer: int, qdec_bits: np.ndarray, b: int, hk: int) -> np.ndarray:
-    """Unit direction of needle i = the group-summed decode query of step i, float64 [n_needles, D]."""
-    q = bf16_bits_to_f64(qdec_bits[: wl.n_needles, b, hk * wl.G:(hk + 1) * wl.G]).sum(axis=1)
+    """Unit direction of needle i = the group-summed decode query of step i mod steps, float64 [n_needles, D]."""
+    steps = [needle_step(wl, i) for i in range(wl.n_needles)]
+    q = bf16_bits_to_f64(qdec_bits[steps, b, hk * wl.G:(hk + 1) * wl.G]).sum(axis=1)
     return q / np.linalg.norm(q, axis=-1, keepdims=True)
 
 
