@@ -1,0 +1,419 @@
+"""Benchmark of the two-stage compressed decode path on one GB300 per rank.
+
+One step = one pass of the whole hot path over one batch of the 32K workload
+(batch 8, Llama3.1-8B-shaped GQA layer: 32 query / 8 KV heads, d_head 128,
+32768-token prompt, budget 1024): SnapKV stage-1 eviction, KT build, then 64
+decode steps of (append, HSA decode).  The pass is captured in one CUDA graph
+and replayed; inputs stay resident in HBM.  `value` is decode tokens per
+second over whole passes (B x 64 tokens per pass, stage 1 included); the
+decode-only rate, the stage-1 time and the HSA kernel's roofline are reported
+beside it.  The prompt K/V (1.07 GB) is streamed every pass, which exceeds
+the 129 MB L2, so no explicit L2 flush is inserted.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HSA decode steps/sec (tokens/s) + achieved HBM GB/s vs roofline, 32K ctx"
+WORKLOAD = "b8_32k"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "hsa_decode_b8_32k.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ["rkv_hsa.cu", "rkv_common.cuh"]:
+        with open(os.path.join(ROOT, "two_stage_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_launch():
+    """DRAM bytes per HSA launch from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    with open(PROFILE_SUMMARY) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+
+def hsa_bytes_per_launch(wl, B1, k2, n):
+    """Algorithmic bytes one fused HSA launch must move at candidate count n (all
+    pairs): KT rows of the k1 kept channels, the K and V rows of the selected
+    blocks, the queries, the fp32 outputs, plus the appended token (read k/v,
+    write the cache rows, read-modify-write its KT column)."""
+    nblk = -(-n // wl.blk)
+    k2e = min(k2, nblk)
+    toks = min(k2e * wl.blk, n)
+    per_pair = (wl.k1 * nblk * 2 + 2 * toks * wl.D * 2 + wl.G * wl.D * 2 + wl.G * wl.D * 4
+                + 4 * wl.D * 2 + 2 * (2 * wl.D * 2))
+    return per_pair * wl.B * wl.Hkv
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from two_stage_kv_gb300 import pipeline, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = synth.WORKLOADS[WORKLOAD]
+    li = synth.layer_inputs(wl)
+    t = lambda bits: pipeline.bf16_tensor(bits, dev)  # noqa: E731
+    k, v, qo = t(li.k), t(li.v), t(li.q_obs)
+    qd, kn, vn = t(li.q_dec), t(li.k_new), t(li.v_new)
+    L = pipeline.Layer(wl, k, v, qo, device=dev)
+    B1, k2 = L.bud.B1, L.bud.k2
+    out_all = torch.empty(wl.steps, wl.B, wl.Hq, wl.D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def tev():
+        # timing events recorded as graph nodes (cudaEventRecordExternal)
+        return torch.cuda.Event(enable_timing=True, external=True)
+
+    # phase-boundary events only: event nodes between every launch would add
+    # several microseconds per decode step to the graph
+    ev = {"s0": tev(), "s1": tev(), "s2": tev(), "d1": tev()}
+
+    def one_pass(record=True):
+        if record:
+            ev["s0"].record()
+        L.stage1(pooled=False)
+        if record:
+            ev["s1"].record()
+        L.build_kt()
+        if record:
+            ev["s2"].record()
+        for s in range(wl.steps):
+            L.step(qd[s], kn[s], vn[s], out=out_all[s], selections=False)
+        if record:
+            ev["d1"].record()
+
+    launches_per_pass = 5 + 1 + wl.steps
+    with torch.cuda.stream(stream):
+        one_pass(record=False)          # sets kernel attributes outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        one_pass(record=True)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    tA, tB = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        tA.record()
+        for _ in range(args.steps):
+            graph.replay()
+        tB.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = tA.elapsed_time(tB)
+    if world > 1:
+        x = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(x.item())
+    ms_pass = ms_total / args.steps
+    tokens_per_pass = wl.B * wl.steps
+    value = world * tokens_per_pass * args.steps / (ms_total / 1e3)
+
+    # per-kernel times from the last replay of the timed region
+    stage1_ms = ev["s0"].elapsed_time(ev["s1"])
+    kt_ms = ev["s1"].elapsed_time(ev["s2"])
+    decode_ms = ev["s2"].elapsed_time(ev["d1"])
+    # the decode phase is 64 back-to-back HSA launches (append fused in): the
+    # average launch duration includes the gaps between launches (conservative)
+    hsa_avg_us = decode_ms * 1e3 / wl.steps
+    bytes_avg = sum(hsa_bytes_per_launch(wl, B1, k2, B1 + s + 1) for s in range(wl.steps)) / wl.steps
+    peak, peak_kind = peaks()
+    achieved = bytes_avg / (hsa_avg_us * 1e-6) / 1e9
+    traffic = ncu_traffic_per_launch()
+    roofline = {"kernel": "hsa_decode_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
+                "fallback 6.8 TB/s", "bytes_per_launch": int(bytes_avg), "avg_launch_us": round(hsa_avg_us, 3),
+                "timing": "decode-phase events of the last timed pass / 64 launches (gaps included)",
+                "l2": "warm within a pass: inputs > L2 but the 190 MB compacted cache is re-read each step"}
+
+    # e2e: host buffers, H2D of the pass's inputs and D2H of its outputs inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host_in = [x.cpu().pin_memory() for x in (k, v, qo, qd, kn, vn)]
+        dev_in = [k, v, qo, qd, kn, vn]
+        host_out = torch.empty(out_all.shape, dtype=out_all.dtype, pin_memory=True)
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+        e2e_steps = max(3, min(args.steps, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(e2e_steps):
+                for d_, h_ in zip(dev_in, host_in):
+                    d_.copy_(h_, non_blocking=True)
+                graph.replay()
+                host_out.copy_(out_all, non_blocking=True)
+            e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            x = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(x.item())
+        e2e = {"value": round(world * tokens_per_pass * e2e_steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+               "ms_per_step": round(e2e_ms / e2e_steps, 4)}
+
+    from two_stage_kv_gb300 import rkv
+    flags = rkv.rkv_read_device_flags()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_pass, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D,
+                   "context": wl.S, "budget": wl.t, "B1": B1, "k2_blocks": k2, "block": wl.blk, "k1": wl.k1,
+                   "decode_steps_per_pass": wl.steps, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: every pass streams the 1.07 GB prompt K/V (> 129 MB L2)",
+                   "graph": "one CUDA graph per pass"},
+        "decode_only": {"tokens_per_s": round(wl.B * wl.steps / (decode_ms / 1e3) * world, 1),
+                        "steps_per_s": round(wl.steps / (decode_ms / 1e3), 1), "ms": round(decode_ms, 4)},
+        "stage1_ms": round(stage1_ms, 4), "kt_build_ms": round(kt_ms, 4),
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_pass * args.steps,
+        "clocks": clk, "device_flags": flags,
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+_ORACLE_SAMPLE = r"""
+import json, math, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import oracle
+from two_stage_kv_gb300 import synth
+wl = synth.WORKLOADS[{wl!r}]
+budget_s = {budget_s}
+f = synth.bf16_bits_to_f64
+qd = synth.q_decode(wl)
+kn, vn = synth.kv_new(wl)
+qo = synth.q_obs(wl, 0, qd)
+r, B1, k2 = oracle.budget_split(wl.S, wl.t, wl.blk, wl.W)
+scale = 1 / math.sqrt(wl.D)
+G = wl.G
+done = 0
+t_total = 0.0
+pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+while t_total < budget_s and done < len(pairs):
+    b, h = pairs[done]
+    kb, vb = synth.kv_slice(wl, 0, b, h, qd)
+    K, V = f(kb), f(vb)
+    t0 = time.perf_counter()
+    keep, _ = oracle.snap_keep(f(qo[b, h * G:(h + 1) * G]), K, B1, wl.W, wl.P, scale)
+    Kc = np.zeros((B1 + wl.steps, wl.D)); Vc = np.zeros_like(Kc)
+    Kc[:B1] = K[keep]; Vc[:B1] = V[keep]
+    kmax, kmin = oracle.build_kt(Kc, B1, wl.blk)
+    n = B1
+    for s in range(wl.steps):
+        Kc[n] = f(kn[s, b, h]); Vc[n] = f(vn[s, b, h])
+        kmax, kmin = oracle.kt_append(kmax, kmin, n, Kc[n], wl.blk)
+        n += 1
+        oracle.hsa_decode(f(qd[s, b, h * G:(h + 1) * G]), Kc, Vc, n, kmax, kmin, wl.blk, wl.k1, k2, scale)
+    t_total += time.perf_counter() - t0
+    done += 1
+print(json.dumps({{"pairs": done, "total_pairs": len(pairs), "seconds": t_total}}))
+"""
+
+
+def oracle_sample(budget_s: float):
+    """Times the oracle (1 thread) on whole (batch, KV head) pairs of one pass."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    code = _ORACLE_SAMPLE.format(root=ROOT, wl=WORKLOAD, budget_s=budget_s)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    from two_stage_kv_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    pass_s = d["seconds"] * d["total_pairs"] / d["pairs"]      # pairs are independent
+    value = wl.B * wl.steps / pass_s
+    return value, d, pass_s
+
+
+def cpu_baseline_obj(budget_s=15.0):
+    value, d, pass_s = oracle_sample(budget_s)
+    return {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{d['pairs']} of {d['total_pairs']} (batch, KV head) pairs of one pass (stage 1, KT, "
+                      f"64 decode steps) in {d['seconds']:.1f} s, scaled by pair count; numpy fp64, 1 thread"}
+
+
+def run_reference(args):
+    from two_stage_kv_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    # each step = one bounded sample (one pair's share of a pass); the run is time-boxed
+    steps_run, secs, pairs = 0, 0.0, 0
+    tbox = 150.0
+    for i in range(args.warmup + args.steps):
+        value, d, pass_s = oracle_sample(0.0)     # exactly one pair per step
+        if i >= args.warmup:
+            steps_run += 1
+            secs += d["seconds"]
+            pairs += d["pairs"]
+        if secs > tbox:
+            break
+    pass_s = secs * (wl.B * wl.Hkv) / max(pairs, 1)
+    value = wl.B * wl.steps / pass_s
+    cores = 1
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": steps_run, "warmup": args.warmup, "ms_per_step": round(secs / max(steps_run, 1) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": wl.B, "context": wl.S, "budget": wl.t,
+                       "decode_steps_per_pass": wl.steps},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{pairs} (batch, KV head) pairs, one per step, each a full share of one "
+                                       f"pass; scaled by the 64 pairs of the batch"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_obj()
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

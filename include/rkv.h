@@ -140,39 +140,48 @@ rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void*
                          int64_t nblk_cap, int32_t blk, void* stream);
 
 /*
- * Stage 2: one HSA decode step.  [RocketKV digest, 方法细节: HSA steps 2-3 and
- * Algorithm 1]  For every (b, KV head h) with the group's queries q_g:
+ * Stage 2: one HSA decode step, optionally fused with the step's append.
+ * [RocketKV digest, 方法细节: HSA steps 1-3 and Algorithm 1]
+ * With k_new/v_new ([B, Hkv, D] bf16) the token is first appended as candidate
+ * n -- k[b,h,n] = k_new, v[b,h,n] = v_new and its KT block updated exactly as
+ * rkv_append_kv does -- and the step attends the n+1 candidates; with both
+ * NULL it attends the first n.  For every (b, KV head h), with the group's
+ * queries q_g and N the attended count:
  *   i1   = top-k1 channels of sum_g |q_g| (equal values: lower channel first);
  *   qbar = sum_g q_g;  P[c] = Kmax[c] if qbar[c] >= 0 else Kmin[c];
- *   s[j] = sum_{c in i1} qbar[c] * P[c, j] for blocks j < nblk = ceil(n/blk);
+ *   s[j] = sum_{c in i1} qbar[c] * P[c, j] for blocks j < nblk = ceil(N/blk);
  *   i2   = top-k2 blocks of s (equal: lower block first; all if k2 >= nblk);
  *   out[b, g] = softmax(q_g . k_t * scale) weighted sum of v_t over the valid
- *               tokens t < n of the blocks in i2 (fp32 output [B, Hq, D]).
+ *               tokens t < N of the blocks in i2 (fp32 output [B, Hq, D]).
  * Arguments
  *   k, v       [B, Hkv, cap, D] bf16 compacted caches, rows [0, n) valid.
- *   kt         KT cache covering [0, n).
+ *   kt         KT cache covering [0, n); nblk_cap must be a multiple of 8.
  *   sel_blocks optional [B, Hkv, k2] int32: i2 ascending, -1 padded.
  *   sel_channels optional [B, Hkv, k1] int32: i1 ascending.
- * Requires 1 <= n <= cap, ceil(n/blk) <= nblk_cap, 1 <= k1 <= D, k2 >= 1,
- * ceil(n/blk) <= 8192.  No workspace: split partials are combined on chip.
+ * Requires 1 <= N <= cap, ceil(N/blk) <= nblk_cap, 1 <= k1 <= D, k2 >= 1,
+ * ceil(N/blk) <= 8192.  No workspace: split partials are combined on chip.
+ * The launch may overlap the tail of the previous kernel on the stream
+ * (programmatic dependent launch); it reads no input before that kernel ends.
  */
-rkv_status rkv_hsa_decode(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap, int64_t n,
-                          const void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
-                          float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+rkv_status rkv_hsa_decode(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int64_t n, void* kt,
+                          int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale, float* out,
+                          int32_t* sel_blocks, int32_t* sel_channels, const void* k_new, const void* v_new,
                           void* stream);
 
 /*
  * RocketKV-MT decode step.  [RocketKV digest, 方法细节: RocketKV-MT -- all KV
  * tokens stay in memory, stage 2 selects only among the stage-1 survivors
  * plus newly generated tokens]
- * Same as rkv_hsa_decode over the candidate sequence t = 0 .. n-1 whose key
+ * Same as rkv_hsa_decode over the candidate sequence t = 0 .. N-1 whose key
  * and value rows are k[b,h,idx[b,h,t]] and v[b,h,idx[b,h,t]] (full caches);
- * kt must be built over that sequence (rkv_build_kt with the same idx).
+ * kt must be built over that sequence (rkv_build_kt with the same idx).  With
+ * k_new/v_new the token is first written to cache row `row` and becomes
+ * candidate n (idx[b,h,n] = row).
  */
-rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap,
-                             const int32_t* idx, int64_t idx_cap, int64_t n, const void* kt,
-                             int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
-                             float* out, int32_t* sel_blocks, int32_t* sel_channels, void* stream);
+rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int32_t* idx,
+                             int64_t idx_cap, int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1,
+                             int32_t k2, float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+                             const void* k_new, const void* v_new, int64_t row, void* stream);
 
 /*
  * Read and clear the library's device error word (synchronises the device).

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from parity_util import ATOL_OUT, check_topk, max_abs, t2bits, t2f64
+from parity_util import ATOL_OUT, SCORE_FLOOR, check_topk, max_abs, t2bits, t2f64
 from two_stage_kv_gb300 import rkv
 from two_stage_kv_gb300.synth import bf16_bits_to_f64, small_random
 
@@ -105,7 +105,8 @@ def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=Fal
     qb, q = _rand(seed + 2, (B, Hq, D), q_scale)
     kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
     nblk = -(-n // blk)
-    kt = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
+    ncap = -(-nblk // 8) * 8
+    kt = torch.empty((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
     sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
     sc = torch.full((B, Hkv, k1), -7, dtype=torch.int32, device=DEV)
@@ -114,11 +115,11 @@ def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=Fal
         idx = np.stack([np.stack([np.sort(rng.choice(rows, n, replace=False)) for _ in range(Hkv)])
                         for _ in range(B)]).astype(np.int32)
         idx_t = torch.from_numpy(idx).to(DEV)
-        rkv.rkv_build_kt(dims, k, rows, n, idx_t, n, blk, kt, nblk)
-        rkv.rkv_hsa_decode_mt(dims, q, k, v, rows, idx_t, n, n, kt, nblk, blk, k1, k2, scale, out, sb, sc)
+        rkv.rkv_build_kt(dims, k, rows, n, idx_t, n, blk, kt, ncap)
+        rkv.rkv_hsa_decode_mt(dims, q, k, v, rows, idx_t, n, n, kt, ncap, blk, k1, k2, scale, out, sb, sc)
     else:
-        rkv.rkv_build_kt(dims, k, rows, n, None, 0, blk, kt, nblk)
-        rkv.rkv_hsa_decode(dims, q, k, v, rows, n, kt, nblk, blk, k1, k2, scale, out, sb, sc)
+        rkv.rkv_build_kt(dims, k, rows, n, None, 0, blk, kt, ncap)
+        rkv.rkv_hsa_decode(dims, q, k, v, rows, n, kt, ncap, blk, k1, k2, scale, out, sb, sc)
     torch.cuda.synchronize()
     out_h, sb_h, sc_h = out.cpu().numpy(), sb.cpu().numpy(), sc.cpu().numpy()
     worst, exempt = 0.0, 0
@@ -181,16 +182,17 @@ def test_hsa_decode_mt_equals_compacted():
     kc = torch.stack([torch.stack([k[b, h, idx_t[b, h].long()] for h in range(Hkv)]) for b in range(B)]).contiguous()
     vc = torch.stack([torch.stack([v[b, h, idx_t[b, h].long()] for h in range(Hkv)]) for b in range(B)]).contiguous()
     nblk = -(-n // blk)
-    kt1 = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
-    kt2 = torch.empty_like(kt1)
-    rkv.rkv_build_kt(dims, k, full, n, idx_t, n, blk, kt1, nblk)
-    rkv.rkv_build_kt(dims, kc, n, n, None, 0, blk, kt2, nblk)
+    ncap = -(-nblk // 8) * 8
+    kt1 = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    kt2 = torch.zeros_like(kt1)
+    rkv.rkv_build_kt(dims, k, full, n, idx_t, n, blk, kt1, ncap)
+    rkv.rkv_build_kt(dims, kc, n, n, None, 0, blk, kt2, ncap)
     o1 = torch.empty(B, Hq, D, device=DEV)
     o2 = torch.empty_like(o1)
     s1 = torch.empty(B, Hkv, k2, dtype=torch.int32, device=DEV)
     s2 = torch.empty_like(s1)
-    rkv.rkv_hsa_decode_mt(dims, q, k, v, full, idx_t, n, n, kt1, nblk, blk, k1, k2, 0.1, o1, s1, None)
-    rkv.rkv_hsa_decode(dims, q, kc, vc, n, n, kt2, nblk, blk, k1, k2, 0.1, o2, s2, None)
+    rkv.rkv_hsa_decode_mt(dims, q, k, v, full, idx_t, n, n, kt1, ncap, blk, k1, k2, 0.1, o1, s1, None)
+    rkv.rkv_hsa_decode(dims, q, kc, vc, n, n, kt2, ncap, blk, k1, k2, 0.1, o2, s2, None)
     torch.cuda.synchronize()
     assert torch.equal(kt1, kt2) and torch.equal(s1, s2) and torch.equal(o1, o2)
 
@@ -201,13 +203,13 @@ def test_hsa_decode_deterministic():
     _, k = _rand(51, (B, Hkv, n, D))
     _, v = _rand(52, (B, Hkv, n, D))
     _, q = _rand(53, (B, Hq, D))
-    nblk = -(-n // blk)
-    kt = torch.empty((B, Hkv, 2, D, nblk), dtype=torch.bfloat16, device=DEV)
-    rkv.rkv_build_kt(dims, k, n, n, None, 0, blk, kt, nblk)
+    ncap = -(-(-(-n // blk)) // 8) * 8
+    kt = torch.empty((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt(dims, k, n, n, None, 0, blk, kt, ncap)
     outs = []
     for _ in range(3):
         o = torch.empty(B, Hq, D, device=DEV)
-        rkv.rkv_hsa_decode(dims, q, k, v, n, n, kt, nblk, blk, 32, 32, 0.1, o)
+        rkv.rkv_hsa_decode(dims, q, k, v, n, n, kt, ncap, blk, 32, 32, 0.1, o)
         outs.append(o)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
@@ -248,11 +250,12 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
                 continue
             # pooled scores (fp32 accumulation of probabilities)
             pg = pooled[b, h, :L].cpu().numpy().astype(np.float64)
-            assert np.max(np.abs(pg - pooled_o) / np.maximum(np.abs(pooled_o), 1e-30)) < 2e-5
+            assert np.max(np.abs(pg - pooled_o) / np.maximum(np.abs(pooled_o), 1e-30)) < 1e-4
             ns = min(n_sink, L)
             assert got[:ns].tolist() == list(range(ns))
             assert got[B1 - min(W, S):].tolist() == list(range(S - min(W, S), S))
-            exempt += check_topk(got[ns:B1 - min(W, S)] - ns, pooled_o[ns:], B1 - min(W, S) - ns, "keep")
+            exempt += check_topk(got[ns:B1 - min(W, S)] - ns, pooled_o[ns:], B1 - min(W, S) - ns, "keep",
+                                 floor=SCORE_FLOOR)
             if compact:
                 assert np.array_equal(t2bits(ko[b, h, :B1]), kb[b, h][got])
                 assert np.array_equal(t2bits(vo[b, h, :B1]), vb[b, h][got])
@@ -275,3 +278,66 @@ def test_snap_evict_parity(B, Hq, Hkv, S, W, P, B1, sink):
 
 def test_snap_evict_mask_mode_and_peaked():
     _snap_case(9, 1, 32, 8, 3000, 32, 63, 400, compact=False, q_scale=4.0)
+
+
+# ------------------------------------------------------------- fused append --
+
+
+@pytest.mark.parametrize("mt", [False, True])
+@pytest.mark.parametrize("n0,blk,k2", [(300, 16, 5), (320, 16, 7), (0, 16, 3), (95, 32, 2), (1000, 8, 40)])
+def test_fused_append_equals_separate(mt, n0, blk, k2):
+    """HSA with the append fused in == rkv_append_kv followed by HSA: caches,
+    candidate rows, KT, selections and outputs all bit-identical."""
+    B, Hq, Hkv, D, k1 = 2, 32, 8, 128, 32
+    dims = (B, Hq, Hkv, D)
+    steps = 3
+    cap = n0 + steps + 5 if not mt else 3 * n0 + 40
+    _, k = _rand(61 + n0, (B, Hkv, cap, D))
+    _, v = _rand(62 + n0, (B, Hkv, cap, D))
+    _, qs = _rand(63, (steps, B, Hq, D))
+    _, kn = _rand(64, (steps, B, Hkv, D))
+    _, vn = _rand(65, (steps, B, Hkv, D))
+    ncap = -(-(-(-(n0 + steps) // blk)) // 8) * 8
+    idx_cap = n0 + steps
+    if mt:
+        rng = np.random.default_rng(66)
+        rows = np.stack([np.stack([np.sort(rng.choice(2 * n0 + 1, n0, replace=False)) for _ in range(Hkv)])
+                         for _ in range(B)]).astype(np.int32)
+        idx = torch.zeros((B, Hkv, idx_cap), dtype=torch.int32, device=DEV)
+        idx[:, :, :n0] = torch.from_numpy(rows).to(DEV)
+    states = []
+    for fused in (False, True):
+        kk, vv = k.clone(), v.clone()
+        kt = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+        ii = idx.clone() if mt else None
+        if n0:
+            rkv.rkv_build_kt(dims, kk, cap, n0, ii, idx_cap, blk, kt, ncap)
+        outs, sels = [], []
+        for s in range(steps):
+            o = torch.empty(B, Hq, D, device=DEV)
+            sb = torch.empty(B, Hkv, k2, dtype=torch.int32, device=DEV)
+            n, row = n0 + s, 2 * n0 + 1 + s
+            if fused:
+                if mt:
+                    rkv.rkv_hsa_decode_mt(dims, qs[s], kk, vv, cap, ii, idx_cap, n, kt, ncap, blk, k1, k2, 0.1, o, sb,
+                                          None, kn[s], vn[s], row)
+                else:
+                    rkv.rkv_hsa_decode(dims, qs[s], kk, vv, cap, n, kt, ncap, blk, k1, k2, 0.1, o, sb, None, kn[s],
+                                       vn[s])
+            else:
+                rkv.rkv_append_kv(dims, kn[s], vn[s], kk, vv, cap, n, row if mt else n, ii, idx_cap, kt, ncap, blk)
+                if mt:
+                    rkv.rkv_hsa_decode_mt(dims, qs[s], kk, vv, cap, ii, idx_cap, n + 1, kt, ncap, blk, k1, k2, 0.1, o,
+                                          sb)
+                else:
+                    rkv.rkv_hsa_decode(dims, qs[s], kk, vv, cap, n + 1, kt, ncap, blk, k1, k2, 0.1, o, sb)
+            outs.append(o)
+            sels.append(sb)
+        torch.cuda.synchronize()
+        states.append((kk, vv, kt, ii, outs, sels))
+    a, b = states
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    if mt:
+        assert torch.equal(a[3], b[3])
+    for s in range(steps):
+        assert torch.equal(a[5][s], b[5][s]) and torch.equal(a[4][s], b[4][s])

@@ -10,7 +10,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/rkv.h"
+#include "rkv.h"
 #include "rkv_internal.h"
 
 namespace {
@@ -77,24 +77,35 @@ rkv_status make_kv_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t 
   return RKV_OK;
 }
 
-rkv_status hsa_common(const rkv_dims& d, const void* q, const void* k, const void* v, int64_t cap,
-                      const int32_t* idx, int64_t idx_cap, int64_t n, const void* kt, int64_t nblk_cap, int32_t blk,
-                      int32_t k1, int32_t k2, float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
-                      void* stream, bool mt) {
+rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_t cap, int32_t* idx,
+                      int64_t idx_cap, int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
+                      float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
+                      const void* v_new, int64_t row, void* stream, bool mt) {
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
+  const bool app = k_new != nullptr;
   if (!q || !k || !v || !kt || !out) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: NULL tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
-    return fail(RKV_ERR_INVALID_ARG, "hsa_decode: q/k/v must be 16-byte aligned");
+  if ((k_new == nullptr) != (v_new == nullptr))
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode: k_new and v_new must both be set or both be NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(kt) || (app && (!aligned16(k_new) ||
+                                                                                    !aligned16(v_new))))
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode: q/k/v/kt/k_new/v_new must be 16-byte aligned");
   if (mt && !idx) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: idx is NULL");
-  if (n < 1 || n > cap) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: n=%lld outside [1, cap=%lld]", (long long)n,
-                                    (long long)cap);
-  if (mt && n > idx_cap) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: n=%lld > idx_cap=%lld", (long long)n,
-                                     (long long)idx_cap);
+  const int64_t n_tot = n + (app ? 1 : 0);
+  if (n < 0 || n_tot < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: no tokens to attend (n=%lld)", (long long)n);
+  if (!mt && n_tot > cap)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode: %lld tokens > cap=%lld", (long long)n_tot, (long long)cap);
+  if (mt && n_tot > idx_cap)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: %lld candidates > idx_cap=%lld", (long long)n_tot,
+                (long long)idx_cap);
+  if (mt && app && (row < 0 || row >= cap))
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: append row %lld outside [0, cap)", (long long)row);
   if (blk < 8 || blk > 128 || blk % 8 != 0)
     return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: block size %d (needs a multiple of 8 in [8,128])", blk);
-  const int64_t nblk = (n + blk - 1) / blk;
+  if (nblk_cap % 8 != 0) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: nblk_cap=%lld is not a multiple of 8",
+                                     (long long)nblk_cap);
+  const int64_t nblk = (n_tot + blk - 1) / blk;
   if (nblk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: ceil(n/blk)=%lld > nblk_cap=%lld",
                                    (long long)nblk, (long long)nblk_cap);
   if (nblk > 8192) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: %lld blocks > 8192", (long long)nblk);
@@ -104,7 +115,10 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, const void* k, const voi
   if (cap >= (int64_t)1 << 31) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: cap >= 2^31");
 
   rkv::HsaArgs a = {};
-  a.q = q; a.k = k; a.v = v; a.kt = kt; a.idx = idx; a.out = out;
+  a.q = q; a.k = k; a.v = v; a.kt = kt; a.idx = idx; a.idx_w = idx; a.out = out;
+  a.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
+  a.row = mt ? row : n;
   a.sel_blocks = sel_blocks; a.sel_channels = sel_channels;
   a.cap = cap; a.nblk_cap = nblk_cap; a.idx_cap = idx_cap;
   a.n = (int32_t)n; a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
@@ -117,8 +131,10 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, const void* k, const voi
   std::memset(&tmV, 0, sizeof(tmV));
   const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
   if (!mt) {
-    if ((s = make_kv_map(&tmK, k, pairs, cap, n, blk, "k")) != RKV_OK) return s;
-    if ((s = make_kv_map(&tmV, v, pairs, cap, n, blk, "v")) != RKV_OK) return s;
+    // rows at or past n (the appended token included) read as zero
+    const int64_t extent = std::max<int64_t>(n, 1);
+    if ((s = make_kv_map(&tmK, k, pairs, cap, extent, blk, "k")) != RKV_OK) return s;
+    if ((s = make_kv_map(&tmV, v, pairs, cap, extent, blk, "v")) != RKV_OK) return s;
   }
   cudaError_t e = rkv::hsa_launch(a, &tmK, &tmV, mt, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "hsa_decode launch");
@@ -250,19 +266,20 @@ rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void*
   return RKV_OK;
 }
 
-rkv_status rkv_hsa_decode(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap, int64_t n,
-                          const void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
-                          float* out, int32_t* sel_blocks, int32_t* sel_channels, void* stream) {
+rkv_status rkv_hsa_decode(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int64_t n, void* kt,
+                          int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale, float* out,
+                          int32_t* sel_blocks, int32_t* sel_channels, const void* k_new, const void* v_new,
+                          void* stream) {
   return hsa_common(d, q, k, v, cap, nullptr, 0, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks, sel_channels,
-                    stream, false);
+                    k_new, v_new, n, stream, false);
 }
 
-rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, const void* k, const void* v, int64_t cap, const int32_t* idx,
-                             int64_t idx_cap, int64_t n, const void* kt, int64_t nblk_cap, int32_t blk, int32_t k1,
-                             int32_t k2, float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
-                             void* stream) {
+rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int32_t* idx, int64_t idx_cap,
+                             int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
+                             float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
+                             const void* v_new, int64_t row, void* stream) {
   return hsa_common(d, q, k, v, cap, idx, idx_cap, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
-                    sel_channels, stream, true);
+                    sel_channels, k_new, v_new, row, stream, true);
 }
 
 rkv_status rkv_read_device_flags(uint32_t* flags) {

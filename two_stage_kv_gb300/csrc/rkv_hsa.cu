@@ -1,32 +1,44 @@
-// Stage 2 of RocketKV: one Hybrid Sparse Attention decode step per launch.
+// Stage 2 of RocketKV: one Hybrid Sparse Attention decode step per launch,
+// optionally fused with the append of the step's new key/value.
 //
 // Method: "RocketKV: Accelerating Long-Context LLM Inference via Two-Stage KV
-// Cache Compression" (papercache digest), section 方法细节, HSA steps 2-3 and
+// Cache Compression" (papercache digest), section 方法细节, HSA steps 1-3 and
 // Algorithm 1 (top-k1 channels of the group sum of |q|, sign of the group sum
 // of q, sign-selected Kmax/Kmin page scores, top-k2 pages, exact attention over
-// the selected pages); RocketKV-MT for the candidate-restricted variant.
+// the selected pages; the Kmax/Kmin store is updated when a key is generated);
+// RocketKV-MT for the candidate-restricted variant.
 //
-// GB300 design.  One thread-block cluster of `ns` CTAs (128 threads each) per
-// (batch row, KV head).  Every CTA of the cluster:
-//   A. loads the group's G query rows, forms sum|q| and sum q per channel in
-//      fp64 (exact for bf16 inputs) and picks the k1 channels by rank;
-//   B. scores its 1/ns slice of the blocks from the channel-major KT cache
-//      (coalesced rows along the block axis) and broadcasts the scores to
-//      every CTA of the cluster through distributed shared memory;
-//   C. ranks its own slice against all scores (strict order: score, then
-//      lower block index) and broadcasts the winners' ranks as slots;
-//   D. TMA-loads the K and V rows of its share of the selected blocks into
-//      128-byte-swizzled shared tiles, runs QK^T and PV with bf16 mma.sync
-//      (G query rows padded to 16; P split into bf16 hi + lo so the PV product
-//      keeps ~16 mantissa bits) and an online softmax in fp32;
-//   E. merges its warps' partial (max, sum, acc), sends the per-head partial to
-//      the CTA that owns that head, and the owners combine the ns partials and
-//      write fp32 outputs.  No global scratch, no atomics, no inter-CTA spins:
-//      the only cluster waits are hardware cluster barriers.
+// GB300 design.  One thread-block cluster of `ns` CTAs (256 threads each) per
+// (batch row, KV head), ns chosen so the grid fits in one wave.  Every CTA:
+//   A. loads the group's G query rows and forms sum|q| and sum q per channel in
+//      fp32 with an error-free TwoSum check (an inexact sum sends the whole CTA
+//      to an fp64 path, so the channel decision is the exact-arithmetic one),
+//      then picks the top-k1 channels;
+//   B. gathers the k1 chosen rows of the channel-major KT cache into shared
+//      memory with 16-byte cp.async, folds the appended key into its block,
+//      and scores every block in fp32;
+//   C. picks the top-k2 blocks and lists them in ascending order (every CTA of
+//      the cluster computes the same list);
+//   D. TMA-loads the K and V rows of its share of the blocks into 128-byte-
+//      swizzled shared tiles (rows past n read as zero; one mbarrier per
+//      block), computes S^T = K Q^T per 16-token step on bf16 mma.sync (tokens
+//      on the M side, G <= 8 heads per 8-wide N tile), a CTA-wide softmax in
+//      fp32, and O^T = V^T P^T with each warp owning 16 output dimensions (P
+//      is split into bf16 hi + lo, so PV keeps ~16 mantissa bits);
+//   E. sends its partial (max, sum, O) for each head over distributed shared
+//      memory to the CTA that owns the head; after one cluster barrier the
+//      owner combines the ns partials and writes fp32 outputs.
+// Both top-k steps are exact (larger first, equal values: lower index): a
+// 256-bucket histogram over [min, max] finds the bucket holding the k-th value
+// and only that bucket's members are ranked pairwise; a radix select on an
+// order-preserving key takes over for degenerate value sets.  No global
+// scratch, no atomics on the data path and no spin on other CTAs: the only
+// cross-CTA waits are hardware cluster barriers.
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 
 #include <algorithm>
+#include <mutex>
 
 namespace rkv {
 
@@ -34,35 +46,221 @@ static __device__ unsigned int g_hsa_err = 0;
 
 namespace {
 
-constexpr int NT = 128;          // threads per CTA
+constexpr int NT = 256;                 // threads per CTA
 constexpr int NWARP = NT / 32;
-constexpr int PART_STRIDE = HD + 2;   // acc[128], max, sum
-constexpr uint32_t FIXED_SMEM = 8192;
-constexpr int MAX_ROUND_ROWS = 256;
+constexpr int PART_STRIDE = HD + 2;     // O[128], max, sum
+constexpr int MAX_ROUND_ROWS = 128;     // K/V rows staged per round (8 steps of 16 tokens)
+constexpr uint32_t KT_TILE_BUDGET = 32 * 1024;
+constexpr int NBUCKET = NT;             // one histogram bucket per thread
+constexpr int MEMBER_MAX = 512;         // boundary-bucket members ranked pairwise
 
-// Fixed shared-memory region (first FIXED_SMEM bytes).
 struct FixedSmem {
-  bf16 qs[16][HD];            // 4096: query rows, rows >= G are zero
-  uint64_t akey[HD];          // 1024: bits of sum|q| (non-negative doubles order like integers)
-  double qbar[HD];            // 1024: sum q
-  float qsel[HD];             //  512: qbar of the kept channels, ascending channel order
-  int32_t rowoff[HD];         //  512: KT row (0..2D) of each kept channel
-  uint64_t mbar[2];           //   16
-  int32_t wcount[NWARP];      //   16
-  int32_t nvalid[MAX_ROUND_ROWS / 8];  // valid tokens of each staged block
+  bf16 qs[16][HD + 8];          // query rows (padded: conflict-free ldmatrix), rows >= G are zero
+  bf16 knew[HD];                // appended key / value of this pair
+  bf16 vnew[HD];
+  float qsel[HD];               // group-summed q of the kept channels, ascending channel
+  int32_t rowoff[HD];           // KT row (0..2*HD) of each kept channel
+  float asum[HD];               // sum_g |q_g| per channel (fp32, exact)
+  float qbar32[HD];
+  uint64_t akey64[HD];          // fp64 fallback
+  double qbar64[HD];
+  uint8_t cflag[HD];
+  int32_t hist[4 * 256];        // bucket histogram; the radix fallback uses 4 x 256
+  int32_t members[MEMBER_MAX];
+  float wmin[NWARP], wmax[NWARP];
+  int32_t wsum[2 * NWARP];
+  int32_t misc[8];
+  float wmaxh[NWARP][16];       // per-warp head maxima of a round
+  float wsumh[NWARP][16];       // per-warp head probability sums of a round
+  uint32_t pfrag[MAX_ROUND_ROWS / 16][2][4][32];   // P^T B fragments per 16-token step, head tile, hi/lo
+  float mrun[16], lrun[16];
+  int32_t nvalid[MAX_ROUND_ROWS / 8];
+  uint64_t mbar[MAX_ROUND_ROWS / 8];    // one per staged block
 };
-static_assert(sizeof(FixedSmem) <= FIXED_SMEM, "fixed smem");
 
-template <bool MT>
-__global__ void __launch_bounds__(NT) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                        const __grid_constant__ CUtensorMap tmV,
-                                                        const HsaArgs a) {
+// Block-wide exclusive scan of a flag.  Returns the prefix, writes the total.
+__device__ __forceinline__ int scan1(bool f, int32_t* wsum, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, f);
+  if (lane == 0) wsum[warp] = __popc(bal);
+  __syncthreads();
+  int pre = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) {
+    const int v = wsum[w];
+    if (w < warp) pre += v;
+    tot += v;
+  }
+  __syncthreads();
+  total = tot;
+  return pre + __popc(bal & ((1u << lane) - 1u));
+}
+
+// Exact top-k of keys[0, n) by MSB-first radix select on order-preserving keys
+// (equal keys: lower index first); writes flag[0, n).
+__device__ void radix_topk(const uint32_t* keys, int n, int k, uint8_t* flag, FixedSmem& fs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 4 * 256; i += NT) fs.hist[i] = 0;
+  __syncthreads();
+  uint32_t prefix = 0, mask = 0;
+  int kk = k;
+  for (int p = 0; p < 4; ++p) {
+    const int shift = 24 - 8 * p;
+    int32_t* h = fs.hist + 256 * p;
+    for (int base = 0; base < n; base += NT) {
+      const int j = base + tid;
+      const uint32_t key = j < n ? keys[j] : 0u;
+      const bool act = (j < n) && ((key & mask) == prefix);
+      const unsigned am = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const unsigned d = (key >> shift) & 255u;
+        const unsigned m = __match_any_sync(am, d);
+        if (lane == __ffs(m) - 1) atomicAdd(&h[d], __popc(m));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int cnt[8];
+      int s = 0;
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        cnt[u] = h[lane * 8 + u];
+        s += cnt[u];
+      }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      int above = incl - s;
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        if (above < kk && above + cnt[u] >= kk) {
+          fs.misc[4] = lane * 8 + u;
+          fs.misc[5] = kk - above;
+        }
+        above += cnt[u];
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)fs.misc[4] << shift;
+    mask |= 255u << shift;
+    kk = fs.misc[5];
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  int eq_taken = 0;
+  for (int base = 0; base < n; base += NT) {
+    const int j = base + tid;
+    const uint32_t key = j < n ? keys[j] : 0u;
+    const bool eq = (j < n) && key == T;
+    int eq_tot;
+    const int eq_before = scan1(eq, fs.wsum, eq_tot);
+    if (j < n) flag[j] = (key > T) || (eq && eq_taken + eq_before < kk);
+    eq_taken += eq_tot;
+  }
+  __syncthreads();
+}
+
+// Exact top-k (0 < k < n) of vals[0, n): flag[j] = 1 for the k largest values,
+// equal values taken in ascending index order.  mn / mx are the minimum and
+// maximum of vals.  The fallback overwrites vals with order-preserving keys.
+// fs.hist must be zero on entry and is zero again on return.
+__device__ void bucket_topk(float* vals, int n, int k, float mn, float mx, uint8_t* flag, FixedSmem& fs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float width = mx - mn;
+  bool fallback = !(width > 0.f) || !isfinite(width);
+  const float inv = fallback ? 0.f : (float)NBUCKET / width;
+  auto bucket = [&](float s) { return min(NBUCKET - 1, (int)((s - mn) * inv)); };
+  if (!fallback) {
+    for (int j = tid; j < n; j += NT) atomicAdd(&fs.hist[bucket(vals[j])], 1);
+    __syncthreads();
+    const int c = fs.hist[tid];
+    int incl = c;   // this thread's bucket and every higher bucket of its warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += t;
+    }
+    if (lane == 0) fs.wsum[warp] = incl;
+    fs.hist[tid] = 0;                 // leave the histogram zeroed for the next caller
+    __syncthreads();
+    int above = incl - c;
+    for (int w = warp + 1; w < NWARP; ++w) above += fs.wsum[w];
+    if (above < k && above + c >= k) {
+      fs.misc[0] = tid;               // boundary bucket
+      fs.misc[1] = k - above;         // its members to take
+      fs.misc[2] = c;                 // its size
+      fs.misc[3] = 0;
+    }
+    __syncthreads();
+    fallback = fs.misc[2] > MEMBER_MAX;
+  }
+  if (!fallback) {
+    const int bb = fs.misc[0], need = fs.misc[1], m = fs.misc[2];
+    for (int j = tid; j < n; j += NT) {
+      const int bk = bucket(vals[j]);
+      flag[j] = bk > bb;
+      if (bk == bb) fs.members[atomicAdd(&fs.misc[3], 1)] = j;
+    }
+    __syncthreads();
+    for (int i = tid; i < m; i += NT) {
+      const int j = fs.members[i];
+      const float s = vals[j];
+      int rk = 0;
+      for (int i2 = 0; i2 < m; ++i2) {
+        const int j2 = fs.members[i2];
+        const float s2 = vals[j2];
+        rk += (s2 > s) || (s2 == s && j2 < j);
+      }
+      if (rk < need) flag[j] = 1;
+    }
+    __syncthreads();
+  } else {
+    uint32_t* keys = reinterpret_cast<uint32_t*>(vals);
+    __syncthreads();
+    for (int j = tid; j < n; j += NT) keys[j] = f2key(vals[j]);
+    __syncthreads();
+    radix_topk(keys, n, k, flag, fs);
+    for (int i = tid; i < 4 * 256; i += NT) fs.hist[i] = 0;
+    __syncthreads();
+  }
+}
+
+// Block-wide min / max of v over the threads (every thread gets the result).
+__device__ __forceinline__ void block_minmax(float& mn, float& mx, FixedSmem& fs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    fs.wmin[warp] = mn;
+    fs.wmax[warp] = mx;
+  }
+  __syncthreads();
+  mn = fs.wmin[0];
+  mx = fs.wmax[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) {
+    mn = fminf(mn, fs.wmin[w]);
+    mx = fmaxf(mx, fs.wmax[w]);
+  }
+}
+
+template <bool MT, int NH>
+__global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                           const __grid_constant__ CUtensorMap tmV,
+                                                           const HsaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   FixedSmem& fs = *reinterpret_cast<FixedSmem*>(smem);
-  uint32_t* skey = reinterpret_cast<uint32_t*>(smem + a.off_scores);
+  bf16* kttile = reinterpret_cast<bf16*>(smem + a.off_tiles);          // phase B (dead before D)
+  float* sval = reinterpret_cast<float*>(smem + a.off_scores);
+  uint8_t* flag = reinterpret_cast<uint8_t*>(smem + a.off_flags);
   int32_t* sel = reinterpret_cast<int32_t*>(smem + a.off_sel);
-  float* part = reinterpret_cast<float*>(smem + a.off_part);
   float* recv = reinterpret_cast<float*>(smem + a.off_recv);
   uint8_t* tK = smem + a.off_tiles;
   uint8_t* tV = tK + 2 * a.tile_half_bytes;
@@ -73,160 +271,233 @@ __global__ void __launch_bounds__(NT) hsa_decode_kernel(const __grid_constant__ 
   const int hk = blockIdx.y, b = blockIdx.z;
   const int pair = b * a.Hkv + hk;
   const int G = a.G;
+  const bool app = a.k_new != nullptr;
+  const int n_old = a.n;                      // tokens before this step's append
+  const int n_tot = a.n + (app ? 1 : 0);      // tokens attended
+  const int nb_new = app ? n_old / a.blk : -1;
+  const int nblk = a.nblk;
 
-  // Every CTA of the cluster must have started before any DSMEM store lands
-  // in it; the matching wait sits just before the first remote store.
-  cluster_arrive_relaxed();
-
-  if (!MT && tid == 0) {
-    prefetch_tmap(&tmK);
-    prefetch_tmap(&tmV);
+  // Prologue that touches no data of the previous kernel.
+  if (tid == 0) {
+    for (int i = 0; i < MAX_ROUND_ROWS / 8; ++i) mbar_init(&fs.mbar[i], 1);
+    fence_mbar_init();
+    if (!MT) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+    }
   }
+  for (int i = tid; i < 4 * 256; i += NT) fs.hist[i] = 0;
+  if (tid < 16) {
+    fs.mrun[tid] = neg_inf();
+    fs.lrun[tid] = 0.f;
+  }
+  // every CTA of the cluster must have started before a DSMEM store reaches it;
+  // the matching wait precedes the first remote store (phase E)
+  cluster_arrive_relaxed();
+  pdl_wait();
+  pdl_launch_dependents();
 
   // ---------------------------------------------------------------- A ------
   {
     const bf16* qg = reinterpret_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)hk * G) * HD;
-    for (int i = tid; i < 16 * (HD / 8); i += NT) {
-      const int r = i / (HD / 8), c = i % (HD / 8);
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (r < G) val = *reinterpret_cast<const uint4*>(qg + (size_t)r * HD + c * 8);
-      *reinterpret_cast<uint4*>(&fs.qs[r][c * 8]) = val;
+    const int r = tid >> 4, c = tid & 15;          // 256 threads = 16 rows x 16 chunks
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < G) val = *reinterpret_cast<const uint4*>(qg + (size_t)r * HD + c * 8);
+    *reinterpret_cast<uint4*>(&fs.qs[r][c * 8]) = val;
+    if (app && tid < 32) {
+      const bf16* src = (tid < 16 ? a.k_new : a.v_new) + (size_t)pair * HD + (tid & 15) * 8;
+      bf16* dst = (tid < 16 ? fs.knew : fs.vnew) + (tid & 15) * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
     }
-  }
-  if (tid == 0) {
-    mbar_init(&fs.mbar[0], 1);
-    fence_mbar_init();
-  }
-  // pad the score keys up to a multiple of 4 with the smallest key
-  {
-    const int npad = (a.nblk + 3) & ~3;
-    for (int j = a.nblk + tid; j < npad; j += NT) skey[j] = 0u;
   }
   __syncthreads();
-  {
-    const int c = tid;  // NT == HD: one thread per channel
-    double sa = 0.0, sq = 0.0;
+  bool inexact = false;
+  float amn = __int_as_float(0x7f800000), amx = neg_inf();
+  if (tid < HD) {
+    float sa = 0.f, sq = 0.f;
     for (int g = 0; g < G; ++g) {
-      const double x = (double)bf2f(fs.qs[g][c]);
-      sa += fabs(x);
-      sq += x;
+      const float x = bf2f(fs.qs[g][tid]);
+      float e1, e2;
+      sa = two_sum(sa, fabsf(x), e1);
+      sq = two_sum(sq, x, e2);
+      inexact |= (e1 != 0.f) | (e2 != 0.f);
     }
-    fs.akey[c] = (uint64_t)__double_as_longlong(sa);
-    fs.qbar[c] = sq;
+    fs.asum[tid] = sa;
+    fs.qbar32[tid] = sq;
+    amn = amx = sa;
+  }
+  const bool use64 = __syncthreads_or(inexact) != 0;
+  if (!use64) {
+    if (a.k1 >= HD) {
+      if (tid < HD) fs.cflag[tid] = 1;
+    } else {
+      block_minmax(amn, amx, fs);
+      bucket_topk(fs.asum, HD, a.k1, amn, amx, fs.cflag, fs);
+    }
+  } else {
+    // rare: some group sum needs more than fp32's 24 bits; redo every channel in fp64
+    if (tid < HD) {
+      double sa = 0.0, sq = 0.0;
+      for (int g = 0; g < G; ++g) {
+        const double x = (double)bf2f(fs.qs[g][tid]);
+        sa += fabs(x);
+        sq += x;
+      }
+      fs.akey64[tid] = (uint64_t)__double_as_longlong(sa);   // non-negative: orders like integers
+      fs.qbar64[tid] = sq;
+    }
+    __syncthreads();
+    if (tid < HD) {
+      const uint64_t mine = fs.akey64[tid];
+      int rk = 0;
+      for (int j = 0; j < HD; ++j) {
+        const uint64_t o = fs.akey64[j];
+        rk += (o > mine) || (o == mine && j < tid);
+      }
+      fs.cflag[tid] = rk < a.k1;
+    }
   }
   __syncthreads();
   {
     const int c = tid;
-    const uint64_t mine = fs.akey[c];
-    int rk = 0;
-#pragma unroll 8
-    for (int j = 0; j < HD; ++j) {
-      const uint64_t o = fs.akey[j];
-      rk += (o > mine) || (o == mine && j < c);
-    }
-    const bool take = rk < a.k1;
+    const bool take = tid < HD && fs.cflag[c];
     const unsigned bal = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) fs.wcount[warp] = __popc(bal);
+    if (lane == 0) fs.wsum[warp] = __popc(bal);
     __syncthreads();
     int pos = __popc(bal & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) pos += fs.wcount[w];
+    for (int w = 0; w < warp; ++w) pos += fs.wsum[w];
     if (take) {
-      const double qb = fs.qbar[c];
+      const double qb = use64 ? fs.qbar64[c] : (double)fs.qbar32[c];
       fs.qsel[pos] = (float)qb;
-      fs.rowoff[pos] = (qb >= 0.0 ? 0 : HD) + c;   // Kmax if the group sum is >= 0
+      fs.rowoff[pos] = (qb >= 0.0 ? 0 : HD) + c;     // Kmax when the group sum is >= 0
       if (rank == 0 && a.sel_channels) a.sel_channels[(size_t)pair * a.k1 + pos] = c;
     }
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- B ------
-  const int per = (a.nblk + ns - 1) / ns;
-  const int lo = (int)rank * per;
-  const int hi = min(a.nblk, lo + per);
-  cluster_wait_acquire();   // pairs with the relaxed arrive at entry
+  const int k1 = a.k1;
+  float smn = __int_as_float(0x7f800000), smx = neg_inf();
   {
     const bf16* ktp = reinterpret_cast<const bf16*>(a.kt) + (size_t)pair * 2 * HD * a.nblk_cap;
-    const int k1 = a.k1;
-    for (int j = lo + tid; j < hi; j += NT) {
-      float s = 0.f;
-      int i = 0;
-      for (; i + 8 <= k1; i += 8) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = bf2f(ktp[(size_t)fs.rowoff[i + u] * a.nblk_cap + j]);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) s = fmaf(fs.qsel[i + u], v[u], s);
+    const int bc = a.kt_chunk;                       // blocks per gathered chunk (multiple of 8)
+    for (int cb0 = 0; cb0 < nblk; cb0 += bc) {
+      const int nb_here = min(bc, nblk - cb0);
+      const int n16 = (nb_here + 7) / 8;
+      for (int row = warp; row < k1; row += NWARP) {
+        const bf16* src = ktp + (size_t)fs.rowoff[row] * a.nblk_cap + cb0;
+        bf16* dst = kttile + (size_t)row * bc;
+        for (int ch = lane; ch < n16; ch += 32) cp_async_16(smem_u32(dst + ch * 8), src + ch * 8);
       }
-      for (; i < k1; ++i) s = fmaf(fs.qsel[i], bf2f(ktp[(size_t)fs.rowoff[i] * a.nblk_cap + j]), s);
-      const uint32_t key = f2key(s);
-      const uint32_t laddr = smem_u32(&skey[j]);
-      for (int d = 0; d < ns; ++d) st_cluster_u32(mapa(laddr, d), key);
+      cp_async_commit();
+      cp_async_wait_all();
+      __syncthreads();
+      if (app && nb_new >= cb0 && nb_new < cb0 + nb_here) {
+        // fold the appended key into its block (a new block starts from it)
+        const int col = nb_new - cb0;
+        const bool fresh = (n_old % a.blk) == 0;
+        for (int i = tid; i < k1; i += NT) {
+          const int ro = fs.rowoff[i];
+          const bf16 kv = fs.knew[ro & (HD - 1)];
+          bf16& slot = kttile[(size_t)i * bc + col];
+          if (fresh) {
+            slot = kv;
+          } else {
+            const float x = bf2f(kv), o = bf2f(slot);
+            if (ro >= HD ? (x < o) : (x > o)) slot = kv;
+          }
+        }
+        __syncthreads();
+      }
+      // two adjacent blocks per thread from one 32-bit load per channel
+      for (int jp = tid; 2 * jp < nb_here; jp += NT) {
+        float s0 = 0.f, s1 = 0.f;
+        const uint32_t* col = reinterpret_cast<const uint32_t*>(kttile) + jp;
+        const int pitch = bc / 2;
+        for (int i = 0; i < k1; ++i) {
+          const uint32_t v = col[(size_t)i * pitch];
+          const float q = fs.qsel[i];
+          s0 = fmaf(q, bf16_lo(v), s0);
+          s1 = fmaf(q, bf16_hi(v), s1);
+        }
+        const int j = 2 * jp;
+        s0 = (s0 == 0.f) ? 0.f : s0;     // -0 -> +0
+        s1 = (s1 == 0.f) ? 0.f : s1;
+        sval[cb0 + j] = s0;
+        smn = fminf(smn, s0);
+        smx = fmaxf(smx, s0);
+        if (j + 1 < nb_here) {
+          sval[cb0 + j + 1] = s1;
+          smn = fminf(smn, s1);
+          smx = fmaxf(smx, s1);
+        }
+      }
+      __syncthreads();
     }
   }
-  cluster_sync();
 
   // ---------------------------------------------------------------- C ------
+  const int k2e = a.k2e;
+  if (k2e >= nblk) {
+    for (int j = tid; j < nblk; j += NT) flag[j] = 1;
+  } else {
+    block_minmax(smn, smx, fs);
+    bucket_topk(sval, nblk, k2e, smn, smx, flag, fs);
+  }
+  __syncthreads();
   {
-    const int nq = (a.nblk + 3) >> 2;
-    const uint4* sk4 = reinterpret_cast<const uint4*>(skey);
-    for (int j = lo + tid; j < hi; j += NT) {
-      const uint32_t mine = skey[j];
-      int rk = 0;
-      for (int o4 = 0; o4 < nq; ++o4) {
-        const uint4 k4 = sk4[o4];
-        const int o = o4 * 4;
-        rk += (k4.x > mine) | ((k4.x == mine) & (o + 0 < j));
-        rk += (k4.y > mine) | ((k4.y == mine) & (o + 1 < j));
-        rk += (k4.z > mine) | ((k4.z == mine) & (o + 2 < j));
-        rk += (k4.w > mine) | ((k4.w == mine) & (o + 3 < j));
-      }
-      if (rk < a.k2e) {
-        const uint32_t laddr = smem_u32(&sel[rk]);
-        for (int d = 0; d < ns; ++d) st_cluster_u32(mapa(laddr, d), (uint32_t)j);
-      }
+    int out = 0;
+    for (int base = 0; base < nblk; base += NT) {
+      const int j = base + tid;
+      const bool f = j < nblk && flag[j];
+      int tot;
+      const int pre = scan1(f, fs.wsum, tot);
+      if (f && out + pre < k2e) sel[out + pre] = j;
+      out += tot;
     }
   }
-  cluster_sync();
+  __syncthreads();
 
   // ---------------------------------------------------------------- D ------
-  // Query A fragments (16 rows x 128 dims) for the 8 k-steps.
-  uint32_t qa[8][4];
+  // Q as the B operand of S^T = K Q^T: heads 8*ht .. 8*ht+7, all 8 k-steps.
+  uint32_t qb[NH][8][2];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int col = ks * 16 + (lane >> 4) * 8;
-    ldsm_x4(smem_u32(&fs.qs[row][col]), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-  }
-
-  float m_run[2] = {neg_inf(), neg_inf()};
-  float l_run[2] = {0.f, 0.f};
-  float acc[16][4];
+  for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int j = 0; j < 4; ++j)
+      ldsm_x4(smem_u32(&fs.qs[8 * ht + (lane & 7)][(4 * j + (lane >> 3)) * 8]), qb[ht][2 * j][0], qb[ht][2 * j][1],
+              qb[ht][2 * j + 1][0], qb[ht][2 * j + 1][1]);
+  // O^T accumulator of this warp's 16 output dimensions: dims 16*warp + lane/4 (+8),
+  // heads 8*ht + 2*(lane%4) + {0, 1}
+  float acc[NH][4];
+#pragma unroll
+  for (int ht = 0; ht < NH; ++ht) acc[ht][0] = acc[ht][1] = acc[ht][2] = acc[ht][3] = 0.f;
 
   const int s_lo = (int)rank * a.chunk;
-  const int s_hi = min(a.k2e, s_lo + a.chunk);
+  const int s_hi = min(k2e, s_lo + a.chunk);
   const uint32_t half = a.tile_half_bytes;
   const int blk = a.blk;
   uint32_t phase = 0;
   unsigned int* err = &g_hsa_err;
+  const int g4 = lane >> 2, t4 = lane & 3;
 
   for (int r0 = s_lo; r0 < s_hi; r0 += a.slots_round) {
     const int nsl = min(a.slots_round, s_hi - r0);
     const int rows = nsl * blk;
-    const int rows16 = (rows + 15) & ~15;
-    if (tid < nsl) fs.nvalid[tid] = min(blk, a.n - sel[r0 + tid] * blk);
+    const int nsteps = (rows + 15) / 16;
+    const int rows16 = nsteps * 16;
+    if (tid < nsl) fs.nvalid[tid] = min(blk, n_tot - sel[r0 + tid] * blk);
     if (!MT) {
-      if (tid == 0) {
-        if (r0 != s_lo) fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&fs.mbar[0], (uint32_t)nsl * blk * 128u * 4u);
-        for (int s = 0; s < nsl; ++s) {
+      if (warp == 0) {
+        if (lane == 0) fence_proxy_async_smem();   // earlier generic accesses to this region come first
+        for (int s = lane; s < nsl; s += 32) mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * 4u);
+        __syncwarp();
+        for (int t = lane; t < nsl * 4; t += 32) {
+          const int s = t >> 2, part = t & 3;          // part: K lo, K hi, V lo, V hi
           const int y = sel[r0 + s] * blk;
-          const uint32_t off = (uint32_t)s * blk * 128u;
-          tma_load_3d(tK + off, &tmK, 0, y, pair, &fs.mbar[0]);
-          tma_load_3d(tK + half + off, &tmK, 64, y, pair, &fs.mbar[0]);
-          tma_load_3d(tV + off, &tmV, 0, y, pair, &fs.mbar[0]);
-          tma_load_3d(tV + half + off, &tmV, 64, y, pair, &fs.mbar[0]);
+          const uint32_t off = (uint32_t)s * blk * 128u + (uint32_t)(part & 1) * half;
+          tma_load_3d(((part >> 1) ? tV : tK) + off, (part >> 1) ? &tmV : &tmK, (part & 1) * 64, y, pair,
+                      &fs.mbar[s]);
         }
       }
     } else {
@@ -238,10 +509,13 @@ __global__ void __launch_bounds__(NT) hsa_decode_kernel(const __grid_constant__ 
         const int slot = r / blk;
         const int t = sel[r0 + slot] * blk + (r - slot * blk);
         const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
-        if (t < a.n) {
+        if (t < n_old) {
           const int64_t prow = min(max((int64_t)ib[t], (int64_t)0), a.cap - 1);
           cp_async_16(smem_u32(tK) + o, kb + prow * HD + ch * 8);
           cp_async_16(smem_u32(tV) + o, vb + prow * HD + ch * 8);
+        } else if (t == n_old && app) {
+          *reinterpret_cast<uint4*>(tK + o) = *reinterpret_cast<const uint4*>(fs.knew + ch * 8);
+          *reinterpret_cast<uint4*>(tV + o) = *reinterpret_cast<const uint4*>(fs.vnew + ch * 8);
         } else {
           *reinterpret_cast<uint4*>(tK + o) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(tV + o) = make_uint4(0, 0, 0, 0);
@@ -249,237 +523,302 @@ __global__ void __launch_bounds__(NT) hsa_decode_kernel(const __grid_constant__ 
       }
       cp_async_commit();
     }
-    // Rows [rows, rows16) of the V tile feed the last PV step with P = 0; keep them finite.
-    for (int i = tid; i < (rows16 - rows) * 16; i += NT) {
-      const int r = rows + (i >> 4), ch = i & 15;
-      *reinterpret_cast<uint4*>(tV + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+    // Rows [rows, rows16) of both tiles enter the last 16-token step with P = 0: keep them finite.
+    for (int i = tid; i < (rows16 - rows) * 32; i += NT) {
+      const int r = rows + (i >> 5), ch = (i >> 1) & 15;
+      *reinterpret_cast<uint4*>(((i & 1) ? tV : tK) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7)) =
+          make_uint4(0, 0, 0, 0);
     }
-    if (!MT) {
-      if (!mbar_wait(&fs.mbar[0], phase, err)) mbar_wait(&fs.mbar[0], phase, err);
-      phase ^= 1u;
-    } else {
-      cp_async_wait_all();
-    }
+    if (MT) cp_async_wait_all();
     __syncthreads();
 
-    for (int c0 = warp * 16; c0 < rows; c0 += NWARP * 16) {
-      // S = Q K^T over tokens c0 .. c0+15 (two n-tiles of 8 tokens)
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // --- S^T = K Q^T for the warp's 16-token step, masked and in log2 units
+    const int c0 = warp * 16;
+    const bool has_step = c0 < rows;
+    float x[NH][4];
 #pragma unroll
-      for (int ks = 0; ks < 8; ks += 2) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int r = c0 + nt * 8 + (lane & 7);
-          const int ch = ks * 2 + (lane >> 3);        // 16-byte chunk of the 128 dims
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(smem_u32(tK) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), b0, b1, b2, b3);
-          mma_bf16(sc[nt], qa[ks], b0, b1);
-          mma_bf16(sc[nt], qa[ks + 1], b2, b3);
+    for (int ht = 0; ht < NH; ++ht) x[ht][0] = x[ht][1] = x[ht][2] = x[ht][3] = neg_inf();
+    if (has_step) {
+      if (!MT) {
+        const int sa = c0 / blk, sb = min((c0 + 15) / blk, nsl - 1);
+        for (int s = sa; s <= sb; ++s)
+          if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
+        if (app) {
+          // the appended token lies past the tensor map's extent (read as zero): write it in
+          for (int s = sa; s <= sb; ++s) {
+            if (sel[r0 + s] != nb_new) continue;
+            const int r = s * blk + (n_old - nb_new * blk);
+            const int ch = lane & 15;
+            const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
+            uint8_t* dst = (lane < 16 ? tK : tV) + o;
+            const bf16* src = (lane < 16 ? fs.knew : fs.vnew) + ch * 8;
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+          }
+          __syncwarp();
         }
       }
-      // mask, scale to log2 units, online softmax
-      float x[2][4];
-      float mx0 = neg_inf(), mx1 = neg_inf();
+      float st[NH][2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = c0 + nt * 8 + 2 * (lane & 3) + (e & 1);
-          const int slot = r / blk;
-          const bool valid = (r < rows) && (r - slot * blk < fs.nvalid[min(slot, nsl - 1)]);
-          const float v = valid ? sc[nt][e] * a.scale_log2 : neg_inf();
-          x[nt][e] = v;
-          if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
-        }
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-      const float c0f = (m_run[0] == neg_inf()) ? 0.f : exp2f(m_run[0] - mn0);
-      const float c1f = (m_run[1] == neg_inf()) ? 0.f : exp2f(m_run[1] - mn1);
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-      float p[2][4];
-      float ps0 = 0.f, ps1 = 0.f;
+        for (int u = 0; u < 2; ++u) st[ht][u][0] = st[ht][u][1] = st[ht][u][2] = st[ht][u][3] = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float mref = (e < 2) ? mn0 : mn1;
-          const float pv = (x[nt][e] == neg_inf()) ? 0.f : exp2f(x[nt][e] - mref);
-          p[nt][e] = pv;
-          if (e < 2) ps0 += pv; else ps1 += pv;
-        }
-      }
-      l_run[0] = l_run[0] * c0f + ps0;
-      l_run[1] = l_run[1] * c1f + ps1;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        acc[i][0] *= c0f;
-        acc[i][1] *= c0f;
-        acc[i][2] *= c1f;
-        acc[i][3] *= c1f;
-      }
-      // P as the A operand (rows = heads, k = 16 tokens), split hi + lo
-      uint32_t ph[4], pl[4];
-      ph[0] = pack_bf16(p[0][0], p[0][1]);
-      ph[1] = pack_bf16(p[0][2], p[0][3]);
-      ph[2] = pack_bf16(p[1][0], p[1][1]);
-      ph[3] = pack_bf16(p[1][2], p[1][3]);
-      pl[0] = pack_bf16(p[0][0] - bf16_lo(ph[0]), p[0][1] - bf16_hi(ph[0]));
-      pl[1] = pack_bf16(p[0][2] - bf16_lo(ph[1]), p[0][3] - bf16_hi(ph[1]));
-      pl[2] = pack_bf16(p[1][0] - bf16_lo(ph[2]), p[1][1] - bf16_hi(ph[2]));
-      pl[3] = pack_bf16(p[1][2] - bf16_lo(ph[3]), p[1][3] - bf16_hi(ph[3]));
-#pragma unroll
-      for (int dt = 0; dt < 16; dt += 2) {
+      for (int ks = 0; ks < 8; ++ks) {
         const int r = c0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = dt + (lane >> 4);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(smem_u32(tV) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), v0, v1, v2, v3);
-        mma_bf16(acc[dt], ph, v0, v1);
-        mma_bf16(acc[dt], pl, v0, v1);
-        mma_bf16(acc[dt + 1], ph, v2, v3);
-        mma_bf16(acc[dt + 1], pl, v2, v3);
+        const int ch = ks * 2 + (lane >> 4);
+        uint32_t ka[4];
+        ldsm_x4(smem_u32(tK) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+        for (int ht = 0; ht < NH; ++ht) mma_bf16(st[ht][ks & 1], ka, qb[ht][ks][0], qb[ht][ks][1]);
+      }
+      // this lane: tokens c0 + lane/4 (e = 0, 1) and + 8 (e = 2, 3); heads 2(lane%4) + (e & 1)
+      const int ta = c0 + g4, tb = ta + 8;
+      const int sla = ta / blk, slb = tb / blk;
+      const bool va = ta < rows && (ta - sla * blk) < fs.nvalid[min(sla, nsl - 1)];
+      const bool vb = tb < rows && (tb - slb * blk) < fs.nvalid[min(slb, nsl - 1)];
+#pragma unroll
+      for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float sv = (st[ht][0][e] + st[ht][1][e]) * a.scale_log2;
+          x[ht][e] = ((e < 2) ? va : vb) ? sv : neg_inf();
+        }
+    }
+    // --- CTA-wide head maxima of this round
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht) {
+      float m0 = fmaxf(x[ht][0], x[ht][2]), m1 = fmaxf(x[ht][1], x[ht][3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      }
+      if (g4 == 0) {
+        fs.wmaxh[warp][8 * ht + 2 * t4] = m0;
+        fs.wmaxh[warp][8 * ht + 2 * t4 + 1] = m1;
       }
     }
-    __syncthreads();   // tiles are reused by the next round
+    __syncthreads();
+    float mnew[NH][2], corr[NH][2];
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 8 * ht + 2 * t4 + hh;
+        float m = fs.mrun[h];
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][h]);
+        const float mo = fs.mrun[h];
+        mnew[ht][hh] = m;
+        corr[ht][hh] = (mo == neg_inf()) ? 0.f : exp2f(mo - m);
+      }
+    // --- probabilities, their head sums, and P^T fragments for every warp
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p[e] = (x[ht][e] == neg_inf()) ? 0.f : exp2f(x[ht][e] - mnew[ht][e & 1]);
+      float s0 = p[0] + p[2], s1 = p[1] + p[3];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      }
+      if (g4 == 0) {
+        fs.wsumh[warp][8 * ht + 2 * t4] = s0;
+        fs.wsumh[warp][8 * ht + 2 * t4 + 1] = s1;
+      }
+      if (has_step) {
+        const uint32_t h0 = pack_bf16(p[0], p[1]), h1 = pack_bf16(p[2], p[3]);
+        const uint32_t l0 = pack_bf16(p[0] - bf16_lo(h0), p[1] - bf16_hi(h0));
+        const uint32_t l1 = pack_bf16(p[2] - bf16_lo(h1), p[3] - bf16_hi(h1));
+        uint32_t* pf = &fs.pfrag[warp][ht][0][0];
+        pf[0 * 32 + lane] = movmatrix_trans(h0);
+        pf[1 * 32 + lane] = movmatrix_trans(h1);
+        pf[2 * 32 + lane] = movmatrix_trans(l0);
+        pf[3 * 32 + lane] = movmatrix_trans(l1);
+      }
+    }
+    __syncthreads();
+    // --- running max / sum (threads < 16 keep the CTA copy) and rescale
+    if (tid < 16) {
+      float m = fs.mrun[tid];
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][tid]);
+      const float c = (fs.mrun[tid] == neg_inf()) ? 0.f : exp2f(fs.mrun[tid] - m);
+      float l = fs.lrun[tid] * c;
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) l += fs.wsumh[w][tid];
+      fs.lrun[tid] = l;
+      fs.mrun[tid] = m;
+    }
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht) {
+      acc[ht][0] *= corr[ht][0];
+      acc[ht][1] *= corr[ht][1];
+      acc[ht][2] *= corr[ht][0];
+      acc[ht][3] *= corr[ht][1];
+    }
+    // --- O^T (dims 16*warp .. +15) += V^T P^T over every 16-token step of the round
+    for (int cs = 0; cs < nsteps; ++cs) {
+      const int r = cs * 16 + (lane & 7) + (lane >> 4) * 8;
+      const int ch = 2 * warp + ((lane >> 3) & 1);
+      uint32_t va4[4];
+      ldsm_x4_t(smem_u32(tV) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), va4[0], va4[1], va4[2], va4[3]);
+#pragma unroll
+      for (int ht = 0; ht < NH; ++ht) {
+        const uint32_t* pf = &fs.pfrag[cs][ht][0][0];
+        mma_bf16(acc[ht], va4, pf[0 * 32 + lane], pf[1 * 32 + lane]);
+        mma_bf16(acc[ht], va4, pf[2 * 32 + lane], pf[3 * 32 + lane]);
+      }
+    }
+    phase ^= 1u;
+    __syncthreads();   // tiles and fragments are reused by the next round
   }
 
   // ---------------------------------------------------------------- E ------
-  l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
-  l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
-  l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
-  l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
-  {
-    const int g0 = lane >> 2, g1 = g0 + 8;
+  const int gown = (G + ns - 1) / ns;
+  cluster_wait_acquire();
 #pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      const int d = dt * 8 + 2 * (lane & 3);
-      if (g0 < G) {
-        float* pp = part + (size_t)(warp * G + g0) * PART_STRIDE + d;
-        pp[0] = acc[dt][0];
-        pp[1] = acc[dt][1];
-      }
-      if (g1 < G) {
-        float* pp = part + (size_t)(warp * G + g1) * PART_STRIDE + d;
-        pp[0] = acc[dt][2];
-        pp[1] = acc[dt][3];
-      }
-    }
-    if ((lane & 3) == 0) {
-      if (g0 < G) {
-        part[(size_t)(warp * G + g0) * PART_STRIDE + HD] = m_run[0];
-        part[(size_t)(warp * G + g0) * PART_STRIDE + HD + 1] = l_run[0];
-      }
-      if (g1 < G) {
-        part[(size_t)(warp * G + g1) * PART_STRIDE + HD] = m_run[1];
-        part[(size_t)(warp * G + g1) * PART_STRIDE + HD + 1] = l_run[1];
+  for (int ht = 0; ht < NH; ++ht) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int g = 8 * ht + 2 * t4 + hh;
+      if (g < G) {
+        const int owner = g % ns, gl = g / ns;
+        const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
+        st_cluster_f32(base + 4u * (16 * warp + g4), acc[ht][hh]);
+        st_cluster_f32(base + 4u * (16 * warp + g4 + 8), acc[ht][2 + hh]);
       }
     }
   }
-  __syncthreads();
-  const int gown = (G + ns - 1) / ns;
-  for (int i = tid; i < G * HD; i += NT) {
-    const int g = i / HD, d = i % HD;
-    float M = neg_inf();
-    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, part[(size_t)(w * G + g) * PART_STRIDE + HD]);
-    float A = 0.f, L = 0.f;
-    for (int w = 0; w < NWARP; ++w) {
-      const float* pp = part + (size_t)(w * G + g) * PART_STRIDE;
-      const float f = (pp[HD] == neg_inf()) ? 0.f : exp2f(pp[HD] - M);
-      A += f * pp[d];
-      L += f * pp[HD + 1];
-    }
-    const int owner = g % ns, gl = g / ns;
-    const uint32_t base = smem_u32(recv + ((size_t)rank * gown + gl) * PART_STRIDE);
-    st_cluster_f32(mapa(base + 4u * d, owner), A);
-    if (d == 0) {
-      st_cluster_f32(mapa(base + 4u * HD, owner), M);
-      st_cluster_f32(mapa(base + 4u * (HD + 1), owner), L);
-    }
+  if (tid < G) {
+    const int owner = tid % ns, gl = tid / ns;
+    const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
+    st_cluster_v2f32(base + 4u * HD, fs.mrun[tid], fs.lrun[tid]);
   }
   cluster_sync();
   for (int gl = 0; gl < gown; ++gl) {
     const int g = gl * ns + (int)rank;
     if (g >= G) break;
-    const int d = tid;
-    float M = neg_inf();
-    for (int r = 0; r < ns; ++r) M = fmaxf(M, recv[((size_t)r * gown + gl) * PART_STRIDE + HD]);
-    float A = 0.f, L = 0.f;
-    for (int r = 0; r < ns; ++r) {
-      const float* pp = recv + ((size_t)r * gown + gl) * PART_STRIDE;
-      const float f = (pp[HD] == neg_inf()) ? 0.f : exp2f(pp[HD] - M);
-      A += f * pp[d];
-      L += f * pp[HD + 1];
+    const float* rp = recv + (size_t)gl * ns * PART_STRIDE;
+    if (tid < HD) {
+      float M = neg_inf();
+      for (int r = 0; r < ns; ++r) M = fmaxf(M, rp[(size_t)r * PART_STRIDE + HD]);
+      float A = 0.f, L = 0.f;
+      for (int r = 0; r < ns; ++r) {
+        const float* pp = rp + (size_t)r * PART_STRIDE;
+        const float f = (pp[HD] == neg_inf()) ? 0.f : exp2f(pp[HD] - M);
+        A = fmaf(f, pp[tid], A);
+        L = fmaf(f, pp[HD + 1], L);
+      }
+      a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = A / L;
     }
-    a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + d] = A / L;
   }
-  if (rank == 0 && a.sel_blocks) {
-    for (int j = tid; j < a.k2; j += NT) {
-      if (j < a.k2e) {
-        const int mine = sel[j];
-        int pos = 0;
-        for (int o = 0; o < a.k2e; ++o) pos += sel[o] < mine;
-        a.sel_blocks[(size_t)pair * a.k2 + pos] = mine;
-      } else {
-        a.sel_blocks[(size_t)pair * a.k2 + j] = -1;
+  if (rank == 0) {
+    if (a.sel_blocks) {
+      for (int j = tid; j < a.k2; j += NT) a.sel_blocks[(size_t)pair * a.k2 + j] = j < k2e ? sel[j] : -1;
+    }
+    if (app) {
+      // persist the appended token: cache row, candidate index (MT) and its KT column
+      if (tid < 32) {
+        bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
+                    ((size_t)pair * a.cap + a.row) * HD + (tid & 15) * 8;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 16 ? fs.knew : fs.vnew) +
+                                                                          (tid & 15) * 8);
+      }
+      if (MT && tid == 32) a.idx_w[(size_t)pair * a.idx_cap + n_old] = (int32_t)a.row;
+      {
+        const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
+        bf16* p = reinterpret_cast<bf16*>(a.kt) + ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
+        const bf16 kv = fs.knew[c];
+        if ((n_old % a.blk) == 0) {
+          *p = kv;
+        } else {
+          const float x = bf2f(kv), o = bf2f(*p);
+          if (m == 1 ? (x < o) : (x > o)) *p = kv;
+        }
       }
     }
   }
 }
 
+int g_num_sms = 0;
+
 }  // namespace
 
 bool hsa_plan(HsaArgs& a) {
-  a.nblk = (a.n + a.blk - 1) / a.blk;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  });
+  const int n_tot = a.n + (a.k_new ? 1 : 0);
+  a.nblk = (n_tot + a.blk - 1) / a.blk;
   a.k2e = std::min(a.k2, a.nblk);
-  int ns = std::min(8, a.k2e);
-  if (ns < 1) ns = 1;
-  a.ns = ns;
-  a.chunk = (a.k2e + ns - 1) / ns;
+  const int pairs = a.B * a.Hkv;
+  // one wave at two CTAs per SM, at most 8 CTAs per cluster, no more CTAs than blocks
+  int ns = std::max(1, (2 * g_num_sms) / std::max(1, pairs));
+  ns = std::min(ns, 8);
+  ns = std::min(ns, a.k2e);
+  a.ns = std::max(ns, 1);
+  a.chunk = (a.k2e + a.ns - 1) / a.ns;
   a.slots_round = std::max(1, std::min(a.chunk, MAX_ROUND_ROWS / a.blk));
-  const int gown = (a.G + ns - 1) / ns;
+  const int nblk8 = (a.nblk + 7) & ~7;
+  int bc = nblk8;
+  if ((uint32_t)a.k1 * bc * 2u > KT_TILE_BUDGET) bc = std::max(8, (int)(KT_TILE_BUDGET / (2u * a.k1)) & ~7);
+  a.kt_chunk = bc;
+  const int gown = (a.G + a.ns - 1) / a.ns;
   auto al = [](uint32_t x, uint32_t q) { return (x + q - 1) / q * q; };
-  uint32_t off = FIXED_SMEM;
+  uint32_t off = al(sizeof(FixedSmem), 128);
+  a.off_x = 0;
   a.off_scores = off;
-  off = al(off + 4u * (uint32_t)((a.nblk + 3) & ~3), 16);
+  off = al(off + 4u * (uint32_t)nblk8, 16);
+  a.off_flags = off;
+  off = al(off + (uint32_t)nblk8, 16);
   a.off_sel = off;
-  off = al(off + 4u * (uint32_t)a.k2e, 16);
-  a.off_part = off;
-  off = al(off + 4u * NWARP * a.G * PART_STRIDE, 16);
+  off = al(off + 4u * (uint32_t)std::max(a.k2e, 1), 16);
   a.off_recv = off;
-  off = al(off + 4u * ns * gown * PART_STRIDE, 1024);
-  a.off_tiles = off;
+  off = al(off + 4u * gown * a.ns * PART_STRIDE, 1024);
+  a.off_tiles = off;                       // K/V tiles; the KT gather tile shares this region
   const uint32_t rows16 = al((uint32_t)(a.slots_round * a.blk), 16);
   a.tile_half_bytes = rows16 * 128u;
-  off += 4u * a.tile_half_bytes;
+  off += std::max(4u * a.tile_half_bytes, al(2u * a.k1 * bc, 16));
   a.smem_bytes = off + 1024u;   // room to align the base to 1024 bytes
   return a.smem_bytes <= 227u * 1024u;
 }
 
 cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV, bool mt,
                        cudaStream_t st) {
-  static bool attr_done[2] = {false, false};
-  auto kern = mt ? hsa_decode_kernel<true> : hsa_decode_kernel<false>;
-  if (!attr_done[mt ? 1 : 0]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done[mt ? 1 : 0] = true;
-  }
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    const void* ks[4] = {(const void*)hsa_decode_kernel<false, 1>, (const void*)hsa_decode_kernel<false, 2>,
+                         (const void*)hsa_decode_kernel<true, 1>, (const void*)hsa_decode_kernel<true, 2>};
+    for (const void* k : ks) {
+      attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (attr_err != cudaSuccess) break;
+    }
+  });
+  if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ns, a.Hkv, a.B);
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = a.smem_bytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.ns;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
+  auto kern = mt ? (a.G > 8 ? hsa_decode_kernel<true, 2> : hsa_decode_kernel<true, 1>)
+                 : (a.G > 8 ? hsa_decode_kernel<false, 2> : hsa_decode_kernel<false, 1>);
   return cudaLaunchKernelEx(&cfg, kern, *tmK, *tmV, a);
 }
 

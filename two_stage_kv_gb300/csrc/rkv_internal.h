@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,23 +15,28 @@ constexpr int HD_HOST = 128;   // head dimension of the implemented path
 // ------------------------------------------------------------ HSA decode ---
 struct HsaArgs {
   const void* q;        // [B, Hq, D] bf16
-  const void* k;        // [B, Hkv, cap, D] bf16
-  const void* v;
-  const void* kt;       // [B, Hkv, 2, D, nblk_cap] bf16
+  void* k;              // [B, Hkv, cap, D] bf16 (written only by a fused append)
+  void* v;
+  void* kt;             // [B, Hkv, 2, D, nblk_cap] bf16 (written only by a fused append)
   const int32_t* idx;   // MT candidate rows [B, Hkv, idx_cap] or nullptr
+  int32_t* idx_w;       // same rows, written by a fused MT append
+  const __nv_bfloat16* k_new;   // [B, Hkv, D] token appended by this step, or nullptr
+  const __nv_bfloat16* v_new;
+  int64_t row;          // cache row of the appended token (n without idx)
   float* out;           // [B, Hq, D] fp32
   int32_t* sel_blocks;  // [B, Hkv, k2] or nullptr
   int32_t* sel_channels;  // [B, Hkv, k1] or nullptr
   int64_t cap, nblk_cap, idx_cap;
-  int32_t n, B, Hq, Hkv, G, blk, k1, k2;
-  int32_t nblk;         // ceil(n / blk)
+  int32_t n, B, Hq, Hkv, G, blk, k1, k2;   // n = candidates before the append
+  int32_t nblk;         // blocks over the attended candidates
   int32_t k2e;          // min(k2, nblk)
   int32_t ns;           // CTAs per cluster (one cluster per (b, kv head))
   int32_t chunk;        // selected blocks per CTA: ceil(k2e / ns)
   int32_t slots_round;  // blocks staged in shared memory per round
+  int32_t kt_chunk;     // blocks per shared-memory KT gather (multiple of 8)
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared-memory layout (bytes)
-  uint32_t off_scores, off_sel, off_part, off_recv, off_tiles, tile_half_bytes, smem_bytes;
+  uint32_t off_x, off_scores, off_flags, off_sel, off_recv, off_tiles, tile_half_bytes, smem_bytes;
 };
 
 // Computes ns/chunk/slots_round and the shared-memory layout.  Returns false if

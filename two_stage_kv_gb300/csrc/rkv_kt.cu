@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(KT_NT) kt_build_kernel(const bf16* k, int64_t 
                                                          bf16* kt, int64_t nblk_cap) {
   __shared__ bf16 tmax[HD][KT_BLOCKS + 2];
   __shared__ bf16 tmin[HD][KT_BLOCKS + 2];
+  pdl_wait();
+  pdl_launch_dependents();
   const int pair = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nblk = (n + blk - 1) / blk;
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(KT_NT) kt_build_kernel(const bf16* k, int64_t 
 __global__ void __launch_bounds__(HD) append_kernel(const bf16* k_new, const bf16* v_new, bf16* k, bf16* v,
                                                     int64_t cap, int64_t n, int64_t row, int32_t* idx,
                                                     int64_t idx_cap, bf16* kt, int64_t nblk_cap, int blk) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int pair = blockIdx.x, c = threadIdx.x;
   const bf16 kv = k_new[(size_t)pair * HD + c];
   const bf16 vv = v_new[(size_t)pair * HD + c];
@@ -95,19 +99,18 @@ cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t
                             int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st) {
   const int64_t nblk = (n + blk - 1) / blk;
   if (nblk == 0 || pairs == 0) return cudaSuccess;
-  kt_build_kernel<<<dim3((unsigned)((nblk + KT_BLOCKS - 1) / KT_BLOCKS), pairs), KT_NT, 0, st>>>(
-      reinterpret_cast<const bf16*>(k), cap, n, idx, idx_cap, blk, reinterpret_cast<bf16*>(kt), nblk_cap);
-  return cudaGetLastError();
+  return launch_pdl(kt_build_kernel, dim3((unsigned)((nblk + KT_BLOCKS - 1) / KT_BLOCKS), pairs), dim3(KT_NT), 0, st,
+                    reinterpret_cast<const bf16*>(k), cap, n, idx, idx_cap, (int)blk, reinterpret_cast<bf16*>(kt),
+                    nblk_cap);
 }
 
 cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
                           int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
                           int32_t pairs, cudaStream_t st) {
   if (pairs == 0) return cudaSuccess;
-  append_kernel<<<pairs, HD, 0, st>>>(reinterpret_cast<const bf16*>(k_new), reinterpret_cast<const bf16*>(v_new),
-                                      reinterpret_cast<bf16*>(k), reinterpret_cast<bf16*>(v), cap, n, row, idx,
-                                      idx_cap, reinterpret_cast<bf16*>(kt), nblk_cap, blk);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel, dim3(pairs), dim3(HD), 0, st, reinterpret_cast<const bf16*>(k_new),
+                    reinterpret_cast<const bf16*>(v_new), reinterpret_cast<bf16*>(k), reinterpret_cast<bf16*>(v), cap, n,
+                    row, idx, idx_cap, reinterpret_cast<bf16*>(kt), nblk_cap, (int)blk);
 }
 
 }  // namespace rkv

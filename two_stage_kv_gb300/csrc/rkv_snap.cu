@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(P_NT) snap_pass_kernel(const __grid_constant__
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
   if (tid == 0) {
     for (int it = 0; it < min(P_NST, ntiles); ++it) {
       const int y = (int)(j0 + (int64_t)it * P_TILE);
@@ -230,6 +232,8 @@ constexpr int POOL_MAX_HALF = 512;
 __global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int RG, int64_t L, int half,
                                                         float* pooled) {
   __shared__ float tile[POOL_TILE + 2 * POOL_MAX_HALF];
+  pdl_wait();
+  pdl_launch_dependents();
   const int pair = blockIdx.y;
   const int64_t j0 = (int64_t)blockIdx.x * POOL_TILE;
   const int span = POOL_TILE + 2 * half;
@@ -286,6 +290,8 @@ __global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled
   __shared__ int wsum[72];
   __shared__ uint32_t sh_digit;
   __shared__ int64_t sh_k;
+  pdl_wait();
+  pdl_launch_dependents();
   const int pair = blockIdx.x, tid = threadIdx.x;
   const float* p = pooled + (size_t)pair * L;
   int32_t* out = keep + (size_t)pair * keep_ld;
@@ -361,6 +367,8 @@ __global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled
 __global__ void __launch_bounds__(256) snap_compact_kernel(const bf16* k, const bf16* v, int64_t cap,
                                                            const int32_t* keep, int64_t keep_ld, int64_t B1,
                                                            bf16* ko, bf16* vo, int64_t out_cap) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int pair = blockIdx.y;
   for (int i = threadIdx.x; i < 32 * 16; i += blockDim.x) {
     const int64_t row = (int64_t)blockIdx.x * 32 + i / 16;
@@ -422,30 +430,30 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, cudaStream_t 
     w += al256((size_t)pairs * p.RG * L * sizeof(float));
     float* pooled = a.pooled_out ? a.pooled_out : reinterpret_cast<float*>(w);
 
-    snap_pass_kernel<1><<<dim3(p.nchunk1, p.RG, pairs), P_NT, P_SMEM, st>>>(*tmK, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(snap_pass_kernel<1>, dim3(p.nchunk1, p.RG, pairs), dim3(P_NT), P_SMEM, st, *tmK, p);
     if (e != cudaSuccess) return e;
     const int nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
-    snap_pass_kernel<2><<<dim3(nchunk2, p.RG, pairs), P_NT, P_SMEM, st>>>(*tmK, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    snap_pool_kernel<<<dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), 256, 0, st>>>(
-        p.scores, p.RG, L, a.pool / 2, pooled);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(snap_pass_kernel<2>, dim3(nchunk2, p.RG, pairs), dim3(P_NT), P_SMEM, st, *tmK, p);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
+                   (const float*)p.scores, (int)p.RG, (int64_t)L, (int)(a.pool / 2), pooled);
+    if (e != cudaSuccess) return e;
     const int n_sink = (int)std::max<int64_t>(0, std::min<int64_t>(a.n_sink, L));
     const int64_t ntop = std::max<int64_t>(0, a.B1 - W - n_sink);
-    snap_select_kernel<<<pairs, SEL_NT, 0, st>>>(pooled, L, a.S, W, n_sink, ntop, a.B1, a.keep, a.keep_ld);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)pooled, (int64_t)L,
+                   (int64_t)a.S, (int)W, (int)n_sink, (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
+    if (e != cudaSuccess) return e;
   } else {
     // every token kept: keep = 0..S-1 (B1 == S enforced by the caller)
-    snap_select_kernel<<<pairs, SEL_NT, 0, st>>>(nullptr, 0, a.S, (int)a.S, 0, 0, a.B1, a.keep, a.keep_ld);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)nullptr, (int64_t)0,
+                               (int64_t)a.S, (int)a.S, 0, (int64_t)0, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
     if (e != cudaSuccess) return e;
   }
   if (a.k_out) {
-    snap_compact_kernel<<<dim3((unsigned)((a.B1 + 31) / 32), pairs), 256, 0, st>>>(
-        reinterpret_cast<const bf16*>(a.k), reinterpret_cast<const bf16*>(a.v), a.cap, a.keep, a.keep_ld, a.B1,
-        reinterpret_cast<bf16*>(a.k_out), reinterpret_cast<bf16*>(a.v_out), a.out_cap);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(snap_compact_kernel, dim3((unsigned)((a.B1 + 31) / 32), pairs), dim3(256), 0, st,
+                               reinterpret_cast<const bf16*>(a.k), reinterpret_cast<const bf16*>(a.v), (int64_t)a.cap,
+                               (const int32_t*)a.keep, (int64_t)a.keep_ld, (int64_t)a.B1,
+                               reinterpret_cast<bf16*>(a.k_out), reinterpret_cast<bf16*>(a.v_out), (int64_t)a.out_cap);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

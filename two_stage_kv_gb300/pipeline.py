@@ -27,6 +27,12 @@ def bf16_tensor(bits, device) -> torch.Tensor:
     return t.to(device, non_blocking=False)
 
 
+def nblk_capacity(tokens: int, blk: int) -> int:
+    """KT capacity in blocks for `tokens` candidates, rounded up to a multiple of 8
+    (the decode kernel gathers KT rows in 16-byte pieces)."""
+    return -(-(-(-tokens // blk)) // 8) * 8
+
+
 @dataclass
 class Budget:
     r: float
@@ -53,7 +59,7 @@ class Layer:
         self.n_sink = n_sink
         B, Hkv, D = wl.B, wl.Hkv, wl.D
         self.cap = self.bud.B1 + wl.steps
-        self.nblk_cap = -(-self.cap // wl.blk)
+        self.nblk_cap = nblk_capacity(self.cap, wl.blk)
         self.kc = torch.empty(B, Hkv, self.cap, D, dtype=torch.bfloat16, device=device)
         self.vc = torch.empty_like(self.kc)
         self.keep = torch.empty(B, Hkv, self.bud.B1, dtype=torch.int32, device=device)
@@ -81,11 +87,22 @@ class Layer:
                           self.nblk_cap, self.wl.blk, stream)
         self.n += 1
 
-    def decode(self, q: torch.Tensor, stream=None, selections: bool = True):
+    def decode(self, q: torch.Tensor, stream=None, selections: bool = True, out: Optional[torch.Tensor] = None):
         wl = self.wl
         rkv.rkv_hsa_decode(self.dims, q, self.kc, self.vc, self.cap, self.n, self.kt, self.nblk_cap, wl.blk, wl.k1,
-                           self.bud.k2, self.scale, self.out, self.sel_blocks if selections else None,
-                           self.sel_channels if selections else None, stream)
+                           self.bud.k2, self.scale, self.out if out is None else out,
+                           self.sel_blocks if selections else None, self.sel_channels if selections else None,
+                           stream)
+
+    def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None,
+             selections: bool = True, out: Optional[torch.Tensor] = None):
+        """One decode step with the append fused into the HSA launch."""
+        wl = self.wl
+        rkv.rkv_hsa_decode(self.dims, q, self.kc, self.vc, self.cap, self.n, self.kt, self.nblk_cap, wl.blk, wl.k1,
+                           self.bud.k2, self.scale, self.out if out is None else out,
+                           self.sel_blocks if selections else None, self.sel_channels if selections else None,
+                           k_new, v_new, stream)
+        self.n += 1
 
     def reset_decode(self):
         """Forget appended tokens (the next stage1() re-creates the compacted caches)."""
@@ -104,7 +121,7 @@ class MTLayer:
         self.v = torch.empty_like(self.k)
         self.budgets = [budget(wl, wl.turn_context(t)) for t in range(wl.n_turns)]
         self.idx_cap = max(b.B1 for b in self.budgets) + wl.steps
-        self.nblk_cap = -(-self.idx_cap // wl.blk)
+        self.nblk_cap = nblk_capacity(self.idx_cap, wl.blk)
         self.idx = torch.zeros(B, Hkv, self.idx_cap, dtype=torch.int32, device=device)
         self.kt = torch.empty(B, Hkv, 2, D, self.nblk_cap, dtype=torch.bfloat16, device=device)
         S_max = wl.turn_context(wl.n_turns - 1)
@@ -152,4 +169,14 @@ class MTLayer:
         k2 = self.budgets[self.turn].k2
         rkv.rkv_hsa_decode_mt(self.dims, q, self.k, self.v, self.cap, self.idx, self.idx_cap, self.n, self.kt,
                               self.nblk_cap, wl.blk, wl.k1, k2, self.scale, self.out, self.sel_blocks,
-                              self.sel_channels, stream)
+                              self.sel_channels, stream=stream)
+
+    def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """One MT decode step with the append (full cache row + candidate index) fused in."""
+        wl = self.wl
+        k2 = self.budgets[self.turn].k2
+        rkv.rkv_hsa_decode_mt(self.dims, q, self.k, self.v, self.cap, self.idx, self.idx_cap, self.n, self.kt,
+                              self.nblk_cap, wl.blk, wl.k1, k2, self.scale, self.out, self.sel_blocks,
+                              self.sel_channels, k_new, v_new, self.rows, stream)
+        self.n += 1
+        self.rows += 1

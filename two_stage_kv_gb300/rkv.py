@@ -50,9 +50,9 @@ _SIGS = {
     "rkv_build_kt": (_i32, [Dims, _vp, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _vp]),
     "rkv_append_kv": (_i32, [Dims, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "rkv_hsa_decode": (_i32, [Dims, _vp, _vp, _vp, _i64, _i64, _vp, _i64, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
-                              _vp]),
+                              _vp, _vp, _vp]),
     "rkv_hsa_decode_mt": (_i32, [Dims, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _i64, _i32, _i32, _i32, _f32,
-                                 _vp, _vp, _vp, _vp]),
+                                 _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "rkv_read_device_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -128,16 +128,17 @@ def rkv_append_kv(dims, k_new, v_new, k, v, cap, n, row, idx, idx_cap, kt, nblk_
 
 
 def rkv_hsa_decode(dims, q, k, v, cap, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks=None,
-                   sel_channels=None, stream=None):
+                   sel_channels=None, k_new=None, v_new=None, stream=None):
     _check(lib().rkv_hsa_decode(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, n, _ptr(kt), nblk_cap, blk, k1, k2,
-                                scale, _ptr(out), _ptr(sel_blocks), _ptr(sel_channels), _stream(stream)))
+                                scale, _ptr(out), _ptr(sel_blocks), _ptr(sel_channels), _ptr(k_new), _ptr(v_new),
+                                _stream(stream)))
 
 
 def rkv_hsa_decode_mt(dims, q, k, v, cap, idx, idx_cap, n, kt, nblk_cap, blk, k1, k2, scale, out,
-                      sel_blocks=None, sel_channels=None, stream=None):
+                      sel_blocks=None, sel_channels=None, k_new=None, v_new=None, row=0, stream=None):
     _check(lib().rkv_hsa_decode_mt(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, _ptr(idx), idx_cap, n, _ptr(kt),
                                    nblk_cap, blk, k1, k2, scale, _ptr(out), _ptr(sel_blocks), _ptr(sel_channels),
-                                   _stream(stream)))
+                                   _ptr(k_new), _ptr(v_new), row, _stream(stream)))
 
 
 def rkv_read_device_flags() -> int:
