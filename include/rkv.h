@@ -114,6 +114,28 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
                           float* pooled_out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Stage-1 eviction for callers that cannot allocate device memory.  The
+ * paper has no counterpart to this entry point; it exists for engines whose
+ * memory pool owns all device memory, plugin hooks that must not call
+ * cudaMalloc, and code running while a stream is captured into a CUDA graph.
+ * Same operation, arguments and results as rkv_snap_evict, minus ws/ws_bytes:
+ * the scratch is a fixed 32 MiB array of device memory inside this library,
+ * held on every GPU that loads the library's device code until the process
+ * exits.  Shapes whose rkv_snap_evict_workspace() exceeds 32 MiB return
+ * RKV_ERR_WORKSPACE with a message giving both sizes.  It calls no cudaMalloc
+ * or cudaFree.  The first call on a device, made with that device current,
+ * looks up the array's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  Every call uses the same array, so calls
+ * that can overlap on the GPU (different streams, or devices sharing the
+ * address) race and must be serialised by the caller.  No part of the scratch
+ * needs to start at zero: each call writes all it reads.
+ */
+rkv_status rkv_snap_evict_noalloc(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v,
+                                  int64_t cap, int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1,
+                                  float scale, int32_t* keep_idx, int64_t keep_ld, void* k_out, void* v_out,
+                                  int64_t out_cap, float* pooled_out, void* stream);
+
+/*
  * KT cache build.  [RocketKV digest, 方法细节: HSA step 1 -- tokens grouped
  * into pages along the sequence, elementwise Kmax and Kmin per page stored
  * aligned along the head dimension]

@@ -143,6 +143,8 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
 
 }  // namespace
 
+void rkv::set_last_error(const char* msg) { g_last_error = msg; }
+
 extern "C" {
 
 const char* rkv_last_error(void) { return g_last_error.c_str(); }

@@ -76,4 +76,7 @@ cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v
 unsigned int hsa_take_device_error();
 unsigned int snap_take_device_error();
 
+// Records the message returned by rkv_last_error() on this host thread.
+void set_last_error(const char* msg);
+
 }  // namespace rkv
