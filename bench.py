@@ -136,6 +136,27 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank helpers (one independent replica per rank, no data-path collective)
+# ---------------------------------------------------------------------------
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank timing over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Units processed by all ranks divided by the slowest rank's time (weak scaling)."""
+    return world * units_per_rank / seconds_max
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -227,14 +248,10 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = tA.elapsed_time(tB)
-    if world > 1:
-        x = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(x.item())
+    ms_total = max_over_ranks(tA.elapsed_time(tB), dev)
     ms_pass = ms_total / args.steps
     tokens_per_pass = wl.B * wl.steps
-    value = world * tokens_per_pass * args.steps / (ms_total / 1e3)
+    value = whole_job_rate(tokens_per_pass * args.steps, world, ms_total / 1e3)
 
     # per-kernel times from the last replay of the timed region
     stage1_ms = ev["s0"].elapsed_time(ev["s1"])
@@ -275,12 +292,9 @@ def run_ours(args, rank, world, local):
                 host_out.copy_(out_all, non_blocking=True)
             e1.record()
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            x = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(x.item())
-        e2e = {"value": round(world * tokens_per_pass * e2e_steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": round(whole_job_rate(tokens_per_pass * e2e_steps, world, e2e_ms / 1e3), 1),
+               "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
                "ms_per_step": round(e2e_ms / e2e_steps, 4)}
 

@@ -3,7 +3,8 @@
 - Index sets (stage-1 keep, channel set i1, block set i2) must be identical,
   except items whose oracle score lies within REL_TIE (relative) of the oracle's
   k-th score: those are exempt from the symmetric difference.  Channel sums are
-  formed in fp64 on both sides, so i1 is compared with no exemption.
+  exact on both sides (fp64 in the oracle; fp32 with an error-free check, else
+  fp64, in the kernel), so i1 is compared with no exemption.
 - Stage-1 scores are sums of softmax probabilities that the kernel forms in
   fp32.  A probability below 2^-126 is subnormal there, so a score below
   SCORE_FLOOR = 1e-30 (128..256 such terms, each off by up to 2^-149, stay
