@@ -77,6 +77,21 @@ rkv_status make_kv_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t 
   return RKV_OK;
 }
 
+// 2-D map over window queries [rows, 128] bf16, box 64 channels x box_rows rows (128-byte swizzle).
+rkv_status make_q_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)rkv::HD_HOST, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)rkv::HD_HOST * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed with %d", (int)r);
+  return RKV_OK;
+}
+
 rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_t cap, int32_t* idx,
                       int64_t idx_cap, int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
                       float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
@@ -224,12 +239,19 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
   a.scale_log2 = scale * 1.4426950408889634f;
   a.keep = keep_idx; a.keep_ld = keep_ld; a.k_out = k_out; a.v_out = v_out; a.pooled_out = pooled_out;
   a.ws = ws; a.ws_bytes = ws_bytes;
-  CUtensorMap tmK;
+  CUtensorMap tmK, tmQ1, tmQ2;
   std::memset(&tmK, 0, sizeof(tmK));
+  std::memset(&tmQ1, 0, sizeof(tmQ1));
+  std::memset(&tmQ2, 0, sizeof(tmQ2));
   if (!keep_all) {
-    if ((s = make_kv_map(&tmK, k, (int64_t)d.batch * d.n_kv_heads, cap, S, 64, "k")) != RKV_OK) return s;
+    const int64_t qrows = (int64_t)d.batch * d.n_q_heads * W;
+    if ((s = make_kv_map(&tmK, k, (int64_t)d.batch * d.n_kv_heads, cap, S, 128, "k")) != RKV_OK) return s;
+    if ((s = make_q_map(&tmQ1, q_obs, qrows, 128)) != RKV_OK) return s;
+    if ((s = make_q_map(&tmQ2, q_obs, qrows, rkv::snap_pass2_rows(d.n_q_heads / d.n_kv_heads, (int32_t)w))) !=
+        RKV_OK)
+      return s;
   }
-  cudaError_t e = rkv::snap_launch(a, &tmK, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = rkv::snap_launch(a, &tmK, &tmQ1, &tmQ2, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "snap_evict launch");
   return RKV_OK;
 }

@@ -63,7 +63,10 @@ struct SnapArgs {
   size_t ws_bytes;
 };
 size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t W);
-cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, cudaStream_t st);
+// Query rows per pass-2 CTA (the MMA N of the key-major pass) for a group of G*W rows.
+int snap_pass2_rows(int32_t G, int32_t W);
+cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmQ1, const CUtensorMap* tmQ2,
+                        cudaStream_t st);
 
 // ------------------------------------------------------------ KT / append ---
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,

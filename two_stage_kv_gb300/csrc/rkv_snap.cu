@@ -24,6 +24,7 @@
 #include "rkv_internal.h"
 
 #include <algorithm>
+#include <mutex>
 
 namespace rkv {
 
@@ -31,197 +32,235 @@ static __device__ unsigned int g_snap_err = 0;
 
 namespace {
 
-constexpr int P_NT = 256;          // 8 warps x 16 query rows = 128 rows per CTA
-constexpr int P_ROWS = 128;
-constexpr int P_TILE = 64;         // keys per TMA tile
-constexpr int P_NST = 4;           // pipeline depth
-constexpr int P_CHUNK = 2048;      // keys per CTA
-constexpr uint32_t P_HALF = P_TILE * 128;            // one 64-dim half of a tile
-constexpr uint32_t P_STAGE = 2 * P_HALF;             // 16 KB
-constexpr uint32_t P_SMEM = P_NST * P_STAGE + 2 * 8 * P_TILE * 4 + 64 + 1024;
+// Score passes on the 5th-generation tensor core.  One CTA = one (pair, row
+// group, key chunk).  Warp 0 streams K tiles (128 keys x 128 dims, two
+// 64-dim TMA boxes with 128-byte swizzle) through a 3-stage ring; warp 1
+// issues tcgen05.mma into one of two TMEM accumulators; warps 2-5 (one per
+// TMEM lane quadrant) drain the accumulators.
+//   pass 1: D[128 query rows x 128 keys] = Q K^T; each epilogue thread owns a
+//           query row and keeps its online softmax (max, sum) over the keys.
+//   pass 2: D[128 keys x Ng query rows] = K Q^T; each epilogue thread owns a
+//           key and sums exp2(logit - lse(row)) over the rows in registers.
+constexpr int T_KEYS = 128;                       // keys per tile
+constexpr int T_NST = 3;                          // smem ring depth
+constexpr int T_NT = 192;                         // 6 warps
+constexpr int P_CHUNK = 2048;                     // keys per CTA
+constexpr int P1_ROWS = 128;                      // query rows per pass-1 CTA (MMA M)
+constexpr int P2_ROWS = 256;                      // query rows per pass-2 CTA (MMA N, max)
+constexpr uint32_t T_KTILE = T_KEYS * 256;        // 32 KB: two 16 KB k-blocks
+constexpr uint32_t T_QMAX = P2_ROWS * 256;        // 64 KB
+constexpr uint32_t T_SMEM = 1024 + T_QMAX + T_NST * T_KTILE + 1024 + 1024;
 
 struct PassArgs {
-  const bf16* q_obs;
   int64_t S, L;                    // L = S - W prefix keys
-  int32_t Hq, Hkv, G, W, R, RG, nchunk1;
+  int32_t Hq, Hkv, G, W, R, RG1, RG2, nchunk1, nq2;
   float scale_log2;
   float2* stats;                   // [pairs][R][nchunk1]
-  float* scores;                   // [pairs][RG][L]
+  float* scores;                   // [pairs][RG2][L]
 };
 
+struct TcSmem {                    // lives after the operand tiles
+  uint64_t full[T_NST], empty[T_NST];
+  uint64_t tfull[2], tempty[2];
+  uint64_t qbar;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  float lse[P2_ROWS];
+};
+
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
+                                        unsigned int* err) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity, err)) return true;
+  *abort_flag = 1;
+  return false;
+}
+
 template <int PASS>
-__global__ void __launch_bounds__(P_NT) snap_pass_kernel(const __grid_constant__ CUtensorMap tmK, const PassArgs a) {
+__global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                            const __grid_constant__ CUtensorMap tmQ,
+                                                            const PassArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
-  uint8_t* tiles = smem;
-  float* colsum = reinterpret_cast<float*>(smem + P_NST * P_STAGE);       // [2][8][64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_NST * P_STAGE + 2 * 8 * P_TILE * 4);
+  uint8_t* sQ = smem;                                   // 2 k-blocks of nq rows x 128 B
+  uint8_t* sK = smem + T_QMAX;                          // T_NST stages of 2 k-blocks x 128 keys x 128 B
+  TcSmem& ts = *reinterpret_cast<TcSmem*>(smem + T_QMAX + T_NST * T_KTILE);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int pair = blockIdx.z, rg = blockIdx.y, chunk = blockIdx.x;
   const int b = pair / a.Hkv, hk = pair % a.Hkv;
+  const int row0 = rg * (PASS == 1 ? P1_ROWS : P2_ROWS);                 // first query row of this CTA
+  const int nq = PASS == 1 ? P1_ROWS : a.nq2;          // MMA M (pass 1) / N (pass 2) query rows
+  const int ncols = PASS == 1 ? T_KEYS : nq;                            // accumulator columns per buffer
+  const uint32_t tcols = PASS == 1 ? 256u : (nq <= 64 ? 128u : (nq <= 128 ? 256u : 512u));
   const int64_t kend = (PASS == 1) ? a.S : a.L;
   const int64_t j0 = (int64_t)chunk * P_CHUNK;
   const int64_t j1 = min(kend, j0 + (int64_t)P_CHUNK);
-  const int ntiles = (int)((j1 - j0 + P_TILE - 1) / P_TILE);
+  const int ntiles = (int)((j1 - j0 + T_KEYS - 1) / T_KEYS);
+  const int qrow_base = (b * a.Hq + hk * a.G) * a.W + row0;             // row in the 2-D q_obs map
+  unsigned int* err = &g_snap_err;
+  volatile int32_t* abort_flag = &ts.abort_flag;
 
   if (tid == 0) {
     prefetch_tmap(&tmK);
-    for (int s = 0; s < P_NST; ++s) mbar_init(&full[s], 1);
+    prefetch_tmap(&tmQ);
+    for (int s = 0; s < T_NST; ++s) {
+      mbar_init(&ts.full[s], 1);
+      mbar_init(&ts.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ts.tfull[i], 1);
+      mbar_init(&ts.tempty[i], 128);
+    }
+    mbar_init(&ts.qbar, 1);
+    ts.abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&ts.tmem_base, tcols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = ts.tmem_base;
   pdl_wait();
   pdl_launch_dependents();
-  if (tid == 0) {
-    for (int it = 0; it < min(P_NST, ntiles); ++it) {
-      const int y = (int)(j0 + (int64_t)it * P_TILE);
-      mbar_arrive_expect_tx(&full[it], P_STAGE);
-      tma_load_3d(tiles + it * P_STAGE, &tmK, 0, y, pair, &full[it]);
-      tma_load_3d(tiles + it * P_STAGE + P_HALF, &tmK, 64, y, pair, &full[it]);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ts.qbar, (uint32_t)nq * 256u);
+      for (int h = 0; h < 2; ++h)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+            "[%4];" ::"r"(smem_u32(sQ + h * nq * 128)),
+            "l"(reinterpret_cast<uint64_t>(&tmQ)), "r"(h * 64), "r"(qrow_base), "r"(smem_u32(&ts.qbar))
+            : "memory");
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % T_NST;
+        if (t >= T_NST && !tc_wait(&ts.empty[s], ((t / T_NST) & 1) ^ 1, abort_flag, err)) break;
+        mbar_arrive_expect_tx(&ts.full[s], T_KTILE);
+        const int y = (int)(j0 + (int64_t)t * T_KEYS);
+        tma_load_3d(sK + s * T_KTILE, &tmK, 0, y, pair, &ts.full[s]);
+        tma_load_3d(sK + s * T_KTILE + T_KTILE / 2, &tmK, 64, y, pair, &ts.full[s]);
+      }
+      // every load issued has landed before the CTA can leave (bounded)
+      for (int t = max(0, ntiles - T_NST); t < ntiles; ++t) mbar_wait(&ts.full[t % T_NST], (t / T_NST) & 1, err);
     }
-  }
-
-  // Query A fragments of this warp's 16 rows (rows >= R are zero).
-  const int rw = rg * P_ROWS + warp * 16;
-  const int ra = rw + (lane >> 2), rb = ra + 8;
-  const bf16* qbase = a.q_obs + ((size_t)b * a.Hq + (size_t)hk * a.G) * a.W * HD;
-  uint32_t qa[8][4];
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA --
+    if (lane == 0 && tc_wait(&ts.qbar, 0, abort_flag, err)) {
+      const uint32_t idesc = PASS == 1 ? idesc_bf16_f32(128, T_KEYS) : idesc_bf16_f32(128, nq);
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % T_NST, buf = t & 1;
+        if (!tc_wait(&ts.full[s], (t / T_NST) & 1, abort_flag, err)) break;
+        if (t >= 2 && !tc_wait(&ts.tempty[buf], ((t >> 1) & 1) ^ 1, abort_flag, err)) break;
+        tc_fence_after();
+        const uint32_t kt = smem_u32(sK + s * T_KTILE), qt = smem_u32(sQ);
+        const uint32_t d = tbase + (uint32_t)(buf * ncols);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const int c = ks * 16 + 2 * (lane & 3);
-    qa[ks][0] = ra < a.R ? *reinterpret_cast<const uint32_t*>(qbase + (size_t)ra * HD + c) : 0u;
-    qa[ks][1] = rb < a.R ? *reinterpret_cast<const uint32_t*>(qbase + (size_t)rb * HD + c) : 0u;
-    qa[ks][2] = ra < a.R ? *reinterpret_cast<const uint32_t*>(qbase + (size_t)ra * HD + c + 8) : 0u;
-    qa[ks][3] = rb < a.R ? *reinterpret_cast<const uint32_t*>(qbase + (size_t)rb * HD + c + 8) : 0u;
-  }
-  const bool va = ra < a.R, vb = rb < a.R;
-  // last key each window row may attend (causal): S - W + (row mod W)
-  const int64_t lima = a.S - a.W + (ra % a.W), limb = a.S - a.W + (rb % a.W);
-
-  float m_a = neg_inf(), m_b = neg_inf(), l_a = 0.f, l_b = 0.f;   // pass 1
-  float lse_a = __int_as_float(0x7f800000), lse_b = lse_a;         // pass 2 (log2 units)
-  if (PASS == 2) {
-    auto lse_of = [&](int r) {
-      const float2* st = a.stats + ((size_t)pair * a.R + r) * a.nchunk1;
-      float M = neg_inf();
-      for (int c = 0; c < a.nchunk1; ++c) M = fmaxf(M, st[c].x);
-      float Ls = 0.f;
-      for (int c = 0; c < a.nchunk1; ++c)
-        if (st[c].x != neg_inf()) Ls += st[c].y * exp2f(st[c].x - M);
-      return M + log2f(Ls);
-    };
-    if (va) lse_a = lse_of(ra);
-    if (vb) lse_b = lse_of(rb);
-  }
-
-  unsigned int* err = &g_snap_err;
-  for (int it = 0; it < ntiles; ++it) {
-    const int st = it % P_NST;
-    if (!mbar_wait(&full[st], (uint32_t)((it / P_NST) & 1), err)) mbar_wait(&full[st], (uint32_t)((it / P_NST) & 1), err);
-    const uint32_t tb = smem_u32(tiles + st * P_STAGE);
-    const int64_t jt = j0 + (int64_t)it * P_TILE;
-
-    float sc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ks += 2) {
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int r = nt * 8 + (lane & 7);
-        const int ch = ks * 2 + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(tb + (uint32_t)(ch >> 3) * P_HALF + swz128(r, ch & 7), b0, b1, b2, b3);
-        mma_bf16(sc[nt], qa[ks], b0, b1);
-        mma_bf16(sc[nt], qa[ks + 1], b2, b3);
+        for (int k = 0; k < 8; ++k) {
+          const int kb = k >> 2, kk = k & 3;
+          const uint64_t kdesc = sdesc_k_sw128(kt + kb * (T_KTILE / 2) + kk * 32);
+          const uint64_t qdesc = sdesc_k_sw128(qt + kb * nq * 128 + kk * 32);
+          if (PASS == 1)
+            tc_mma_bf16(d, qdesc, kdesc, idesc, k > 0);
+          else
+            tc_mma_bf16(d, kdesc, qdesc, idesc, k > 0);
+        }
+        tc_commit(&ts.empty[s]);
+        tc_commit(&ts.tfull[buf]);
       }
     }
-
+  } else {
+    // ----------------------------------------------------------- epilogue --
+    const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
+    const int r_loc = 32 * quad + lane;              // TMEM lane of this thread
+    const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16);
     if (PASS == 1) {
-      float xa[16], xb[16];
-      float ma = neg_inf(), mb = neg_inf();
+      const int r = row0 + r_loc;                    // query row in the group
+      const bool rvalid = r < a.R;
+      const int64_t lim = a.S - a.W + (rvalid ? (r % a.W) : 0);    // last key this row attends
+      float m = neg_inf(), l = 0.f;
+      for (int t = 0; t < ntiles; ++t) {
+        const int buf = t & 1;
+        if (!tc_wait(&ts.tfull[buf], (t >> 1) & 1, abort_flag, err)) break;
+        tc_fence_after();
+        float v[4][32];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + buf * ncols + 32 * c, v[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&ts.tempty[buf]);
+        const int64_t jt = j0 + (int64_t)t * T_KEYS;
+        const bool full_tile = jt + T_KEYS <= a.S - a.W;       // every row attends every key
+        float tm = neg_inf();
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int64_t j = jt + nt * 8 + 2 * (lane & 3) + e;
-          const float x0 = (va && j < a.S && j <= lima) ? sc[nt][e] * a.scale_log2 : neg_inf();
-          const float x1 = (vb && j < a.S && j <= limb) ? sc[nt][2 + e] * a.scale_log2 : neg_inf();
-          xa[nt * 2 + e] = x0;
-          xb[nt * 2 + e] = x1;
-          ma = fmaxf(ma, x0);
-          mb = fmaxf(mb, x1);
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x = v[c][i] * a.scale_log2;
+            if (!full_tile) {
+              const int64_t j = jt + 32 * c + i;
+              if (j >= a.S || j > lim) x = neg_inf();
+            }
+            v[c][i] = x;
+            tm = fmaxf(tm, x);
+          }
+        const float mn = fmaxf(m, tm);
+        float sum = 0.f;
+        if (mn != neg_inf()) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sum += exp2f(v[c][i] - mn);
         }
+        l = (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + sum;
+        m = mn;
       }
-      const float na = fmaxf(m_a, ma), nb = fmaxf(m_b, mb);
-      float sa = 0.f, sb = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        sa += (xa[i] == neg_inf()) ? 0.f : exp2f(xa[i] - na);
-        sb += (xb[i] == neg_inf()) ? 0.f : exp2f(xb[i] - nb);
-      }
-      l_a = ((m_a == neg_inf()) ? 0.f : l_a * exp2f(m_a - na)) + sa;
-      l_b = ((m_b == neg_inf()) ? 0.f : l_b * exp2f(m_b - nb)) + sb;
-      m_a = na;
-      m_b = nb;
-      __syncthreads();
+      if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + chunk] = make_float2(m, l);
     } else {
-      float* cs = colsum + (it & 1) * 8 * P_TILE + warp * P_TILE;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        float v[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int64_t j = jt + nt * 8 + 2 * (lane & 3) + e;
-          const bool kj = j < a.L;
-          const float pa = (va && kj) ? exp2f(sc[nt][e] * a.scale_log2 - lse_a) : 0.f;
-          const float pb = (vb && kj) ? exp2f(sc[nt][2 + e] * a.scale_log2 - lse_b) : 0.f;
-          float s = pa + pb;
-          s += __shfl_xor_sync(0xffffffffu, s, 4);
-          s += __shfl_xor_sync(0xffffffffu, s, 8);
-          s += __shfl_xor_sync(0xffffffffu, s, 16);
-          v[e] = s;
+      // log2-domain normaliser of every query row of this CTA (rows past R: +inf -> weight 0)
+      for (int i = r_loc; i < nq; i += 128) {
+        const int r = row0 + i;
+        float lse = __int_as_float(0x7f800000);
+        if (r < a.R) {
+          const float2* st = a.stats + ((size_t)pair * a.R + r) * a.nchunk1;
+          float M = neg_inf();
+          for (int c = 0; c < a.nchunk1; ++c) M = fmaxf(M, st[c].x);
+          float Ls = 0.f;
+          for (int c = 0; c < a.nchunk1; ++c)
+            if (st[c].x != neg_inf()) Ls += st[c].y * exp2f(st[c].x - M);
+          lse = M + log2f(Ls);
         }
-        if (lane < 4) {
-          cs[nt * 8 + 2 * lane] = v[0];
-          cs[nt * 8 + 2 * lane + 1] = v[1];
-        }
+        ts.lse[i] = lse;
       }
-      __syncthreads();
-      if (tid < P_TILE) {
-        const float* c2 = colsum + (it & 1) * 8 * P_TILE;
-        float s = 0.f;
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // epilogue warps only
+      for (int t = 0; t < ntiles; ++t) {
+        const int buf = t & 1;
+        if (!tc_wait(&ts.tfull[buf], (t >> 1) & 1, abort_flag, err)) break;
+        tc_fence_after();
+        float sum = 0.f;
+        for (int c0 = 0; c0 < nq; c0 += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + buf * ncols + c0, v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int w = 0; w < 8; ++w) s += c2[w * P_TILE + tid];
-        const int64_t j = jt + tid;
-        if (j < a.L) a.scores[((size_t)pair * a.RG + rg) * a.L + j] = s;
+          for (int i = 0; i < 32; ++i) sum += exp2f(fmaf(v[i], a.scale_log2, -ts.lse[c0 + i]));
+        }
+        tc_fence_before();
+        mbar_arrive(&ts.tempty[buf]);
+        const int64_t j = j0 + (int64_t)t * T_KEYS + r_loc;
+        if (j < a.L) a.scores[((size_t)pair * a.RG2 + rg) * a.L + j] = sum;
       }
-    }
-    if (tid == 0 && it + P_NST < ntiles) {
-      fence_proxy_async_smem();
-      const int y = (int)(j0 + (int64_t)(it + P_NST) * P_TILE);
-      mbar_arrive_expect_tx(&full[st], P_STAGE);
-      tma_load_3d(tiles + st * P_STAGE, &tmK, 0, y, pair, &full[st]);
-      tma_load_3d(tiles + st * P_STAGE + P_HALF, &tmK, 64, y, pair, &full[st]);
     }
   }
-
-  if (PASS == 1) {
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      const float moa = __shfl_xor_sync(0xffffffffu, m_a, o), loa = __shfl_xor_sync(0xffffffffu, l_a, o);
-      const float mob = __shfl_xor_sync(0xffffffffu, m_b, o), lob = __shfl_xor_sync(0xffffffffu, l_b, o);
-      const float na = fmaxf(m_a, moa), nb = fmaxf(m_b, mob);
-      l_a = ((m_a == neg_inf()) ? 0.f : l_a * exp2f(m_a - na)) + ((moa == neg_inf()) ? 0.f : loa * exp2f(moa - na));
-      l_b = ((m_b == neg_inf()) ? 0.f : l_b * exp2f(m_b - nb)) + ((mob == neg_inf()) ? 0.f : lob * exp2f(mob - nb));
-      m_a = na;
-      m_b = nb;
-    }
-    if ((lane & 3) == 0) {
-      if (va) a.stats[((size_t)pair * a.R + ra) * a.nchunk1 + chunk] = make_float2(m_a, l_a);
-      if (vb) a.stats[((size_t)pair * a.R + rb) * a.nchunk1 + chunk] = make_float2(m_b, l_b);
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, tcols);
   }
 }
 
@@ -390,29 +429,31 @@ size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32
   const int64_t pairs = (int64_t)B * Hkv;
   const int G = Hq / Hkv;
   const int64_t R = (int64_t)G * W;
-  const int64_t RG = (R + P_ROWS - 1) / P_ROWS;
+  const int64_t RG = (R + P2_ROWS - 1) / P2_ROWS;
   const int64_t L = std::max<int64_t>(S - W, 0);
   const int64_t nchunk1 = (S + P_CHUNK - 1) / P_CHUNK;
   return al256((size_t)pairs * R * nchunk1 * sizeof(float2)) + al256((size_t)pairs * RG * L * sizeof(float)) +
          al256((size_t)pairs * L * sizeof(float));
 }
 
-cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+int snap_pass2_rows(int32_t G, int32_t W) { return std::min(P2_ROWS, (G * W + 31) & ~31); }
+
+cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmQ1, const CUtensorMap* tmQ2,
+                        cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
   const int pairs = a.B * a.Hkv;
   const int W = (int)std::min<int64_t>(a.W, a.S);
   const int64_t L = a.S - W;
   const bool keep_all = a.B1 >= a.S || L <= 0;
   if (!keep_all) {
     PassArgs p;
-    p.q_obs = reinterpret_cast<const bf16*>(a.q_obs);
     p.S = a.S;
     p.L = L;
     p.Hq = a.Hq;
@@ -420,23 +461,26 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, cudaStream_t 
     p.G = a.G;
     p.W = W;
     p.R = a.G * W;
-    p.RG = (p.R + P_ROWS - 1) / P_ROWS;
+    p.RG1 = (p.R + P1_ROWS - 1) / P1_ROWS;
+    p.RG2 = (p.R + P2_ROWS - 1) / P2_ROWS;
+    p.nq2 = snap_pass2_rows(a.G, W);
     p.nchunk1 = (int)((a.S + P_CHUNK - 1) / P_CHUNK);
     p.scale_log2 = a.scale_log2;
     uint8_t* w = reinterpret_cast<uint8_t*>(a.ws);
     p.stats = reinterpret_cast<float2*>(w);
     w += al256((size_t)pairs * p.R * p.nchunk1 * sizeof(float2));
     p.scores = reinterpret_cast<float*>(w);
-    w += al256((size_t)pairs * p.RG * L * sizeof(float));
+    w += al256((size_t)pairs * p.RG2 * L * sizeof(float));
     float* pooled = a.pooled_out ? a.pooled_out : reinterpret_cast<float*>(w);
 
-    cudaError_t e = launch_pdl(snap_pass_kernel<1>, dim3(p.nchunk1, p.RG, pairs), dim3(P_NT), P_SMEM, st, *tmK, p);
+    cudaError_t e = launch_pdl(snap_pass_kernel<1>, dim3(p.nchunk1, p.RG1, pairs), dim3(T_NT), T_SMEM, st, *tmK,
+                               *tmQ1, p);
     if (e != cudaSuccess) return e;
     const int nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
-    e = launch_pdl(snap_pass_kernel<2>, dim3(nchunk2, p.RG, pairs), dim3(P_NT), P_SMEM, st, *tmK, p);
+    e = launch_pdl(snap_pass_kernel<2>, dim3(nchunk2, p.RG2, pairs), dim3(T_NT), T_SMEM, st, *tmK, *tmQ2, p);
     if (e != cudaSuccess) return e;
     e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
-                   (const float*)p.scores, (int)p.RG, (int64_t)L, (int)(a.pool / 2), pooled);
+                   (const float*)p.scores, (int)p.RG2, (int64_t)L, (int)(a.pool / 2), pooled);
     if (e != cudaSuccess) return e;
     const int n_sink = (int)std::max<int64_t>(0, std::min<int64_t>(a.n_sink, L));
     const int64_t ntop = std::max<int64_t>(0, a.B1 - W - n_sink);
