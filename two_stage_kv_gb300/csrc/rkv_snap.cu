@@ -43,7 +43,7 @@ namespace {
 //           key and sums exp2(logit - lse(row)) over the rows in registers.
 constexpr int T_KEYS = 128;                       // keys per tile
 constexpr int T_NST = 3;                          // smem ring depth
-constexpr int T_NT = 192;                         // 6 warps
+constexpr int T_NT = 320;                         // producer, MMA, two sets of 4 epilogue warps
 constexpr int P_CHUNK = 2048;                     // keys per CTA
 constexpr int P1_ROWS = 128;                      // query rows per pass-1 CTA (MMA M)
 constexpr int P2_ROWS = 256;                      // query rows per pass-2 CTA (MMA N, max)
@@ -66,6 +66,7 @@ struct TcSmem {                    // lives after the operand tiles
   uint32_t tmem_base;
   int32_t abort_flag;
   float lse[P2_ROWS];
+  float2 part[128];                // pass 1: (max, sum) of the second epilogue set, per row
 };
 
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
@@ -175,54 +176,73 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
     }
   } else {
     // ----------------------------------------------------------- epilogue --
+    // Two sets of four warps; set e drains TMEM buffer e, i.e. tiles t with t % 2 == e.
+    const int eset = (warp - 2) >> 2;                // 0 or 1
     const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
     const int r_loc = 32 * quad + lane;              // TMEM lane of this thread
-    const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16);
+    const int etid = (warp - 2) * 32 + lane;         // 0 .. 255 over both sets
+    const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16) + (uint32_t)(eset * ncols);
+    const int S32 = (int)a.S, L32 = (int)a.L, j032 = (int)j0;
     if (PASS == 1) {
       const int r = row0 + r_loc;                    // query row in the group
       const bool rvalid = r < a.R;
-      const int64_t lim = a.S - a.W + (rvalid ? (r % a.W) : 0);    // last key this row attends
+      const int lim = S32 - a.W + (rvalid ? (r % a.W) : 0);     // last key this row attends
       float m = neg_inf(), l = 0.f;
-      for (int t = 0; t < ntiles; ++t) {
-        const int buf = t & 1;
-        if (!tc_wait(&ts.tfull[buf], (t >> 1) & 1, abort_flag, err)) break;
+      for (int t = eset; t < ntiles; t += 2) {
+        if (!tc_wait(&ts.tfull[eset], (t >> 1) & 1, abort_flag, err)) break;
         tc_fence_after();
         float v[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + buf * ncols + 32 * c, v[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + 32 * c, v[c]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&ts.tempty[buf]);
-        const int64_t jt = j0 + (int64_t)t * T_KEYS;
-        const bool full_tile = jt + T_KEYS <= a.S - a.W;       // every row attends every key
+        mbar_arrive(&ts.tempty[eset]);
+        const int jt = j032 + t * T_KEYS;
         float tm = neg_inf();
+        if (jt + T_KEYS <= S32 - a.W) {              // every row attends every key of the tile
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x = v[c][i] * a.scale_log2;
-            if (!full_tile) {
-              const int64_t j = jt + 32 * c + i;
-              if (j >= a.S || j > lim) x = neg_inf();
+            for (int i = 0; i < 32; ++i) {
+              v[c][i] *= a.scale_log2;
+              tm = fmaxf(tm, v[c][i]);
             }
-            v[c][i] = x;
-            tm = fmaxf(tm, x);
-          }
+        } else {
+          const int jmax = min(S32 - 1, lim) - jt;    // last attended column of this tile
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float x = (32 * c + i <= jmax) ? v[c][i] * a.scale_log2 : neg_inf();
+              v[c][i] = x;
+              tm = fmaxf(tm, x);
+            }
+        }
         const float mn = fmaxf(m, tm);
-        float sum = 0.f;
+        float s0 = 0.f, s1 = 0.f;
         if (mn != neg_inf()) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sum += exp2f(v[c][i] - mn);
+            for (int i = 0; i < 32; i += 2) {
+              s0 += exp2f(v[c][i] - mn);
+              s1 += exp2f(v[c][i + 1] - mn);
+            }
         }
-        l = (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + sum;
+        l = (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (s0 + s1);
         m = mn;
       }
-      if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + chunk] = make_float2(m, l);
+      if (eset == 1) ts.part[r_loc] = make_float2(m, l);
+      asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+      if (eset == 0) {
+        const float2 o = ts.part[r_loc];
+        const float mn = fmaxf(m, o.x);
+        const float ls = (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (o.x == neg_inf() ? 0.f : o.y * exp2f(o.x - mn));
+        if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + chunk] = make_float2(mn, ls);
+      }
     } else {
       // log2-domain normaliser of every query row of this CTA (rows past R: +inf -> weight 0)
-      for (int i = r_loc; i < nq; i += 128) {
+      for (int i = etid; i < nq; i += 256) {
         const int r = row0 + i;
         float lse = __int_as_float(0x7f800000);
         if (r < a.R) {
@@ -236,23 +256,27 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
         }
         ts.lse[i] = lse;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");   // epilogue warps only
-      for (int t = 0; t < ntiles; ++t) {
-        const int buf = t & 1;
-        if (!tc_wait(&ts.tfull[buf], (t >> 1) & 1, abort_flag, err)) break;
+      asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+      for (int t = eset; t < ntiles; t += 2) {
+        if (!tc_wait(&ts.tfull[eset], (t >> 1) & 1, abort_flag, err)) break;
         tc_fence_after();
-        float sum = 0.f;
-        for (int c0 = 0; c0 < nq; c0 += 32) {
-          float v[32];
-          tmem_ld32(lane_addr + buf * ncols + c0, v);
+        float s0 = 0.f, s1 = 0.f;
+        for (int c0 = 0; c0 < nq; c0 += 64) {
+          float v[2][32];
+          tmem_ld32(lane_addr + c0, v[0]);
+          if (c0 + 32 < nq) tmem_ld32(lane_addr + c0 + 32, v[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sum += exp2f(fmaf(v[i], a.scale_log2, -ts.lse[c0 + i]));
+          for (int i = 0; i < 32; ++i) s0 += exp2f(fmaf(v[0][i], a.scale_log2, -ts.lse[c0 + i]));
+          if (c0 + 32 < nq) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s1 += exp2f(fmaf(v[1][i], a.scale_log2, -ts.lse[c0 + 32 + i]));
+          }
         }
         tc_fence_before();
-        mbar_arrive(&ts.tempty[buf]);
-        const int64_t j = j0 + (int64_t)t * T_KEYS + r_loc;
-        if (j < a.L) a.scores[((size_t)pair * a.RG2 + rg) * a.L + j] = sum;
+        mbar_arrive(&ts.tempty[eset]);
+        const int j = j032 + t * T_KEYS + r_loc;
+        if (j < L32) a.scores[((size_t)pair * a.RG2 + rg) * a.L + j] = s0 + s1;
       }
     }
   }
