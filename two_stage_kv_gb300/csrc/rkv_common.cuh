@@ -259,6 +259,40 @@ __device__ __forceinline__ uint32_t f2key(float f) {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Hardware 2^x (PTX ex2.approx.ftz: relative error about 2^-22, results below
+// 2^-126 flushed to zero, ex2(-inf) = +0).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Paired fp32 arithmetic (PTX f32x2, sm_100 and later): one instruction for
+// two lanes of a float2, round-to-nearest as the scalar forms.
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  return (uint64_t)__float_as_uint(v.x) | ((uint64_t)__float_as_uint(v.y) << 32);
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t u) {
+  return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
+}
+__device__ __forceinline__ float2 fma_f2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 add_f2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+
+// max of three (PTX three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Dynamic shared memory rounded up to a 1024-byte boundary (the 128-byte TMA
 // swizzle repeats every 1024 bytes); launches reserve 1024 extra bytes.
 __device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {

@@ -65,7 +65,7 @@ struct TcSmem {                    // lives after the operand tiles
   uint64_t qbar;
   uint32_t tmem_base;
   int32_t abort_flag;
-  float lse[P2_ROWS];
+  __align__(16) float nlse[P2_ROWS];   // pass 2: -log2(sum) of every query row
   float2 part[128];                // pass 1: (max, sum) of the second epilogue set, per row
 };
 
@@ -198,17 +198,34 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
         tc_fence_before();
         mbar_arrive(&ts.tempty[eset]);
         const int jt = j032 + t * T_KEYS;
-        float tm = neg_inf();
-        if (jt + T_KEYS <= S32 - a.W) {              // every row attends every key of the tile
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float mn;
+        if (jt + T_KEYS <= S32 - a.W) {
+          // every row attends every key of the tile: the maximum of the raw
+          // logits scales to the maximum of the scaled ones (scale > 0)
+          float x0 = v[0][0], x1 = v[1][0], x2 = v[2][0], x3 = v[3][0];
+#pragma unroll
+          for (int i = 1; i < 31; i += 2) {
+            x0 = fmax3(x0, v[0][i], v[0][i + 1]);
+            x1 = fmax3(x1, v[1][i], v[1][i + 1]);
+            x2 = fmax3(x2, v[2][i], v[2][i + 1]);
+            x3 = fmax3(x3, v[3][i], v[3][i + 1]);
+          }
+          x0 = fmax3(x0, x1, v[0][31]);
+          x2 = fmax3(x2, x3, v[1][31]);
+          x0 = fmax3(x0, x2, fmaxf(v[2][31], v[3][31]));
+          mn = fmaxf(m, x0 * a.scale_log2);
+          const float2 sc = make_float2(a.scale_log2, a.scale_log2), nm = make_float2(-mn, -mn);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v[c][i] *= a.scale_log2;
-              tm = fmaxf(tm, v[c][i]);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x = fma_f2(make_float2(v[c][i], v[c][i + 1]), sc, nm);
+              acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3], make_float2(ex2_ftz(x.x), ex2_ftz(x.y)));
             }
         } else {
           const int jmax = min(S32 - 1, lim) - jt;    // last attended column of this tile
+          float tm = neg_inf();
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -217,19 +234,18 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
               v[c][i] = x;
               tm = fmaxf(tm, x);
             }
-        }
-        const float mn = fmaxf(m, tm);
-        float s0 = 0.f, s1 = 0.f;
-        if (mn != neg_inf()) {
+          mn = fmaxf(m, tm);
+          if (mn != neg_inf()) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              s0 += exp2f(v[c][i] - mn);
-              s1 += exp2f(v[c][i + 1] - mn);
-            }
+              for (int i = 0; i < 32; i += 2)
+                acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3],
+                                           make_float2(ex2_ftz(v[c][i] - mn), ex2_ftz(v[c][i + 1] - mn)));
+          }
         }
-        l = (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (s0 + s1);
+        const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
+        l = (m == neg_inf() ? 0.f : l * ex2_ftz(m - mn)) + (s01.x + s01.y);
         m = mn;
       }
       if (eset == 1) ts.part[r_loc] = make_float2(m, l);
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
         if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + chunk] = make_float2(mn, ls);
       }
     } else {
-      // log2-domain normaliser of every query row of this CTA (rows past R: +inf -> weight 0)
+      // negated log2-domain normaliser of every query row of this CTA (rows past R: -inf -> weight 0)
       for (int i = etid; i < nq; i += 256) {
         const int r = row0 + i;
         float lse = __int_as_float(0x7f800000);
@@ -254,29 +270,39 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
             if (st[c].x != neg_inf()) Ls += st[c].y * exp2f(st[c].x - M);
           lse = M + log2f(Ls);
         }
-        ts.lse[i] = lse;
+        ts.nlse[i] = -lse;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
       for (int t = eset; t < ntiles; t += 2) {
         if (!tc_wait(&ts.tfull[eset], (t >> 1) & 1, abort_flag, err)) break;
         tc_fence_after();
-        float s0 = 0.f, s1 = 0.f;
-        for (int c0 = 0; c0 < nq; c0 += 64) {
-          float v[2][32];
-          tmem_ld32(lane_addr + c0, v[0]);
-          if (c0 + 32 < nq) tmem_ld32(lane_addr + c0 + 32, v[1]);
-          tmem_wait_ld();
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 sc = make_float2(a.scale_log2, a.scale_log2);
+        const float4* nl4 = reinterpret_cast<const float4*>(ts.nlse);
+        auto sum32 = [&](const float* v, int c0) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s0 += exp2f(fmaf(v[0][i], a.scale_log2, -ts.lse[c0 + i]));
-          if (c0 + 32 < nq) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s1 += exp2f(fmaf(v[1][i], a.scale_log2, -ts.lse[c0 + 32 + i]));
+          for (int i = 0; i < 32; i += 4) {
+            const float4 nl = nl4[(c0 + i) >> 2];   // same address across the warp: broadcast
+            const float2 x0 = fma_f2(make_float2(v[i], v[i + 1]), sc, make_float2(nl.x, nl.y));
+            const float2 x1 = fma_f2(make_float2(v[i + 2], v[i + 3]), sc, make_float2(nl.z, nl.w));
+            acc[(i >> 2) & 3] = add_f2(acc[(i >> 2) & 3], make_float2(ex2_ftz(x0.x), ex2_ftz(x0.y)));
+            acc[((i >> 2) + 2) & 3] = add_f2(acc[((i >> 2) + 2) & 3], make_float2(ex2_ftz(x1.x), ex2_ftz(x1.y)));
           }
+        };
+        for (int c0 = 0; c0 < nq; c0 += 64) {        // nq is a multiple of 32
+          float v[2][32];
+          const bool two = c0 + 32 < nq;
+          tmem_ld32(lane_addr + c0, v[0]);
+          if (two) tmem_ld32(lane_addr + c0 + 32, v[1]);
+          tmem_wait_ld();
+          sum32(v[0], c0);
+          if (two) sum32(v[1], c0 + 32);
         }
+        const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
         tc_fence_before();
         mbar_arrive(&ts.tempty[eset]);
         const int j = j032 + t * T_KEYS + r_loc;
-        if (j < L32) a.scores[((size_t)pair * a.RG2 + rg) * a.L + j] = s0 + s1;
+        if (j < L32) a.scores[((size_t)pair * a.RG2 + rg) * a.L + j] = s01.x + s01.y;
       }
     }
   }
