@@ -142,6 +142,19 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 __device__ __forceinline__ void st_cluster_v2f32(uint32_t addr, float a, float b) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
+// Asynchronous stores into another CTA's shared memory that count their bytes
+// on that CTA's mbarrier (complete_tx): the receiver waits on its own barrier,
+// the sender needs no cluster barrier.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v2f32(uint32_t addr, float a, float b, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(remote_bar)
+               : "memory");
+}
 
 // ------------------------------------------------ tcgen05 (5th-gen tensor core) --
 // Allocate ncols TMEM columns (power of two, >= 32); one whole warp executes it.

@@ -76,6 +76,7 @@ struct FixedSmem {
   float mrun[16], lrun[16];
   int32_t nvalid[MAX_ROUND_ROWS / 8];
   uint64_t mbar[MAX_ROUND_ROWS / 8];    // one per staged block
+  uint64_t ebar;                        // partials of the heads this CTA owns (phase E)
 };
 
 // Block-wide exclusive scan of a flag.  Returns the prefix, writes the total.
@@ -280,7 +281,11 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // Prologue that touches no data of the previous kernel.
   if (tid == 0) {
     for (int i = 0; i < MAX_ROUND_ROWS / 8; ++i) mbar_init(&fs.mbar[i], 1);
+    mbar_init(&fs.ebar, 1);
     fence_mbar_init();
+    // every CTA of the cluster sends its (O, max, sum) of each head this CTA owns
+    const int gmine = (int)rank < G ? (G - (int)rank + ns - 1) / ns : 0;
+    if (gmine > 0) mbar_arrive_expect_tx(&fs.ebar, (uint32_t)(gmine * ns * PART_STRIDE * 4));
     if (!MT) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -296,6 +301,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   cluster_arrive_relaxed();
   pdl_wait();
   pdl_launch_dependents();
+  // rank 0 persists the appended key's KT column at the end; fetch the old column now
+  bf16 kt_old = __float2bfloat16(0.f);
+  bf16* kt_col = nullptr;
+  if (rank == 0 && app) {
+    const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
+    kt_col = reinterpret_cast<bf16*>(a.kt) + ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
+    if ((n_old % a.blk) != 0) kt_old = *kt_col;
+  }
 
   // ---------------------------------------------------------------- A ------
   {
@@ -488,12 +501,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     const int rows16 = nsteps * 16;
     if (tid < nsl) fs.nvalid[tid] = min(blk, n_tot - sel[r0 + tid] * blk);
     if (!MT) {
-      if (warp == 0) {
+      {
+        // the copies are spread over all warps: one warp issuing them all serialises them
         if (lane == 0) fence_proxy_async_smem();   // earlier generic accesses to this region come first
-        for (int s = lane; s < nsl; s += 32) mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * 4u);
+        if (warp == 0)
+          for (int s = lane; s < nsl; s += 32) mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * 4u);
         __syncwarp();
-        for (int t = lane; t < nsl * 4; t += 32) {
-          const int s = t >> 2, part = t & 3;          // part: K lo, K hi, V lo, V hi
+        const int part = warp & 3;                   // K lo, K hi, V lo, V hi
+        for (int s = (warp >> 2) + 2 * lane; s < nsl; s += 64) {
           const int y = sel[r0 + s] * blk;
           const uint32_t off = (uint32_t)s * blk * 128u + (uint32_t)(part & 1) * half;
           tma_load_3d(((part >> 1) ? tV : tK) + off, (part >> 1) ? &tmV : &tmK, (part & 1) * 64, y, pair,
@@ -677,27 +692,35 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   }
 
   // ---------------------------------------------------------------- E ------
+  // Partials go to the owner of each head (head g: CTA g % ns) with st.async,
+  // which counts their bytes on the owner's ebar; only owners wait.
   const int gown = (G + ns - 1) / ns;
-  cluster_wait_acquire();
+  cluster_wait_acquire();      // every CTA of the cluster has started and armed its ebar
+  {
+    const uint32_t ebar_local = smem_u32(&fs.ebar);
 #pragma unroll
-  for (int ht = 0; ht < NH; ++ht) {
+    for (int ht = 0; ht < NH; ++ht) {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int g = 8 * ht + 2 * t4 + hh;
-      if (g < G) {
-        const int owner = g % ns, gl = g / ns;
-        const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
-        st_cluster_f32(base + 4u * (16 * warp + g4), acc[ht][hh]);
-        st_cluster_f32(base + 4u * (16 * warp + g4 + 8), acc[ht][2 + hh]);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int g = 8 * ht + 2 * t4 + hh;
+        if (g < G) {
+          const int owner = g % ns, gl = g / ns;
+          const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
+          const uint32_t bar = mapa(ebar_local, owner);
+          st_async_f32(base + 4u * (16 * warp + g4), acc[ht][hh], bar);
+          st_async_f32(base + 4u * (16 * warp + g4 + 8), acc[ht][2 + hh], bar);
+        }
       }
     }
+    if (tid < G) {
+      const int owner = tid % ns, gl = tid / ns;
+      const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
+      st_async_v2f32(base + 4u * HD, fs.mrun[tid], fs.lrun[tid], mapa(ebar_local, owner));
+    }
   }
-  if (tid < G) {
-    const int owner = tid % ns, gl = tid / ns;
-    const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
-    st_cluster_v2f32(base + 4u * HD, fs.mrun[tid], fs.lrun[tid]);
+  if ((int)rank < G) {
+    if (!mbar_wait(&fs.ebar, 0, err)) mbar_wait(&fs.ebar, 0, err);
   }
-  cluster_sync();
   for (int gl = 0; gl < gown; ++gl) {
     const int g = gl * ns + (int)rank;
     if (g >= G) break;
@@ -730,13 +753,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       if (MT && tid == 32) a.idx_w[(size_t)pair * a.idx_cap + n_old] = (int32_t)a.row;
       {
         const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
-        bf16* p = reinterpret_cast<bf16*>(a.kt) + ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
         const bf16 kv = fs.knew[c];
         if ((n_old % a.blk) == 0) {
-          *p = kv;
+          *kt_col = kv;
         } else {
-          const float x = bf2f(kv), o = bf2f(*p);
-          if (m == 1 ? (x < o) : (x > o)) *p = kv;
+          const float x = bf2f(kv), o = bf2f(kt_old);
+          if (m == 1 ? (x < o) : (x > o)) *kt_col = kv;
         }
       }
     }
