@@ -77,6 +77,22 @@ rkv_status make_kv_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t 
   return RKV_OK;
 }
 
+// 2-D map over the KT cache viewed as [pairs * 2 * 128 rows, nblk_cap] bf16, box
+// box_cols blocks x 256 rows (all Kmax and Kmin rows of one pair), no swizzle.
+rkv_status make_kt_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t nblk_cap, int box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)nblk_cap, (cuuint64_t)pairs * 2 * rkv::HD_HOST};
+  cuuint64_t strides[1] = {(cuuint64_t)nblk_cap * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, 2 * rkv::HD_HOST};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled(kt) failed with %d", (int)r);
+  return RKV_OK;
+}
+
 // 2-D map over window queries [rows, 128] bf16, box 64 channels x box_rows rows (128-byte swizzle).
 rkv_status make_q_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
   auto fn = encode_fn();
@@ -141,9 +157,10 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.scale_log2 = scale * 1.4426950408889634f;
   if (!rkv::hsa_plan(a)) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: shared memory plan does not fit");
 
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmK, tmV, tmKT;
   std::memset(&tmK, 0, sizeof(tmK));
   std::memset(&tmV, 0, sizeof(tmV));
+  std::memset(&tmKT, 0, sizeof(tmKT));
   const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
   if (!mt) {
     // rows at or past n (the appended token included) read as zero
@@ -151,7 +168,10 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
     if ((s = make_kv_map(&tmK, k, pairs, cap, extent, blk, "k")) != RKV_OK) return s;
     if ((s = make_kv_map(&tmV, v, pairs, cap, extent, blk, "v")) != RKV_OK) return s;
   }
-  cudaError_t e = rkv::hsa_launch(a, &tmK, &tmV, mt, reinterpret_cast<cudaStream_t>(stream));
+  if (a.kt_spec) {
+    if ((s = make_kt_map(&tmKT, kt, pairs, nblk_cap, a.cpr)) != RKV_OK) return s;
+  }
+  cudaError_t e = rkv::hsa_launch(a, &tmK, &tmV, &tmKT, mt, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "hsa_decode launch");
   return RKV_OK;
 }

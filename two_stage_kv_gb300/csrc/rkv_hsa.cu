@@ -77,6 +77,9 @@ struct FixedSmem {
   int32_t nvalid[MAX_ROUND_ROWS / 8];
   uint64_t mbar[MAX_ROUND_ROWS / 8];    // one per staged block
   uint64_t ebar;                        // partials of the heads this CTA owns (phase E)
+  uint64_t ktbar;                       // KT prefetch (phase B)
+  uint64_t sbar;                        // every block score and score bound of the cluster (phase B)
+  float2 rbound[8 * NWARP];             // (min, max) of the scores of each warp of each CTA
 };
 
 // Block-wide exclusive scan of a flag.  Returns the prefix, writes the total.
@@ -254,6 +257,7 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, FixedSmem& fs
 template <bool MT, int NH>
 __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                            const __grid_constant__ CUtensorMap tmV,
+                                                           const __grid_constant__ CUtensorMap tmKT,
                                                            const HsaArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -277,12 +281,21 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   const int n_tot = a.n + (app ? 1 : 0);      // tokens attended
   const int nb_new = app ? n_old / a.blk : -1;
   const int nblk = a.nblk;
+  const int cpr = a.cpr;
+  const int jlo = (int)rank * cpr;                       // blocks this CTA scores: [jlo, jhi)
+  const int jhi = min(nblk, jlo + cpr);
+  const bool spec = a.kt_spec != 0;
+  const bool own_new = app && nb_new >= jlo && nb_new < jhi;   // this CTA holds the appended key's block
 
   // Prologue that touches no data of the previous kernel.
   if (tid == 0) {
     for (int i = 0; i < MAX_ROUND_ROWS / 8; ++i) mbar_init(&fs.mbar[i], 1);
     mbar_init(&fs.ebar, 1);
+    mbar_init(&fs.ktbar, 1);
+    mbar_init(&fs.sbar, 1);
     fence_mbar_init();
+    // every CTA of the cluster sends its scores and its warps' score bounds to every CTA
+    mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(nblk * 4 + ns * NWARP * 8));
     // every CTA of the cluster sends its (O, max, sum) of each head this CTA owns
     const int gmine = (int)rank < G ? (G - (int)rank + ns - 1) / ns : 0;
     if (gmine > 0) mbar_arrive_expect_tx(&fs.ebar, (uint32_t)(gmine * ns * PART_STRIDE * 4));
@@ -290,6 +303,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
     }
+    if (spec) prefetch_tmap(&tmKT);
   }
   for (int i = tid; i < 4 * 256; i += NT) fs.hist[i] = 0;
   if (tid < 16) {
@@ -301,13 +315,20 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   cluster_arrive_relaxed();
   pdl_wait();
   pdl_launch_dependents();
-  // rank 0 persists the appended key's KT column at the end; fetch the old column now
+  // KT rows do not depend on the query: with the prefetch, all 2*D rows of this
+  // CTA's blocks are in flight while the channels are chosen
+  if (spec && tid == 0 && jhi > jlo) {
+    mbar_arrive_expect_tx(&fs.ktbar, (uint32_t)(2 * HD * cpr * 2));
+    tma_load_2d(kttile, &tmKT, jlo, pair * 2 * HD, &fs.ktbar);
+  }
+  // the CTA holding the appended key's block persists its KT column; without
+  // the prefetch it fetches the old column now and writes the new one at the end
   bf16 kt_old = __float2bfloat16(0.f);
   bf16* kt_col = nullptr;
-  if (rank == 0 && app) {
+  if (own_new) {
     const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
     kt_col = reinterpret_cast<bf16*>(a.kt) + ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
-    if ((n_old % a.blk) != 0) kt_old = *kt_col;
+    if (!spec && (n_old % a.blk) != 0) kt_old = *kt_col;
   }
 
   // ---------------------------------------------------------------- A ------
@@ -389,63 +410,119 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   __syncthreads();
 
   // ---------------------------------------------------------------- B ------
+  // CTA `rank` scores blocks [jlo, jhi) and sends every score (and the min / max
+  // of each warp's scores) to every CTA of the cluster with st.async; each CTA
+  // then holds all nblk scores once its sbar completes.  A score is the fp32
+  // sum over the k1 chosen channels of qbar * (Kmax or Kmin), four threads per
+  // block pair splitting the channels.
   const int k1 = a.k1;
   float smn = __int_as_float(0x7f800000), smx = neg_inf();
+  cluster_wait_acquire();      // every CTA of the cluster has started and armed its barriers
   {
+    const uint32_t sbar_local = smem_u32(&fs.sbar);
+    const uint32_t sval_local = smem_u32(sval);
     const bf16* ktp = reinterpret_cast<const bf16*>(a.kt) + (size_t)pair * 2 * HD * a.nblk_cap;
-    const int bc = a.kt_chunk;                       // blocks per gathered chunk (multiple of 8)
-    for (int cb0 = 0; cb0 < nblk; cb0 += bc) {
-      const int nb_here = min(bc, nblk - cb0);
-      const int n16 = (nb_here + 7) / 8;
-      for (int row = warp; row < k1; row += NWARP) {
-        const bf16* src = ktp + (size_t)fs.rowoff[row] * a.nblk_cap + cb0;
-        bf16* dst = kttile + (size_t)row * bc;
-        for (int ch = lane; ch < n16; ch += 32) cp_async_16(smem_u32(dst + ch * 8), src + ch * 8);
-      }
-      cp_async_commit();
-      cp_async_wait_all();
-      __syncthreads();
-      if (app && nb_new >= cb0 && nb_new < cb0 + nb_here) {
-        // fold the appended key into its block (a new block starts from it)
-        const int col = nb_new - cb0;
-        const bool fresh = (n_old % a.blk) == 0;
-        for (int i = tid; i < k1; i += NT) {
-          const int ro = fs.rowoff[i];
-          const bf16 kv = fs.knew[ro & (HD - 1)];
-          bf16& slot = kttile[(size_t)i * bc + col];
-          if (fresh) {
+    const int bc = spec ? cpr : a.kt_chunk;          // columns per tile (multiple of 8)
+    const int cg = tid & 3, bp = tid >> 2;           // channel group, block pair within a 128-block span
+    for (int cb0 = jlo; cb0 < jhi; cb0 += bc) {
+      const int nb_here = min(bc, jhi - cb0);
+      if (spec) {
+        if (!mbar_wait(&fs.ktbar, 0, &g_hsa_err)) mbar_wait(&fs.ktbar, 0, &g_hsa_err);
+        if (own_new) {
+          // fold the appended key into its block in every KT row and persist the column
+          const int col = nb_new - cb0;
+          const int m = tid >> 7, c = tid & (HD - 1);
+          const bf16 kv = fs.knew[c];
+          bf16& slot = kttile[(size_t)tid * bc + col];
+          if ((n_old % a.blk) == 0) {
             slot = kv;
           } else {
             const float x = bf2f(kv), o = bf2f(slot);
-            if (ro >= HD ? (x < o) : (x > o)) slot = kv;
+            if (m == 1 ? (x < o) : (x > o)) slot = kv;
+          }
+          *kt_col = slot;
+        }
+      } else {
+        if (cb0 > jlo) __syncthreads();              // the previous chunk's scores are done with the tile
+        const int n16 = (nb_here + 7) / 8;
+        for (int row = warp; row < k1; row += NWARP) {
+          const bf16* src = ktp + (size_t)fs.rowoff[row] * a.nblk_cap + cb0;
+          bf16* dst = kttile + (size_t)row * bc;
+          for (int ch = lane; ch < n16; ch += 32) cp_async_16(smem_u32(dst + ch * 8), src + ch * 8);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+        if (own_new && nb_new >= cb0 && nb_new < cb0 + nb_here) {
+          const int col = nb_new - cb0;
+          const bool fresh = (n_old % a.blk) == 0;
+          for (int i = tid; i < k1; i += NT) {
+            const int ro = fs.rowoff[i];
+            const bf16 kv = fs.knew[ro & (HD - 1)];
+            bf16& slot = kttile[(size_t)i * bc + col];
+            if (fresh) {
+              slot = kv;
+            } else {
+              const float x = bf2f(kv), o = bf2f(slot);
+              if (ro >= HD ? (x < o) : (x > o)) slot = kv;
+            }
           }
         }
-        __syncthreads();
       }
-      // two adjacent blocks per thread from one 32-bit load per channel
-      for (int jp = tid; 2 * jp < nb_here; jp += NT) {
+      __syncthreads();
+      const uint32_t* tile32 = reinterpret_cast<const uint32_t*>(kttile);
+      const int pitch = bc / 2;
+      for (int jb = 0; jb < nb_here; jb += 128) {      // warp-uniform trip count
+        const int jp = (jb >> 1) + bp;
+        const bool live = 2 * jp < nb_here;
+        const int jpc = live ? jp : 0;
         float s0 = 0.f, s1 = 0.f;
-        const uint32_t* col = reinterpret_cast<const uint32_t*>(kttile) + jp;
-        const int pitch = bc / 2;
-        for (int i = 0; i < k1; ++i) {
-          const uint32_t v = col[(size_t)i * pitch];
+        for (int i = cg; i < k1; i += 4) {
+          const int row = spec ? fs.rowoff[i] : i;
+          const uint32_t v = tile32[(size_t)row * pitch + jpc];
           const float q = fs.qsel[i];
           s0 = fmaf(q, bf16_lo(v), s0);
           s1 = fmaf(q, bf16_hi(v), s1);
         }
-        const int j = 2 * jp;
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
         s0 = (s0 == 0.f) ? 0.f : s0;     // -0 -> +0
         s1 = (s1 == 0.f) ? 0.f : s1;
-        sval[cb0 + j] = s0;
-        smn = fminf(smn, s0);
-        smx = fmaxf(smx, s0);
-        if (j + 1 < nb_here) {
-          sval[cb0 + j + 1] = s1;
+        const int j = cb0 + 2 * jp;
+        const bool v0 = live, v1 = live && 2 * jp + 1 < nb_here;
+        if (v0) {
+          smn = fminf(smn, s0);
+          smx = fmaxf(smx, s0);
+        }
+        if (v1) {
           smn = fminf(smn, s1);
           smx = fmaxf(smx, s1);
         }
+        if (cg < 2 && (cg == 0 ? v0 : v1)) {
+          const float sv = cg == 0 ? s0 : s1;
+          const uint32_t off = 4u * (uint32_t)(j + cg);
+          for (int d = 0; d < ns; ++d) st_async_f32(mapa(sval_local + off, d), sv, mapa(sbar_local, d));
+        }
       }
-      __syncthreads();
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      smn = fminf(smn, __shfl_xor_sync(0xffffffffu, smn, o));
+      smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, o));
+    }
+    if (lane < ns) {
+      const uint32_t off = smem_u32(&fs.rbound[(int)rank * NWARP + warp]);
+      st_async_v2f32(mapa(off, lane), smn, smx, mapa(sbar_local, lane));
+    }
+    if (!mbar_wait(&fs.sbar, 0, &g_hsa_err)) mbar_wait(&fs.sbar, 0, &g_hsa_err);
+    smn = __int_as_float(0x7f800000);
+    smx = neg_inf();
+    for (int i = 0; i < ns * NWARP; ++i) {
+      const float2 r = fs.rbound[i];
+      smn = fminf(smn, r.x);
+      smx = fmaxf(smx, r.y);
     }
   }
 
@@ -454,7 +531,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   if (k2e >= nblk) {
     for (int j = tid; j < nblk; j += NT) flag[j] = 1;
   } else {
-    block_minmax(smn, smx, fs);
     bucket_topk(sval, nblk, k2e, smn, smx, flag, fs);
   }
   __syncthreads();
@@ -695,7 +771,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // Partials go to the owner of each head (head g: CTA g % ns) with st.async,
   // which counts their bytes on the owner's ebar; only owners wait.
   const int gown = (G + ns - 1) / ns;
-  cluster_wait_acquire();      // every CTA of the cluster has started and armed its ebar
   {
     const uint32_t ebar_local = smem_u32(&fs.ebar);
 #pragma unroll
@@ -738,12 +813,22 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = A / L;
     }
   }
+  if (own_new && !spec) {
+    const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
+    const bf16 kv = fs.knew[c];
+    if ((n_old % a.blk) == 0) {
+      *kt_col = kv;
+    } else {
+      const float x = bf2f(kv), o = bf2f(kt_old);
+      if (m == 1 ? (x < o) : (x > o)) *kt_col = kv;
+    }
+  }
   if (rank == 0) {
     if (a.sel_blocks) {
       for (int j = tid; j < a.k2; j += NT) a.sel_blocks[(size_t)pair * a.k2 + j] = j < k2e ? sel[j] : -1;
     }
     if (app) {
-      // persist the appended token: cache row, candidate index (MT) and its KT column
+      // persist the appended token: cache row and candidate index (MT)
       if (tid < 32) {
         bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
                     ((size_t)pair * a.cap + a.row) * HD + (tid & 15) * 8;
@@ -751,16 +836,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
                                                                           (tid & 15) * 8);
       }
       if (MT && tid == 32) a.idx_w[(size_t)pair * a.idx_cap + n_old] = (int32_t)a.row;
-      {
-        const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
-        const bf16 kv = fs.knew[c];
-        if ((n_old % a.blk) == 0) {
-          *kt_col = kv;
-        } else {
-          const float x = bf2f(kv), o = bf2f(kt_old);
-          if (m == 1 ? (x < o) : (x > o)) *kt_col = kv;
-        }
-      }
     }
   }
 }
@@ -789,9 +864,15 @@ bool hsa_plan(HsaArgs& a) {
   a.chunk = (a.k2e + a.ns - 1) / a.ns;
   a.slots_round = std::max(1, std::min(a.chunk, MAX_ROUND_ROWS / a.blk));
   const int nblk8 = (a.nblk + 7) & ~7;
-  int bc = nblk8;
+  // blocks scored per CTA; with at most HSA_SPEC_MAX_COLS of them every KT row of
+  // the CTA's blocks is prefetched at launch, otherwise the chosen rows are
+  // gathered in chunks after the channel choice
+  a.cpr = std::max(8, (((a.nblk + a.ns - 1) / a.ns) + 7) & ~7);
+  a.kt_spec = a.cpr <= HSA_SPEC_MAX_COLS ? 1 : 0;
+  int bc = a.cpr;
   if ((uint32_t)a.k1 * bc * 2u > KT_TILE_BUDGET) bc = std::max(8, (int)(KT_TILE_BUDGET / (2u * a.k1)) & ~7);
   a.kt_chunk = bc;
+  const uint32_t kt_tile_bytes = a.kt_spec ? 2u * HD * a.cpr * 2u : 2u * a.k1 * bc;
   const int gown = (a.G + a.ns - 1) / a.ns;
   auto al = [](uint32_t x, uint32_t q) { return (x + q - 1) / q * q; };
   uint32_t off = al(sizeof(FixedSmem), 128);
@@ -807,13 +888,13 @@ bool hsa_plan(HsaArgs& a) {
   a.off_tiles = off;                       // K/V tiles; the KT gather tile shares this region
   const uint32_t rows16 = al((uint32_t)(a.slots_round * a.blk), 16);
   a.tile_half_bytes = rows16 * 128u;
-  off += std::max(4u * a.tile_half_bytes, al(2u * a.k1 * bc, 16));
+  off += std::max(4u * a.tile_half_bytes, al(kt_tile_bytes, 16));
   a.smem_bytes = off + 1024u;   // room to align the base to 1024 bytes
   return a.smem_bytes <= 227u * 1024u;
 }
 
-cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV, bool mt,
-                       cudaStream_t st) {
+cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmKT,
+                       bool mt, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -841,7 +922,7 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   cfg.numAttrs = 2;
   auto kern = mt ? (a.G > 8 ? hsa_decode_kernel<true, 2> : hsa_decode_kernel<true, 1>)
                  : (a.G > 8 ? hsa_decode_kernel<false, 2> : hsa_decode_kernel<false, 1>);
-  return cudaLaunchKernelEx(&cfg, kern, *tmK, *tmV, a);
+  return cudaLaunchKernelEx(&cfg, kern, *tmK, *tmV, *tmKT, a);
 }
 
 unsigned int hsa_take_device_error() {

@@ -34,6 +34,8 @@ struct HsaArgs {
   int32_t chunk;        // selected blocks per CTA: ceil(k2e / ns)
   int32_t slots_round;  // blocks staged in shared memory per round
   int32_t kt_chunk;     // blocks per shared-memory KT gather (multiple of 8)
+  int32_t cpr;          // blocks scored per CTA of the cluster (multiple of 8); CTA r scores [r*cpr, r*cpr + cpr)
+  int32_t kt_spec;      // 1: each CTA prefetches all 2*D KT rows of its blocks with one TMA box at launch
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared-memory layout (bytes)
   uint32_t off_x, off_scores, off_flags, off_sel, off_recv, off_tiles, tile_half_bytes, smem_bytes;
@@ -42,8 +44,9 @@ struct HsaArgs {
 // Computes ns/chunk/slots_round and the shared-memory layout.  Returns false if
 // the configuration does not fit on the device.
 bool hsa_plan(HsaArgs& a);
-cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV, bool mt,
-                       cudaStream_t st);
+cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmKT,
+                       bool mt, cudaStream_t st);
+constexpr int HSA_SPEC_MAX_COLS = 128;   // KT columns per CTA for the launch-time prefetch (256 rows x 128 x 2 B)
 
 // ------------------------------------------------------------ stage 1 -------
 struct SnapArgs {
