@@ -74,7 +74,6 @@ struct FixedSmem {
   float wsumh[NWARP][16];       // per-warp head probability sums of a round
   uint32_t pfrag[MAX_ROUND_ROWS / 16][2][4][32];   // P^T B fragments per 16-token step, head tile, hi/lo
   float mrun[16], lrun[16];
-  int32_t nvalid[MAX_ROUND_ROWS / 8];
   uint64_t mbar[MAX_ROUND_ROWS / 8];    // one per staged block
   uint64_t ebar;                        // partials of the heads this CTA owns (phase E)
   uint64_t ktbar;                       // KT prefetch (phase B)
@@ -517,12 +516,18 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       st_async_v2f32(mapa(off, lane), smn, smx, mapa(sbar_local, lane));
     }
     if (!mbar_wait(&fs.sbar, 0, &g_hsa_err)) mbar_wait(&fs.sbar, 0, &g_hsa_err);
-    smn = __int_as_float(0x7f800000);
-    smx = neg_inf();
-    for (int i = 0; i < ns * NWARP; ++i) {
-      const float2 r = fs.rbound[i];
-      smn = fminf(smn, r.x);
-      smx = fmaxf(smx, r.y);
+    {
+      // every warp combines the ns * NWARP (<= 64) bounds, two per lane
+      const int nb = ns * NWARP;
+      const float2 r0 = lane < nb ? fs.rbound[lane] : make_float2(__int_as_float(0x7f800000), neg_inf());
+      const float2 r1 = lane + 32 < nb ? fs.rbound[lane + 32] : make_float2(__int_as_float(0x7f800000), neg_inf());
+      smn = fminf(r0.x, r1.x);
+      smx = fmaxf(r0.y, r1.y);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        smn = fminf(smn, __shfl_xor_sync(0xffffffffu, smn, o));
+        smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, o));
+      }
     }
   }
 
@@ -575,11 +580,11 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     const int rows = nsl * blk;
     const int nsteps = (rows + 15) / 16;
     const int rows16 = nsteps * 16;
-    if (tid < nsl) fs.nvalid[tid] = min(blk, n_tot - sel[r0 + tid] * blk);
     if (!MT) {
       {
-        // the copies are spread over all warps: one warp issuing them all serialises them
-        if (lane == 0) fence_proxy_async_smem();   // earlier generic accesses to this region come first
+        // The copies are spread over all warps: one warp issuing them all serialises them.
+        // The region was last read through the generic proxy before a barrier (write
+        // after read), so no proxy fence is needed.
         if (warp == 0)
           for (int s = lane; s < nsl; s += 32) mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * 4u);
         __syncwarp();
@@ -621,7 +626,8 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           make_uint4(0, 0, 0, 0);
     }
     if (MT) cp_async_wait_all();
-    __syncthreads();
+    // cp.async rows and zero rows come from every thread; TMA rows are waited for per slot
+    if (MT || rows16 != rows) __syncthreads();
 
     // --- S^T = K Q^T for the warp's 16-token step, masked and in log2 units
     const int c0 = warp * 16;
@@ -665,8 +671,8 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       // this lane: tokens c0 + lane/4 (e = 0, 1) and + 8 (e = 2, 3); heads 2(lane%4) + (e & 1)
       const int ta = c0 + g4, tb = ta + 8;
       const int sla = ta / blk, slb = tb / blk;
-      const bool va = ta < rows && (ta - sla * blk) < fs.nvalid[min(sla, nsl - 1)];
-      const bool vb = tb < rows && (tb - slb * blk) < fs.nvalid[min(slb, nsl - 1)];
+      const bool va = ta < rows && sel[r0 + sla] * blk + (ta - sla * blk) < n_tot;
+      const bool vb = tb < rows && sel[r0 + slb] * blk + (tb - slb * blk) < n_tot;
 #pragma unroll
       for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
@@ -764,7 +770,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       }
     }
     phase ^= 1u;
-    __syncthreads();   // tiles and fragments are reused by the next round
+    if (r0 + a.slots_round < s_hi) __syncthreads();   // tiles and fragments are reused by the next round
   }
 
   // ---------------------------------------------------------------- E ------
@@ -801,14 +807,29 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     if (g >= G) break;
     const float* rp = recv + (size_t)gl * ns * PART_STRIDE;
     if (tid < HD) {
-      float M = neg_inf();
-      for (int r = 0; r < ns; ++r) M = fmaxf(M, rp[(size_t)r * PART_STRIDE + HD]);
+      // all loads first (ns <= 8), then the rescaled sums in rank order
+      float mr[8], lr[8], vr[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        mr[r] = neg_inf();
+        lr[r] = 0.f;
+        vr[r] = 0.f;
+        if (r < ns) {
+          const float2 ml = *reinterpret_cast<const float2*>(rp + (size_t)r * PART_STRIDE + HD);
+          mr[r] = ml.x;
+          lr[r] = ml.y;
+          vr[r] = rp[(size_t)r * PART_STRIDE + tid];
+        }
+      }
+      float M = mr[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r) M = fmaxf(M, mr[r]);
       float A = 0.f, L = 0.f;
-      for (int r = 0; r < ns; ++r) {
-        const float* pp = rp + (size_t)r * PART_STRIDE;
-        const float f = (pp[HD] == neg_inf()) ? 0.f : exp2f(pp[HD] - M);
-        A = fmaf(f, pp[tid], A);
-        L = fmaf(f, pp[HD + 1], L);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float f = (mr[r] == neg_inf()) ? 0.f : exp2f(mr[r] - M);
+        A = fmaf(f, vr[r], A);
+        L = fmaf(f, lr[r], L);
       }
       a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = A / L;
     }
