@@ -94,15 +94,22 @@ def test_append_matches_rebuild():
 # --------------------------------------------------------------- HSA decode --
 
 
-def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=False, full_rows=None):
+def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=False, full_rows=None,
+              k_scale=1.0, kmod=None, qmod=None):
     D = 128
     G = Hq // Hkv
     dims = (B, Hq, Hkv, D)
     scale = 1 / math.sqrt(D)
     rows = full_rows if mt else n + cap_extra
-    kb, k = _rand(seed, (B, Hkv, rows, D))
+    kb = small_random(seed, (B, Hkv, rows, D), k_scale)
+    if kmod is not None:
+        kb = kmod(kb)
+    k = _bf16(kb)
     vb, v = _rand(seed + 1, (B, Hkv, rows, D))
-    qb, q = _rand(seed + 2, (B, Hq, D), q_scale)
+    qb = small_random(seed + 2, (B, Hq, D), q_scale)
+    if qmod is not None:
+        qb = qmod(qb)
+    q = _bf16(qb)
     kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
     nblk = -(-n // blk)
     ncap = -(-nblk // 8) * 8
@@ -161,6 +168,23 @@ def test_hsa_decode_parity(B, Hq, Hkv, n, blk, k1, k2):
 def test_hsa_decode_peaked_attention():
     # large queries make the softmax nearly one-hot: checks the P hi/lo split
     _hsa_case(7, 1, 32, 8, 700, 16, 32, 8, q_scale=6.0)
+
+
+def test_hsa_decode_all_ties():
+    # q = 0: every channel sum and every block score ties, so both selections fall
+    # back to the radix path and take the lowest indices; attention is uniform
+    _hsa_case(11, 1, 32, 8, 900, 16, 32, 12, qmod=np.zeros_like)
+
+
+def test_hsa_decode_crowded_boundary_bucket():
+    # block 0 holds huge keys and every other block tiny ones: all but one score
+    # share a histogram bucket (more members than the pairwise ranking takes),
+    # which sends the block selection to the radix path
+    def kmod(kb):
+        kb = kb.copy()
+        kb[:, :, :16, :] = 0x42C8            # bf16 100.0
+        return kb
+    _hsa_case(12, 1, 32, 8, 700 * 16, 16, 32, 50, k_scale=1e-3, kmod=kmod)
 
 
 @pytest.mark.parametrize("n,blk,k2", [(250, 16, 6), (97, 8, 20), (600, 32, 4)])
