@@ -452,6 +452,209 @@ __global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled
   }
 }
 
+// Fused pool + select for prompts whose prefix fits one CTA: the row-group
+// sums of one pair go to shared memory once, each thread max-pools E = h + 1
+// consecutive positions (window 2h + 1) from a van Herk split of the window
+// around its own range, the order-preserving keys replace the scores in
+// place, and the radix select plus the ascending write-out run on shared
+// memory.  Same result as snap_pool + snap_select.
+constexpr int PS_NT = 1024;
+constexpr int PS_MAX_WORDS = 54 * 1024;        // padded shared words (216 KB)
+
+__device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }   // one pad word per 32: no bank conflicts
+
+// shared words needed for prefix length L and half window h (0 if the fused path does not apply)
+int pool_select_words(int64_t L, int h) {
+  const int E = h + 1;
+  if (L <= 0 || E > 32) return 0;
+  const int64_t nq = (L + E - 1) / E;
+  if (nq > PS_NT) return 0;
+  const int64_t U = nq * E + 2 * E;
+  const int64_t words = U + U / 32 + 1;
+  return words <= PS_MAX_WORDS ? (int)words : 0;
+}
+
+__global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float* scores, int RG, int64_t L64,
+                                                                    int h, int64_t S, int W, int n_sink,
+                                                                    int64_t ntop, int64_t B1, int32_t* keep,
+                                                                    int64_t keep_ld, float* pooled_out) {
+  extern __shared__ __align__(16) uint32_t xs[];
+  __shared__ int hist[256];
+  __shared__ int wsum[PS_NT / 32];
+  __shared__ uint32_t sh_digit;
+  __shared__ int sh_k;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int pair = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int L = (int)L64;
+  const int E = h + 1;
+  const int nq = (L + E - 1) / E;
+  const int U = nq * E + 2 * E;
+  int32_t* out = keep + (size_t)pair * keep_ld;
+  for (int i = tid; i < n_sink; i += PS_NT) out[i] = i;
+  for (int i = tid; i < W; i += PS_NT) out[B1 - W + i] = (int32_t)(S - W + i);
+
+  // scores of position j = u - h at u (minus infinity outside [0, L))
+  const float* sc = scores + (size_t)pair * RG * L;
+  for (int u0 = tid; u0 < U; u0 += 8 * PS_NT) {
+    float v[8];                                  // eight independent loads in flight per thread
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int j = u0 + t * PS_NT - h;
+      v[t] = (j >= 0 && j < L) ? __ldg(sc + j) : neg_inf();
+    }
+    for (int r = 1; r < RG; ++r) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int j = u0 + t * PS_NT - h;
+        if (j >= 0 && j < L) v[t] += __ldg(sc + (size_t)r * L + j);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int u = u0 + t * PS_NT;
+      if (u < U) xs[ps_pad(u)] = __float_as_uint(v[t]);
+    }
+  }
+  __syncthreads();
+
+  // max-pool of outputs [a, a + E): the window of output a + i is u in [a+i, a+i+2h];
+  // [a+E-1, a+2E-2] is common to all of them, the rest is a suffix of
+  // [a, a+E-2] and a prefix of [a+2E-1, a+3E-3]
+  float pv[32];
+  const int a = tid * E;
+  const bool mine = tid < nq;
+  if (mine) {
+    auto X = [&](int u) { return __uint_as_float(xs[ps_pad(u)]); };
+    float m = neg_inf();
+    for (int i = 0; i < E; ++i) m = fmaxf(m, X(a + E - 1 + i));
+    float r = neg_inf();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < E) {
+        pv[i] = r;
+        r = fmaxf(r, X(a + 2 * E - 1 + i));
+      }
+    }
+    float l = neg_inf();
+#pragma unroll
+    for (int i = 31; i >= 0; --i) {
+      if (i < E) {
+        pv[i] = fmax3(pv[i], l, m);
+        if (i > 0) l = fmaxf(l, X(a + i - 1));
+      }
+    }
+    if (pooled_out) {
+      float* po = pooled_out + (size_t)pair * L;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < E && a + i < L) po[a + i] = pv[i];
+    }
+  }
+  __syncthreads();
+  // keys of the candidates [n_sink, L) replace the scores; 0 elsewhere
+  if (mine) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < E) {
+        const int j = a + i;
+        xs[ps_pad(j)] = (j >= n_sink && j < L) ? f2key(pv[i]) : 0u;
+      }
+    }
+  }
+  const int ncand = L - n_sink;
+  if (ntop >= ncand) {
+    for (int j = n_sink + tid; j < L; j += PS_NT) out[j] = j;
+    return;
+  }
+  __syncthreads();
+
+  // radix select of the ntop-th largest key, 8 bits at a time from the top
+  uint32_t prefix = 0, mask = 0;
+  int k = (int)ntop;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    for (int j = n_sink + tid; j - tid < L; j += PS_NT) {
+      const bool in = j < L;
+      const uint32_t key = in ? xs[ps_pad(j)] : 0u;
+      const bool act = in && (key & mask) == prefix;
+      const unsigned am = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const unsigned d = (key >> shift) & 255u;
+        const unsigned mm = __match_any_sync(am, d);
+        if (lane == __ffs(mm) - 1) atomicAdd(&hist[d], __popc(mm));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int c[8];
+      int sum = 0;
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        c[u] = hist[lane * 8 + u];
+        sum += c[u];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      int above = incl - sum;
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        if (above < k && above + c[u] >= k) {
+          sh_digit = (uint32_t)(lane * 8 + u);
+          sh_k = k - above;
+        }
+        above += c[u];
+      }
+    }
+    __syncthreads();
+    prefix |= sh_digit << shift;
+    mask |= 255u << shift;
+    k = sh_k;
+  }
+  // keys > T are taken, and the first k keys equal to T in index order
+  const uint32_t T = prefix;
+  uint32_t gt = 0, eq = 0;
+  if (mine) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < E) {
+        const int j = a + i;
+        if (j >= n_sink && j < L) {
+          const uint32_t key = xs[ps_pad(j)];
+          gt |= (uint32_t)(key > T) << i;
+          eq |= (uint32_t)(key == T) << i;
+        }
+      }
+    }
+  }
+  // exclusive prefix over threads of (count > T, count == T), packed 16 + 16 bits
+  const uint32_t packed = (uint32_t)__popc(gt) | ((uint32_t)__popc(eq) << 16);   // each total <= 32768
+  uint32_t incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[warp] = (int)incl;
+  __syncthreads();
+  uint32_t before = incl - packed;
+  for (int w = 0; w < warp; ++w) before += (uint32_t)wsum[w];
+  const int gt_before = (int)(before & 0xffffu), eq_before = (int)(before >> 16);
+  int pos = n_sink + gt_before + min(k, eq_before);
+  int eq_seen = eq_before;
+  for (uint32_t bits = gt | eq; bits; bits &= bits - 1u) {
+    const int i = __ffs(bits) - 1;
+    const bool is_eq = (eq >> i) & 1;
+    if (!is_eq || eq_seen < k) out[pos++] = a + i;
+    if (is_eq) ++eq_seen;
+  }
+}
+
 // K_c[i] = K[keep[i]], V_c[i] = V[keep[i]].
 __global__ void __launch_bounds__(256) snap_compact_kernel(const bf16* k, const bf16* v, int64_t cap,
                                                            const int32_t* keep, int64_t keep_ld, int64_t B1,
@@ -491,11 +694,13 @@ int snap_pass2_rows(int32_t G, int32_t W) { return std::min(P2_ROWS, (G * W + 31
 cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmQ1, const CUtensorMap* tmQ2,
                         cudaStream_t st) {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
+  static cudaError_t attr_err = cudaSuccess, ps_attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+    ps_attr_err = cudaFuncSetAttribute(snap_pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PS_MAX_WORDS * 4);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int pairs = a.B * a.Hkv;
@@ -529,14 +734,23 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     const int nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
     e = launch_pdl(snap_pass_kernel<2>, dim3(nchunk2, p.RG2, pairs), dim3(T_NT), T_SMEM, st, *tmK, *tmQ2, p);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
-                   (const float*)p.scores, (int)p.RG2, (int64_t)L, (int)(a.pool / 2), pooled);
-    if (e != cudaSuccess) return e;
     const int n_sink = (int)std::max<int64_t>(0, std::min<int64_t>(a.n_sink, L));
     const int64_t ntop = std::max<int64_t>(0, a.B1 - W - n_sink);
-    e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)pooled, (int64_t)L,
-                   (int64_t)a.S, (int)W, (int)n_sink, (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
-    if (e != cudaSuccess) return e;
+    const int half = (int)(a.pool / 2);
+    const int ps_words = pool_select_words(L, half);
+    if (ps_words > 0 && ps_attr_err == cudaSuccess) {
+      e = launch_pdl(snap_pool_select_kernel, dim3(pairs), dim3(PS_NT), (size_t)ps_words * 4u, st,
+                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, (int64_t)a.S, (int)W, (int)n_sink,
+                     (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.pooled_out);
+      if (e != cudaSuccess) return e;
+    } else {
+      e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
+                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, pooled);
+      if (e != cudaSuccess) return e;
+      e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)pooled, (int64_t)L,
+                     (int64_t)a.S, (int)W, (int)n_sink, (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
+      if (e != cudaSuccess) return e;
+    }
   } else {
     // every token kept: keep = 0..S-1 (B1 == S enforced by the caller)
     cudaError_t e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)nullptr, (int64_t)0,
