@@ -65,7 +65,7 @@ def peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ["rkv_hsa.cu", "rkv_common.cuh"]:
+    for f in ["rkv_hsa.cu", "rkv_common.cuh", "rkv_internal.h", "rkv_api.cu"]:
         with open(os.path.join(ROOT, "two_stage_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
