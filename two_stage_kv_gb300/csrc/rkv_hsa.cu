@@ -9,14 +9,18 @@
 // RocketKV-MT for the candidate-restricted variant.
 //
 // GB300 design.  One thread-block cluster of `ns` CTAs (256 threads each) per
-// (batch row, KV head), ns chosen so the grid fits in one wave.  Every CTA:
+// (batch row, KV head), ns chosen so the grid fits in one wave.  CTA r:
+//   0. at launch prefetches, with one 2-D TMA box, every KT row (Kmax and Kmin
+//      of all 128 channels) of its share of the blocks, [r*cpr, r*cpr + cpr);
+//      the KT rows do not depend on the query, so the load overlaps step A
+//      (shares wider than 128 blocks gather the chosen rows in step B instead);
 //   A. loads the group's G query rows and forms sum|q| and sum q per channel in
 //      fp32 with an error-free TwoSum check (an inexact sum sends the whole CTA
 //      to an fp64 path, so the channel decision is the exact-arithmetic one),
 //      then picks the top-k1 channels;
-//   B. gathers the k1 chosen rows of the channel-major KT cache into shared
-//      memory with 16-byte cp.async, folds the appended key into its block,
-//      and scores every block in fp32;
+//   B. folds the appended key into its block, scores its own blocks in fp32
+//      and sends every score, and each warp's score bounds, to every CTA of
+//      the cluster with st.async, counted on the receivers' mbarriers;
 //   C. picks the top-k2 blocks and lists them in ascending order (every CTA of
 //      the cluster computes the same list);
 //   D. TMA-loads the K and V rows of its share of the blocks into 128-byte-
@@ -25,15 +29,15 @@
 //      on the M side, G <= 8 heads per 8-wide N tile), a CTA-wide softmax in
 //      fp32, and O^T = V^T P^T with each warp owning 16 output dimensions (P
 //      is split into bf16 hi + lo, so PV keeps ~16 mantissa bits);
-//   E. sends its partial (max, sum, O) for each head over distributed shared
-//      memory to the CTA that owns the head; after one cluster barrier the
-//      owner combines the ns partials and writes fp32 outputs.
+//   E. sends its partial (max, sum, O) for each head with st.async to the CTA
+//      that owns the head, whose mbarrier counts the bytes; the owner combines
+//      the ns partials and writes fp32 outputs.
 // Both top-k steps are exact (larger first, equal values: lower index): a
 // 256-bucket histogram over [min, max] finds the bucket holding the k-th value
 // and only that bucket's members are ranked pairwise; a radix select on an
 // order-preserving key takes over for degenerate value sets.  No global
-// scratch, no atomics on the data path and no spin on other CTAs: the only
-// cross-CTA waits are hardware cluster barriers.
+// scratch and no atomics on the data path; the cross-CTA waits are one
+// hardware cluster barrier at launch and bounded mbarrier waits.
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 

@@ -17,9 +17,11 @@
 //   snap_select   exact top-k of the pooled scores (radix select on an
 //                 order-preserving key, equal keys: lower index first) written
 //                 in ascending index order, plus sinks and the window;
+//   snap_pool_select  the two above fused in one CTA per pair when the prefix
+//                 fits shared memory (up to 1024 x 32 positions);
 //   snap_compact  gather of the kept K and V rows (skipped in MT mask mode).
 // The two score passes stream K with 3-D TMA tiles (128-byte swizzle) through
-// a 4-stage mbarrier ring and run Q K^T on bf16 mma.sync with fp32 accumulation.
+// a 3-stage mbarrier ring and run the contraction on tcgen05.mma into TMEM.
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 
