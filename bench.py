@@ -332,6 +332,8 @@ import oracle
 from two_stage_kv_gb300 import synth
 wl = synth.WORKLOADS[{wl!r}]
 budget_s = {budget_s}
+start = {start}
+max_pairs = {max_pairs}
 f = synth.bf16_bits_to_f64
 qd = synth.q_decode(wl)
 kn, vn = synth.kv_new(wl)
@@ -342,8 +344,9 @@ G = wl.G
 done = 0
 t_total = 0.0
 pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
-while t_total < budget_s and done < len(pairs):
-    b, h = pairs[done]
+limit = min(len(pairs), max_pairs)
+while done < limit and (done == 0 or t_total < budget_s):
+    b, h = pairs[(start + done) % len(pairs)]
     kb, vb = synth.kv_slice(wl, 0, b, h, qd)
     K, V = f(kb), f(vb)
     t0 = time.perf_counter()
@@ -363,12 +366,14 @@ print(json.dumps({{"pairs": done, "total_pairs": len(pairs), "seconds": t_total}
 """
 
 
-def oracle_sample(budget_s: float):
-    """Times the oracle (1 thread) on whole (batch, KV head) pairs of one pass."""
+def oracle_sample(budget_s: float, start: int = 0, max_pairs: int = 1 << 30):
+    """Times the oracle (1 thread) on whole (batch, KV head) pairs of one pass: at
+    least one pair, then more while the budget lasts (at most max_pairs),
+    starting from pair `start`."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
-    code = _ORACLE_SAMPLE.format(root=ROOT, wl=WORKLOAD, budget_s=budget_s)
+    code = _ORACLE_SAMPLE.format(root=ROOT, wl=WORKLOAD, budget_s=budget_s, start=start, max_pairs=max_pairs)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
@@ -394,7 +399,7 @@ def run_reference(args):
     steps_run, secs, pairs = 0, 0.0, 0
     tbox = 150.0
     for i in range(args.warmup + args.steps):
-        value, d, pass_s = oracle_sample(0.0)     # exactly one pair per step
+        value, d, pass_s = oracle_sample(0.0, start=i, max_pairs=1)     # exactly one pair per step
         if i >= args.warmup:
             steps_run += 1
             secs += d["seconds"]
