@@ -259,20 +259,43 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
         if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + chunk] = make_float2(mn, ls);
       }
     } else {
-      // negated log2-domain normaliser of every query row of this CTA (rows past R: -inf -> weight 0)
-      for (int i = etid; i < nq; i += 256) {
+      // negated log2-domain normaliser of every query row of this CTA (rows past R:
+      // -inf -> weight 0), combined from pass 1's per-chunk (max, sum); tpr adjacent
+      // threads share a row and load its chunk statistics eight at a time
+      {
+        const int tpr = 256 / nq;                      // nq is a multiple of 32: 1, 2, 4 or 8
+        const int i = etid / tpr, p = etid - i * tpr;
         const int r = row0 + i;
-        float lse = __int_as_float(0x7f800000);
+        float M = neg_inf(), Ls = 0.f;
         if (r < a.R) {
           const float2* st = a.stats + ((size_t)pair * a.R + r) * a.nchunk1;
-          float M = neg_inf();
-          for (int c = 0; c < a.nchunk1; ++c) M = fmaxf(M, st[c].x);
-          float Ls = 0.f;
-          for (int c = 0; c < a.nchunk1; ++c)
-            if (st[c].x != neg_inf()) Ls += st[c].y * exp2f(st[c].x - M);
-          lse = M + log2f(Ls);
+          for (int c0 = p; c0 < a.nchunk1; c0 += 8 * tpr) {
+            float2 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int c = c0 + u * tpr;
+              v[u] = c < a.nchunk1 ? st[c] : make_float2(neg_inf(), 0.f);
+            }
+            float mb = M;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mb = fmaxf(mb, v[u].x);
+            if (mb != neg_inf()) {
+              Ls = (M == neg_inf()) ? 0.f : Ls * exp2f(M - mb);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                if (v[u].x != neg_inf()) Ls += v[u].y * exp2f(v[u].x - mb);
+              M = mb;
+            }
+          }
         }
-        ts.nlse[i] = -lse;
+        for (int o = 1; o < tpr; o <<= 1) {
+          const float Mo = __shfl_xor_sync(0xffffffffu, M, o), Lo = __shfl_xor_sync(0xffffffffu, Ls, o);
+          const float Mn = fmaxf(M, Mo);
+          if (Mn != neg_inf())
+            Ls = ((M == neg_inf()) ? 0.f : Ls * exp2f(M - Mn)) + ((Mo == neg_inf()) ? 0.f : Lo * exp2f(Mo - Mn));
+          M = Mn;
+        }
+        if (p == 0) ts.nlse[i] = (r < a.R) ? -(M + log2f(Ls)) : neg_inf();
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
       for (int t = eset; t < ntiles; t += 2) {
