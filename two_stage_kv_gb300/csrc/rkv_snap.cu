@@ -51,11 +51,11 @@ constexpr int P1_ROWS = 128;                      // query rows per pass-1 CTA (
 constexpr int P2_ROWS = 256;                      // query rows per pass-2 CTA (MMA N, max)
 constexpr uint32_t T_KTILE = T_KEYS * 256;        // 32 KB: two 16 KB k-blocks
 constexpr uint32_t T_QMAX = P2_ROWS * 256;        // 64 KB
-constexpr uint32_t T_SMEM = 1024 + T_QMAX + T_NST * T_KTILE + 1024 + 1024;
 
 struct PassArgs {
   int64_t S, L;                    // L = S - W prefix keys
   int32_t Hq, Hkv, G, W, R, RG1, RG2, nchunk1, nq2;
+  int32_t pairs, nchunk2;
   float scale_log2;
   float2* stats;                   // [pairs][R][nchunk1]
   float* scores;                   // [pairs][RG2][L]
@@ -64,12 +64,14 @@ struct PassArgs {
 struct TcSmem {                    // lives after the operand tiles
   uint64_t full[T_NST], empty[T_NST];
   uint64_t tfull[2], tempty[2];
-  uint64_t qbar;
+  uint64_t qbar, qfree;            // Q tile loaded / no longer read by the MMAs
   uint32_t tmem_base;
   int32_t abort_flag;
   __align__(16) float nlse[P2_ROWS];   // pass 2: -log2(sum) of every query row
   float2 part[128];                // pass 1: (max, sum) of the second epilogue set, per row
 };
+// 1024 bytes of slack to align the base, the operand tiles, then the barriers and row data
+constexpr uint32_t T_SMEM = 1024 + T_QMAX + T_NST * T_KTILE + (uint32_t)((sizeof(TcSmem) + 127) / 128 * 128);
 
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
                                         unsigned int* err) {
@@ -77,6 +79,42 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   if (mbar_wait(bar, parity, err)) return true;
   *abort_flag = 1;
   return false;
+}
+
+// OR of p over the 256 epilogue threads (named barrier 1), the same in every one.
+__device__ __forceinline__ bool epi_any(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
+
+// One work item = (pair, row group, key chunk of P_CHUNK keys).  The grid is
+// persistent: CTA c takes the contiguous items [c*n/grid, (c+1)*n/grid), so
+// the K stream, the MMAs and the epilogue run across item boundaries without
+// draining; the Q tile is reloaded only when (pair, row group) changes.
+struct PassItem {
+  int pair, rg, chunk, ntiles;
+  int64_t j0;
+};
+template <int PASS>
+__device__ __forceinline__ PassItem pass_item(const PassArgs& a, int item) {
+  const int nchunk = PASS == 1 ? a.nchunk1 : a.nchunk2;
+  const int RGp = PASS == 1 ? a.RG1 : a.RG2;
+  PassItem it;
+  it.chunk = item % nchunk;
+  const int t2 = item / nchunk;
+  it.rg = t2 % RGp;
+  it.pair = t2 / RGp;
+  const int64_t kend = (PASS == 1) ? a.S : a.L;
+  it.j0 = (int64_t)it.chunk * P_CHUNK;
+  const int64_t j1 = min(kend, it.j0 + (int64_t)P_CHUNK);
+  it.ntiles = (int)((j1 - it.j0 + T_KEYS - 1) / T_KEYS);
+  return it;
 }
 
 template <int PASS>
@@ -90,17 +128,12 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
   TcSmem& ts = *reinterpret_cast<TcSmem*>(smem + T_QMAX + T_NST * T_KTILE);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int pair = blockIdx.z, rg = blockIdx.y, chunk = blockIdx.x;
-  const int b = pair / a.Hkv, hk = pair % a.Hkv;
-  const int row0 = rg * (PASS == 1 ? P1_ROWS : P2_ROWS);                 // first query row of this CTA
   const int nq = PASS == 1 ? P1_ROWS : a.nq2;          // MMA M (pass 1) / N (pass 2) query rows
   const int ncols = PASS == 1 ? T_KEYS : nq;                            // accumulator columns per buffer
   const uint32_t tcols = PASS == 1 ? 256u : (nq <= 64 ? 128u : (nq <= 128 ? 256u : 512u));
-  const int64_t kend = (PASS == 1) ? a.S : a.L;
-  const int64_t j0 = (int64_t)chunk * P_CHUNK;
-  const int64_t j1 = min(kend, j0 + (int64_t)P_CHUNK);
-  const int ntiles = (int)((j1 - j0 + T_KEYS - 1) / T_KEYS);
-  const int qrow_base = (b * a.Hq + hk * a.G) * a.W + row0;             // row in the 2-D q_obs map
+  const int nitems = a.pairs * (PASS == 1 ? a.RG1 * a.nchunk1 : a.RG2 * a.nchunk2);
+  const int ib = (int)((int64_t)blockIdx.x * nitems / gridDim.x);
+  const int ie = (int)((int64_t)(blockIdx.x + 1) * nitems / gridDim.x);
   unsigned int* err = &g_snap_err;
   volatile int32_t* abort_flag = &ts.abort_flag;
 
@@ -116,6 +149,7 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
       mbar_init(&ts.tempty[i], 128);
     }
     mbar_init(&ts.qbar, 1);
+    mbar_init(&ts.qfree, 1);
     ts.abort_flag = 0;
     fence_mbar_init();
   }
@@ -133,202 +167,246 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
-      mbar_arrive_expect_tx(&ts.qbar, (uint32_t)nq * 256u);
-      for (int h = 0; h < 2; ++h)
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-            "[%4];" ::"r"(smem_u32(sQ + h * nq * 128)),
-            "l"(reinterpret_cast<uint64_t>(&tmQ)), "r"(h * 64), "r"(qrow_base), "r"(smem_u32(&ts.qbar))
-            : "memory");
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % T_NST;
-        if (t >= T_NST && !tc_wait(&ts.empty[s], ((t / T_NST) & 1) ^ 1, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&ts.full[s], T_KTILE);
-        const int y = (int)(j0 + (int64_t)t * T_KEYS);
-        tma_load_3d(sK + s * T_KTILE, &tmK, 0, y, pair, &ts.full[s]);
-        tma_load_3d(sK + s * T_KTILE + T_KTILE / 2, &tmK, 64, y, pair, &ts.full[s]);
+      int T = 0, nload = 0, key = -1;
+      for (int item = ib; item < ie && !*abort_flag; ++item) {
+        const PassItem it = pass_item<PASS>(a, item);
+        const int k = it.pair * (PASS == 1 ? a.RG1 : a.RG2) + it.rg;
+        if (k != key) {
+          // the MMAs of the previous Q tile have completed before it is overwritten
+          if (nload > 0 && !tc_wait(&ts.qfree, (nload - 1) & 1, abort_flag, err)) break;
+          const int b = it.pair / a.Hkv, hk = it.pair % a.Hkv;
+          const int qrow = (b * a.Hq + hk * a.G) * a.W + it.rg * (PASS == 1 ? P1_ROWS : P2_ROWS);
+          mbar_arrive_expect_tx(&ts.qbar, (uint32_t)nq * 256u);
+          for (int h = 0; h < 2; ++h)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                "%3}], [%4];" ::"r"(smem_u32(sQ + h * nq * 128)),
+                "l"(reinterpret_cast<uint64_t>(&tmQ)), "r"(h * 64), "r"(qrow), "r"(smem_u32(&ts.qbar))
+                : "memory");
+          ++nload;
+          key = k;
+        }
+        for (int t = 0; t < it.ntiles; ++t, ++T) {
+          const int s = T % T_NST;
+          if (T >= T_NST && !tc_wait(&ts.empty[s], ((T / T_NST) & 1) ^ 1, abort_flag, err)) break;
+          mbar_arrive_expect_tx(&ts.full[s], T_KTILE);
+          const int y = (int)(it.j0 + (int64_t)t * T_KEYS);
+          tma_load_3d(sK + s * T_KTILE, &tmK, 0, y, it.pair, &ts.full[s]);
+          tma_load_3d(sK + s * T_KTILE + T_KTILE / 2, &tmK, 64, y, it.pair, &ts.full[s]);
+        }
       }
       // every load issued has landed before the CTA can leave (bounded)
-      for (int t = max(0, ntiles - T_NST); t < ntiles; ++t) mbar_wait(&ts.full[t % T_NST], (t / T_NST) & 1, err);
+      for (int t = max(0, T - T_NST); t < T; ++t) mbar_wait(&ts.full[t % T_NST], (t / T_NST) & 1, err);
+      if (nload > 0) mbar_wait(&ts.qbar, (nload - 1) & 1, err);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA --
-    if (lane == 0 && tc_wait(&ts.qbar, 0, abort_flag, err)) {
+    if (lane == 0) {
       const uint32_t idesc = PASS == 1 ? idesc_bf16_f32(128, T_KEYS) : idesc_bf16_f32(128, nq);
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % T_NST, buf = t & 1;
-        if (!tc_wait(&ts.full[s], (t / T_NST) & 1, abort_flag, err)) break;
-        if (t >= 2 && !tc_wait(&ts.tempty[buf], ((t >> 1) & 1) ^ 1, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t kt = smem_u32(sK + s * T_KTILE), qt = smem_u32(sQ);
-        const uint32_t d = tbase + (uint32_t)(buf * ncols);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int kb = k >> 2, kk = k & 3;
-          const uint64_t kdesc = sdesc_k_sw128(kt + kb * (T_KTILE / 2) + kk * 32);
-          const uint64_t qdesc = sdesc_k_sw128(qt + kb * nq * 128 + kk * 32);
-          if (PASS == 1)
-            tc_mma_bf16(d, qdesc, kdesc, idesc, k > 0);
-          else
-            tc_mma_bf16(d, kdesc, qdesc, idesc, k > 0);
+      int T = 0, nload = 0, key = -1;
+      bool ok = true;
+      for (int item = ib; item < ie && ok; ++item) {
+        const PassItem it = pass_item<PASS>(a, item);
+        const int k = it.pair * (PASS == 1 ? a.RG1 : a.RG2) + it.rg;
+        if (k != key) {
+          if (nload > 0) tc_commit(&ts.qfree);        // arrives once every MMA issued so far is done
+          if (!tc_wait(&ts.qbar, nload & 1, abort_flag, err)) break;
+          ++nload;
+          key = k;
         }
-        tc_commit(&ts.empty[s]);
-        tc_commit(&ts.tfull[buf]);
+        for (int t = 0; t < it.ntiles; ++t, ++T) {
+          const int s = T % T_NST, buf = T & 1;
+          if (!tc_wait(&ts.full[s], (T / T_NST) & 1, abort_flag, err)) { ok = false; break; }
+          if (T >= 2 && !tc_wait(&ts.tempty[buf], ((T >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kt = smem_u32(sK + s * T_KTILE), qt = smem_u32(sQ);
+          const uint32_t d = tbase + (uint32_t)(buf * ncols);
+#pragma unroll
+          for (int kk8 = 0; kk8 < 8; ++kk8) {
+            const int kb = kk8 >> 2, kk = kk8 & 3;
+            const uint64_t kdesc = sdesc_k_sw128(kt + kb * (T_KTILE / 2) + kk * 32);
+            const uint64_t qdesc = sdesc_k_sw128(qt + kb * nq * 128 + kk * 32);
+            if (PASS == 1)
+              tc_mma_bf16(d, qdesc, kdesc, idesc, kk8 > 0);
+            else
+              tc_mma_bf16(d, kdesc, qdesc, idesc, kk8 > 0);
+          }
+          tc_commit(&ts.empty[s]);
+          tc_commit(&ts.tfull[buf]);
+        }
       }
     }
   } else {
     // ----------------------------------------------------------- epilogue --
-    // Two sets of four warps; set e drains TMEM buffer e, i.e. tiles t with t % 2 == e.
+    // Two sets of four warps; set e drains TMEM buffer e, i.e. the tiles T of the
+    // CTA's stream with T % 2 == e.
     const int eset = (warp - 2) >> 2;                // 0 or 1
     const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
     const int r_loc = 32 * quad + lane;              // TMEM lane of this thread
     const int etid = (warp - 2) * 32 + lane;         // 0 .. 255 over both sets
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16) + (uint32_t)(eset * ncols);
-    const int S32 = (int)a.S, L32 = (int)a.L, j032 = (int)j0;
-    if (PASS == 1) {
-      const int r = row0 + r_loc;                    // query row in the group
-      const bool rvalid = r < a.R;
-      const int lim = S32 - a.W + (rvalid ? (r % a.W) : 0);     // last key this row attends
-      float m = neg_inf(), l = 0.f;
-      for (int t = eset; t < ntiles; t += 2) {
-        if (!tc_wait(&ts.tfull[eset], (t >> 1) & 1, abort_flag, err)) break;
-        tc_fence_after();
-        float v[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + 32 * c, v[c]);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&ts.tempty[eset]);
-        const int jt = j032 + t * T_KEYS;
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float mn;
-        if (jt + T_KEYS <= S32 - a.W) {
-          // every row attends every key of the tile: the maximum of the raw
-          // logits scales to the maximum of the scaled ones (scale > 0)
-          float x0 = v[0][0], x1 = v[1][0], x2 = v[2][0], x3 = v[3][0];
-#pragma unroll
-          for (int i = 1; i < 31; i += 2) {
-            x0 = fmax3(x0, v[0][i], v[0][i + 1]);
-            x1 = fmax3(x1, v[1][i], v[1][i + 1]);
-            x2 = fmax3(x2, v[2][i], v[2][i + 1]);
-            x3 = fmax3(x3, v[3][i], v[3][i + 1]);
-          }
-          x0 = fmax3(x0, x1, v[0][31]);
-          x2 = fmax3(x2, x3, v[1][31]);
-          x0 = fmax3(x0, x2, fmaxf(v[2][31], v[3][31]));
-          mn = fmaxf(m, x0 * a.scale_log2);
-          const float2 sc = make_float2(a.scale_log2, a.scale_log2), nm = make_float2(-mn, -mn);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 x = fma_f2(make_float2(v[c][i], v[c][i + 1]), sc, nm);
-              acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3], make_float2(ex2_ftz(x.x), ex2_ftz(x.y)));
-            }
-        } else {
-          const int jmax = min(S32 - 1, lim) - jt;    // last attended column of this tile
-          float tm = neg_inf();
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float x = (32 * c + i <= jmax) ? v[c][i] * a.scale_log2 : neg_inf();
-              v[c][i] = x;
-              tm = fmaxf(tm, x);
-            }
-          mn = fmaxf(m, tm);
-          if (mn != neg_inf()) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; i += 2)
-                acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3],
-                                           make_float2(ex2_ftz(v[c][i] - mn), ex2_ftz(v[c][i + 1] - mn)));
-          }
-        }
-        const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
-        l = (m == neg_inf() ? 0.f : l * ex2_ftz(m - mn)) + (s01.x + s01.y);
-        m = mn;
-      }
-      if (eset == 1) ts.part[r_loc] = make_float2(m, l);
-      asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
-      if (eset == 0) {
-        const float2 o = ts.part[r_loc];
-        const float mn = fmaxf(m, o.x);
-        const float ls = (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (o.x == neg_inf() ? 0.f : o.y * exp2f(o.x - mn));
-        if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + chunk] = make_float2(mn, ls);
-      }
-    } else {
-      // negated log2-domain normaliser of every query row of this CTA (rows past R:
-      // -inf -> weight 0), combined from pass 1's per-chunk (max, sum); tpr adjacent
-      // threads share a row and load its chunk statistics eight at a time
-      {
-        const int tpr = 256 / nq;                      // nq is a multiple of 32: 1, 2, 4 or 8
-        const int i = etid / tpr, p = etid - i * tpr;
-        const int r = row0 + i;
-        float M = neg_inf(), Ls = 0.f;
-        if (r < a.R) {
-          const float2* st = a.stats + ((size_t)pair * a.R + r) * a.nchunk1;
-          for (int c0 = p; c0 < a.nchunk1; c0 += 8 * tpr) {
-            float2 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int c = c0 + u * tpr;
-              v[u] = c < a.nchunk1 ? st[c] : make_float2(neg_inf(), 0.f);
-            }
-            float mb = M;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mb = fmaxf(mb, v[u].x);
-            if (mb != neg_inf()) {
-              Ls = (M == neg_inf()) ? 0.f : Ls * exp2f(M - mb);
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                if (v[u].x != neg_inf()) Ls += v[u].y * exp2f(v[u].x - mb);
-              M = mb;
-            }
-          }
-        }
-        for (int o = 1; o < tpr; o <<= 1) {
-          const float Mo = __shfl_xor_sync(0xffffffffu, M, o), Lo = __shfl_xor_sync(0xffffffffu, Ls, o);
-          const float Mn = fmaxf(M, Mo);
-          if (Mn != neg_inf())
-            Ls = ((M == neg_inf()) ? 0.f : Ls * exp2f(M - Mn)) + ((Mo == neg_inf()) ? 0.f : Lo * exp2f(Mo - Mn));
-          M = Mn;
-        }
-        if (p == 0) ts.nlse[i] = (r < a.R) ? -(M + log2f(Ls)) : neg_inf();
-      }
-      asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
-      for (int t = eset; t < ntiles; t += 2) {
-        if (!tc_wait(&ts.tfull[eset], (t >> 1) & 1, abort_flag, err)) break;
-        tc_fence_after();
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float2 sc = make_float2(a.scale_log2, a.scale_log2);
-        const float4* nl4 = reinterpret_cast<const float4*>(ts.nlse);
-        auto sum32 = [&](const float* v, int c0) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 nl = nl4[(c0 + i) >> 2];   // same address across the warp: broadcast
-            const float2 x0 = fma_f2(make_float2(v[i], v[i + 1]), sc, make_float2(nl.x, nl.y));
-            const float2 x1 = fma_f2(make_float2(v[i + 2], v[i + 3]), sc, make_float2(nl.z, nl.w));
-            acc[(i >> 2) & 3] = add_f2(acc[(i >> 2) & 3], make_float2(ex2_ftz(x0.x), ex2_ftz(x0.y)));
-            acc[((i >> 2) + 2) & 3] = add_f2(acc[((i >> 2) + 2) & 3], make_float2(ex2_ftz(x1.x), ex2_ftz(x1.y)));
-          }
-        };
-        for (int c0 = 0; c0 < nq; c0 += 64) {        // nq is a multiple of 32
-          float v[2][32];
-          const bool two = c0 + 32 < nq;
-          tmem_ld32(lane_addr + c0, v[0]);
-          if (two) tmem_ld32(lane_addr + c0 + 32, v[1]);
+    const int S32 = (int)a.S, L32 = (int)a.L;
+    int T0 = 0, key = -1;                            // first tile of the item in the CTA's stream
+    for (int item = ib; item < ie; ++item) {
+      const PassItem it = pass_item<PASS>(a, item);
+      const int j032 = (int)it.j0;
+      const int pair = it.pair;
+      const int row0 = it.rg * (PASS == 1 ? P1_ROWS : P2_ROWS);
+      const int tfirst = (T0 & 1) == eset ? 0 : 1;   // this set's first tile of the item
+      if (PASS == 1) {
+        const int r = row0 + r_loc;                  // query row in the group
+        const bool rvalid = r < a.R;
+        const int lim = S32 - a.W + (rvalid ? (r % a.W) : 0);     // last key this row attends
+        float m = neg_inf(), l = 0.f;
+        for (int t = tfirst; t < it.ntiles; t += 2) {
+          const int T = T0 + t;
+          if (!tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err)) break;
+          tc_fence_after();
+          // online softmax over the tile's four 32-key chunks; the next chunk's
+          // TMEM load is in flight while one is reduced (64 value registers)
+          const int jt = j032 + t * T_KEYS;
+          const bool full_tile = jt + T_KEYS <= S32 - a.W;   // every row attends every key of the tile
+          const int jmax = min(S32 - 1, lim) - jt;           // last attended column of the tile
+          float va[32], vb[32];
+          tmem_ld32(lane_addr, va);
           tmem_wait_ld();
-          sum32(v[0], c0);
-          if (two) sum32(v[1], c0 + 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float* cur = (c & 1) ? vb : va;
+            if (c < 3) tmem_ld32(lane_addr + 32 * (c + 1), (c & 1) ? va : vb);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            float mn;
+            if (full_tile) {
+              // the maximum of the raw logits scales to the maximum of the scaled ones (scale > 0)
+              float x0 = fmax3(cur[0], cur[1], cur[2]), x1 = fmax3(cur[3], cur[4], cur[5]);
+#pragma unroll
+              for (int i = 6; i < 30; i += 4) {
+                x0 = fmax3(x0, cur[i], cur[i + 1]);
+                x1 = fmax3(x1, cur[i + 2], cur[i + 3]);
+              }
+              x0 = fmax3(x0, x1, fmaxf(cur[30], cur[31]));
+              mn = fmaxf(m, x0 * a.scale_log2);
+              const float2 sc = make_float2(a.scale_log2, a.scale_log2), nm = make_float2(-mn, -mn);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 x = fma_f2(make_float2(cur[i], cur[i + 1]), sc, nm);
+                acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3], make_float2(ex2_ftz(x.x), ex2_ftz(x.y)));
+              }
+            } else {
+              float tm = neg_inf();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float x = (32 * c + i <= jmax) ? cur[i] * a.scale_log2 : neg_inf();
+                cur[i] = x;
+                tm = fmaxf(tm, x);
+              }
+              mn = fmaxf(m, tm);
+              if (mn != neg_inf()) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                  acc[(i >> 1) & 3] =
+                      add_f2(acc[(i >> 1) & 3], make_float2(ex2_ftz(cur[i] - mn), ex2_ftz(cur[i + 1] - mn)));
+              }
+            }
+            const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
+            if (mn != neg_inf()) {
+              l = (m == neg_inf() ? 0.f : l * ex2_ftz(m - mn)) + (s01.x + s01.y);
+              m = mn;
+            }
+            if (c < 3) tmem_wait_ld();
+          }
+          tc_fence_before();
+          mbar_arrive(&ts.tempty[eset]);
         }
-        const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
-        tc_fence_before();
-        mbar_arrive(&ts.tempty[eset]);
-        const int j = j032 + t * T_KEYS + r_loc;
-        if (j < L32) a.scores[((size_t)pair * a.RG2 + rg) * a.L + j] = s01.x + s01.y;
+        if (eset == 1) ts.part[r_loc] = make_float2(m, l);
+        asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+        if (eset == 0) {
+          const float2 o = ts.part[r_loc];
+          const float mn = fmaxf(m, o.x);
+          const float ls =
+              (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (o.x == neg_inf() ? 0.f : o.y * exp2f(o.x - mn));
+          if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + it.chunk] = make_float2(mn, ls);
+        }
+      } else {
+        const int k = pair * a.RG2 + it.rg;
+        if (k != key) {
+          key = k;
+          asm volatile("bar.sync 1, 256;" ::: "memory");   // both sets are done with the old normalisers
+          // negated log2-domain normaliser of every query row (rows past R:
+          // -inf -> weight 0), combined from pass 1's per-chunk (max, sum); tpr
+          // adjacent threads share a row and load its chunk statistics eight at a time
+          const int tpr = 256 / nq;                      // nq is a multiple of 32: 1, 2, 4 or 8
+          const int i = etid / tpr, p = etid - i * tpr;
+          const int r = row0 + i;
+          float M = neg_inf(), Ls = 0.f;
+          if (r < a.R) {
+            const float2* st = a.stats + ((size_t)pair * a.R + r) * a.nchunk1;
+            for (int c0 = p; c0 < a.nchunk1; c0 += 8 * tpr) {
+              float2 v[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int c = c0 + u * tpr;
+                v[u] = c < a.nchunk1 ? st[c] : make_float2(neg_inf(), 0.f);
+              }
+              float mb = M;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) mb = fmaxf(mb, v[u].x);
+              if (mb != neg_inf()) {
+                Ls = (M == neg_inf()) ? 0.f : Ls * exp2f(M - mb);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                  if (v[u].x != neg_inf()) Ls += v[u].y * exp2f(v[u].x - mb);
+                M = mb;
+              }
+            }
+          }
+          for (int o = 1; o < tpr; o <<= 1) {
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, o), Lo = __shfl_xor_sync(0xffffffffu, Ls, o);
+            const float Mn = fmaxf(M, Mo);
+            if (Mn != neg_inf())
+              Ls = ((M == neg_inf()) ? 0.f : Ls * exp2f(M - Mn)) + ((Mo == neg_inf()) ? 0.f : Lo * exp2f(Mo - Mn));
+            M = Mn;
+          }
+          if (p == 0) ts.nlse[i] = (r < a.R) ? -(M + log2f(Ls)) : neg_inf();
+          asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+        }
+        for (int t = tfirst; t < it.ntiles; t += 2) {
+          const int T = T0 + t;
+          if (!tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err)) break;
+          tc_fence_after();
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float2 sc = make_float2(a.scale_log2, a.scale_log2);
+          const float4* nl4 = reinterpret_cast<const float4*>(ts.nlse);
+          auto sum32 = [&](const float* v, int c0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 nl = nl4[(c0 + i) >> 2];   // same address across the warp: broadcast
+              const float2 x0 = fma_f2(make_float2(v[i], v[i + 1]), sc, make_float2(nl.x, nl.y));
+              const float2 x1 = fma_f2(make_float2(v[i + 2], v[i + 3]), sc, make_float2(nl.z, nl.w));
+              acc[(i >> 2) & 3] = add_f2(acc[(i >> 2) & 3], make_float2(ex2_ftz(x0.x), ex2_ftz(x0.y)));
+              acc[((i >> 2) + 2) & 3] = add_f2(acc[((i >> 2) + 2) & 3], make_float2(ex2_ftz(x1.x), ex2_ftz(x1.y)));
+            }
+          };
+          for (int c0 = 0; c0 < nq; c0 += 64) {        // nq is a multiple of 32
+            float v[2][32];
+            const bool two = c0 + 32 < nq;
+            tmem_ld32(lane_addr + c0, v[0]);
+            if (two) tmem_ld32(lane_addr + c0 + 32, v[1]);
+            tmem_wait_ld();
+            sum32(v[0], c0);
+            if (two) sum32(v[1], c0 + 32);
+          }
+          const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
+          tc_fence_before();
+          mbar_arrive(&ts.tempty[eset]);
+          const int j = j032 + t * T_KEYS + r_loc;
+          if (j < L32) a.scores[((size_t)pair * a.RG2 + it.rg) * a.L + j] = s01.x + s01.y;
+        }
       }
+      T0 += it.ntiles;
+      // a barrier per item (part[] is free again) that also agrees on giving up
+      if (epi_any(*abort_flag != 0)) break;
     }
   }
   tc_fence_before();
@@ -701,6 +779,18 @@ __global__ void __launch_bounds__(256) snap_compact_kernel(const bf16* k, const 
 
 size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
+int snap_num_sms() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  });
+  return n;
+}
+
 }  // namespace
 
 size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t W) {
@@ -753,11 +843,15 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     w += al256((size_t)pairs * p.RG2 * L * sizeof(float));
     float* pooled = a.pooled_out ? a.pooled_out : reinterpret_cast<float*>(w);
 
-    cudaError_t e = launch_pdl(snap_pass_kernel<1>, dim3(p.nchunk1, p.RG1, pairs), dim3(T_NT), T_SMEM, st, *tmK,
-                               *tmQ1, p);
+    p.pairs = pairs;
+    p.nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
+    // persistent grids: one CTA per SM (the ring and Q tile fill the shared memory)
+    const int items1 = pairs * p.RG1 * p.nchunk1, items2 = pairs * p.RG2 * p.nchunk2;
+    cudaError_t e = launch_pdl(snap_pass_kernel<1>, dim3((unsigned)std::min(items1, snap_num_sms())), dim3(T_NT),
+                               T_SMEM, st, *tmK, *tmQ1, p);
     if (e != cudaSuccess) return e;
-    const int nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
-    e = launch_pdl(snap_pass_kernel<2>, dim3(nchunk2, p.RG2, pairs), dim3(T_NT), T_SMEM, st, *tmK, *tmQ2, p);
+    e = launch_pdl(snap_pass_kernel<2>, dim3((unsigned)std::min(items2, snap_num_sms())), dim3(T_NT), T_SMEM, st,
+                   *tmK, *tmQ2, p);
     if (e != cudaSuccess) return e;
     const int n_sink = (int)std::max<int64_t>(0, std::min<int64_t>(a.n_sink, L));
     const int64_t ntop = std::max<int64_t>(0, a.B1 - W - n_sink);
