@@ -290,6 +290,7 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
     (1, 32, 8, 4096, 32, 63, 1209, 0),      # the 4K workload's shape
     (2, 32, 8, 5000, 32, 63, 700, 0),       # ragged S
     (1, 64, 8, 3000, 32, 63, 500, 0),       # G * W = 256 rows (two row groups)
+    (2, 128, 8, 2600, 32, 63, 400, 0),      # G * W = 512 rows: both passes reload Q inside a CTA
     (1, 8, 8, 2100, 32, 7, 300, 4),         # G = 1, pool 7, sinks
     (1, 24, 8, 1500, 32, 1, 100, 0),        # G = 3 (96 rows), no pooling
     (1, 32, 8, 200, 32, 63, 200, 0),        # B1 == S: keep all
