@@ -136,6 +136,34 @@ rkv_status rkv_snap_evict_noalloc(rkv_dims d, const void* q_obs, int32_t W, cons
                                   int64_t out_cap, float* pooled_out, void* stream);
 
 /*
+ * Stage-1 compaction with the KT cache built on the way.  [RocketKV digest,
+ * 方法细节: stage 1 permanently drops the evicted tokens; HSA step 1 keeps
+ * per-page elementwise Kmax / Kmin of the keys]
+ * For every (batch b, KV head h) and i < B1:
+ *   k_out[b,h,i] = k[b,h,keep_idx[b,h,i]],  v_out[b,h,i] = v[b,h,keep_idx[b,h,i]];
+ * and for every block j of blk consecutive compacted rows (the last one
+ * partial), over its rows [j*blk, min(B1, (j+1)*blk)):
+ *   kt[b,h,0,c,j] = max k_out[.,c],  kt[b,h,1,c,j] = min k_out[.,c].
+ * Equal to rkv_snap_evict's compaction followed by rkv_build_kt on the
+ * compacted cache (bit for bit), in one pass over the kept rows; run
+ * rkv_snap_evict in mask mode (k_out = v_out = NULL) first to get keep_idx.
+ * Arguments
+ *   k, v       [B, Hkv, cap, D] bf16 prompt caches (16-byte aligned).
+ *   keep_idx   [B, Hkv, keep_ld] int32 rows to keep (entries are clamped into
+ *              [0, cap)); keep_ld >= B1.
+ *   k_out,v_out[B, Hkv, out_cap, D] bf16 compacted caches, B1 <= out_cap;
+ *              must not overlap k, v.
+ *   kt         [B, Hkv, 2, D, nblk_cap] bf16 (16-byte aligned), nblk_cap a
+ *              multiple of 8 and >= ceil(B1 / blk); columns [0, ceil(B1/blk))
+ *              are written.
+ * Errors: RKV_ERR_INVALID_ARG for NULL or misaligned pointers and the size
+ * rules above; RKV_ERR_CUDA if the launch fails.
+ */
+rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
+                          int64_t keep_ld, int64_t B1, void* k_out, void* v_out, int64_t out_cap, int32_t blk, void* kt,
+                          int64_t nblk_cap, void* stream);
+
+/*
  * KT cache build.  [RocketKV digest, 方法细节: HSA step 1 -- tokens grouped
  * into pages along the sequence, elementwise Kmax and Kmin per page stored
  * aligned along the head dimension]

@@ -83,6 +83,11 @@ D4 = (1, 32, 8, 128)
                                 1 << 30, stream=0), 1),
     (lambda: rkv.rkv_snap_evict(D4, 16, 32, 16, 16, 100, 100, 63, 0, 99, 0.1, 16, 99, 16, None, 99, None, 256,
                                 1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt(D4, 16, 16, 100, 16, 50, 50, 16, 16, 50, 16, 16, 6, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt(D4, 16, 16, 100, 16, 50, 50, 16, 16, 40, 16, 16, 8, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt(D4, 8, 16, 100, 16, 50, 50, 16, 16, 50, 16, 16, 8, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt(D4, 16, 16, 100, 16, 50, 50, 16, 16, 50, 16, 16, 0, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt(D4, 16, 16, 100, 16, 40, 50, 16, 16, 50, 16, 16, 8, stream=0), 1),
     (lambda: rkv.rkv_build_kt(D4, 16, 10, 20, None, 0, 16, 16, 4, stream=0), 1),
     (lambda: rkv.rkv_build_kt(D4, 16, 100, 100, None, 0, 16, 16, 6, stream=0), 1),
     (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 11, None, 0, 16, 10, 16, stream=0), 1),
@@ -100,6 +105,7 @@ def test_empty_batch_is_a_no_op(lib):
     d0 = (0, 32, 8, 128)
     rkv.rkv_hsa_decode(d0, None, None, None, 0, 0, None, 0, 16, 8, 4, 0.1, None, stream=0)
     rkv.rkv_build_kt(d0, None, 0, 0, None, 0, 16, None, 0, stream=0)
+    rkv.rkv_compact_kt(d0, None, None, 0, None, 0, 0, None, None, 0, 16, None, 0, stream=0)
     rkv.rkv_append_kv(d0, None, None, None, None, 0, 0, 0, None, 0, None, 0, 16, stream=0)
     rkv.rkv_snap_evict(d0, None, 32, None, None, 0, 0, 63, 0, 0, 0.1, None, 0, None, None, 0, None, None, 0, stream=0)
 

@@ -48,6 +48,39 @@ def test_build_kt_bit_exact(n, blk, cap_extra):
     assert torch.isnan(kt[..., nblk:].float()).all()
 
 
+@pytest.mark.parametrize("B1,blk,cap", [(300, 16, 1000), (1, 16, 50), (1000, 32, 3000), (77, 8, 200),
+                                         (259, 128, 600), (2000, 16, 2100)])
+def test_compact_kt_bit_exact(B1, blk, cap):
+    """Compaction with the KT cache built on the way equals the oracle's gather of
+    the kept rows and its Kmax / Kmin of the compacted keys, bit for bit, and
+    writes nothing past B1 rows or ceil(B1 / blk) KT columns."""
+    B, Hq, Hkv, D = 2, 8, 2, 128
+    kb, k = _rand(21 + B1, (B, Hkv, cap, D))
+    vb, v = _rand(22 + B1, (B, Hkv, cap, D))
+    rng = np.random.default_rng(B1)
+    keep = np.stack([np.stack([np.sort(rng.choice(cap, B1, replace=False)) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32)
+    keep_t = torch.from_numpy(keep).to(DEV)
+    out_cap = B1 + 5
+    nblk = -(-B1 // blk)
+    ncap = -(-(nblk + 1) // 8) * 8
+    ko = torch.full((B, Hkv, out_cap, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vo = torch.full_like(ko, float("nan"))
+    kt = torch.full((B, Hkv, 2, D, ncap), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_compact_kt((B, Hq, Hkv, D), k, v, cap, keep_t, B1, B1, ko, vo, out_cap, blk, kt, ncap)
+    torch.cuda.synchronize()
+    kbits, vbits, got = t2bits(ko), t2bits(vo), t2f64(kt)
+    kf = bf16_bits_to_f64(kb)
+    for b in range(B):
+        for h in range(Hkv):
+            assert np.array_equal(kbits[b, h, :B1], oracle.compact(kb[b, h], keep[b, h]))
+            assert np.array_equal(vbits[b, h, :B1], oracle.compact(vb[b, h], keep[b, h]))
+            kmax, kmin = oracle.build_kt(oracle.compact(kf[b, h], keep[b, h]), B1, blk)
+            assert np.array_equal(got[b, h, 0, :, :nblk], kmax) and np.array_equal(got[b, h, 1, :, :nblk], kmin)
+    assert torch.isnan(ko[:, :, B1:].float()).all() and torch.isnan(vo[:, :, B1:].float()).all()
+    assert torch.isnan(kt[..., nblk:].float()).all()
+
+
 def test_build_kt_mt_rows():
     B, Hq, Hkv, D, full, n, blk = 1, 4, 2, 128, 500, 173, 16
     kb, k = _rand(3, (B, Hkv, full, D))

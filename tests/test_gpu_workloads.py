@@ -52,12 +52,20 @@ def _needle_recall(wl, needles, keep, sel_steps, k2):
 
 
 def run_single_turn(wl, layer=0, max_pairs=64, steps=None, fused=True):
+    """fused: stage 1 in mask mode + rkv_compact_kt and decode steps with the append
+    fused in; otherwise stage 1 with its own compaction, rkv_build_kt, and separate
+    append and decode calls."""
     li = synth.layer_inputs(wl, layer)
     G, D, blk, k1 = wl.G, wl.D, wl.blk, wl.k1
     scale = 1 / math.sqrt(D)
     L = pipeline.Layer(wl, _t(li.k), _t(li.v), _t(li.q_obs), device=DEV)
     bud = L.bud
-    L.stage1()
+    if fused:
+        # stage 1 in mask mode, then compaction with the KT cache built on the way
+        L.stage1_select()
+        L.compact_kt()
+    else:
+        L.stage1()
     torch.cuda.synchronize()
     keep = L.keep.cpu().numpy()
     pairs = _pairs(wl, max_pairs)
@@ -79,7 +87,8 @@ def run_single_turn(wl, layer=0, max_pairs=64, steps=None, fused=True):
         Kc[:bud.B1] = K[got]
         Vc[:bud.B1] = f64(li.v[b, h])[got]
         states[(b, h)] = [Kc, Vc]
-    L.build_kt()
+    if not fused:
+        L.build_kt()
     torch.cuda.synchronize()
     for (b, h), st in states.items():
         kmax, kmin = oracle.build_kt(st[0], bud.B1, blk)

@@ -293,6 +293,27 @@ rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const
   return RKV_OK;
 }
 
+rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
+                          int64_t keep_ld, int64_t B1, void* k_out, void* v_out, int64_t out_cap, int32_t blk, void* kt,
+                          int64_t nblk_cap, void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0 || B1 == 0) return RKV_OK;
+  if (!k || !v || !keep_idx || !k_out || !v_out || !kt) return fail(RKV_ERR_INVALID_ARG, "compact_kt: NULL pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out) || !aligned16(kt))
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt: k, v, k_out, v_out and kt must be 16-byte aligned");
+  if (cap < 1 || B1 < 0 || B1 > out_cap || keep_ld < B1)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt: need cap >= 1, 0 <= B1 <= out_cap and keep_ld >= B1");
+  if (blk < 1) return fail(RKV_ERR_INVALID_ARG, "compact_kt: blk < 1");
+  if (nblk_cap % 8 != 0) return fail(RKV_ERR_INVALID_ARG, "compact_kt: nblk_cap=%lld is not a multiple of 8",
+                                     (long long)nblk_cap);
+  if ((B1 + blk - 1) / blk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "compact_kt: nblk_cap too small");
+  cudaError_t e = rkv::compact_kt_launch(k, v, cap, keep_idx, keep_ld, B1, blk, k_out, v_out, out_cap, kt, nblk_cap,
+                                         d.batch * d.n_kv_heads, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "compact_kt launch");
+  return RKV_OK;
+}
+
 rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
                          int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
                          void* stream) {

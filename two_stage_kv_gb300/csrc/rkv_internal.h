@@ -74,6 +74,9 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
 // ------------------------------------------------------------ KT / append ---
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
                             int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st);
+cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
+                              int64_t B1, int blk, void* ko, void* vo, int64_t out_cap, void* kt, int64_t nblk_cap,
+                              int pairs, cudaStream_t st);
 cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
                           int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
                           int32_t pairs, cudaStream_t st);

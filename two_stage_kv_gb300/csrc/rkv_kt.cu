@@ -93,6 +93,88 @@ __global__ void __launch_bounds__(HD) append_kernel(const bf16* k_new, const bf1
   if (idx && c == 0) idx[(size_t)pair * idx_cap + n] = (int32_t)row;
 }
 
+// Compaction with the KT cache built on the way: K_c[i] = K[keep[i]],
+// V_c[i] = V[keep[i]] for i < B1, and per block of blk compacted rows the
+// elementwise Kmax / Kmin of K_c (same values and order as kt_build_kernel).
+// One CTA = 16 blocks of one pair; thread (chunk ch, block bl) copies the
+// 16-byte chunk ch (8 channels) of every row of block bl and folds it into
+// its maxima / minima, so no cross-thread reduction is needed; the KT tile is
+// transposed in shared memory and written as 32-byte runs per channel row.
+constexpr int CK_BLOCKS = 16;
+constexpr int CK_NT = 256;
+
+__global__ void __launch_bounds__(CK_NT) compact_kt_kernel(const bf16* k, const bf16* v, int64_t cap,
+                                                           const int32_t* keep, int64_t keep_ld, int64_t B1, int blk,
+                                                           bf16* ko, bf16* vo, int64_t out_cap, bf16* kt,
+                                                           int64_t nblk_cap) {
+  __shared__ __align__(16) bf16 tile[2 * HD][CK_BLOCKS];   // row m*HD + c, column = block in the CTA
+  pdl_wait();
+  pdl_launch_dependents();
+  const int pair = blockIdx.y;
+  const int ch = threadIdx.x & 15, bl = threadIdx.x >> 4;
+  const int64_t nblk = (B1 + blk - 1) / blk;
+  const int64_t jb0 = (int64_t)blockIdx.x * CK_BLOCKS;
+  const int64_t jb = jb0 + bl;
+  float mx[8], mn[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mx[e] = neg_inf();
+    mn[e] = -neg_inf();
+  }
+  if (jb < nblk) {
+    const int64_t t0 = jb * blk, t1 = min(B1, t0 + blk);
+    const int32_t* kp = keep + (size_t)pair * keep_ld;
+    const bf16* ks = k + (size_t)pair * cap * HD + ch * 8;
+    const bf16* vs = v + (size_t)pair * cap * HD + ch * 8;
+    bf16* kd = ko + (size_t)pair * out_cap * HD + ch * 8;
+    bf16* vd = vo + (size_t)pair * out_cap * HD + ch * 8;
+    for (int64_t tb = t0; tb < t1; tb += 4) {
+      uint4 kr[4], vr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {            // four rows in flight
+        if (tb + u < t1) {
+          const int64_t src = min(max((int64_t)kp[tb + u], (int64_t)0), cap - 1);
+          kr[u] = *reinterpret_cast<const uint4*>(ks + src * HD);
+          vr[u] = *reinterpret_cast<const uint4*>(vs + src * HD);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (tb + u < t1) {
+          *reinterpret_cast<uint4*>(kd + (tb + u) * HD) = kr[u];
+          *reinterpret_cast<uint4*>(vd + (tb + u) * HD) = vr[u];
+          const uint32_t w[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = bf16_lo(w[q]), hi = bf16_hi(w[q]);
+            mx[2 * q] = fmaxf(mx[2 * q], lo);
+            mn[2 * q] = fminf(mn[2 * q], lo);
+            mx[2 * q + 1] = fmaxf(mx[2 * q + 1], hi);
+            mn[2 * q + 1] = fminf(mn[2 * q + 1], hi);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // the values are bf16 already: the conversion back is exact
+    tile[ch * 8 + e][bl] = __float2bfloat16_rn(mx[e]);
+    tile[HD + ch * 8 + e][bl] = __float2bfloat16_rn(mn[e]);
+  }
+  __syncthreads();
+  const int row = threadIdx.x;                   // KT row m*HD + c
+  const int nb = (int)min((int64_t)CK_BLOCKS, nblk - jb0);
+  bf16* dst = kt + ((size_t)pair * 2 * HD + row) * nblk_cap + jb0;   // 16-byte aligned: nblk_cap % 8 == 0
+  if (nb == CK_BLOCKS) {
+    const uint4* srcp = reinterpret_cast<const uint4*>(&tile[row][0]);
+    reinterpret_cast<uint4*>(dst)[0] = srcp[0];
+    reinterpret_cast<uint4*>(dst)[1] = srcp[1];
+  } else {
+    for (int i = 0; i < nb; ++i) dst[i] = tile[row][i];
+  }
+}
+
 }  // namespace
 
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
@@ -111,6 +193,16 @@ cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v
   return launch_pdl(append_kernel, dim3(pairs), dim3(HD), 0, st, reinterpret_cast<const bf16*>(k_new),
                     reinterpret_cast<const bf16*>(v_new), reinterpret_cast<bf16*>(k), reinterpret_cast<bf16*>(v), cap, n,
                     row, idx, idx_cap, reinterpret_cast<bf16*>(kt), nblk_cap, (int)blk);
+}
+
+cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
+                              int64_t B1, int blk, void* ko, void* vo, int64_t out_cap, void* kt, int64_t nblk_cap,
+                              int pairs, cudaStream_t st) {
+  const int64_t nblk = (B1 + blk - 1) / blk;
+  return launch_pdl(compact_kt_kernel, dim3((unsigned)((nblk + CK_BLOCKS - 1) / CK_BLOCKS), pairs), dim3(CK_NT), 0, st,
+                    reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v), cap, keep, keep_ld, B1, blk,
+                    reinterpret_cast<bf16*>(ko), reinterpret_cast<bf16*>(vo), out_cap, reinterpret_cast<bf16*>(kt),
+                    nblk_cap);
 }
 
 }  // namespace rkv

@@ -82,6 +82,19 @@ class Layer:
     def build_kt(self, stream=None):
         rkv.rkv_build_kt(self.dims, self.kc, self.cap, self.n, None, 0, self.wl.blk, self.kt, self.nblk_cap, stream)
 
+    def stage1_select(self, stream=None, pooled: bool = True):
+        """Stage 1 in mask mode: only the keep list (and optionally the pooled scores)."""
+        wl = self.wl
+        rkv.rkv_snap_evict(self.dims, self.q_obs, wl.W, self.k, self.v, self.cap_in, wl.S, wl.P, self.n_sink,
+                           self.bud.B1, self.scale, self.keep, self.bud.B1, None, None, 0,
+                           self.pooled if pooled else None, self.ws, self.ws_bytes, stream)
+
+    def compact_kt(self, stream=None):
+        """Compaction of the kept rows with the KT cache built on the way (after stage1_select)."""
+        rkv.rkv_compact_kt(self.dims, self.k, self.v, self.cap_in, self.keep, self.bud.B1, self.bud.B1, self.kc,
+                           self.vc, self.cap, self.wl.blk, self.kt, self.nblk_cap, stream)
+        self.n = self.bud.B1
+
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         rkv.rkv_append_kv(self.dims, k_new, v_new, self.kc, self.vc, self.cap, self.n, self.n, None, 0, self.kt,
                           self.nblk_cap, self.wl.blk, stream)

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
 
 # Every symbol include/rkv.h declares.
 EXPORTED = ["rkv_last_error", "rkv_abi_version", "rkv_budget_split", "rkv_snap_evict_workspace",
-            "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
+            "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
             "rkv_read_device_flags"]
 
 
@@ -49,6 +49,7 @@ _SIGS = {
                               _i64, _vp, _vp, _sz, _vp]),
     "rkv_snap_evict_noalloc": (_i32, [Dims, _vp, _i32, _vp, _vp, _i64, _i64, _i32, _i32, _i64, _f32, _vp, _i64, _vp,
                                       _vp, _i64, _vp, _vp]),
+    "rkv_compact_kt": (_i32, [Dims, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp]),
     "rkv_build_kt": (_i32, [Dims, _vp, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _vp]),
     "rkv_append_kv": (_i32, [Dims, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "rkv_hsa_decode": (_i32, [Dims, _vp, _vp, _vp, _i64, _i64, _vp, _i64, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
@@ -126,6 +127,11 @@ def rkv_snap_evict_noalloc(dims, q_obs, W, k, v, cap, S, pool_kernel, n_sink, B1
     _check(lib().rkv_snap_evict_noalloc(_dims(dims), _ptr(q_obs), W, _ptr(k), _ptr(v), cap, S, pool_kernel, n_sink,
                                         B1, scale, _ptr(keep_idx), keep_ld, _ptr(k_out), _ptr(v_out), out_cap,
                                         _ptr(pooled_out), _stream(stream)))
+
+
+def rkv_compact_kt(dims, k, v, cap, keep_idx, keep_ld, B1, k_out, v_out, out_cap, blk, kt, nblk_cap, stream=None):
+    _check(lib().rkv_compact_kt(_dims(dims), _ptr(k), _ptr(v), cap, _ptr(keep_idx), keep_ld, B1, _ptr(k_out),
+                                _ptr(v_out), out_cap, blk, _ptr(kt), nblk_cap, _stream(stream)))
 
 
 def rkv_build_kt(dims, k, cap, n, idx, idx_cap, blk, kt, nblk_cap, stream=None):
