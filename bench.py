@@ -203,17 +203,22 @@ def run_ours(args, rank, world, local):
     # several microseconds per decode step to the graph
     ev = {"s0": tev(), "s1": tev(), "s2": tev(), "d1": tev()}
 
-    def one_pass(record=True):
+    def one_pass(record=True, lay=None, q_=None, kn_=None, vn_=None, out_=None):
+        lay = L if lay is None else lay
+        q_ = qd if q_ is None else q_
+        kn_ = kn if kn_ is None else kn_
+        vn_ = vn if vn_ is None else vn_
+        out_ = out_all if out_ is None else out_
         if record:
             ev["s0"].record()
-        L.stage1_select(pooled=False)
+        lay.stage1_select(pooled=False)
         if record:
             ev["s1"].record()
-        L.compact_kt()
+        lay.compact_kt()
         if record:
             ev["s2"].record()
         for s in range(wl.steps):
-            L.step(qd[s], kn[s], vn[s], out=out_all[s], selections=False)
+            lay.step(q_[s], kn_[s], vn_[s], out=out_[s], selections=False)
         if record:
             ev["d1"].record()
 
@@ -277,32 +282,53 @@ def run_ours(args, rank, world, local):
                 "timing": "decode-phase events of the last timed pass / 64 launches (gaps included)",
                 "l2": "warm within a pass: inputs > L2 but the 190 MB compacted cache is re-read each step"}
 
-    # e2e: host buffers, H2D of the pass's inputs and D2H of its outputs inside the timed region
+    # e2e: host buffers, H2D of the pass's inputs and D2H of its outputs inside the
+    # timed region.  Two device input sets: the inputs of pass i+1 cross the
+    # host link while pass i computes (a pass reuses a set once the pass two
+    # before it, and its D2H, are done).
     e2e = None
     if not args.no_e2e:
         host_in = [x.cpu().pin_memory() for x in (k, v, qo, qd, kn, vn)]
-        dev_in = [k, v, qo, qd, kn, vn]
-        host_out = torch.empty(out_all.shape, dtype=out_all.dtype, pin_memory=True)
+        sets = [dict(inp=[k, v, qo, qd, kn, vn], out=out_all, graph=graph)]
+        inp_b = [torch.empty_like(x) for x in (k, v, qo, qd, kn, vn)]
+        L_b = pipeline.Layer(wl, inp_b[0], inp_b[1], inp_b[2], device=dev)
+        out_b = torch.empty_like(out_all)
+        graph_b = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_b, stream=stream):
+            one_pass(record=False, lay=L_b, q_=inp_b[3], kn_=inp_b[4], vn_=inp_b[5], out_=out_b)
+        sets.append(dict(inp=inp_b, out=out_b, graph=graph_b))
+        host_out = [torch.empty(out_all.shape, dtype=out_all.dtype, pin_memory=True) for _ in range(2)]
         h2d = sum(x.numel() * x.element_size() for x in host_in)
-        d2h = host_out.numel() * host_out.element_size()
-        e2e_steps = max(3, min(args.steps, 20))
+        d2h = host_out[0].numel() * host_out[0].element_size()
+        e2e_steps = max(4, min(args.steps, 20))
+        copy_stream = torch.cuda.Stream(device=dev)
+        ev_copied = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record()
-            for _ in range(e2e_steps):
-                for d_, h_ in zip(dev_in, host_in):
+        e0.record(copy_stream)
+        for i in range(e2e_steps):
+            st_ = sets[i % 2]
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(ev_done[i % 2])
+                for d_, h_ in zip(st_["inp"], host_in):
                     d_.copy_(h_, non_blocking=True)
-                graph.replay()
-                host_out.copy_(out_all, non_blocking=True)
-            e1.record()
+                ev_copied[i % 2].record(copy_stream)
+            with torch.cuda.stream(stream):
+                stream.wait_event(ev_copied[i % 2])
+                st_["graph"].replay()
+                host_out[i % 2].copy_(st_["out"], non_blocking=True)
+                ev_done[i % 2].record(stream)
+        e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         e2e = {"value": round(whole_job_rate(tokens_per_pass * e2e_steps, world, e2e_ms / 1e3), 1),
                "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
-               "ms_per_step": round(e2e_ms / e2e_steps, 4)}
+               "ms_per_step": round(e2e_ms / e2e_steps, 4),
+               "note": "two device input sets: a pass's H2D overlaps the previous pass's compute"}
 
     from two_stage_kv_gb300 import rkv
     flags = rkv.rkv_read_device_flags()
