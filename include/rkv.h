@@ -209,7 +209,10 @@ rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void*
  *   sel_blocks optional [B, Hkv, k2] int32: i2 ascending, -1 padded.
  *   sel_channels optional [B, Hkv, k1] int32: i1 ascending.
  * Requires 1 <= N <= cap, ceil(N/blk) <= nblk_cap, 1 <= k1 <= D, k2 >= 1,
- * ceil(N/blk) <= 8192.  No workspace: split partials are combined on chip.
+ * 1 <= blk <= 128 (RKV_ERR_UNSUPPORTED otherwise), ceil(N/blk) <= 8192.
+ * Block sizes that are multiples of 8 stream the selected K/V blocks with TMA;
+ * other sizes (1 gives token-level selection) gather the rows one by one.
+ * No workspace: split partials are combined on chip.
  * The launch may overlap the tail of the previous kernel on the stream
  * (programmatic dependent launch); it reads no input before that kernel ends.
  */

@@ -66,7 +66,8 @@ D4 = (1, 32, 8, 128)
     (lambda: rkv.rkv_hsa_decode(D4, 0, 16, 16, 100, 10, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 0, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 101, 16, 10, 16, 8, 4, 0.1, 16, stream=0), 1),
-    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 12, 8, 4, 0.1, 16, stream=0), 2),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 16, 129, 8, 4, 0.1, 16, stream=0), 2),
+    (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 104, 0, 8, 4, 0.1, 16, stream=0), 2),
     (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 3, 16, 8, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 16, 0, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_hsa_decode(D4, 16, 16, 16, 100, 100, 16, 10, 16, 129, 4, 0.1, 16, stream=0), 1),

@@ -193,6 +193,10 @@ def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=Fal
     (1, 32, 8, 1, 16, 32, 4),         # a single token
     (1, 32, 8, 4096, 128, 20, 3),     # block 128
     (1, 32, 8, 20000, 16, 32, 300),   # many blocks, several rounds per CTA
+    (1, 32, 8, 700, 1, 32, 40),       # token-level blocks (SparQ-like), gathered rows
+    (2, 32, 8, 500, 4, 32, 10),       # block 4, gathered rows
+    (1, 64, 8, 333, 12, 64, 7),       # block 12 (not a multiple of 8), G = 8
+    (1, 32, 8, 300, 1, 128, 20),      # k1 = D and block 1: exact top-k of qbar . k (Exact-TopK)
 ])
 def test_hsa_decode_parity(B, Hq, Hkv, n, blk, k1, k2):
     _hsa_case(100 + n, B, Hq, Hkv, n, blk, k1, k2)
@@ -220,7 +224,34 @@ def test_hsa_decode_crowded_boundary_bucket():
     _hsa_case(12, 1, 32, 8, 700 * 16, 16, 32, 50, k_scale=1e-3, kmod=kmod)
 
 
-@pytest.mark.parametrize("n,blk,k2", [(250, 16, 6), (97, 8, 20), (600, 32, 4)])
+def test_hsa_decode_exact_topk_pin():
+    """k1 = D and block 1: the block score is qbar . k_j exactly, so the chosen tokens
+    are the plain top-k2 of qbar . k (lowest index on ties) and the output is
+    attention over them (the pages' Exact-TopK special case)."""
+    B, Hq, Hkv, D, n, k2 = 1, 32, 8, 128, 400, 24
+    G = Hq // Hkv
+    dims = (B, Hq, Hkv, D)
+    kb, k = _rand(61, (B, Hkv, n, D))
+    vb, v = _rand(62, (B, Hkv, n, D))
+    qb, q = _rand(63, (B, Hq, D))
+    ncap = -(-n // 8) * 8
+    kt = torch.empty((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    sb = torch.empty((B, Hkv, k2), dtype=torch.int32, device=DEV)
+    rkv.rkv_build_kt(dims, k, n, n, None, 0, 1, kt, ncap)
+    rkv.rkv_hsa_decode(dims, q, k, v, n, n, kt, ncap, 1, D, k2, 1 / math.sqrt(D), out, sb, None)
+    torch.cuda.synchronize()
+    kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
+    out_h, sb_h = out.cpu().numpy(), sb.cpu().numpy()
+    for h in range(Hkv):
+        qbar = qf[0, h * G:(h + 1) * G].sum(axis=0)
+        s = kf[0, h] @ qbar
+        check_topk(sb_h[0, h], s, k2, "exact top-k tokens")
+        y = oracle.attention(qf[0, h * G:(h + 1) * G], kf[0, h][sb_h[0, h]], vf[0, h][sb_h[0, h]], 1 / math.sqrt(D))
+        assert max_abs(out_h[0, h * G:(h + 1) * G], y) <= ATOL_OUT
+
+
+@pytest.mark.parametrize("n,blk,k2", [(250, 16, 6), (97, 8, 20), (600, 32, 4), (300, 4, 12), (150, 1, 30)])
 def test_hsa_decode_mt_parity(n, blk, k2):
     _hsa_case(300 + n, 2, 32, 8, n, blk, 32, k2, mt=True, full_rows=3 * n + 11)
 

@@ -132,8 +132,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
                 (long long)idx_cap);
   if (mt && app && (row < 0 || row >= cap))
     return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt: append row %lld outside [0, cap)", (long long)row);
-  if (blk < 8 || blk > 128 || blk % 8 != 0)
-    return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: block size %d (needs a multiple of 8 in [8,128])", blk);
+  if (blk < 1 || blk > 128) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: block size %d outside [1,128]", blk);
   if (nblk_cap % 8 != 0) return fail(RKV_ERR_INVALID_ARG, "hsa_decode: nblk_cap=%lld is not a multiple of 8",
                                      (long long)nblk_cap);
   const int64_t nblk = (n_tot + blk - 1) / blk;
@@ -155,6 +154,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.n = (int32_t)n; a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
   a.blk = blk; a.k1 = k1; a.k2 = k2;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.tma_kv = (!mt && blk % 8 == 0) ? 1 : 0;
   if (!rkv::hsa_plan(a)) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: shared memory plan does not fit");
 
   CUtensorMap tmK, tmV, tmKT;
@@ -162,7 +162,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   std::memset(&tmV, 0, sizeof(tmV));
   std::memset(&tmKT, 0, sizeof(tmKT));
   const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
-  if (!mt) {
+  if (a.tma_kv) {
     // rows at or past n (the appended token included) read as zero
     const int64_t extent = std::max<int64_t>(n, 1);
     if ((s = make_kv_map(&tmK, k, pairs, cap, extent, blk, "k")) != RKV_OK) return s;

@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     // every CTA of the cluster sends its (O, max, sum) of each head this CTA owns
     const int gmine = (int)rank < G ? (G - (int)rank + ns - 1) / ns : 0;
     if (gmine > 0) mbar_arrive_expect_tx(&fs.ebar, (uint32_t)(gmine * ns * PART_STRIDE * 4));
-    if (!MT) {
+    if (!MT && a.tma_kv) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
     }
@@ -578,13 +578,16 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   uint32_t phase = 0;
   unsigned int* err = &g_hsa_err;
   const int g4 = lane >> 2, t4 = lane & 3;
+  // K/V rows arrive by TMA (block rows contiguous, blk a multiple of 8) or are
+  // gathered row by row with cp.async (MT candidate rows, or other block sizes)
+  const bool gat = MT || a.tma_kv == 0;
 
   for (int r0 = s_lo; r0 < s_hi; r0 += a.slots_round) {
     const int nsl = min(a.slots_round, s_hi - r0);
     const int rows = nsl * blk;
     const int nsteps = (rows + 15) / 16;
     const int rows16 = nsteps * 16;
-    if (!MT) {
+    if (!gat) {
       {
         // The copies are spread over all warps: one warp issuing them all serialises them.
         // The region was last read through the generic proxy before a barrier (write
@@ -603,14 +606,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     } else {
       const bf16* kb = reinterpret_cast<const bf16*>(a.k) + (size_t)pair * a.cap * HD;
       const bf16* vb = reinterpret_cast<const bf16*>(a.v) + (size_t)pair * a.cap * HD;
-      const int32_t* ib = a.idx + (size_t)pair * a.idx_cap;
+      const int32_t* ib = MT ? a.idx + (size_t)pair * a.idx_cap : nullptr;
       for (int i = tid; i < rows * 16; i += NT) {
         const int r = i >> 4, ch = i & 15;
         const int slot = r / blk;
         const int t = sel[r0 + slot] * blk + (r - slot * blk);
         const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
         if (t < n_old) {
-          const int64_t prow = min(max((int64_t)ib[t], (int64_t)0), a.cap - 1);
+          const int64_t prow = MT ? min(max((int64_t)ib[t], (int64_t)0), a.cap - 1) : (int64_t)t;
           cp_async_16(smem_u32(tK) + o, kb + prow * HD + ch * 8);
           cp_async_16(smem_u32(tV) + o, vb + prow * HD + ch * 8);
         } else if (t == n_old && app) {
@@ -629,9 +632,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       *reinterpret_cast<uint4*>(((i & 1) ? tV : tK) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7)) =
           make_uint4(0, 0, 0, 0);
     }
-    if (MT) cp_async_wait_all();
+    if (gat) cp_async_wait_all();
     // cp.async rows and zero rows come from every thread; TMA rows are waited for per slot
-    if (MT || rows16 != rows) __syncthreads();
+    if (gat || rows16 != rows) __syncthreads();
 
     // --- S^T = K Q^T for the warp's 16-token step, masked and in log2 units
     const int c0 = warp * 16;
@@ -640,7 +643,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
 #pragma unroll
     for (int ht = 0; ht < NH; ++ht) x[ht][0] = x[ht][1] = x[ht][2] = x[ht][3] = neg_inf();
     if (has_step) {
-      if (!MT) {
+      if (!gat) {
         const int sa = c0 / blk, sb = min((c0 + 15) / blk, nsl - 1);
         for (int s = sa; s <= sb; ++s)
           if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
