@@ -237,8 +237,30 @@ rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_
                              const void* k_new, const void* v_new, int64_t row, void* stream);
 
 /*
+ * HSA decode step for a batch whose rows hold different numbers of candidates
+ * (ragged batch).  [RocketKV digest, 方法细节: HSA steps 1-3 and Algorithm 1,
+ * per request]  Same computation, arguments and results as rkv_hsa_decode,
+ * except that batch row b attends its own N_b = n_rows[b] (+1 with the fused
+ * append) candidates: blocks, k2 (capped at row b's block count), the
+ * appended row index (n_rows[b]) and the KT column it updates are per row.
+ *   n_rows     [B] int32 DEVICE array, candidates before the step's append; it
+ *              is read when the kernel starts (after the previous kernel on the
+ *              stream has finished), so a graph can replay with new lengths.
+ *              The library does not update it.
+ *   n_max      host upper bound of n_rows: sizes the launch and is checked like
+ *              rkv_hsa_decode's n (n_max (+1) <= cap, ceil(n_max (+1) / blk) <=
+ *              nblk_cap).  An entry outside [1, n_max] is clamped into it and
+ *              sets bit 1 of the device error word.
+ */
+rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, int64_t cap, const int32_t* n_rows,
+                                 int64_t n_max, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
+                                 float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+                                 const void* k_new, const void* v_new, void* stream);
+
+/*
  * Read and clear the library's device error word (synchronises the device).
  * Bit 0: a bounded wait for an asynchronous copy gave up in some kernel.
+ * Bit 1: a per-row length read from device memory was out of range.
  * Returns RKV_ERR_TIMEOUT if any bit was set, RKV_OK otherwise.
  */
 rkv_status rkv_read_device_flags(uint32_t* flags);

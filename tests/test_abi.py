@@ -89,6 +89,9 @@ D4 = (1, 32, 8, 128)
     (lambda: rkv.rkv_compact_kt(D4, 8, 16, 100, 16, 50, 50, 16, 16, 50, 16, 16, 8, stream=0), 1),
     (lambda: rkv.rkv_compact_kt(D4, 16, 16, 100, 16, 50, 50, 16, 16, 50, 16, 16, 0, stream=0), 1),
     (lambda: rkv.rkv_compact_kt(D4, 16, 16, 100, 16, 40, 50, 16, 16, 50, 16, 16, 8, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_ragged(D4, 16, 16, 16, 100, None, 50, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_ragged(D4, 16, 16, 16, 100, 16, 0, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_ragged(D4, 16, 16, 16, 100, 16, 101, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_build_kt(D4, 16, 10, 20, None, 0, 16, 16, 4, stream=0), 1),
     (lambda: rkv.rkv_build_kt(D4, 16, 100, 100, None, 0, 16, 16, 6, stream=0), 1),
     (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 11, None, 0, 16, 10, 16, stream=0), 1),

@@ -224,6 +224,75 @@ def test_hsa_decode_crowded_boundary_bucket():
     _hsa_case(12, 1, 32, 8, 700 * 16, 16, 32, 50, k_scale=1e-3, kmod=kmod)
 
 
+@pytest.mark.parametrize("append", [False, True])
+def test_hsa_decode_ragged_rows(append):
+    """Rows with different candidate counts in one launch: every row matches the
+    oracle on its own n (and its own appended token and KT block)."""
+    B, Hq, Hkv, D, blk, k1, k2 = 3, 32, 8, 128, 16, 32, 8
+    G = Hq // Hkv
+    n_rows = [300, 1000, 57]
+    n_max, cap = max(n_rows), 1100
+    dims = (B, Hq, Hkv, D)
+    kb, k = _rand(81, (B, Hkv, cap, D))
+    vb, v = _rand(82, (B, Hkv, cap, D))
+    qb, q = _rand(83, (B, Hq, D))
+    nb_, knew = _rand(84, (B, Hkv, D))
+    vnb, vnew = _rand(85, (B, Hkv, D))
+    ncap = -(-(-(-(n_max + 1) // blk)) // 8) * 8
+    kt = torch.empty((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    for b in range(B):             # each row's KT covers its own candidates
+        rkv.rkv_build_kt((1, Hq, Hkv, D), k[b:b + 1], cap, n_rows[b], None, 0, blk, kt[b:b + 1], ncap)
+    n_dev = torch.tensor(n_rows, dtype=torch.int32, device=DEV)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
+    scale = 1 / math.sqrt(D)
+    rkv.rkv_hsa_decode_ragged(dims, q, k, v, cap, n_dev, n_max, kt, ncap, blk, k1, k2, scale, out, sb, None,
+                              knew if append else None, vnew if append else None)
+    torch.cuda.synchronize()
+    assert rkv.rkv_read_device_flags() == 0
+    kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
+    out_h, sb_h, kt_h = out.cpu().numpy(), sb.cpu().numpy(), t2f64(kt)
+    worst = 0.0
+    for b in range(B):
+        n = n_rows[b] + (1 if append else 0)
+        for h in range(Hkv):
+            Kc, Vc = kf[b, h, :n].copy(), vf[b, h, :n].copy()
+            if append:
+                Kc[-1] = bf16_bits_to_f64(nb_)[b, h]
+                Vc[-1] = bf16_bits_to_f64(vnb)[b, h]
+                assert np.array_equal(t2bits(k[b, h, n - 1]), nb_[b, h])   # the row was persisted
+            kmax, kmin = oracle.build_kt(Kc, n, blk)
+            nblk = kmax.shape[1]
+            assert np.array_equal(kt_h[b, h, 0, :, :nblk], kmax) and np.array_equal(kt_h[b, h, 1, :, :nblk], kmin)
+            qg = qf[b, h * G:(h + 1) * G]
+            res = oracle.hsa_decode(qg, Kc, Vc, n, kmax, kmin, blk, k1, k2, scale)
+            k2e = min(k2, nblk)
+            check_topk(sb_h[b, h, :k2e], res["s"], k2, f"row {b} blocks")
+            assert np.all(sb_h[b, h, k2e:] == -1)
+            y = oracle.attention_over_blocks(qg, Kc, Vc, n, sb_h[b, h, :k2e], blk, scale)
+            worst = max(worst, max_abs(out_h[b, h * G:(h + 1) * G], y))
+    assert worst <= ATOL_OUT, worst
+
+
+def test_hsa_decode_ragged_length_out_of_range_flagged():
+    B, Hq, Hkv, D, blk = 2, 32, 8, 128, 16
+    cap, n_max = 400, 300
+    dims = (B, Hq, Hkv, D)
+    _, k = _rand(91, (B, Hkv, cap, D))
+    _, v = _rand(92, (B, Hkv, cap, D))
+    _, q = _rand(93, (B, Hq, D))
+    ncap = 24
+    kt = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt(dims, k, cap, n_max, None, 0, blk, kt, ncap)
+    n_dev = torch.tensor([200, 5000], dtype=torch.int32, device=DEV)     # 5000 > n_max: clamped
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    rkv.rkv_hsa_decode_ragged(dims, q, k, v, cap, n_dev, n_max, kt, ncap, blk, 32, 4, 0.1, out)
+    with pytest.raises(rkv.RkvError) as e:
+        rkv.rkv_read_device_flags()
+    assert "0x2" in str(e.value)
+    assert torch.isfinite(out).all()
+
+
 def test_hsa_decode_exact_topk_pin():
     """k1 = D and block 1: the block score is qbar . k_j exactly, so the chosen tokens
     are the plain top-k2 of qbar . k (lowest index on ties) and the output is

@@ -111,7 +111,7 @@ rkv_status make_q_map(CUtensorMap* m, const void* base, int64_t rows, int box_ro
 rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_t cap, int32_t* idx,
                       int64_t idx_cap, int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
                       float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
-                      const void* v_new, int64_t row, void* stream, bool mt) {
+                      const void* v_new, int64_t row, void* stream, bool mt, const int32_t* n_rows = nullptr) {
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
@@ -151,7 +151,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.row = mt ? row : n;
   a.sel_blocks = sel_blocks; a.sel_channels = sel_channels;
   a.cap = cap; a.nblk_cap = nblk_cap; a.idx_cap = idx_cap;
-  a.n = (int32_t)n; a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
+  a.n = (int32_t)n; a.n_rows = n_rows; a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
   a.blk = blk; a.k1 = k1; a.k2 = k2;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.tma_kv = (!mt && blk % 8 == 0) ? 1 : 0;
@@ -163,8 +163,9 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   std::memset(&tmKT, 0, sizeof(tmKT));
   const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
   if (a.tma_kv) {
-    // rows at or past n (the appended token included) read as zero
-    const int64_t extent = std::max<int64_t>(n, 1);
+    // rows at or past n (the appended token included) read as zero; with
+    // per-row lengths every row up to cap is readable and the kernel masks
+    const int64_t extent = n_rows ? cap : std::max<int64_t>(n, 1);
     if ((s = make_kv_map(&tmK, k, pairs, cap, extent, blk, "k")) != RKV_OK) return s;
     if ((s = make_kv_map(&tmV, v, pairs, cap, extent, blk, "v")) != RKV_OK) return s;
   }
@@ -347,12 +348,24 @@ rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_
                     sel_channels, k_new, v_new, row, stream, true);
 }
 
+rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, int64_t cap, const int32_t* n_rows,
+                                 int64_t n_max, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
+                                 float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
+                                 const void* k_new, const void* v_new, void* stream) {
+  if (d.batch > 0 && !n_rows) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_ragged: n_rows is NULL");
+  if (n_max < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_ragged: n_max=%lld < 1", (long long)n_max);
+  return hsa_common(d, q, k, v, cap, nullptr, 0, n_max, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
+                    sel_channels, k_new, v_new, 0, stream, false, n_rows);
+}
+
 rkv_status rkv_read_device_flags(uint32_t* flags) {
   if (!flags) return fail(RKV_ERR_INVALID_ARG, "read_device_flags: NULL");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "read_device_flags");
   *flags = rkv::hsa_take_device_error() | rkv::snap_take_device_error();
-  if (*flags) return fail(RKV_ERR_TIMEOUT, "device flags 0x%x: a bounded wait gave up", *flags);
+  if (*flags)
+    return fail(RKV_ERR_TIMEOUT, "device flags 0x%x (bit 0: a bounded wait gave up, bit 1: a per-row length was "
+                "out of range)", *flags);
   return RKV_OK;
 }
 

@@ -17,6 +17,8 @@ typedef __nv_bfloat16 bf16;
 
 // Device error bits (each translation unit owns one word; see rkv_api.cu).
 constexpr unsigned int ERR_WAIT_TIMEOUT = 1u;
+// A per-row length read from device memory was out of range (clamped).
+constexpr unsigned int ERR_BAD_LENGTH = 2u;
 
 // Upper bound for any single wait on an asynchronous copy (nanoseconds of
 // %globaltimer).  A wait that runs past it sets ERR_WAIT_TIMEOUT and returns.

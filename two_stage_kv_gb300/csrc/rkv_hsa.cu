@@ -257,7 +257,7 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, FixedSmem& fs
   }
 }
 
-template <bool MT, int NH>
+template <bool MT, int NH, bool RAG>
 __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                            const __grid_constant__ CUtensorMap tmV,
                                                            const __grid_constant__ CUtensorMap tmKT,
@@ -280,15 +280,17 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   const int pair = b * a.Hkv + hk;
   const int G = a.G;
   const bool app = a.k_new != nullptr;
-  const int n_old = a.n;                      // tokens before this step's append
-  const int n_tot = a.n + (app ? 1 : 0);      // tokens attended
-  const int nb_new = app ? n_old / a.blk : -1;
-  const int nblk = a.nblk;
   const int cpr = a.cpr;
   const int jlo = (int)rank * cpr;                       // blocks this CTA scores: [jlo, jhi)
-  const int jhi = min(nblk, jlo + cpr);
   const bool spec = a.kt_spec != 0;
-  const bool own_new = app && nb_new >= jlo && nb_new < jhi;   // this CTA holds the appended key's block
+  // Lengths: launch constants, worked out while the previous kernel may still
+  // run; with per-row lengths (RAG) they are redone from n_rows after the wait.
+  int n_old = a.n;                                       // tokens before this step's append
+  int n_tot = a.n + (app ? 1 : 0);                       // tokens attended
+  int nb_new = app ? n_old / a.blk : -1;
+  int nblk = a.nblk;
+  int jhi = min(nblk, jlo + cpr);
+  bool own_new = app && nb_new >= jlo && nb_new < jhi;   // this CTA holds the appended key's block
 
   // Prologue that touches no data of the previous kernel.
   if (tid == 0) {
@@ -297,8 +299,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     mbar_init(&fs.ktbar, 1);
     mbar_init(&fs.sbar, 1);
     fence_mbar_init();
-    // every CTA of the cluster sends its scores and its warps' score bounds to every CTA
-    mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(nblk * 4 + ns * NWARP * 8));
+    // every CTA of the cluster sends its scores and its warps' score bounds to every
+    // CTA (per-row lengths are only known after the dependency wait: armed below)
+    if (!RAG) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(a.nblk * 4 + ns * NWARP * 8));
     // every CTA of the cluster sends its (O, max, sum) of each head this CTA owns
     const int gmine = (int)rank < G ? (G - (int)rank + ns - 1) / ns : 0;
     if (gmine > 0) mbar_arrive_expect_tx(&fs.ebar, (uint32_t)(gmine * ns * PART_STRIDE * 4));
@@ -318,6 +321,20 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   cluster_arrive_relaxed();
   pdl_wait();
   pdl_launch_dependents();
+  if (RAG) {
+    // this batch row's length, clamped into [1, the call's maximum] (an entry out
+    // of range raises ERR_BAD_LENGTH)
+    const int nr = a.n_rows[b];
+    n_old = min(max(nr, 1), a.n);
+    if (nr != n_old && tid == 0 && rank == 0) atomicOr(&g_hsa_err, ERR_BAD_LENGTH);
+    n_tot = n_old + (app ? 1 : 0);
+    nb_new = app ? n_old / a.blk : -1;
+    nblk = (n_tot + a.blk - 1) / a.blk;
+    jhi = min(nblk, jlo + cpr);
+    own_new = app && nb_new >= jlo && nb_new < jhi;
+    // (a remote byte count arriving before this arrival is fine: the phase needs both)
+    if (tid == 0) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(nblk * 4 + ns * NWARP * 8));
+  }
   // KT rows do not depend on the query: with the prefetch, all 2*D rows of this
   // CTA's blocks are in flight while the channels are chosen
   if (spec && tid == 0 && jhi > jlo) {
@@ -536,7 +553,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   }
 
   // ---------------------------------------------------------------- C ------
-  const int k2e = a.k2e;
+  const int k2e = RAG ? min(a.k2, nblk) : a.k2e;
   if (k2e >= nblk) {
     for (int j = tid; j < nblk; j += NT) flag[j] = 1;
   } else {
@@ -571,8 +588,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
 #pragma unroll
   for (int ht = 0; ht < NH; ++ht) acc[ht][0] = acc[ht][1] = acc[ht][2] = acc[ht][3] = 0.f;
 
-  const int s_lo = (int)rank * a.chunk;
-  const int s_hi = min(k2e, s_lo + a.chunk);
+  const int chunk = RAG ? (k2e + ns - 1) / ns : a.chunk;   // blocks per CTA (at most the plan's chunk)
+  const int s_lo = (int)rank * chunk;
+  const int s_hi = min(k2e, s_lo + chunk);
   const uint32_t half = a.tile_half_bytes;
   const int blk = a.blk;
   uint32_t phase = 0;
@@ -859,7 +877,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       // persist the appended token: cache row and candidate index (MT)
       if (tid < 32) {
         bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
-                    ((size_t)pair * a.cap + a.row) * HD + (tid & 15) * 8;
+                    ((size_t)pair * a.cap + (MT ? a.row : (int64_t)n_old)) * HD + (tid & 15) * 8;
         *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 16 ? fs.knew : fs.vnew) +
                                                                           (tid & 15) * 8);
       }
@@ -926,8 +944,9 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    const void* ks[4] = {(const void*)hsa_decode_kernel<false, 1>, (const void*)hsa_decode_kernel<false, 2>,
-                         (const void*)hsa_decode_kernel<true, 1>, (const void*)hsa_decode_kernel<true, 2>};
+    const void* ks[6] = {(const void*)hsa_decode_kernel<false, 1, false>, (const void*)hsa_decode_kernel<false, 2, false>,
+                         (const void*)hsa_decode_kernel<true, 1, false>, (const void*)hsa_decode_kernel<true, 2, false>,
+                         (const void*)hsa_decode_kernel<false, 1, true>, (const void*)hsa_decode_kernel<false, 2, true>};
     for (const void* k : ks) {
       attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       if (attr_err != cudaSuccess) break;
@@ -948,8 +967,11 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  auto kern = mt ? (a.G > 8 ? hsa_decode_kernel<true, 2> : hsa_decode_kernel<true, 1>)
-                 : (a.G > 8 ? hsa_decode_kernel<false, 2> : hsa_decode_kernel<false, 1>);
+  // per-row lengths (ragged batches) take their own instantiation: the uniform
+  // kernels keep every length a launch constant
+  auto kern = mt ? (a.G > 8 ? hsa_decode_kernel<true, 2, false> : hsa_decode_kernel<true, 1, false>)
+          : a.n_rows ? (a.G > 8 ? hsa_decode_kernel<false, 2, true> : hsa_decode_kernel<false, 1, true>)
+                     : (a.G > 8 ? hsa_decode_kernel<false, 2, false> : hsa_decode_kernel<false, 1, false>);
   return cudaLaunchKernelEx(&cfg, kern, *tmK, *tmV, *tmKT, a);
 }
 

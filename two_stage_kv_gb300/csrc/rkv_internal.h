@@ -27,7 +27,8 @@ struct HsaArgs {
   int32_t* sel_blocks;  // [B, Hkv, k2] or nullptr
   int32_t* sel_channels;  // [B, Hkv, k1] or nullptr
   int64_t cap, nblk_cap, idx_cap;
-  int32_t n, B, Hq, Hkv, G, blk, k1, k2;   // n = candidates before the append
+  int32_t n, B, Hq, Hkv, G, blk, k1, k2;   // n = candidates before the append (ragged: the rows' maximum)
+  const int32_t* n_rows; // ragged: [B] candidates before the append per batch row (device), else nullptr
   int32_t nblk;         // blocks over the attended candidates
   int32_t k2e;          // min(k2, nblk)
   int32_t ns;           // CTAs per cluster (one cluster per (b, kv head))

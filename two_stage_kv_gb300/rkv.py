@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
 # Every symbol include/rkv.h declares.
 EXPORTED = ["rkv_last_error", "rkv_abi_version", "rkv_budget_split", "rkv_snap_evict_workspace",
             "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
+            "rkv_hsa_decode_ragged",
             "rkv_read_device_flags"]
 
 
@@ -56,6 +57,8 @@ _SIGS = {
                               _vp, _vp, _vp]),
     "rkv_hsa_decode_mt": (_i32, [Dims, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _i64, _i32, _i32, _i32, _f32,
                                  _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "rkv_hsa_decode_ragged": (_i32, [Dims, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _i32, _i32, _f32, _vp,
+                                     _vp, _vp, _vp, _vp, _vp]),
     "rkv_read_device_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -156,6 +159,14 @@ def rkv_hsa_decode_mt(dims, q, k, v, cap, idx, idx_cap, n, kt, nblk_cap, blk, k1
     _check(lib().rkv_hsa_decode_mt(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, _ptr(idx), idx_cap, n, _ptr(kt),
                                    nblk_cap, blk, k1, k2, scale, _ptr(out), _ptr(sel_blocks), _ptr(sel_channels),
                                    _ptr(k_new), _ptr(v_new), row, _stream(stream)))
+
+
+def rkv_hsa_decode_ragged(dims, q, k, v, cap, n_rows, n_max, kt, nblk_cap, blk, k1, k2, scale, out,
+                          sel_blocks=None, sel_channels=None, k_new=None, v_new=None, stream=None):
+    """HSA decode with a per-batch-row candidate count n_rows ([B] int32 on the device)."""
+    _check(lib().rkv_hsa_decode_ragged(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, _ptr(n_rows), n_max, _ptr(kt),
+                                       nblk_cap, blk, k1, k2, scale, _ptr(out), _ptr(sel_blocks),
+                                       _ptr(sel_channels), _ptr(k_new), _ptr(v_new), _stream(stream)))
 
 
 def rkv_read_device_flags() -> int:
