@@ -117,6 +117,13 @@ __device__ __forceinline__ PassItem pass_item(const PassArgs& a, int item) {
   return it;
 }
 
+// Pass 2 walks a CTA's items backwards: with the same partition as pass 1 (one
+// row group per pair), the K chunks a CTA read last in pass 1 are still in L2.
+template <int PASS>
+__device__ __forceinline__ int item_at(int ib, int ie, int ii) {
+  return PASS == 2 ? ie - 1 - (ii - ib) : ii;
+}
+
 template <int PASS>
 __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constant__ CUtensorMap tmK,
                                                             const __grid_constant__ CUtensorMap tmQ,
@@ -168,8 +175,8 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       int T = 0, nload = 0, key = -1;
-      for (int item = ib; item < ie && !*abort_flag; ++item) {
-        const PassItem it = pass_item<PASS>(a, item);
+      for (int ii = ib; ii < ie && !*abort_flag; ++ii) {
+        const PassItem it = pass_item<PASS>(a, item_at<PASS>(ib, ie, ii));
         const int k = it.pair * (PASS == 1 ? a.RG1 : a.RG2) + it.rg;
         if (k != key) {
           // the MMAs of the previous Q tile have completed before it is overwritten
@@ -205,8 +212,8 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
       const uint32_t idesc = PASS == 1 ? idesc_bf16_f32(128, T_KEYS) : idesc_bf16_f32(128, nq);
       int T = 0, nload = 0, key = -1;
       bool ok = true;
-      for (int item = ib; item < ie && ok; ++item) {
-        const PassItem it = pass_item<PASS>(a, item);
+      for (int ii = ib; ii < ie && ok; ++ii) {
+        const PassItem it = pass_item<PASS>(a, item_at<PASS>(ib, ie, ii));
         const int k = it.pair * (PASS == 1 ? a.RG1 : a.RG2) + it.rg;
         if (k != key) {
           if (nload > 0) tc_commit(&ts.qfree);        // arrives once every MMA issued so far is done
@@ -247,8 +254,8 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16) + (uint32_t)(eset * ncols);
     const int S32 = (int)a.S, L32 = (int)a.L;
     int T0 = 0, key = -1;                            // first tile of the item in the CTA's stream
-    for (int item = ib; item < ie; ++item) {
-      const PassItem it = pass_item<PASS>(a, item);
+    for (int ii = ib; ii < ie; ++ii) {
+      const PassItem it = pass_item<PASS>(a, item_at<PASS>(ib, ie, ii));
       const int j032 = (int)it.j0;
       const int pair = it.pair;
       const int row0 = it.rg * (PASS == 1 ? P1_ROWS : P2_ROWS);
