@@ -164,6 +164,21 @@ rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap,
                           int64_t nblk_cap, void* stream);
 
 /*
+ * rkv_compact_kt writing the compacted rows into pages: row i of batch row b
+ * (for every KV head h) goes to slot i % blk of page block_table[b, i / blk]:
+ *   k_pages[page, h, i % blk] = k[b, h, keep_idx[b, h, i]], likewise for v;
+ * KT as rkv_compact_kt (per (b, h), logical block order).
+ *   k_pages,v_pages [num_pages, Hkv, blk, D] bf16 pools (16-byte aligned).
+ *   block_table     [B, bt_stride] int32 DEVICE array, bt_stride >= ceil(B1/blk);
+ *                   page ids are clamped into [0, num_pages).
+ * Errors as rkv_compact_kt.
+ */
+rkv_status rkv_compact_kt_paged(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
+                                int64_t keep_ld, int64_t B1, void* k_pages, void* v_pages, int64_t num_pages,
+                                const int32_t* block_table, int64_t bt_stride, int32_t blk, void* kt,
+                                int64_t nblk_cap, void* stream);
+
+/*
  * KT cache build.  [RocketKV digest, 方法细节: HSA step 1 -- tokens grouped
  * into pages along the sequence, elementwise Kmax and Kmin per page stored
  * aligned along the head dimension]
@@ -258,9 +273,32 @@ rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, in
                                  const void* k_new, const void* v_new, void* stream);
 
 /*
+ * HSA decode step over paged K/V caches.  [RocketKV digest, 方法细节: HSA steps
+ * 1-3 and Algorithm 1; a page is one HSA block]  Same computation, arguments
+ * and results as rkv_hsa_decode_ragged, except that the K and V rows live in
+ * pools of pages of blk rows shared by every batch row:
+ *   k_pages,v_pages [num_pages, Hkv, blk, D] bf16 (16-byte aligned);
+ *   block_table     [B, bt_stride] int32 DEVICE array: logical block j of batch
+ *                   row b (its tokens j*blk .. j*blk+blk-1) is page
+ *                   block_table[b, j] of the pools, for every KV head;
+ *   n_rows          [B] int32 DEVICE array of candidates before the append, or
+ *                   NULL: every row has n_max.
+ * With the fused append the token goes to slot n % blk of page
+ * block_table[b, n / blk], which the caller must have assigned.  KT stays
+ * per (b, h) in logical block order, as for the dense caches.  Page ids out
+ * of [0, num_pages) are clamped and set bit 1 of the device error word.
+ * Requires n_max (+1) <= bt_stride * blk and the limits of rkv_hsa_decode.
+ */
+rkv_status rkv_hsa_decode_paged(rkv_dims d, const void* q, void* k_pages, void* v_pages, int64_t num_pages,
+                                const int32_t* block_table, int64_t bt_stride, const int32_t* n_rows, int64_t n_max,
+                                void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
+                                float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
+                                const void* v_new, void* stream);
+
+/*
  * Read and clear the library's device error word (synchronises the device).
  * Bit 0: a bounded wait for an asynchronous copy gave up in some kernel.
- * Bit 1: a per-row length read from device memory was out of range.
+ * Bit 1: a per-row length or page id read from device memory was out of range.
  * Returns RKV_ERR_TIMEOUT if any bit was set, RKV_OK otherwise.
  */
 rkv_status rkv_read_device_flags(uint32_t* flags);

@@ -293,6 +293,93 @@ def test_hsa_decode_ragged_length_out_of_range_flagged():
     assert torch.isfinite(out).all()
 
 
+def _page_table(rng, B, nblk_row, extra):
+    """A random block table [B, nblk_row] over num_pages = B * nblk_row + extra pages (all distinct)."""
+    num_pages = B * nblk_row + extra
+    return rng.permutation(num_pages)[:B * nblk_row].reshape(B, nblk_row).astype(np.int32), num_pages
+
+
+@pytest.mark.parametrize("blk", [16, 4])
+def test_compact_kt_paged_matches_dense(blk):
+    B, Hq, Hkv, D, cap, B1 = 2, 8, 2, 128, 900, 333
+    dims = (B, Hq, Hkv, D)
+    _, k = _rand(101, (B, Hkv, cap, D))
+    _, v = _rand(102, (B, Hkv, cap, D))
+    rng = np.random.default_rng(7)
+    keep = np.stack([np.stack([np.sort(rng.choice(cap, B1, replace=False)) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32)
+    keep_t = torch.from_numpy(keep).to(DEV)
+    nblk = -(-B1 // blk)
+    ncap = -(-nblk // 8) * 8
+    bt, num_pages = _page_table(rng, B, nblk, 5)
+    bt_t = torch.from_numpy(bt).to(DEV)
+    ko = torch.zeros((B, Hkv, nblk * blk, D), dtype=torch.bfloat16, device=DEV)
+    vo = torch.zeros_like(ko)
+    ktd = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    kp = torch.zeros((num_pages, Hkv, blk, D), dtype=torch.bfloat16, device=DEV)
+    vp = torch.zeros_like(kp)
+    ktp = torch.zeros_like(ktd)
+    rkv.rkv_compact_kt(dims, k, v, cap, keep_t, B1, B1, ko, vo, nblk * blk, blk, ktd, ncap)
+    rkv.rkv_compact_kt_paged(dims, k, v, cap, keep_t, B1, B1, kp, vp, num_pages, bt_t, nblk, blk, ktp, ncap)
+    torch.cuda.synchronize()
+    assert torch.equal(ktd, ktp)
+    for b in range(B):
+        for j in range(nblk):
+            r = min(blk, B1 - j * blk)
+            assert torch.equal(kp[bt[b, j], :, :r], ko[b, :, j * blk:j * blk + r])
+            assert torch.equal(vp[bt[b, j], :, :r], vo[b, :, j * blk:j * blk + r])
+
+
+@pytest.mark.parametrize("blk,append", [(16, False), (16, True), (4, True)])
+def test_hsa_decode_paged_equals_dense(blk, append):
+    """Paged pools addressed through a block table give bit-identical results to the
+    dense caches (same rows, same order), with per-row lengths and the fused append
+    landing in slot n % blk of page block_table[b, n / blk]."""
+    B, Hq, Hkv, D, k1, k2 = 3, 32, 8, 128, 32, 8
+    n_rows = [300, 611, 57]
+    n_max = max(n_rows)
+    nblk_row = -(-(n_max + 1) // blk)
+    cap = nblk_row * blk
+    dims = (B, Hq, Hkv, D)
+    _, k = _rand(111, (B, Hkv, cap, D))
+    _, v = _rand(112, (B, Hkv, cap, D))
+    _, q = _rand(113, (B, Hq, D))
+    _, knew = _rand(114, (B, Hkv, D))
+    _, vnew = _rand(115, (B, Hkv, D))
+    rng = np.random.default_rng(11)
+    bt, num_pages = _page_table(rng, B, nblk_row, 3)
+    bt_t = torch.from_numpy(bt).to(DEV)
+    kp = torch.zeros((num_pages, Hkv, blk, D), dtype=torch.bfloat16, device=DEV)
+    vp = torch.zeros_like(kp)
+    for b in range(B):
+        for j in range(nblk_row):
+            kp[bt[b, j]] = k[b, :, j * blk:(j + 1) * blk]
+            vp[bt[b, j]] = v[b, :, j * blk:(j + 1) * blk]
+    ncap = -(-nblk_row // 8) * 8
+    ktd = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    for b in range(B):
+        rkv.rkv_build_kt((1, Hq, Hkv, D), k[b:b + 1], cap, n_rows[b], None, 0, blk, ktd[b:b + 1], ncap)
+    ktp = ktd.clone()
+    n_dev = torch.tensor(n_rows, dtype=torch.int32, device=DEV)
+    scale = 1 / math.sqrt(D)
+    od = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    op = torch.empty_like(od)
+    sd = torch.empty((B, Hkv, k2), dtype=torch.int32, device=DEV)
+    sp = torch.empty_like(sd)
+    kn_, vn_ = (knew, vnew) if append else (None, None)
+    rkv.rkv_hsa_decode_ragged(dims, q, k, v, cap, n_dev, n_max, ktd, ncap, blk, k1, k2, scale, od, sd, None, kn_, vn_)
+    rkv.rkv_hsa_decode_paged(dims, q, kp, vp, num_pages, bt_t, nblk_row, n_dev, n_max, ktp, ncap, blk, k1, k2, scale,
+                             op, sp, None, kn_, vn_)
+    torch.cuda.synchronize()
+    assert rkv.rkv_read_device_flags() == 0
+    assert torch.equal(sd, sp) and torch.equal(od, op) and torch.equal(ktd, ktp)
+    if append:
+        for b in range(B):
+            n = n_rows[b]
+            assert torch.equal(kp[bt[b, n // blk], :, n % blk], k[b, :, n])
+            assert torch.equal(vp[bt[b, n // blk], :, n % blk], v[b, :, n])
+
+
 def test_hsa_decode_exact_topk_pin():
     """k1 = D and block 1: the block score is qbar . k_j exactly, so the chosen tokens
     are the plain top-k2 of qbar . k (lowest index on ties) and the output is

@@ -111,7 +111,8 @@ rkv_status make_q_map(CUtensorMap* m, const void* base, int64_t rows, int box_ro
 rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_t cap, int32_t* idx,
                       int64_t idx_cap, int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
                       float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
-                      const void* v_new, int64_t row, void* stream, bool mt, const int32_t* n_rows = nullptr) {
+                      const void* v_new, int64_t row, void* stream, bool mt, const int32_t* n_rows = nullptr,
+                      const int32_t* block_table = nullptr, int64_t bt_stride = 0, int64_t num_pages = 0) {
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
@@ -151,7 +152,8 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.row = mt ? row : n;
   a.sel_blocks = sel_blocks; a.sel_channels = sel_channels;
   a.cap = cap; a.nblk_cap = nblk_cap; a.idx_cap = idx_cap;
-  a.n = (int32_t)n; a.n_rows = n_rows; a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
+  a.n = (int32_t)n; a.n_rows = n_rows; a.B = d.batch;
+  a.block_table = block_table; a.bt_stride = bt_stride; a.num_pages = num_pages; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
   a.blk = blk; a.k1 = k1; a.k2 = k2;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.tma_kv = (!mt && blk % 8 == 0) ? 1 : 0;
@@ -162,7 +164,12 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   std::memset(&tmV, 0, sizeof(tmV));
   std::memset(&tmKT, 0, sizeof(tmKT));
   const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
-  if (a.tma_kv) {
+  if (a.tma_kv && block_table) {
+    // one (page, KV head) slab of blk rows per box; the kernel masks rows past n
+    const int64_t slabs = num_pages * d.n_kv_heads;
+    if ((s = make_kv_map(&tmK, k, slabs, blk, blk, blk, "k pages")) != RKV_OK) return s;
+    if ((s = make_kv_map(&tmV, v, slabs, blk, blk, blk, "v pages")) != RKV_OK) return s;
+  } else if (a.tma_kv) {
     // rows at or past n (the appended token included) read as zero; with
     // per-row lengths every row up to cap is readable and the kernel masks
     const int64_t extent = n_rows ? cap : std::max<int64_t>(n, 1);
@@ -315,6 +322,33 @@ rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap,
   return RKV_OK;
 }
 
+rkv_status rkv_compact_kt_paged(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
+                                int64_t keep_ld, int64_t B1, void* k_pages, void* v_pages, int64_t num_pages,
+                                const int32_t* block_table, int64_t bt_stride, int32_t blk, void* kt,
+                                int64_t nblk_cap, void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0 || B1 == 0) return RKV_OK;
+  if (!k || !v || !keep_idx || !k_pages || !v_pages || !block_table || !kt)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: NULL pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(kt))
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: k, v, k_pages, v_pages and kt must be 16-byte aligned");
+  if (cap < 1 || B1 < 0 || keep_ld < B1)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: need cap >= 1, B1 >= 0 and keep_ld >= B1");
+  if (blk < 1) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: blk < 1");
+  const int64_t nblk = (B1 + blk - 1) / blk;
+  if (bt_stride < nblk) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: bt_stride < ceil(B1/blk)");
+  if (num_pages < 1) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: num_pages < 1");
+  if (nblk_cap % 8 != 0) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: nblk_cap=%lld is not a multiple of 8",
+                                     (long long)nblk_cap);
+  if (nblk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: nblk_cap too small");
+  cudaError_t e = rkv::compact_kt_launch(k, v, cap, keep_idx, keep_ld, B1, blk, k_pages, v_pages, 0, kt, nblk_cap,
+                                         d.batch * d.n_kv_heads, reinterpret_cast<cudaStream_t>(stream), block_table,
+                                         bt_stride, num_pages, d.n_kv_heads);
+  if (e != cudaSuccess) return cuda_fail(e, "compact_kt_paged launch");
+  return RKV_OK;
+}
+
 rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
                          int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
                          void* stream) {
@@ -356,6 +390,24 @@ rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, in
   if (n_max < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_ragged: n_max=%lld < 1", (long long)n_max);
   return hsa_common(d, q, k, v, cap, nullptr, 0, n_max, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
                     sel_channels, k_new, v_new, 0, stream, false, n_rows);
+}
+
+rkv_status rkv_hsa_decode_paged(rkv_dims d, const void* q, void* k_pages, void* v_pages, int64_t num_pages,
+                                const int32_t* block_table, int64_t bt_stride, const int32_t* n_rows, int64_t n_max,
+                                void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
+                                float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
+                                const void* v_new, void* stream) {
+  if (d.batch > 0 && !block_table) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_paged: block_table is NULL");
+  if (n_max < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_paged: n_max=%lld < 1", (long long)n_max);
+  if (num_pages < 1 || num_pages * (int64_t)d.n_kv_heads * blk >= ((int64_t)1 << 31))
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_paged: num_pages=%lld outside [1, 2^31 / (Hkv * blk))",
+                (long long)num_pages);
+  if (blk < 1 || bt_stride < 1 || bt_stride > ((int64_t)1 << 31) / blk)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_paged: bt_stride=%lld, blk=%d", (long long)bt_stride, blk);
+  // a row's logical capacity is bt_stride pages of blk rows
+  return hsa_common(d, q, k_pages, v_pages, bt_stride * blk, nullptr, 0, n_max, kt, nblk_cap, blk, k1, k2, scale,
+                    out, sel_blocks, sel_channels, k_new, v_new, 0, stream, false, n_rows, block_table, bt_stride,
+                    num_pages);
 }
 
 rkv_status rkv_read_device_flags(uint32_t* flags) {

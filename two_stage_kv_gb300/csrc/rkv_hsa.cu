@@ -257,7 +257,10 @@ __device__ __forceinline__ void block_minmax(float& mn, float& mx, FixedSmem& fs
   }
 }
 
-template <bool MT, int NH, bool RAG>
+// RAG: lengths read after the dependency wait (n_rows, or the call's n when
+// n_rows is NULL); PG: K/V in pages of blk rows, [num_pages, Hkv, blk, D], found
+// through a per-row block table (implies RAG).
+template <bool MT, int NH, bool RAG, bool PG>
 __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                            const __grid_constant__ CUtensorMap tmV,
                                                            const __grid_constant__ CUtensorMap tmKT,
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   float* sval = reinterpret_cast<float*>(smem + a.off_scores);
   uint8_t* flag = reinterpret_cast<uint8_t*>(smem + a.off_flags);
   int32_t* sel = reinterpret_cast<int32_t*>(smem + a.off_sel);
+  int32_t* bt_s = reinterpret_cast<int32_t*>(smem + a.off_bt);         // paged: page of each block
   float* recv = reinterpret_cast<float*>(smem + a.off_recv);
   uint8_t* tK = smem + a.off_tiles;
   uint8_t* tV = tK + 2 * a.tile_half_bytes;
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   if (RAG) {
     // this batch row's length, clamped into [1, the call's maximum] (an entry out
     // of range raises ERR_BAD_LENGTH)
-    const int nr = a.n_rows[b];
+    const int nr = a.n_rows ? a.n_rows[b] : a.n;
     n_old = min(max(nr, 1), a.n);
     if (nr != n_old && tid == 0 && rank == 0) atomicOr(&g_hsa_err, ERR_BAD_LENGTH);
     n_tot = n_old + (app ? 1 : 0);
@@ -334,6 +338,17 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     own_new = app && nb_new >= jlo && nb_new < jhi;
     // (a remote byte count arriving before this arrival is fine: the phase needs both)
     if (tid == 0) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(nblk * 4 + ns * NWARP * 8));
+  }
+  if (PG) {
+    // this row's block table (published by the barriers of phase A); a page id out
+    // of range is clamped and raises ERR_BAD_LENGTH
+    const int32_t* btr = a.block_table + (size_t)b * a.bt_stride;
+    for (int j = tid; j < nblk; j += NT) {
+      const int pg = btr[j];
+      const int pc = min(max(pg, 0), (int)a.num_pages - 1);
+      if (pg != pc && rank == 0) atomicOr(&g_hsa_err, ERR_BAD_LENGTH);
+      bt_s[j] = pc;
+    }
   }
   // KT rows do not depend on the query: with the prefetch, all 2*D rows of this
   // CTA's blocks are in flight while the channels are chosen
@@ -615,15 +630,16 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         __syncwarp();
         const int part = warp & 3;                   // K lo, K hi, V lo, V hi
         for (int s = (warp >> 2) + 2 * lane; s < nsl; s += 64) {
-          const int y = sel[r0 + s] * blk;
+          // dense: rows sel*blk.. of the pair's cache; paged: the whole (page, head) slab
+          const int y = PG ? 0 : sel[r0 + s] * blk;
+          const int z = PG ? bt_s[sel[r0 + s]] * a.Hkv + hk : pair;
           const uint32_t off = (uint32_t)s * blk * 128u + (uint32_t)(part & 1) * half;
-          tma_load_3d(((part >> 1) ? tV : tK) + off, (part >> 1) ? &tmV : &tmK, (part & 1) * 64, y, pair,
-                      &fs.mbar[s]);
+          tma_load_3d(((part >> 1) ? tV : tK) + off, (part >> 1) ? &tmV : &tmK, (part & 1) * 64, y, z, &fs.mbar[s]);
         }
       }
     } else {
-      const bf16* kb = reinterpret_cast<const bf16*>(a.k) + (size_t)pair * a.cap * HD;
-      const bf16* vb = reinterpret_cast<const bf16*>(a.v) + (size_t)pair * a.cap * HD;
+      const bf16* kb = reinterpret_cast<const bf16*>(a.k) + (PG ? (size_t)0 : (size_t)pair * a.cap * HD);
+      const bf16* vb = reinterpret_cast<const bf16*>(a.v) + (PG ? (size_t)0 : (size_t)pair * a.cap * HD);
       const int32_t* ib = MT ? a.idx + (size_t)pair * a.idx_cap : nullptr;
       for (int i = tid; i < rows * 16; i += NT) {
         const int r = i >> 4, ch = i & 15;
@@ -631,7 +647,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         const int t = sel[r0 + slot] * blk + (r - slot * blk);
         const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
         if (t < n_old) {
-          const int64_t prow = MT ? min(max((int64_t)ib[t], (int64_t)0), a.cap - 1) : (int64_t)t;
+          // row of token t: MT candidate row, paged (page, head) slab row, or t itself
+          const int64_t prow = MT ? min(max((int64_t)ib[t], (int64_t)0), a.cap - 1)
+                               : PG ? ((int64_t)bt_s[t / blk] * a.Hkv + hk) * blk + (t % blk) : (int64_t)t;
           cp_async_16(smem_u32(tK) + o, kb + prow * HD + ch * 8);
           cp_async_16(smem_u32(tV) + o, vb + prow * HD + ch * 8);
         } else if (t == n_old && app) {
@@ -877,7 +895,8 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       // persist the appended token: cache row and candidate index (MT)
       if (tid < 32) {
         bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
-                    ((size_t)pair * a.cap + (MT ? a.row : (int64_t)n_old)) * HD + (tid & 15) * 8;
+                    (PG ? (((size_t)bt_s[nb_new] * a.Hkv + hk) * blk + (size_t)(n_old % blk))
+                        : (size_t)pair * a.cap + (MT ? a.row : (int64_t)n_old)) * HD + (tid & 15) * 8;
         *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 16 ? fs.knew : fs.vnew) +
                                                                           (tid & 15) * 8);
       }
@@ -929,6 +948,8 @@ bool hsa_plan(HsaArgs& a) {
   off = al(off + (uint32_t)nblk8, 16);
   a.off_sel = off;
   off = al(off + 4u * (uint32_t)std::max(a.k2e, 1), 16);
+  a.off_bt = off;
+  if (a.block_table) off = al(off + 4u * (uint32_t)nblk8, 16);
   a.off_recv = off;
   off = al(off + 4u * gown * a.ns * PART_STRIDE, 1024);
   a.off_tiles = off;                       // K/V tiles; the KT gather tile shares this region
@@ -944,9 +965,11 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    const void* ks[6] = {(const void*)hsa_decode_kernel<false, 1, false>, (const void*)hsa_decode_kernel<false, 2, false>,
-                         (const void*)hsa_decode_kernel<true, 1, false>, (const void*)hsa_decode_kernel<true, 2, false>,
-                         (const void*)hsa_decode_kernel<false, 1, true>, (const void*)hsa_decode_kernel<false, 2, true>};
+    const void* ks[8] = {
+        (const void*)hsa_decode_kernel<false, 1, false, false>, (const void*)hsa_decode_kernel<false, 2, false, false>,
+        (const void*)hsa_decode_kernel<true, 1, false, false>, (const void*)hsa_decode_kernel<true, 2, false, false>,
+        (const void*)hsa_decode_kernel<false, 1, true, false>, (const void*)hsa_decode_kernel<false, 2, true, false>,
+        (const void*)hsa_decode_kernel<false, 1, true, true>, (const void*)hsa_decode_kernel<false, 2, true, true>};
     for (const void* k : ks) {
       attr_err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       if (attr_err != cudaSuccess) break;
@@ -969,9 +992,11 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   cfg.numAttrs = 2;
   // per-row lengths (ragged batches) take their own instantiation: the uniform
   // kernels keep every length a launch constant
-  auto kern = mt ? (a.G > 8 ? hsa_decode_kernel<true, 2, false> : hsa_decode_kernel<true, 1, false>)
-          : a.n_rows ? (a.G > 8 ? hsa_decode_kernel<false, 2, true> : hsa_decode_kernel<false, 1, true>)
-                     : (a.G > 8 ? hsa_decode_kernel<false, 2, false> : hsa_decode_kernel<false, 1, false>);
+  const bool wide = a.G > 8;
+  auto kern = mt ? (wide ? hsa_decode_kernel<true, 2, false, false> : hsa_decode_kernel<true, 1, false, false>)
+          : a.block_table ? (wide ? hsa_decode_kernel<false, 2, true, true> : hsa_decode_kernel<false, 1, true, true>)
+          : a.n_rows ? (wide ? hsa_decode_kernel<false, 2, true, false> : hsa_decode_kernel<false, 1, true, false>)
+                     : (wide ? hsa_decode_kernel<false, 2, false, false> : hsa_decode_kernel<false, 1, false, false>);
   return cudaLaunchKernelEx(&cfg, kern, *tmK, *tmV, *tmKT, a);
 }
 

@@ -29,6 +29,8 @@ struct HsaArgs {
   int64_t cap, nblk_cap, idx_cap;
   int32_t n, B, Hq, Hkv, G, blk, k1, k2;   // n = candidates before the append (ragged: the rows' maximum)
   const int32_t* n_rows; // ragged: [B] candidates before the append per batch row (device), else nullptr
+  const int32_t* block_table;  // paged: [B, bt_stride] page of each logical block (device), else nullptr
+  int64_t bt_stride, num_pages;  // paged: K/V pools are [num_pages, Hkv, blk, D]
   int32_t nblk;         // blocks over the attended candidates
   int32_t k2e;          // min(k2, nblk)
   int32_t ns;           // CTAs per cluster (one cluster per (b, kv head))
@@ -40,7 +42,7 @@ struct HsaArgs {
   int32_t tma_kv;       // 1: K/V block rows by TMA (blk a multiple of 8, no idx); 0: gathered rows
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared-memory layout (bytes)
-  uint32_t off_x, off_scores, off_flags, off_sel, off_recv, off_tiles, tile_half_bytes, smem_bytes;
+  uint32_t off_x, off_scores, off_flags, off_sel, off_bt, off_recv, off_tiles, tile_half_bytes, smem_bytes;
 };
 
 // Computes ns/chunk/slots_round and the shared-memory layout.  Returns false if
@@ -78,7 +80,8 @@ cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t
                             int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st);
 cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
                               int64_t B1, int blk, void* ko, void* vo, int64_t out_cap, void* kt, int64_t nblk_cap,
-                              int pairs, cudaStream_t st);
+                              int pairs, cudaStream_t st, const int32_t* bt = nullptr, int64_t bt_stride = 0,
+                              int64_t num_pages = 0, int Hkv = 1);
 cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
                           int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
                           int32_t pairs, cudaStream_t st);

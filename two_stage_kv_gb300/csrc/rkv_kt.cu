@@ -106,7 +106,8 @@ constexpr int CK_NT = 256;
 __global__ void __launch_bounds__(CK_NT) compact_kt_kernel(const bf16* k, const bf16* v, int64_t cap,
                                                            const int32_t* keep, int64_t keep_ld, int64_t B1, int blk,
                                                            bf16* ko, bf16* vo, int64_t out_cap, bf16* kt,
-                                                           int64_t nblk_cap) {
+                                                           int64_t nblk_cap, const int32_t* bt, int64_t bt_stride,
+                                                           int64_t num_pages, int Hkv) {
   __shared__ __align__(16) bf16 tile[2 * HD][CK_BLOCKS];   // row m*HD + c, column = block in the CTA
   pdl_wait();
   pdl_launch_dependents();
@@ -126,8 +127,18 @@ __global__ void __launch_bounds__(CK_NT) compact_kt_kernel(const bf16* k, const 
     const int32_t* kp = keep + (size_t)pair * keep_ld;
     const bf16* ks = k + (size_t)pair * cap * HD + ch * 8;
     const bf16* vs = v + (size_t)pair * cap * HD + ch * 8;
-    bf16* kd = ko + (size_t)pair * out_cap * HD + ch * 8;
-    bf16* vd = vo + (size_t)pair * out_cap * HD + ch * 8;
+    // output rows: the pair's compacted cache, or (paged) the block's (page, head)
+    // slab of blk rows, indexed from the block's first row t0
+    size_t obase = (size_t)pair * out_cap * HD;
+    int64_t rbase = 0;                       // compacted row of the first output row
+    if (bt) {
+      const int b = pair / Hkv, h = pair % Hkv;
+      const int64_t pg = min(max((int64_t)bt[(size_t)b * bt_stride + jb], (int64_t)0), num_pages - 1);
+      obase = (size_t)(pg * Hkv + h) * blk * HD;
+      rbase = t0;
+    }
+    bf16* kd = ko + obase + ch * 8;
+    bf16* vd = vo + obase + ch * 8;
     for (int64_t tb = t0; tb < t1; tb += 4) {
       uint4 kr[4], vr[4];
 #pragma unroll
@@ -141,8 +152,8 @@ __global__ void __launch_bounds__(CK_NT) compact_kt_kernel(const bf16* k, const 
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (tb + u < t1) {
-          *reinterpret_cast<uint4*>(kd + (tb + u) * HD) = kr[u];
-          *reinterpret_cast<uint4*>(vd + (tb + u) * HD) = vr[u];
+          *reinterpret_cast<uint4*>(kd + (tb + u - rbase) * HD) = kr[u];
+          *reinterpret_cast<uint4*>(vd + (tb + u - rbase) * HD) = vr[u];
           const uint32_t w[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -197,12 +208,13 @@ cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v
 
 cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
                               int64_t B1, int blk, void* ko, void* vo, int64_t out_cap, void* kt, int64_t nblk_cap,
-                              int pairs, cudaStream_t st) {
+                              int pairs, cudaStream_t st, const int32_t* bt, int64_t bt_stride, int64_t num_pages,
+                              int Hkv) {
   const int64_t nblk = (B1 + blk - 1) / blk;
   return launch_pdl(compact_kt_kernel, dim3((unsigned)((nblk + CK_BLOCKS - 1) / CK_BLOCKS), pairs), dim3(CK_NT), 0, st,
                     reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v), cap, keep, keep_ld, B1, blk,
                     reinterpret_cast<bf16*>(ko), reinterpret_cast<bf16*>(vo), out_cap, reinterpret_cast<bf16*>(kt),
-                    nblk_cap);
+                    nblk_cap, bt, bt_stride, num_pages, Hkv);
 }
 
 }  // namespace rkv

@@ -20,8 +20,8 @@ STATUS_NAMES = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
 
 # Every symbol include/rkv.h declares.
 EXPORTED = ["rkv_last_error", "rkv_abi_version", "rkv_budget_split", "rkv_snap_evict_workspace",
-            "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
-            "rkv_hsa_decode_ragged",
+            "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_compact_kt_paged", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
+            "rkv_hsa_decode_ragged", "rkv_hsa_decode_paged",
             "rkv_read_device_flags"]
 
 
@@ -51,6 +51,8 @@ _SIGS = {
     "rkv_snap_evict_noalloc": (_i32, [Dims, _vp, _i32, _vp, _vp, _i64, _i64, _i32, _i32, _i64, _f32, _vp, _i64, _vp,
                                       _vp, _i64, _vp, _vp]),
     "rkv_compact_kt": (_i32, [Dims, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp]),
+    "rkv_compact_kt_paged": (_i32, [Dims, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _i64, _i32, _vp,
+                                    _i64, _vp]),
     "rkv_build_kt": (_i32, [Dims, _vp, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _vp]),
     "rkv_append_kv": (_i32, [Dims, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i32, _vp]),
     "rkv_hsa_decode": (_i32, [Dims, _vp, _vp, _vp, _i64, _i64, _vp, _i64, _i32, _i32, _i32, _f32, _vp, _vp, _vp,
@@ -59,6 +61,8 @@ _SIGS = {
                                  _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "rkv_hsa_decode_ragged": (_i32, [Dims, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _i32, _i32, _f32, _vp,
                                      _vp, _vp, _vp, _vp, _vp]),
+    "rkv_hsa_decode_paged": (_i32, [Dims, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _i32, _i32,
+                                    _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "rkv_read_device_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -137,6 +141,13 @@ def rkv_compact_kt(dims, k, v, cap, keep_idx, keep_ld, B1, k_out, v_out, out_cap
                                 _ptr(v_out), out_cap, blk, _ptr(kt), nblk_cap, _stream(stream)))
 
 
+def rkv_compact_kt_paged(dims, k, v, cap, keep_idx, keep_ld, B1, k_pages, v_pages, num_pages, block_table, bt_stride,
+                         blk, kt, nblk_cap, stream=None):
+    _check(lib().rkv_compact_kt_paged(_dims(dims), _ptr(k), _ptr(v), cap, _ptr(keep_idx), keep_ld, B1, _ptr(k_pages),
+                                      _ptr(v_pages), num_pages, _ptr(block_table), bt_stride, blk, _ptr(kt), nblk_cap,
+                                      _stream(stream)))
+
+
 def rkv_build_kt(dims, k, cap, n, idx, idx_cap, blk, kt, nblk_cap, stream=None):
     _check(lib().rkv_build_kt(_dims(dims), _ptr(k), cap, n, _ptr(idx), idx_cap, blk, _ptr(kt), nblk_cap,
                               _stream(stream)))
@@ -167,6 +178,16 @@ def rkv_hsa_decode_ragged(dims, q, k, v, cap, n_rows, n_max, kt, nblk_cap, blk, 
     _check(lib().rkv_hsa_decode_ragged(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, _ptr(n_rows), n_max, _ptr(kt),
                                        nblk_cap, blk, k1, k2, scale, _ptr(out), _ptr(sel_blocks),
                                        _ptr(sel_channels), _ptr(k_new), _ptr(v_new), _stream(stream)))
+
+
+def rkv_hsa_decode_paged(dims, q, k_pages, v_pages, num_pages, block_table, bt_stride, n_rows, n_max, kt, nblk_cap,
+                         blk, k1, k2, scale, out, sel_blocks=None, sel_channels=None, k_new=None, v_new=None,
+                         stream=None):
+    """HSA decode over paged K/V pools [num_pages, Hkv, blk, D] addressed by a block table."""
+    _check(lib().rkv_hsa_decode_paged(_dims(dims), _ptr(q), _ptr(k_pages), _ptr(v_pages), num_pages,
+                                      _ptr(block_table), bt_stride, _ptr(n_rows), n_max, _ptr(kt), nblk_cap, blk, k1,
+                                      k2, scale, _ptr(out), _ptr(sel_blocks), _ptr(sel_channels), _ptr(k_new),
+                                      _ptr(v_new), _stream(stream)))
 
 
 def rkv_read_device_flags() -> int:
