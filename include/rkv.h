@@ -104,7 +104,9 @@ size_t rkv_snap_evict_workspace(rkv_dims d, int64_t S, int32_t W);
  *              written (keep_ld >= B1; MT callers point it at their idx rows).
  *   k_out,v_out[B, Hkv, out_cap, D] bf16 compacted caches (rows [0, B1)
  *              written).  Both NULL = MT mask mode: only keep_idx is written.
- *   pooled_out optional [B, Hkv, S-W] fp32 pooled scores (NULL = skip).
+ *   pooled_out optional [B, Hkv, S-W] fp32 pooled scores (NULL = skip); the
+ *              ranking itself uses log2 of the scores, so scores below the
+ *              fp32 range (written here as 0) still rank exactly.
  *   ws         workspace of rkv_snap_evict_workspace() bytes.
  * k/v and k_out/v_out must not overlap.
  */

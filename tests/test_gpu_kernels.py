@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from parity_util import ATOL_OUT, SCORE_FLOOR, check_topk, max_abs, t2bits, t2f64
+from parity_util import ATOL_OUT, check_topk, max_abs, t2bits, t2f64
 from two_stage_kv_gb300 import rkv
 from two_stage_kv_gb300.synth import bf16_bits_to_f64, small_random
 
@@ -498,8 +498,7 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
             ns = min(n_sink, L)
             assert got[:ns].tolist() == list(range(ns))
             assert got[B1 - min(W, S):].tolist() == list(range(S - min(W, S), S))
-            exempt += check_topk(got[ns:B1 - min(W, S)] - ns, pooled_o[ns:], B1 - min(W, S) - ns, "keep",
-                                 floor=SCORE_FLOOR)
+            exempt += check_topk(got[ns:B1 - min(W, S)] - ns, pooled_o[ns:], B1 - min(W, S) - ns, "keep")
             if compact:
                 assert np.array_equal(t2bits(ko[b, h, :B1]), kb[b, h][got])
                 assert np.array_equal(t2bits(vo[b, h, :B1]), vb[b, h][got])

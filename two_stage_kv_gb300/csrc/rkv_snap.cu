@@ -382,18 +382,43 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
           const int T = T0 + t;
           if (!tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err)) break;
           tc_fence_after();
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          // the key's score is kept as log2 of the sum of its probabilities,
+          // log2 sum_c 2^(y_c) with y_c = logit * scale - lse_c (log2 units): a
+          // running maximum over 32-row chunks keeps scores far below the fp32
+          // range exact in rank, so the keep set does not depend on underflow
           const float2 sc = make_float2(a.scale_log2, a.scale_log2);
           const float4* nl4 = reinterpret_cast<const float4*>(ts.nlse);
-          auto sum32 = [&](const float* v, int c0) {
+          float lm = neg_inf(), ls = 0.f;
+          auto lse32 = [&](float* v, int c0) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               const float4 nl = nl4[(c0 + i) >> 2];   // same address across the warp: broadcast
               const float2 x0 = fma_f2(make_float2(v[i], v[i + 1]), sc, make_float2(nl.x, nl.y));
               const float2 x1 = fma_f2(make_float2(v[i + 2], v[i + 3]), sc, make_float2(nl.z, nl.w));
-              acc[(i >> 2) & 3] = add_f2(acc[(i >> 2) & 3], make_float2(ex2_ftz(x0.x), ex2_ftz(x0.y)));
-              acc[((i >> 2) + 2) & 3] = add_f2(acc[((i >> 2) + 2) & 3], make_float2(ex2_ftz(x1.x), ex2_ftz(x1.y)));
+              v[i] = x0.x;
+              v[i + 1] = x0.y;
+              v[i + 2] = x1.x;
+              v[i + 3] = x1.y;
             }
+            float x0 = fmax3(v[0], v[1], v[2]), x1 = fmax3(v[3], v[4], v[5]);
+#pragma unroll
+            for (int i = 6; i < 30; i += 4) {
+              x0 = fmax3(x0, v[i], v[i + 1]);
+              x1 = fmax3(x1, v[i + 2], v[i + 3]);
+            }
+            const float mn = fmaxf(lm, fmax3(x0, x1, fmaxf(v[30], v[31])));
+            if (mn == neg_inf()) return;                 // rows past the group (or all masked)
+            const float2 nm = make_float2(-mn, -mn);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 d = add_f2(make_float2(v[i], v[i + 1]), nm);
+              acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3], make_float2(ex2_ftz(d.x), ex2_ftz(d.y)));
+            }
+            const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
+            ls = (lm == neg_inf() ? 0.f : ls * ex2_ftz(lm - mn)) + (s01.x + s01.y);
+            lm = mn;
           };
           for (int c0 = 0; c0 < nq; c0 += 64) {        // nq is a multiple of 32
             float v[2][32];
@@ -401,14 +426,13 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
             tmem_ld32(lane_addr + c0, v[0]);
             if (two) tmem_ld32(lane_addr + c0 + 32, v[1]);
             tmem_wait_ld();
-            sum32(v[0], c0);
-            if (two) sum32(v[1], c0 + 32);
+            lse32(v[0], c0);
+            if (two) lse32(v[1], c0 + 32);
           }
-          const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
           tc_fence_before();
           mbar_arrive(&ts.tempty[eset]);
           const int j = j032 + t * T_KEYS + r_loc;
-          if (j < L32) a.scores[((size_t)pair * a.RG2 + it.rg) * a.L + j] = s01.x + s01.y;
+          if (j < L32) a.scores[((size_t)pair * a.RG2 + it.rg) * a.L + j] = lm == neg_inf() ? neg_inf() : lm + log2f(ls);
         }
       }
       T0 += it.ntiles;
@@ -424,12 +448,21 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
   }
 }
 
-// Sum of the row-group partials (fixed order), then max-pool (clipped ends).
+// log2(2^a + 2^b) for log2-domain scores (-inf is an empty sum).
+__device__ __forceinline__ float log2_add(float a, float b) {
+  const float m = fmaxf(a, b);
+  if (m == neg_inf()) return m;
+  return m + log2f(exp2f(a - m) + exp2f(b - m));
+}
+
+// Sum of the row-group partials (fixed order, log2 domain), then max-pool
+// (clipped ends).  pooled_log gets log2 of the pooled scores (what the select
+// ranks); pooled_out, if set, the scores themselves (0 below the fp32 range).
 constexpr int POOL_TILE = 1024;
 constexpr int POOL_MAX_HALF = 512;
 
 __global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int RG, int64_t L, int half,
-                                                        float* pooled) {
+                                                        float* pooled_log, float* pooled_out) {
   __shared__ float tile[POOL_TILE + 2 * POOL_MAX_HALF];
   pdl_wait();
   pdl_launch_dependents();
@@ -440,8 +473,8 @@ __global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int
     const int64_t j = j0 - half + i;
     float v = neg_inf();
     if (j >= 0 && j < L) {
-      v = 0.f;
-      for (int r = 0; r < RG; ++r) v += scores[((size_t)pair * RG + r) * L + j];
+      v = scores[((size_t)pair * RG) * L + j];
+      for (int r = 1; r < RG; ++r) v = log2_add(v, scores[((size_t)pair * RG + r) * L + j]);
     }
     tile[i] = v;
   }
@@ -451,7 +484,8 @@ __global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int
     if (j >= L) break;
     float m = tile[i];
     for (int t = 1; t <= 2 * half; ++t) m = fmaxf(m, tile[i + t]);
-    pooled[(size_t)pair * L + j] = m;
+    pooled_log[(size_t)pair * L + j] = m;
+    if (pooled_out) pooled_out[(size_t)pair * L + j] = exp2f(m);
   }
 }
 
@@ -613,11 +647,11 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
       const int j = u0 + t * PS_NT - h;
       v[t] = (j >= 0 && j < L) ? __ldg(sc + j) : neg_inf();
     }
-    for (int r = 1; r < RG; ++r) {
+    for (int r = 1; r < RG; ++r) {              // row-group partials, log2 domain
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int j = u0 + t * PS_NT - h;
-        if (j >= 0 && j < L) v[t] += __ldg(sc + (size_t)r * L + j);
+        if (j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * L + j));
       }
     }
 #pragma unroll
@@ -658,7 +692,7 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
       float* po = pooled_out + (size_t)pair * L;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (i < E && a + i < L) po[a + i] = pv[i];
+        if (i < E && a + i < L) po[a + i] = exp2f(pv[i]);
     }
   }
   __syncthreads();
@@ -848,7 +882,7 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     w += al256((size_t)pairs * p.R * p.nchunk1 * sizeof(float2));
     p.scores = reinterpret_cast<float*>(w);
     w += al256((size_t)pairs * p.RG2 * L * sizeof(float));
-    float* pooled = a.pooled_out ? a.pooled_out : reinterpret_cast<float*>(w);
+    float* pooled_log = reinterpret_cast<float*>(w);   // log2 pooled scores (separate pool + select)
 
     p.pairs = pairs;
     p.nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
@@ -871,9 +905,9 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
       if (e != cudaSuccess) return e;
     } else {
       e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
-                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, pooled);
+                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, pooled_log, a.pooled_out);
       if (e != cudaSuccess) return e;
-      e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)pooled, (int64_t)L,
+      e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)pooled_log, (int64_t)L,
                      (int64_t)a.S, (int)W, (int)n_sink, (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
       if (e != cudaSuccess) return e;
     }
