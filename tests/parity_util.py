@@ -29,7 +29,7 @@ def t2f64(t):
     return bf16_bits_to_f64(t2bits(t))
 
 
-def check_topk(gpu_idx, scores, k, what="", rel=REL_TIE, floor=0.0):
+def check_topk(gpu_idx, scores, k, what="", rel=REL_TIE):
     """Returns the number of tie-exempt differences; asserts everything else."""
     from oracle import kth_value, topk_lowest_index
     gpu_idx = np.asarray(gpu_idx, dtype=np.int64)
@@ -44,8 +44,6 @@ def check_topk(gpu_idx, scores, k, what="", rel=REL_TIE, floor=0.0):
     kth = kth_value(scores, k)
     diff = np.setxor1d(gpu_idx, ref)
     exempt = np.abs(scores[diff] - kth) <= rel * abs(kth)
-    if kth <= floor:
-        exempt |= scores[diff] <= floor
     assert np.all(exempt), (f"{what}: non-exempt differences at {diff[~exempt][:10]} "
                             f"(scores {scores[diff[~exempt][:10]]}, k-th {kth})")
     return int(diff.size)
