@@ -267,7 +267,8 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
         float m = neg_inf(), l = 0.f;
         for (int t = tfirst; t < it.ntiles; t += 2) {
           const int T = T0 + t;
-          if (!tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err)) break;
+          // the warp gives up together: the TMEM loads below are warp-collective
+          if (!__all_sync(0xffffffffu, tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err))) break;
           tc_fence_after();
           // online softmax over the tile's four 32-key chunks; the next chunk's
           // TMEM load is in flight while one is reduced (64 value registers)
@@ -380,45 +381,27 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
         }
         for (int t = tfirst; t < it.ntiles; t += 2) {
           const int T = T0 + t;
-          if (!tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err)) break;
+          // the warp gives up together: the TMEM loads below are warp-collective
+          if (!__all_sync(0xffffffffu, tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err))) break;
           tc_fence_after();
-          // the key's score is kept as log2 of the sum of its probabilities,
-          // log2 sum_c 2^(y_c) with y_c = logit * scale - lse_c (log2 units): a
-          // running maximum over 32-row chunks keeps scores far below the fp32
-          // range exact in rank, so the keep set does not depend on underflow
+          // the key's score is written as log2 of the sum of its probabilities,
+          // sum_c 2^(y_c) with y_c = logit * scale - lse_c (log2 units).  A plain
+          // fp32 sum is exact to about 2^-17 relative while it stays above 2^-100
+          // (flushed terms are below 2^-126 each, at most 512 of them); a warp with
+          // a smaller sum re-reads its accumulator and takes a log-sum-exp over
+          // 32-row chunks instead, so scores far below the fp32 range keep their rank
           const float2 sc = make_float2(a.scale_log2, a.scale_log2);
           const float4* nl4 = reinterpret_cast<const float4*>(ts.nlse);
-          float lm = neg_inf(), ls = 0.f;
-          auto lse32 = [&](float* v, int c0) {
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          auto sum32 = [&](const float* v, int c0) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               const float4 nl = nl4[(c0 + i) >> 2];   // same address across the warp: broadcast
               const float2 x0 = fma_f2(make_float2(v[i], v[i + 1]), sc, make_float2(nl.x, nl.y));
               const float2 x1 = fma_f2(make_float2(v[i + 2], v[i + 3]), sc, make_float2(nl.z, nl.w));
-              v[i] = x0.x;
-              v[i + 1] = x0.y;
-              v[i + 2] = x1.x;
-              v[i + 3] = x1.y;
+              acc[(i >> 2) & 3] = add_f2(acc[(i >> 2) & 3], make_float2(ex2_ftz(x0.x), ex2_ftz(x0.y)));
+              acc[((i >> 2) + 2) & 3] = add_f2(acc[((i >> 2) + 2) & 3], make_float2(ex2_ftz(x1.x), ex2_ftz(x1.y)));
             }
-            float x0 = fmax3(v[0], v[1], v[2]), x1 = fmax3(v[3], v[4], v[5]);
-#pragma unroll
-            for (int i = 6; i < 30; i += 4) {
-              x0 = fmax3(x0, v[i], v[i + 1]);
-              x1 = fmax3(x1, v[i + 2], v[i + 3]);
-            }
-            const float mn = fmaxf(lm, fmax3(x0, x1, fmaxf(v[30], v[31])));
-            if (mn == neg_inf()) return;                 // rows past the group (or all masked)
-            const float2 nm = make_float2(-mn, -mn);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 d = add_f2(make_float2(v[i], v[i + 1]), nm);
-              acc[(i >> 1) & 3] = add_f2(acc[(i >> 1) & 3], make_float2(ex2_ftz(d.x), ex2_ftz(d.y)));
-            }
-            const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
-            ls = (lm == neg_inf() ? 0.f : ls * ex2_ftz(lm - mn)) + (s01.x + s01.y);
-            lm = mn;
           };
           for (int c0 = 0; c0 < nq; c0 += 64) {        // nq is a multiple of 32
             float v[2][32];
@@ -426,8 +409,54 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
             tmem_ld32(lane_addr + c0, v[0]);
             if (two) tmem_ld32(lane_addr + c0 + 32, v[1]);
             tmem_wait_ld();
-            lse32(v[0], c0);
-            if (two) lse32(v[1], c0 + 32);
+            sum32(v[0], c0);
+            if (two) sum32(v[1], c0 + 32);
+          }
+          const float2 s01 = add_f2(add_f2(acc[0], acc[1]), add_f2(acc[2], acc[3]));
+          const float lin = s01.x + s01.y;
+          float lm = neg_inf(), ls = 0.f;
+          if (__any_sync(0xffffffffu, lin < 0x1p-100f)) {
+            auto lse32 = [&](float* v, int c0) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 nl = nl4[(c0 + i) >> 2];
+                const float2 x0 = fma_f2(make_float2(v[i], v[i + 1]), sc, make_float2(nl.x, nl.y));
+                const float2 x1 = fma_f2(make_float2(v[i + 2], v[i + 3]), sc, make_float2(nl.z, nl.w));
+                v[i] = x0.x;
+                v[i + 1] = x0.y;
+                v[i + 2] = x1.x;
+                v[i + 3] = x1.y;
+              }
+              float x0 = fmax3(v[0], v[1], v[2]), x1 = fmax3(v[3], v[4], v[5]);
+#pragma unroll
+              for (int i = 6; i < 30; i += 4) {
+                x0 = fmax3(x0, v[i], v[i + 1]);
+                x1 = fmax3(x1, v[i + 2], v[i + 3]);
+              }
+              const float mn = fmaxf(lm, fmax3(x0, x1, fmaxf(v[30], v[31])));
+              if (mn == neg_inf()) return;               // rows past the group (or all masked)
+              const float2 nm = make_float2(-mn, -mn);
+              float2 e[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 d = add_f2(make_float2(v[i], v[i + 1]), nm);
+                e[(i >> 1) & 3] = add_f2(e[(i >> 1) & 3], make_float2(ex2_ftz(d.x), ex2_ftz(d.y)));
+              }
+              const float2 t01 = add_f2(add_f2(e[0], e[1]), add_f2(e[2], e[3]));
+              ls = (lm == neg_inf() ? 0.f : ls * ex2_ftz(lm - mn)) + (t01.x + t01.y);
+              lm = mn;
+            };
+            for (int c0 = 0; c0 < nq; c0 += 32) {
+              float v[32];
+              tmem_ld32(lane_addr + c0, v);
+              tmem_wait_ld();
+              lse32(v, c0);
+            }
+          }
+          if (lin >= 0x1p-100f) {
+            lm = 0.f;
+            ls = lin;
           }
           tc_fence_before();
           mbar_arrive(&ts.tempty[eset]);
