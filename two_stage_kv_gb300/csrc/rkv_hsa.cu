@@ -17,7 +17,8 @@
 //   A. loads the group's G query rows and forms sum|q| and sum q per channel in
 //      fp32 with an error-free TwoSum check (an inexact sum sends the whole CTA
 //      to an fp64 path, so the channel decision is the exact-arithmetic one),
-//      then picks the top-k1 channels;
+//      then picks the top-k1 channels by rank (two threads count, for each
+//      channel, the channels ahead of it);
 //   B. folds the appended key into its block, scores its own blocks in fp32
 //      and sends every score, and each warp's score bounds, to every CTA of
 //      the cluster with st.async, counted on the receivers' mbarriers;
@@ -32,8 +33,8 @@
 //   E. sends its partial (max, sum, O) for each head with st.async to the CTA
 //      that owns the head, whose mbarrier counts the bytes; the owner combines
 //      the ns partials and writes fp32 outputs.
-// Both top-k steps are exact (larger first, equal values: lower index): a
-// 256-bucket histogram over [min, max] finds the bucket holding the k-th value
+// Both top-k steps are exact (larger first, equal values: lower index).  For
+// the blocks, a 256-bucket histogram over [min, max] finds the bucket holding the k-th value
 // and only that bucket's members are ranked pairwise; a radix select on an
 // order-preserving key takes over for degenerate value sets.  No global
 // scratch and no atomics on the data path; the cross-CTA waits are one
@@ -68,7 +69,6 @@ struct FixedSmem {
   float qbar32[HD];
   uint64_t akey64[HD];          // fp64 fallback
   double qbar64[HD];
-  uint8_t cflag[HD];
   int32_t hist[4 * 256];        // bucket histogram; the radix fallback uses 4 x 256
   int32_t members[MEMBER_MAX];
   float wmin[NWARP], wmax[NWARP];
@@ -381,7 +381,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   }
   __syncthreads();
   bool inexact = false;
-  float amn = __int_as_float(0x7f800000), amx = neg_inf();
   if (tid < HD) {
     float sa = 0.f, sq = 0.f;
     for (int g = 0; g < G; ++g) {
@@ -393,15 +392,27 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     }
     fs.asum[tid] = sa;
     fs.qbar32[tid] = sq;
-    amn = amx = sa;
   }
   const bool use64 = __syncthreads_or(inexact) != 0;
+  // Top-k1 channels by rank: channel c = tid / 2 is taken when fewer than k1
+  // channels have a larger sum, or an equal sum and a lower index.  The two
+  // threads of a channel count the even and the odd groups of four channels.
+  const int c = tid >> 1, hc = tid & 1;
+  int rk = 0;
   if (!use64) {
-    if (a.k1 >= HD) {
-      if (tid < HD) fs.cflag[tid] = 1;
-    } else {
-      block_minmax(amn, amx, fs);
-      bucket_topk(fs.asum, HD, a.k1, amn, amx, fs.cflag, fs);
+    if (a.k1 < HD) {
+      const float mine = fs.asum[c];
+      const float4* a4 = reinterpret_cast<const float4*>(fs.asum);
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        const int q4 = 2 * i + hc;                 // the two halves hit different banks
+        const float4 v = a4[q4];
+        const int j = 4 * q4;
+        rk += (int)(v.x > mine) + (int)((v.x == mine) & (j < c));
+        rk += (int)(v.y > mine) + (int)((v.y == mine) & (j + 1 < c));
+        rk += (int)(v.z > mine) + (int)((v.z == mine) & (j + 2 < c));
+        rk += (int)(v.w > mine) + (int)((v.w == mine) & (j + 3 < c));
+      }
     }
   } else {
     // rare: some group sum needs more than fp32's 24 bits; redo every channel in fp64
@@ -416,20 +427,18 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       fs.qbar64[tid] = sq;
     }
     __syncthreads();
-    if (tid < HD) {
-      const uint64_t mine = fs.akey64[tid];
-      int rk = 0;
-      for (int j = 0; j < HD; ++j) {
+    if (a.k1 < HD) {
+      const uint64_t mine = fs.akey64[c];
+      for (int j = hc; j < HD; j += 2) {
         const uint64_t o = fs.akey64[j];
-        rk += (o > mine) || (o == mine && j < tid);
+        rk += (o > mine) || (o == mine && j < c);
       }
-      fs.cflag[tid] = rk < a.k1;
     }
   }
-  __syncthreads();
+  rk += __shfl_xor_sync(0xffffffffu, rk, 1);
   {
-    const int c = tid;
-    const bool take = tid < HD && fs.cflag[c];
+    // the kept channels in ascending order
+    const bool take = hc == 0 && rk < a.k1;
     const unsigned bal = __ballot_sync(0xffffffffu, take);
     if (lane == 0) fs.wsum[warp] = __popc(bal);
     __syncthreads();
