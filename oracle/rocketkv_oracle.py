@@ -38,6 +38,13 @@ Readings where the pages are silent or ambiguous (each marked READING below):
   R10 multi-turn: stage-2 candidates are the stage-1 survivors (ascending)
      followed by the tokens decoded since; blocks are formed over that
      compacted index sequence and K/V rows are read from the full cache.
+  R11 multi-turn, the other reading (built beside R10): blocks are the fixed
+     runs of blk rows of the full cache itself.  A row is a candidate when
+     stage 1 kept it (prompt rows [0, n_prompt)) or when it was decoded after
+     that prompt (rows >= n_prompt).  Kmax/Kmin of a block run over its
+     candidate rows only; a block without candidates scores -inf; the block
+     holding the newest row is always chosen (it scores +inf) when it holds a
+     candidate; attention covers the candidate rows of the chosen blocks.
 """
 from __future__ import annotations
 
@@ -343,6 +350,83 @@ def hsa_decode_mt(q_group: np.ndarray, Kfull: np.ndarray, Vfull: np.ndarray, idx
     to hsa_decode on the rows Kfull[idx] (the full history stays in memory)."""
     rows = np.asarray(idx[:n], dtype=np.int64)
     return hsa_decode(q_group, Kfull[rows], Vfull[rows], n, kmax, kmin, blk, k1, k2, scale)
+
+
+# ---------------------------------------------------------------------------
+# RocketKV-MT over the physical cache  [RKV "方法细节": RocketKV-MT]  (READING R11)
+# ---------------------------------------------------------------------------
+
+
+def candidate_rows(keep: np.ndarray, n_prompt: int, n: int) -> np.ndarray:
+    """Which of the rows [0, n) stage 2 may attend: the kept prompt rows and
+    every row decoded after the prompt (the model "selects from the N input
+    tokens plus newly generated tokens")."""
+    cand = np.zeros(n, dtype=bool)
+    keep = np.asarray(keep, dtype=np.int64)
+    cand[keep[keep < min(n_prompt, n)]] = True
+    cand[n_prompt:] = True
+    return cand
+
+
+def build_kt_masked(Kfull: np.ndarray, n: int, cand: np.ndarray,
+                    blk: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Kmax / Kmin of each run of blk rows of the full cache over its candidate
+    rows [D, nblk], and whether the block holds any candidate.  Blocks without
+    one keep zeros (they are never scored)."""
+    D = Kfull.shape[1]
+    nblk = (n + blk - 1) // blk
+    kmax = np.zeros((D, nblk))
+    kmin = np.zeros((D, nblk))
+    has = np.zeros(nblk, dtype=bool)
+    for b in range(nblk):
+        rows = [r for r in range(b * blk, min(n, (b + 1) * blk)) if cand[r]]
+        if rows:
+            has[b] = True
+            kmax[:, b] = Kfull[rows].max(axis=0)
+            kmin[:, b] = Kfull[rows].min(axis=0)
+    return kmax, kmin, has
+
+
+def kt_append_masked(kmax: np.ndarray, kmin: np.ndarray, has: np.ndarray, n: int, k_new: np.ndarray,
+                     blk: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Fold decoded row n (always a candidate) into block n // blk: the first
+    candidate of a block sets its bounds, later ones widen them."""
+    b = n // blk
+    D = k_new.shape[0]
+    if b >= kmax.shape[1]:
+        grow = b + 1 - kmax.shape[1]
+        kmax = np.concatenate([kmax, np.zeros((D, grow))], axis=1)
+        kmin = np.concatenate([kmin, np.zeros((D, grow))], axis=1)
+        has = np.concatenate([has, np.zeros(grow, dtype=bool)])
+    if not has[b]:
+        kmax[:, b] = k_new
+        kmin[:, b] = k_new
+        has[b] = True
+    else:
+        kmax[:, b] = np.maximum(kmax[:, b], k_new)
+        kmin[:, b] = np.minimum(kmin[:, b], k_new)
+    return kmax, kmin, has
+
+
+def hsa_decode_mt_masked(q_group: np.ndarray, Kfull: np.ndarray, Vfull: np.ndarray, n: int, cand: np.ndarray,
+                         kmax: np.ndarray, kmin: np.ndarray, has: np.ndarray, blk: int, k1: int, k2: int,
+                         scale: float) -> Dict[str, np.ndarray]:
+    """One HSA step over the blocks of the full cache (READING R11): Algorithm
+    1's scores on the candidate-only bounds, blocks without a candidate at
+    -inf, the newest row's block at +inf, top-k2 blocks, then attention over
+    the candidate rows of those blocks."""
+    nblk = (n + blk - 1) // blk
+    i1, qbar = hsa_channels(q_group, k1)
+    s = hsa_block_scores(qbar, i1, kmax[:, :nblk], kmin[:, :nblk])
+    s = np.where(has[:nblk], s, -np.inf)
+    tail = (n - 1) // blk
+    if has[tail]:
+        s[tail] = np.inf
+    i2 = topk_lowest_index(s, k2)
+    tok = block_tokens(i2, n, blk)
+    tok = tok[cand[tok]]
+    y = attention(q_group, Kfull[tok], Vfull[tok], scale)
+    return {"y": y, "i1": i1, "i2": i2, "s": s, "tok": tok}
 
 
 # ---------------------------------------------------------------------------

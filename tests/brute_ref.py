@@ -82,3 +82,39 @@ def hsa(qg, Kc, Vc, n, kmax, kmin, blk, k1, k2, scale):
         tot = sum(e)
         y.append([sum(e[t] * Vc[toks[t]][d] for t in range(len(toks))) / tot for d in range(D)])
     return y, i1, i2, s
+
+
+def hsa_masked(qg, K, V, n, cand, blk, k1, k2, scale):
+    """RocketKV-MT over fixed blocks of the full cache (the other multi-turn
+    reading): bounds over candidate rows only, blocks without a candidate
+    last, the newest row's block first, attention over the candidate rows of
+    the chosen blocks.  Returns (y, i1, i2)."""
+    G, D = len(qg), len(qg[0])
+    a = [sum(abs(qg[g][c]) for g in range(G)) for c in range(D)]
+    i1 = full_sort_topk(a, k1)
+    nblk = (n + blk - 1) // blk
+    s = []
+    for b in range(nblk):
+        rows = [r for r in range(b * blk, min(n, (b + 1) * blk)) if cand[r]]
+        if not rows:
+            s.append(-math.inf)
+            continue
+        tot = 0.0
+        for c in i1:
+            qs = sum(qg[g][c] for g in range(G))
+            col = [K[r][c] for r in rows]
+            tot += qs * (max(col) if qs >= 0 else min(col))
+        s.append(tot)
+    tail = (n - 1) // blk
+    if s[tail] != -math.inf:
+        s[tail] = math.inf
+    i2 = full_sort_topk(s, k2)
+    toks = [b * blk + i for b in i2 for i in range(blk) if b * blk + i < n and cand[b * blk + i]]
+    y = []
+    for g in range(G):
+        logits = [_dot(qg[g], K[j]) * scale for j in toks]
+        m = max(logits)
+        e = [math.exp(x - m) for x in logits]
+        tot = sum(e)
+        y.append([sum(e[t] * V[toks[t]][d] for t in range(len(toks))) / tot for d in range(D)])
+    return y, i1, i2

@@ -338,6 +338,117 @@ def test_mt_identity():
 
 
 # ---------------------------------------------------------------------------
+# Multi-turn over the blocks of the full cache (the other reading)
+# ---------------------------------------------------------------------------
+
+
+def _masked_case(seed, n, n_prompt, blk, D=8, G=2, dens=0.3):
+    r = _rng(seed)
+    K = r.standard_normal((n, D))
+    V = r.standard_normal((n, D))
+    qg = r.standard_normal((G, D))
+    keep = np.sort(r.choice(n_prompt, max(1, int(dens * n_prompt)), replace=False))
+    cand = oracle.candidate_rows(keep, n_prompt, n)
+    return qg, K, V, keep, cand
+
+
+@pytest.mark.parametrize("seed,n,n_prompt,blk,k1,k2", [
+    (40, 37, 30, 4, 3, 2), (41, 50, 50, 5, 8, 3), (42, 23, 17, 1, 8, 4),
+    (43, 64, 40, 8, 2, 30), (44, 45, 44, 3, 5, 1),
+])
+def test_mt_masked_vs_brute_force(seed, n, n_prompt, blk, k1, k2):
+    qg, K, V, keep, cand = _masked_case(seed, n, n_prompt, blk)
+    kmax, kmin, has = oracle.build_kt_masked(K, n, cand, blk)
+    res = oracle.hsa_decode_mt_masked(qg, K, V, n, cand, kmax, kmin, has, blk, k1, k2, 0.3)
+    y, i1, i2 = brute_ref.hsa_masked(qg.tolist(), K.tolist(), V.tolist(), n, cand.tolist(), blk, k1, k2, 0.3)
+    assert res["i1"].tolist() == i1
+    assert res["i2"].tolist() == i2
+    np.testing.assert_allclose(res["y"], np.array(y), rtol=1e-12, atol=1e-12)
+
+
+def test_mt_masked_candidates():
+    # kept prompt rows plus every row decoded after the prompt
+    cand = oracle.candidate_rows(np.array([0, 3, 7, 9]), 8, 12)
+    assert np.flatnonzero(cand).tolist() == [0, 3, 7, 8, 9, 10, 11]
+
+
+def test_mt_masked_full_attention_when_k2_covers():
+    qg, K, V, keep, cand = _masked_case(45, 90, 70, 8, D=16, G=4)
+    kmax, kmin, has = oracle.build_kt_masked(K, 90, cand, 8)
+    res = oracle.hsa_decode_mt_masked(qg, K, V, 90, cand, kmax, kmin, has, 8, 4, 1000, 0.25)
+    np.testing.assert_allclose(res["y"], _sdpa(qg, K, V, 0.25, np.flatnonzero(cand)), rtol=1e-12, atol=1e-12)
+
+
+def test_mt_masked_bounds_skip_other_rows():
+    qg, K, V, keep, cand = _masked_case(46, 80, 64, 8)
+    K[~cand] = 1e3 * np.sign(_rng(47).standard_normal(K[~cand].shape))   # never a bound
+    kmax, kmin, has = oracle.build_kt_masked(K, 80, cand, 8)
+    ref_max = torch.from_numpy(np.where(cand[:, None], K, -np.inf)).reshape(10, 8, -1).amax(dim=1).numpy().T
+    ref_min = torch.from_numpy(np.where(cand[:, None], K, np.inf)).reshape(10, 8, -1).amin(dim=1).numpy().T
+    ref_has = cand.reshape(10, 8).any(axis=1)
+    assert has.tolist() == ref_has.tolist()
+    assert np.array_equal(kmax[:, has], ref_max[:, has]) and np.array_equal(kmin[:, has], ref_min[:, has])
+    assert np.all(np.abs(kmax[:, has]) < 1e3)
+
+
+def test_mt_masked_tail_always_chosen():
+    qg, K, V, keep, cand = _masked_case(48, 100, 90, 8, D=16, G=4)
+    K[96:] = -5.0 * qg.sum(axis=0)          # the newest block scores lowest of all
+    kmax, kmin, has = oracle.build_kt_masked(K, 100, cand, 8)
+    res = oracle.hsa_decode_mt_masked(qg, K, V, 100, cand, kmax, kmin, has, 8, 16, 2, 0.25)
+    assert 12 in res["i2"].tolist()
+    finite = res["s"][np.isfinite(res["s"])]
+    assert res["s"][12] == np.inf and len(finite) == has.sum() - 1
+
+
+def test_mt_masked_other_rows_do_not_matter():
+    qg, K, V, keep, cand = _masked_case(49, 70, 60, 4)
+    kmax, kmin, has = oracle.build_kt_masked(K, 70, cand, 4)
+    a = oracle.hsa_decode_mt_masked(qg, K, V, 70, cand, kmax, kmin, has, 4, 4, 5, 0.3)
+    r = _rng(50)
+    K2, V2 = K.copy(), V.copy()
+    K2[~cand] = r.standard_normal(K2[~cand].shape) * 10
+    V2[~cand] = r.standard_normal(V2[~cand].shape) * 10
+    kmax2, kmin2, has2 = oracle.build_kt_masked(K2, 70, cand, 4)
+    b = oracle.hsa_decode_mt_masked(qg, K2, V2, 70, cand, kmax2, kmin2, has2, 4, 4, 5, 0.3)
+    assert a["i2"].tolist() == b["i2"].tolist()
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-12, atol=1e-12)
+
+
+def test_mt_masked_matches_candidate_reading_on_whole_blocks():
+    # Candidate sets made of whole blocks, decoded rows from a block boundary,
+    # and a newest block that is chosen anyway: both multi-turn readings form
+    # the same blocks, pick the same ones and attend the same rows.
+    r = _rng(51)
+    G, D, blk, n_prompt, n = 4, 16, 8, 160, 180
+    K = r.standard_normal((n, D))
+    V = r.standard_normal((n, D))
+    qg = r.standard_normal((G, D))
+    K[176:] = 3.0 * np.sign(qg.sum(axis=0))
+    kept_blocks = np.sort(r.choice(n_prompt // blk, 7, replace=False))
+    keep = (kept_blocks[:, None] * blk + np.arange(blk)).reshape(-1)
+    cand = oracle.candidate_rows(keep, n_prompt, n)
+    kmax, kmin, has = oracle.build_kt_masked(K, n, cand, blk)
+    a = oracle.hsa_decode_mt_masked(qg, K, V, n, cand, kmax, kmin, has, blk, 6, 4, 0.25)
+    idx = np.flatnonzero(cand)
+    km10, kn10 = oracle.build_kt_mt(K, idx, idx.size, blk)
+    b = oracle.hsa_decode_mt(qg, K, V, idx, idx.size, km10, kn10, blk, 6, 4, 0.25)
+    phys = np.flatnonzero(has)                   # compacted block i <-> physical block phys[i]
+    assert phys[b["i2"]].tolist() == a["i2"].tolist()
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-12, atol=1e-12)
+
+
+def test_kt_append_masked_equals_rebuild():
+    qg, K, V, keep, cand = _masked_case(52, 75, 61, 6)
+    kmax, kmin, has = oracle.build_kt_masked(K, 61, cand, 6)
+    for n in range(61, 75):
+        kmax, kmin, has = oracle.kt_append_masked(kmax, kmin, has, n, K[n], 6)
+    rmax, rmin, rhas = oracle.build_kt_masked(K, 75, cand, 6)
+    assert has.tolist() == rhas.tolist()
+    assert np.array_equal(kmax, rmax) and np.array_equal(kmin, rmin)
+
+
+# ---------------------------------------------------------------------------
 # Brute force of the whole pipeline on tiny inputs
 # ---------------------------------------------------------------------------
 
@@ -408,6 +519,22 @@ def test_mutation_window_denominator_fails_sdpa(monkeypatch):
     pos = np.tile(np.arange(26, 30), 2)
     ref = _sdpa_probs(q.reshape(8, 8), K, pos)[:, :26].sum(axis=0)
     assert not np.allclose(wrong(q, K, 1 / math.sqrt(8)), ref, rtol=1e-6)
+
+
+def test_mutation_unforced_tail_fails_brute_force(monkeypatch):
+    # forgetting to force the newest block in must be caught by the brute force
+    def wrong(q_group, Kfull, Vfull, n, cand, kmax, kmin, has, blk, k1, k2, scale):
+        nblk = (n + blk - 1) // blk
+        i1, qbar = ro.hsa_channels(q_group, k1)
+        s = np.where(has[:nblk], ro.hsa_block_scores(qbar, i1, kmax[:, :nblk], kmin[:, :nblk]), -np.inf)
+        return {"i1": i1, "i2": ro.topk_lowest_index(s, k2), "s": s}
+    monkeypatch.setattr(ro, "hsa_decode_mt_masked", wrong)
+    qg, K, V, keep, cand = _masked_case(53, 100, 90, 8, D=16, G=4)
+    K[96:] = -5.0 * qg.sum(axis=0)
+    kmax, kmin, has = ro.build_kt_masked(K, 100, cand, 8)
+    res = ro.hsa_decode_mt_masked(qg, K, V, 100, cand, kmax, kmin, has, 8, 16, 2, 0.25)
+    _, _, i2 = brute_ref.hsa_masked(qg.tolist(), K.tolist(), V.tolist(), 100, cand.tolist(), 8, 16, 2, 0.25)
+    assert res["i2"].tolist() != i2
 
 
 def test_mutation_transposed_kt_fails_library():
