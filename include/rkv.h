@@ -254,6 +254,55 @@ rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_
                              const void* k_new, const void* v_new, int64_t row, void* stream);
 
 /*
+ * RocketKV-MT, the reading over fixed blocks of the full cache.  [RocketKV
+ * digest, 方法细节: RocketKV-MT -- every token stays in memory; stage 2
+ * chooses among the N surviving input tokens plus the newly generated ones]
+ * The pages leave open whether stage 2's blocks run over the survivors'
+ * sequence (rkv_hsa_decode_mt) or over the full cache; these three calls
+ * build the second reading.  Rows [0, n_prompt) of the full cache are the
+ * prompt that stage 1 filtered; row r < n_prompt is a candidate when bit r of
+ * the mask is set, and every row r >= n_prompt (decoded after that prompt)
+ * is a candidate.
+ *   mask  [B, Hkv, mask_ld] uint32 DEVICE array, bit r = word r / 32, bit
+ *         r % 32; mask_ld >= ceil(n_prompt / 32); 4-byte aligned.
+ *
+ * rkv_keep_mask: mask bits [0, n_prompt) = the rows listed in keep_idx[b,h,
+ * 0:B1] (the keep list of rkv_snap_evict in mask mode); entries outside
+ * [0, n_prompt) are ignored.
+ */
+rkv_status rkv_keep_mask(rkv_dims d, const int32_t* keep_idx, int64_t keep_ld, int64_t B1, int64_t n_prompt,
+                         uint32_t* mask, int64_t mask_ld, void* stream);
+
+/*
+ * KT over fixed blocks of the full cache, candidate rows only: for block j,
+ * Kmax / Kmin over the candidate rows of [j*blk, min(n, (j+1)*blk)); a block
+ * without candidates stores zeros.  Layout and size rules as rkv_build_kt
+ * (no idx); n_prompt <= n <= cap.
+ */
+rkv_status rkv_build_kt_masked(rkv_dims d, const void* k, int64_t cap, int64_t n, const uint32_t* mask,
+                               int64_t mask_ld, int64_t n_prompt, int32_t blk, void* kt, int64_t nblk_cap,
+                               void* stream);
+
+/*
+ * HSA decode step of that reading.  Same arguments and rules as rkv_hsa_decode
+ * (n = rows of the full cache in use, the fused append writes row n, which is
+ * a candidate), plus the mask and n_prompt <= n.  Per (b, h):
+ *   bounds  Kmax / Kmin of block j over its candidate rows (the fused append
+ *           starts a block's bounds when it holds no earlier candidate);
+ *   s[j]    Algorithm 1's score, -inf for a block without candidates, +inf
+ *           for the block of the newest row N-1 when it holds a candidate;
+ *   i2      top-k2 of s as rkv_hsa_decode (equal: lower block first);
+ *   out     attention over the candidate rows of the blocks in i2.
+ * Errors as rkv_hsa_decode, plus RKV_ERR_INVALID_ARG for a NULL or misaligned
+ * mask, n_prompt outside [0, min(n, cap)] or mask_ld < ceil(n_prompt / 32).
+ */
+rkv_status rkv_hsa_decode_mt_masked(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int64_t n,
+                                    const uint32_t* mask, int64_t mask_ld, int64_t n_prompt, void* kt,
+                                    int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale, float* out,
+                                    int32_t* sel_blocks, int32_t* sel_channels, const void* k_new, const void* v_new,
+                                    void* stream);
+
+/*
  * HSA decode step for a batch whose rows hold different numbers of candidates
  * (ragged batch).  [RocketKV digest, 方法细节: HSA steps 1-3 and Algorithm 1,
  * per request]  Same computation, arguments and results as rkv_hsa_decode,

@@ -97,6 +97,21 @@ D4 = (1, 32, 8, 128)
     (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 11, None, 0, 16, 10, 16, stream=0), 1),
     (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 160, 160, None, 0, 16, 10, 16, stream=0), 1),
     (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 10, 16, 10, 16, 10, 16, stream=0), 1),
+    # masked multi-turn: NULL / misaligned mask, n_prompt past n, mask rows too short
+    (lambda: rkv.rkv_hsa_decode_mt_masked(D4, 16, 16, 16, 100, 90, None, 4, 80, 16, 16, 16, 8, 4, 0.1, 16,
+                                          stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_mt_masked(D4, 16, 16, 16, 100, 90, 18, 4, 80, 16, 16, 16, 8, 4, 0.1, 16,
+                                          stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_mt_masked(D4, 16, 16, 16, 100, 90, 16, 4, 91, 16, 16, 16, 8, 4, 0.1, 16,
+                                          stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_mt_masked(D4, 16, 16, 16, 100, 90, 16, 2, 80, 16, 16, 16, 8, 4, 0.1, 16,
+                                          stream=0), 1),
+    (lambda: rkv.rkv_keep_mask(D4, None, 50, 50, 100, 16, 4, stream=0), 1),
+    (lambda: rkv.rkv_keep_mask(D4, 16, 40, 50, 100, 16, 4, stream=0), 1),
+    (lambda: rkv.rkv_keep_mask(D4, 16, 50, 50, 100, 16, 3, stream=0), 1),
+    (lambda: rkv.rkv_build_kt_masked(D4, 16, 100, 90, None, 4, 80, 16, 16, 8, stream=0), 1),
+    (lambda: rkv.rkv_build_kt_masked(D4, 16, 100, 90, 16, 4, 91, 16, 16, 8, stream=0), 1),
+    (lambda: rkv.rkv_build_kt_masked(D4, 16, 100, 90, 16, 2, 80, 16, 16, 8, stream=0), 1),
 ])
 def test_invalid_arguments_rejected_on_host(lib, call, status):
     with pytest.raises(rkv.RkvError) as e:

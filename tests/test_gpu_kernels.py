@@ -585,3 +585,135 @@ def test_fused_append_equals_separate(mt, n0, blk, k2):
         assert torch.equal(a[3], b[3])
     for s in range(steps):
         assert torch.equal(a[5][s], b[5][s]) and torch.equal(a[4][s], b[4][s])
+
+
+# ----------------------------------------- multi-turn over full-cache blocks --
+
+
+def _check_blocks_masked(got, s, k2, what):
+    """check_topk for scores with +-inf entries: an infinite k-th score admits no tie band."""
+    k = min(k2, s.shape[0])
+    if np.isfinite(oracle.kth_value(s, k)):
+        return check_topk(got, s, k2, what)
+    assert got.tolist() == oracle.topk_lowest_index(s, k).tolist(), what
+    return 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n_prompt,n_dec,blk,k1,k2,dens", [
+    (2, 32, 8, 300, 0, 16, 32, 5, 0.3),       # G = 4, ragged tail
+    (1, 32, 8, 517, 5, 16, 16, 9, 0.2),       # decoded rows share a block with the prompt's last rows
+    (1, 64, 8, 1000, 3, 32, 64, 11, 0.5),     # G = 8, block 32
+    (1, 32, 2, 333, 1, 8, 128, 40, 0.1),      # G = 16, block 8, all channels
+    (1, 32, 8, 700, 2, 1, 32, 40, 0.3),       # token-level blocks, gathered rows
+    (1, 32, 8, 333, 4, 12, 32, 7, 0.25),      # block 12, gathered rows
+    (2, 32, 8, 130, 0, 16, 32, 64, 0.3),      # k2 >= blocks
+    (1, 32, 8, 5000, 0, 16, 32, 30, 0.02),    # mostly empty blocks
+    (1, 32, 8, 600, 0, 16, 32, 50, 0.02),     # fewer blocks with candidates than k2
+])
+def test_hsa_decode_mt_masked_parity(B, Hq, Hkv, n_prompt, n_dec, blk, k1, k2, dens):
+    """The multi-turn reading over fixed blocks of the full cache: keep-list mask,
+    candidate-only KT (bit-exact) and a few decode steps with the fused append,
+    each against the oracle."""
+    D, G, steps = 128, Hq // Hkv, 4
+    dims = (B, Hq, Hkv, D)
+    scale = 1 / math.sqrt(D)
+    seed = n_prompt + 7 * blk + k2
+    cap = n_prompt + n_dec + steps + 5
+    kb, k = _rand(seed, (B, Hkv, cap, D))
+    vb, v = _rand(seed + 1, (B, Hkv, cap, D))
+    qb = small_random(seed + 2, (steps, B, Hq, D))
+    knb = small_random(seed + 3, (steps, B, Hkv, D))
+    vnb = small_random(seed + 4, (steps, B, Hkv, D))
+    kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
+    knf, vnf = bf16_bits_to_f64(knb), bf16_bits_to_f64(vnb)
+    rng = np.random.default_rng(seed)
+    nkeep = max(1, int(dens * n_prompt))
+    keep = np.stack([np.stack([np.sort(rng.choice(n_prompt, nkeep, replace=False)) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32)
+    keep_t = torch.from_numpy(keep).to(DEV)
+    mask_ld = -(-cap // 32)
+    mask = torch.full((B, Hkv, mask_ld), -1, dtype=torch.int32, device=DEV)
+    rkv.rkv_keep_mask(dims, keep_t, nkeep, nkeep, n_prompt, mask, mask_ld)
+    n = n_prompt + n_dec
+    ncap = -(-(-(-cap // blk)) // 8) * 8
+    kt = torch.full((B, Hkv, 2, D, ncap), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt_masked(dims, k, cap, n, mask, mask_ld, n_prompt, blk, kt, ncap)
+    torch.cuda.synchronize()
+    words = mask.cpu().numpy().view(np.uint32)
+    ktg = t2f64(kt)
+    state = {}
+    for b in range(B):
+        for h in range(Hkv):
+            cand = oracle.candidate_rows(keep[b, h], n_prompt, cap)
+            bits = np.unpackbits(words[b, h, :-(-n_prompt // 32)].view(np.uint8), bitorder="little")[:n_prompt]
+            assert bits.astype(bool).tolist() == cand[:n_prompt].tolist(), "mask bits"
+            kmax, kmin, has = oracle.build_kt_masked(kf[b, h], n, cand, blk)
+            nb = kmax.shape[1]
+            assert np.array_equal(ktg[b, h, 0, :, :nb], kmax) and np.array_equal(ktg[b, h, 1, :, :nb], kmin)
+            state[(b, h)] = [kmax, kmin, has, cand]
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
+    sc = torch.full((B, Hkv, k1), -7, dtype=torch.int32, device=DEV)
+    kn_t, vn_t, q_t = _bf16(knb), _bf16(vnb), _bf16(qb)
+    worst, exempt = 0.0, 0
+    for s in range(steps):
+        fused = s != 2                      # step 2 attends without appending
+        rkv.rkv_hsa_decode_mt_masked(dims, q_t[s], k, v, cap, n, mask, mask_ld, n_prompt, kt, ncap, blk, k1, k2,
+                                     scale, out, sb, sc, kn_t[s] if fused else None, vn_t[s] if fused else None)
+        torch.cuda.synchronize()
+        if fused:
+            kf[:, :, n] = knf[s]
+            vf[:, :, n] = vnf[s]
+        n_att = n + (1 if fused else 0)
+        out_h, sb_h, sc_h = out.cpu().numpy(), sb.cpu().numpy(), sc.cpu().numpy()
+        for (b, h), st in state.items():
+            if fused:
+                st[0], st[1], st[2] = oracle.kt_append_masked(st[0], st[1], st[2], n, knf[s, b, h], blk)
+            qg = qf[s, b, h * G:(h + 1) * G]
+            res = oracle.hsa_decode_mt_masked(qg, kf[b, h], vf[b, h], n_att, st[3], st[0], st[1], st[2], blk, k1,
+                                              k2, scale)
+            assert sc_h[b, h].tolist() == res["i1"].tolist(), "channel set differs"
+            k2e = min(k2, res["s"].shape[0])
+            exempt += _check_blocks_masked(sb_h[b, h, :k2e], res["s"], k2, f"step {s} blocks")
+            assert np.all(sb_h[b, h, k2e:] == -1)
+            if np.array_equal(sb_h[b, h, :k2e], res["i2"]):
+                y = res["y"]
+            else:
+                tok = oracle.block_tokens(sb_h[b, h, :k2e], n_att, blk)
+                tok = tok[st[3][tok]]
+                y = oracle.attention(qg, kf[b, h][tok], vf[b, h][tok], scale)
+            worst = max(worst, max_abs(out_h[b, h * G:(h + 1) * G], y))
+        n = n_att
+    ktg = t2f64(kt)
+    for (b, h), st in state.items():
+        nb = st[0].shape[1]
+        assert np.array_equal(ktg[b, h, 0, :, :nb], st[0]) and np.array_equal(ktg[b, h, 1, :, :nb], st[1])
+    assert worst <= ATOL_OUT, worst
+
+
+def test_hsa_decode_mt_masked_all_candidates_equals_dense():
+    """With every prompt row kept, the reading over full-cache blocks scores the
+    same blocks as the dense decode; with k2 large enough to take the newest
+    block anyway, both return the same blocks and bit-identical outputs."""
+    B, Hq, Hkv, D, n, blk, k1 = 2, 32, 8, 128, 640, 16, 32
+    k2 = n // blk
+    dims = (B, Hq, Hkv, D)
+    kb, k = _rand(61, (B, Hkv, n + 8, D))
+    vb, v = _rand(62, (B, Hkv, n + 8, D))
+    _, q = _rand(63, (B, Hq, D))
+    keep = torch.arange(n, dtype=torch.int32, device=DEV).expand(B, Hkv, n).contiguous()
+    mask = torch.zeros((B, Hkv, n // 32), dtype=torch.int32, device=DEV)
+    rkv.rkv_keep_mask(dims, keep, n, n, n, mask, n // 32)
+    ncap = n // blk
+    kt1 = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    kt2 = torch.zeros_like(kt1)
+    rkv.rkv_build_kt_masked(dims, k, n + 8, n, mask, n // 32, n, blk, kt1, ncap)
+    rkv.rkv_build_kt(dims, k, n + 8, n, None, 0, blk, kt2, ncap)
+    o1 = torch.empty(B, Hq, D, device=DEV)
+    o2 = torch.empty_like(o1)
+    s1 = torch.empty(B, Hkv, k2, dtype=torch.int32, device=DEV)
+    s2 = torch.empty_like(s1)
+    rkv.rkv_hsa_decode_mt_masked(dims, q, k, v, n + 8, n, mask, n // 32, n, kt1, ncap, blk, k1, k2, 0.1, o1, s1)
+    rkv.rkv_hsa_decode(dims, q, k, v, n + 8, n, kt2, ncap, blk, k1, k2, 0.1, o2, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(kt1, kt2) and torch.equal(s1, s2) and torch.equal(o1, o2)

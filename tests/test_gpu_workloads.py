@@ -147,16 +147,30 @@ def run_single_turn(wl, layer=0, max_pairs=64, steps=None, fused=True):
             "pairs": len(pairs)}
 
 
-def run_mt(wl, max_pairs=32, steps=None, fused=True):
+def _masked_blocks_ok(got, s, k2, what):
+    k = min(k2, s.shape[0])
+    if np.isfinite(oracle.kth_value(s, k)):
+        return check_topk(got, s, k2, what)
+    assert got.tolist() == oracle.topk_lowest_index(s, k).tolist(), what
+    return 0
+
+
+def run_mt(wl, max_pairs=32, steps=None, fused=True, reading="candidates", dev_stats=None):
+    """Multi-turn run checked against the oracle on sampled pairs.  With
+    dev_stats (a dict), also records, every 8th step, how much of full
+    attention's probability mass (over every row of the cache) the attended
+    rows carry, and how many rows were attended."""
     G, D, blk, k1 = wl.G, wl.D, wl.blk, wl.k1
     scale = 1 / math.sqrt(D)
-    mt = pipeline.MTLayer(wl, device=DEV)
+    full_blocks = reading == "full_blocks"
+    mt = pipeline.MTLayer(wl, device=DEV, reading=reading)
     pairs = _pairs(wl, max_pairs)
     kfull = np.zeros((wl.B, wl.Hkv, mt.cap, D), dtype=np.uint16)
     vfull = np.zeros_like(kfull)
     rows = 0
     worst, exempt = 0.0, 0
     nsteps = wl.steps if steps is None else steps
+    devs = []
     for turn in range(wl.n_turns):
         kc, vc = synth.kv_full(wl, 0, None, turn=turn)
         T = kc.shape[2]
@@ -180,19 +194,29 @@ def run_mt(wl, max_pairs=32, steps=None, fused=True):
         torch.cuda.synchronize()
         ktg = t2f64(mt.kt)
         state = {}
+        n_prompt = rows
+        if full_blocks:
+            words = mt.mask.cpu().numpy().view(np.uint32)
         for (b, h) in pairs:
             cand = list(idx[b, h, :bud.B1])
-            kmax, kmin = oracle.build_kt_mt(f64(kfull[b, h]), np.array(cand), bud.B1, blk)
+            if full_blocks:
+                cm = oracle.candidate_rows(np.array(cand), n_prompt, mt.cap)
+                bits = np.unpackbits(words[b, h, :-(-n_prompt // 32)].view(np.uint8), bitorder="little")[:n_prompt]
+                assert bits.astype(bool).tolist() == cm[:n_prompt].tolist()
+                kmax, kmin, has = oracle.build_kt_masked(f64(kfull[b, h]), rows, cm, blk)
+                state[(b, h)] = [cm, kmax, kmin, has]
+            else:
+                kmax, kmin = oracle.build_kt_mt(f64(kfull[b, h]), np.array(cand), bud.B1, blk)
+                state[(b, h)] = [cand, kmax, kmin]
             assert np.array_equal(ktg[b, h, 0, :, :kmax.shape[1]], kmax)
             assert np.array_equal(ktg[b, h, 1, :, :kmin.shape[1]], kmin)
-            state[(b, h)] = [cand, kmax, kmin]
         qd = synth.q_decode(wl, 0, turn=turn)
         kn, vn = synth.kv_new(wl, 0, turn=turn)
         n = bud.B1
         for s in range(wl.steps):
             kfull[:, :, rows] = kn[s]
             vfull[:, :, rows] = vn[s]
-            if fused:
+            if fused or full_blocks:
                 mt.step(_t(qd[s]), _t(kn[s]), _t(vn[s]))
             else:
                 mt.append(_t(kn[s]), _t(vn[s]))
@@ -204,30 +228,82 @@ def run_mt(wl, max_pairs=32, steps=None, fused=True):
                 sb = mt.sel_blocks.cpu().numpy()
                 sc = mt.sel_channels.cpu().numpy()
             for (b, h), st in state.items():
-                st[0].append(rows)
-                st[1], st[2] = oracle.kt_append(st[1], st[2], n, f64(kn[s, b, h]), blk)
+                if full_blocks:
+                    st[1], st[2], st[3] = oracle.kt_append_masked(st[1], st[2], st[3], rows, f64(kn[s, b, h]), blk)
+                else:
+                    st[0].append(rows)
+                    st[1], st[2] = oracle.kt_append(st[1], st[2], n, f64(kn[s, b, h]), blk)
                 if s >= nsteps:
                     continue
                 qg = f64(qd[s, b, h * G:(h + 1) * G])
-                cand = np.array(st[0])
-                res = oracle.hsa_decode_mt(qg, f64(kfull[b, h]), f64(vfull[b, h]), cand, n + 1, st[1], st[2], blk,
-                                           k1, bud.k2, scale)
+                kf, vf = f64(kfull[b, h]), f64(vfull[b, h])
+                if full_blocks:
+                    res = oracle.hsa_decode_mt_masked(qg, kf, vf, rows + 1, st[0], st[1], st[2], st[3], blk, k1,
+                                                      bud.k2, scale)
+                    k2e = min(bud.k2, res["s"].shape[0])
+                    exempt += _masked_blocks_ok(sb[b, h, :k2e], res["s"], bud.k2, f"turn {turn} step {s} blocks")
+                else:
+                    cand = np.array(st[0])
+                    res = oracle.hsa_decode_mt(qg, kf, vf, cand, n + 1, st[1], st[2], blk, k1, bud.k2, scale)
+                    k2e = min(bud.k2, res["s"].shape[0])
+                    exempt += check_topk(sb[b, h, :k2e], res["s"], bud.k2, f"turn {turn} step {s} blocks")
                 assert sc[b, h].tolist() == res["i1"].tolist()
-                k2e = min(bud.k2, res["s"].shape[0])
-                exempt += check_topk(sb[b, h, :k2e], res["s"], bud.k2, f"turn {turn} step {s} blocks")
                 if np.array_equal(sb[b, h, :k2e], res["i2"]):
                     y = res["y"]
+                elif full_blocks:
+                    tok = oracle.block_tokens(sb[b, h, :k2e], rows + 1, blk)
+                    tok = tok[st[0][tok]]
+                    y = oracle.attention(qg, kf[tok], vf[tok], scale)
                 else:
-                    y = oracle.attention_over_blocks(qg, f64(kfull[b, h])[cand], f64(vfull[b, h])[cand], n + 1,
-                                                     sb[b, h, :k2e], blk, scale)
+                    y = oracle.attention_over_blocks(qg, kf[cand], vf[cand], n + 1, sb[b, h, :k2e], blk, scale)
                 worst = max(worst, max_abs(out[b, h * G:(h + 1) * G], y))
+                if dev_stats is not None and s % 8 == 7:
+                    # share of full attention's probability mass (over every row of
+                    # the cache) that falls on the rows this step attended
+                    if full_blocks:
+                        att = oracle.block_tokens(sb[b, h, :k2e], rows + 1, blk)
+                        att = att[st[0][att]]
+                    else:
+                        att = np.asarray(st[0], dtype=np.int64)[oracle.block_tokens(sb[b, h, :k2e], n + 1, blk)]
+                    lg = qg @ kf[:rows + 1].T * scale
+                    pr = np.exp(lg - lg.max(axis=1, keepdims=True))
+                    pr /= pr.sum(axis=1, keepdims=True)
+                    devs.append((float(pr[:, att].sum(axis=1).mean()), att.size))
             rows += 1
             n += 1
         torch.cuda.synchronize()
-        assert np.array_equal(mt.idx.cpu().numpy()[:, :, bud.B1:n],
-                              np.broadcast_to(np.arange(rows - wl.steps, rows), (wl.B, wl.Hkv, wl.steps)))
+        if not full_blocks:
+            assert np.array_equal(mt.idx.cpu().numpy()[:, :, bud.B1:n],
+                                  np.broadcast_to(np.arange(rows - wl.steps, rows), (wl.B, wl.Hkv, wl.steps)))
     assert worst <= ATOL_OUT, worst
+    if dev_stats is not None:
+        dev_stats["full_attention_mass_covered"] = round(float(np.mean([d[0] for d in devs])), 4)
+        dev_stats["rows_attended_per_step"] = round(float(np.mean([d[1] for d in devs])), 1)
     return {"worst": worst, "exempt": exempt}
+
+
+def time_mt_steps(wl, reading):
+    """Mean device time of one fused multi-turn decode step (CUDA events, all
+    turns, after one untimed turn-1 pass)."""
+    mt = pipeline.MTLayer(wl, device=DEV, reading=reading)
+    per = []
+    for turn in range(wl.n_turns):
+        kc, vc = synth.kv_full(wl, 0, None, turn=turn)
+        mt.add_prompt(_t(kc), _t(vc))
+        mt.stage1(_t(synth.q_obs(wl, 0, None, turn=turn)))
+        mt.build_kt()
+        qd = _t(synth.q_decode(wl, 0, turn=turn))
+        kn, vn = synth.kv_new(wl, 0, turn=turn)
+        knt, vnt = _t(kn), _t(vn)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in range(wl.steps):
+            mt.step(qd[s], knt[s], vnt[s])
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) * 1e3 / wl.steps)
+    return per
 
 
 # ------------------------------------------------------------ reduced sizes --
@@ -251,6 +327,11 @@ def test_single_turn_reduced(name, fused):
 @pytest.mark.parametrize("fused", [False, True])
 def test_mt_reduced(fused):
     r = run_mt(SMALL["mt_b4_16k"], fused=fused)
+    assert r["worst"] <= ATOL_OUT
+
+
+def test_mt_full_blocks_reduced():
+    r = run_mt(SMALL["mt_b4_16k"], reading="full_blocks")
     assert r["worst"] <= ATOL_OUT
 
 
@@ -279,3 +360,16 @@ def test_full_l70b_b32_32k(layer):
 
 def test_full_mt_b4_16k():
     print("mt_b4_16k", run_mt(WORKLOADS["mt_b4_16k"], max_pairs=12))
+
+
+def test_full_mt_b4_16k_both_readings():
+    """Both multi-turn readings on the full workload: parity on sampled pairs,
+    then the per-step device time of each, the rows attended and the share of
+    full attention's probability mass they carry (printed; both readings fetch
+    the same k2 blocks per step)."""
+    wl = WORKLOADS["mt_b4_16k"]
+    for reading in ("candidates", "full_blocks"):
+        st = {}
+        r = run_mt(wl, max_pairs=8, reading=reading, dev_stats=st)
+        per = time_mt_steps(wl, reading)
+        print("mt_b4_16k", reading, r, st, "us per step by turn", [round(x, 2) for x in per])

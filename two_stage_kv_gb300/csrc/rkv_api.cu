@@ -112,7 +112,8 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
                       int64_t idx_cap, int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
                       float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
                       const void* v_new, int64_t row, void* stream, bool mt, const int32_t* n_rows = nullptr,
-                      const int32_t* block_table = nullptr, int64_t bt_stride = 0, int64_t num_pages = 0) {
+                      const int32_t* block_table = nullptr, int64_t bt_stride = 0, int64_t num_pages = 0,
+                      const uint32_t* mask = nullptr, int64_t mask_ld = 0, int64_t n_prompt = 0) {
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
@@ -154,6 +155,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.cap = cap; a.nblk_cap = nblk_cap; a.idx_cap = idx_cap;
   a.n = (int32_t)n; a.n_rows = n_rows; a.B = d.batch;
   a.block_table = block_table; a.bt_stride = bt_stride; a.num_pages = num_pages; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
+  a.mask = mask; a.mask_ld = mask_ld; a.n_prompt = n_prompt;
   a.blk = blk; a.k1 = k1; a.k2 = k2;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.tma_kv = (!mt && blk % 8 == 0) ? 1 : 0;
@@ -301,6 +303,47 @@ rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const
   return RKV_OK;
 }
 
+rkv_status rkv_keep_mask(rkv_dims d, const int32_t* keep_idx, int64_t keep_ld, int64_t B1, int64_t n_prompt,
+                         uint32_t* mask, int64_t mask_ld, void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0 || n_prompt == 0) return RKV_OK;
+  if (!keep_idx || !mask) return fail(RKV_ERR_INVALID_ARG, "keep_mask: NULL keep_idx or mask");
+  if (reinterpret_cast<uintptr_t>(mask) % 4 != 0 || reinterpret_cast<uintptr_t>(keep_idx) % 4 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "keep_mask: keep_idx and mask must be 4-byte aligned");
+  if (n_prompt < 0 || B1 < 0 || keep_ld < B1)
+    return fail(RKV_ERR_INVALID_ARG, "keep_mask: need n_prompt >= 0 and 0 <= B1 <= keep_ld");
+  if (mask_ld < (n_prompt + 31) / 32)
+    return fail(RKV_ERR_INVALID_ARG, "keep_mask: mask_ld=%lld < ceil(n_prompt/32)", (long long)mask_ld);
+  cudaError_t e = rkv::keep_mask_launch(keep_idx, keep_ld, B1, n_prompt, mask, mask_ld, d.batch * d.n_kv_heads,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "keep_mask launch");
+  return RKV_OK;
+}
+
+rkv_status rkv_build_kt_masked(rkv_dims d, const void* k, int64_t cap, int64_t n, const uint32_t* mask,
+                               int64_t mask_ld, int64_t n_prompt, int32_t blk, void* kt, int64_t nblk_cap,
+                               void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0 || n == 0) return RKV_OK;
+  if (!k || !kt || !mask) return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: NULL k, kt or mask");
+  if (!aligned16(k)) return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: k must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(mask) % 4 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: mask must be 4-byte aligned");
+  if (blk < 1) return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: blk < 1");
+  if (n < 0 || n > cap) return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: n=%lld out of range", (long long)n);
+  if (n_prompt < 0 || n_prompt > n)
+    return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: n_prompt=%lld outside [0, n]", (long long)n_prompt);
+  if (mask_ld < (n_prompt + 31) / 32)
+    return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: mask_ld=%lld < ceil(n_prompt/32)", (long long)mask_ld);
+  if ((n + blk - 1) / blk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "build_kt_masked: nblk_cap too small");
+  cudaError_t e = rkv::kt_build_launch(k, cap, n, nullptr, 0, blk, kt, nblk_cap, d.batch * d.n_kv_heads,
+                                       reinterpret_cast<cudaStream_t>(stream), mask, mask_ld, n_prompt);
+  if (e != cudaSuccess) return cuda_fail(e, "build_kt_masked launch");
+  return RKV_OK;
+}
+
 rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
                           int64_t keep_ld, int64_t B1, void* k_out, void* v_out, int64_t out_cap, int32_t blk, void* kt,
                           int64_t nblk_cap, void* stream) {
@@ -380,6 +423,23 @@ rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_
                              const void* v_new, int64_t row, void* stream) {
   return hsa_common(d, q, k, v, cap, idx, idx_cap, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
                     sel_channels, k_new, v_new, row, stream, true);
+}
+
+rkv_status rkv_hsa_decode_mt_masked(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int64_t n,
+                                    const uint32_t* mask, int64_t mask_ld, int64_t n_prompt, void* kt,
+                                    int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale, float* out,
+                                    int32_t* sel_blocks, int32_t* sel_channels, const void* k_new, const void* v_new,
+                                    void* stream) {
+  if (!mask) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: mask is NULL");
+  if (reinterpret_cast<uintptr_t>(mask) % 4 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: mask must be 4-byte aligned");
+  if (n_prompt < 0 || n_prompt > n || n_prompt > cap)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: n_prompt=%lld outside [0, min(n, cap)]",
+                (long long)n_prompt);
+  if (mask_ld < (n_prompt + 31) / 32)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: mask_ld=%lld < ceil(n_prompt/32)", (long long)mask_ld);
+  return hsa_common(d, q, k, v, cap, nullptr, 0, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks, sel_channels,
+                    k_new, v_new, n, stream, false, nullptr, nullptr, 0, 0, mask, mask_ld, n_prompt);
 }
 
 rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, int64_t cap, const int32_t* n_rows,

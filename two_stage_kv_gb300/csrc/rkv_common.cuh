@@ -71,6 +71,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
 }
 
 // ---------------------------------------------------------------- TMA -------
+// Any set bit among bits [lo, hi) of the bit array m (bit r: word r / 32, bit r % 32).
+__device__ __forceinline__ bool mask_any(const uint32_t* m, int64_t lo, int64_t hi) {
+  for (int64_t w = lo >> 5; lo < hi && w <= ((hi - 1) >> 5); ++w) {
+    uint32_t bits = __ldg(m + w);
+    const int64_t b0 = w << 5;
+    if (lo > b0) bits &= ~0u << (int)(lo - b0);
+    if (hi < b0 + 32) bits &= (1u << (int)(hi - b0)) - 1u;
+    if (bits) return true;
+  }
+  return false;
+}
+
+// Whether rows [lo, hi) hold a candidate of the masked multi-turn reading: a
+// prompt row (< n_prompt) whose bit is set, or any row decoded after the prompt.
+__device__ __forceinline__ bool cand_any(const uint32_t* m, int64_t n_prompt, int64_t lo, int64_t hi) {
+  if (hi <= lo) return false;
+  if (hi > n_prompt) return true;
+  return mask_any(m, lo, hi);
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

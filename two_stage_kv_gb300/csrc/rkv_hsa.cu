@@ -83,6 +83,7 @@ struct FixedSmem {
   uint64_t ktbar;                       // KT prefetch (phase B)
   uint64_t sbar;                        // every block score and score bound of the cluster (phase B)
   float2 rbound[8 * NWARP];             // (min, max) of the scores of each warp of each CTA
+  uint32_t relig[MAX_ROUND_ROWS / 32];  // masked MT: candidate rows of the staged round
 };
 
 // Block-wide exclusive scan of a flag.  Returns the prefix, writes the total.
@@ -179,7 +180,8 @@ __device__ void bucket_topk(float* vals, int n, int k, float mn, float mx, uint8
   const float width = mx - mn;
   bool fallback = !(width > 0.f) || !isfinite(width);
   const float inv = fallback ? 0.f : (float)NBUCKET / width;
-  auto bucket = [&](float s) { return min(NBUCKET - 1, (int)((s - mn) * inv)); };
+  // (clamped at both ends: -inf / +inf entries of the masked multi-turn reading)
+  auto bucket = [&](float s) { return max(0, min(NBUCKET - 1, (int)((s - mn) * inv))); };
   if (!fallback) {
     for (int j = tid; j < n; j += NT) atomicAdd(&fs.hist[bucket(vals[j])], 1);
     __syncthreads();
@@ -235,32 +237,14 @@ __device__ void bucket_topk(float* vals, int n, int k, float mn, float mx, uint8
   }
 }
 
-// Block-wide min / max of v over the threads (every thread gets the result).
-__device__ __forceinline__ void block_minmax(float& mn, float& mx, FixedSmem& fs) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) {
-    fs.wmin[warp] = mn;
-    fs.wmax[warp] = mx;
-  }
-  __syncthreads();
-  mn = fs.wmin[0];
-  mx = fs.wmax[0];
-#pragma unroll
-  for (int w = 1; w < NWARP; ++w) {
-    mn = fminf(mn, fs.wmin[w]);
-    mx = fmaxf(mx, fs.wmax[w]);
-  }
-}
-
 // RAG: lengths read after the dependency wait (n_rows, or the call's n when
 // n_rows is NULL); PG: K/V in pages of blk rows, [num_pages, Hkv, blk, D], found
-// through a per-row block table (implies RAG).
-template <bool MT, int NH, bool RAG, bool PG>
+// through a per-row block table (implies RAG); MK: the multi-turn reading over
+// fixed blocks of the full cache, where only candidate rows (stage-1 survivors
+// of the prompt, every row decoded after it) count: bounds, blocks without a
+// candidate never chosen, the newest row's block always chosen, attention over
+// candidate rows only.
+template <bool MT, int NH, bool RAG, bool PG, bool MK = false>
 __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                            const __grid_constant__ CUtensorMap tmV,
                                                            const __grid_constant__ CUtensorMap tmKT,
@@ -358,12 +342,17 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   }
   // the CTA holding the appended key's block persists its KT column; without
   // the prefetch it fetches the old column now and writes the new one at the end
+  const uint32_t* mrow = MK ? a.mask + (size_t)pair * a.mask_ld : nullptr;
+  // the appended key starts its block's bounds when the block holds no earlier
+  // candidate, and widens them otherwise
+  bool fresh_new = (n_old % a.blk) == 0;
+  if (MK && own_new && !fresh_new) fresh_new = !cand_any(mrow, a.n_prompt, (int64_t)nb_new * a.blk, n_old);
   bf16 kt_old = __float2bfloat16(0.f);
   bf16* kt_col = nullptr;
   if (own_new) {
     const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
     kt_col = reinterpret_cast<bf16*>(a.kt) + ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
-    if (!spec && (n_old % a.blk) != 0) kt_old = *kt_col;
+    if (!spec && !fresh_new) kt_old = *kt_col;
   }
 
   // ---------------------------------------------------------------- A ------
@@ -468,6 +457,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     const bf16* ktp = reinterpret_cast<const bf16*>(a.kt) + (size_t)pair * 2 * HD * a.nblk_cap;
     const int bc = spec ? cpr : a.kt_chunk;          // columns per tile (multiple of 8)
     const int cg = tid & 3, bp = tid >> 2;           // channel group, block pair within a 128-block span
+    if (MK) {
+      // which of this CTA's blocks hold a candidate (read after the barrier before scoring)
+      for (int j = jlo + tid; j < jhi; j += NT)
+        flag[j] = cand_any(mrow, a.n_prompt, (int64_t)j * a.blk, min((int64_t)(j + 1) * a.blk, (int64_t)n_tot)) ? 1
+                                                                                                                : 0;
+    }
     for (int cb0 = jlo; cb0 < jhi; cb0 += bc) {
       const int nb_here = min(bc, jhi - cb0);
       if (spec) {
@@ -478,7 +473,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           const int m = tid >> 7, c = tid & (HD - 1);
           const bf16 kv = fs.knew[c];
           bf16& slot = kttile[(size_t)tid * bc + col];
-          if ((n_old % a.blk) == 0) {
+          if (fresh_new) {
             slot = kv;
           } else {
             const float x = bf2f(kv), o = bf2f(slot);
@@ -499,7 +494,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         __syncthreads();
         if (own_new && nb_new >= cb0 && nb_new < cb0 + nb_here) {
           const int col = nb_new - cb0;
-          const bool fresh = (n_old % a.blk) == 0;
+          const bool fresh = fresh_new;
           for (int i = tid; i < k1; i += NT) {
             const int ro = fs.rowoff[i];
             const bf16 kv = fs.knew[ro & (HD - 1)];
@@ -536,11 +531,21 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         s1 = (s1 == 0.f) ? 0.f : s1;
         const int j = cb0 + 2 * jp;
         const bool v0 = live, v1 = live && 2 * jp + 1 < nb_here;
-        if (v0) {
+        bool f0 = v0, f1 = v1;                       // finite scores (the bucket range)
+        if (MK) {
+          // a block without a candidate scores -inf, the newest row's block +inf
+          const int tail = (n_tot - 1) / a.blk;
+          const float pinf = __int_as_float(0x7f800000);
+          if (v0) s0 = !flag[j] ? neg_inf() : (j == tail ? pinf : s0);
+          if (v1) s1 = !flag[j + 1] ? neg_inf() : (j + 1 == tail ? pinf : s1);
+          f0 = v0 && isfinite(s0);
+          f1 = v1 && isfinite(s1);
+        }
+        if (f0) {
           smn = fminf(smn, s0);
           smx = fmaxf(smx, s0);
         }
-        if (v1) {
+        if (f1) {
           smn = fminf(smn, s1);
           smx = fmaxf(smx, s1);
         }
@@ -677,9 +682,20 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       *reinterpret_cast<uint4*>(((i & 1) ? tV : tK) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7)) =
           make_uint4(0, 0, 0, 0);
     }
+    if (MK && tid < MAX_ROUND_ROWS) {
+      // candidate rows of this round, one bit per staged row
+      bool e = false;
+      if (tid < rows) {
+        const int slot = tid / blk;
+        const int t = sel[r0 + slot] * blk + (tid - slot * blk);
+        e = t < n_tot && (t >= a.n_prompt || ((__ldg(mrow + (t >> 5)) >> (t & 31)) & 1u) != 0);
+      }
+      const unsigned bm = __ballot_sync(0xffffffffu, e);
+      if (lane == 0) fs.relig[warp] = bm;
+    }
     if (gat) cp_async_wait_all();
     // cp.async rows and zero rows come from every thread; TMA rows are waited for per slot
-    if (gat || rows16 != rows) __syncthreads();
+    if (gat || rows16 != rows || MK) __syncthreads();
 
     // --- S^T = K Q^T for the warp's 16-token step, masked and in log2 units
     const int c0 = warp * 16;
@@ -723,8 +739,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       // this lane: tokens c0 + lane/4 (e = 0, 1) and + 8 (e = 2, 3); heads 2(lane%4) + (e & 1)
       const int ta = c0 + g4, tb = ta + 8;
       const int sla = ta / blk, slb = tb / blk;
-      const bool va = ta < rows && sel[r0 + sla] * blk + (ta - sla * blk) < n_tot;
-      const bool vb = tb < rows && sel[r0 + slb] * blk + (tb - slb * blk) < n_tot;
+      bool va = ta < rows && sel[r0 + sla] * blk + (ta - sla * blk) < n_tot;
+      bool vb = tb < rows && sel[r0 + slb] * blk + (tb - slb * blk) < n_tot;
+      if (MK) {
+        va = va && ((fs.relig[ta >> 5] >> (ta & 31)) & 1u) != 0;
+        vb = vb && ((fs.relig[tb >> 5] >> (tb & 31)) & 1u) != 0;
+      }
 #pragma unroll
       for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
@@ -889,7 +909,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   if (own_new && !spec) {
     const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
     const bf16 kv = fs.knew[c];
-    if ((n_old % a.blk) == 0) {
+    if (fresh_new) {
       *kt_col = kv;
     } else {
       const float x = bf2f(kv), o = bf2f(kt_old);
@@ -974,7 +994,9 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    const void* ks[8] = {
+    const void* ks[10] = {
+        (const void*)hsa_decode_kernel<false, 1, false, false, true>,
+        (const void*)hsa_decode_kernel<false, 2, false, false, true>,
         (const void*)hsa_decode_kernel<false, 1, false, false>, (const void*)hsa_decode_kernel<false, 2, false, false>,
         (const void*)hsa_decode_kernel<true, 1, false, false>, (const void*)hsa_decode_kernel<true, 2, false, false>,
         (const void*)hsa_decode_kernel<false, 1, true, false>, (const void*)hsa_decode_kernel<false, 2, true, false>,
@@ -1003,6 +1025,8 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   // kernels keep every length a launch constant
   const bool wide = a.G > 8;
   auto kern = mt ? (wide ? hsa_decode_kernel<true, 2, false, false> : hsa_decode_kernel<true, 1, false, false>)
+          : a.mask ? (wide ? hsa_decode_kernel<false, 2, false, false, true>
+                           : hsa_decode_kernel<false, 1, false, false, true>)
           : a.block_table ? (wide ? hsa_decode_kernel<false, 2, true, true> : hsa_decode_kernel<false, 1, true, true>)
           : a.n_rows ? (wide ? hsa_decode_kernel<false, 2, true, false> : hsa_decode_kernel<false, 1, true, false>)
                      : (wide ? hsa_decode_kernel<false, 2, false, false> : hsa_decode_kernel<false, 1, false, false>);

@@ -31,6 +31,8 @@ struct HsaArgs {
   const int32_t* n_rows; // ragged: [B] candidates before the append per batch row (device), else nullptr
   const int32_t* block_table;  // paged: [B, bt_stride] page of each logical block (device), else nullptr
   int64_t bt_stride, num_pages;  // paged: K/V pools are [num_pages, Hkv, blk, D]
+  const uint32_t* mask;  // masked MT: [B, Hkv, mask_ld] bit r = prompt row r kept by stage 1, else nullptr
+  int64_t mask_ld, n_prompt;     // rows >= n_prompt (decoded after the prompt) are always candidates
   int32_t nblk;         // blocks over the attended candidates
   int32_t k2e;          // min(k2, nblk)
   int32_t ns;           // CTAs per cluster (one cluster per (b, kv head))
@@ -77,7 +79,10 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
 
 // ------------------------------------------------------------ KT / append ---
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
-                            int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st);
+                            int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st,
+                            const uint32_t* mask = nullptr, int64_t mask_ld = 0, int64_t n_prompt = 0);
+cudaError_t keep_mask_launch(const int32_t* keep, int64_t keep_ld, int64_t B1, int64_t n_prompt, uint32_t* mask,
+                             int64_t mask_ld, int32_t pairs, cudaStream_t st);
 cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
                               int64_t B1, int blk, void* ko, void* vo, int64_t out_cap, void* kt, int64_t nblk_cap,
                               int pairs, cudaStream_t st, const int32_t* bt = nullptr, int64_t bt_stride = 0,

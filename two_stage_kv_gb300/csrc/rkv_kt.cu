@@ -16,10 +16,14 @@ constexpr int KT_NT = 256;
 
 // One CTA per (pair, 64 blocks): warps reduce 8 blocks each over coalesced
 // 256-byte key rows, the results are transposed in shared memory and written
-// as 128-byte runs along the block axis.
+// as 128-byte runs along the block axis.  With a mask (the multi-turn reading
+// over fixed blocks of the full cache) only candidate rows count: prompt rows
+// (< n_prompt) whose bit is set and every later row; a block without one
+// stores zeros.
 __global__ void __launch_bounds__(KT_NT) kt_build_kernel(const bf16* k, int64_t cap, int64_t n,
                                                          const int32_t* idx, int64_t idx_cap, int blk,
-                                                         bf16* kt, int64_t nblk_cap) {
+                                                         bf16* kt, int64_t nblk_cap, const uint32_t* mask,
+                                                         int64_t mask_ld, int64_t n_prompt) {
   __shared__ bf16 tmax[HD][KT_BLOCKS + 2];
   __shared__ bf16 tmin[HD][KT_BLOCKS + 2];
   pdl_wait();
@@ -30,6 +34,7 @@ __global__ void __launch_bounds__(KT_NT) kt_build_kernel(const bf16* k, int64_t 
   const int64_t jb0 = (int64_t)blockIdx.x * KT_BLOCKS;
   const bf16* kp = k + (size_t)pair * cap * HD;
   const int32_t* ip = idx ? idx + (size_t)pair * idx_cap : nullptr;
+  const uint32_t* mp = mask ? mask + (size_t)pair * mask_ld : nullptr;
   for (int u = 0; u < KT_BLOCKS / 8; ++u) {
     const int jl = warp * (KT_BLOCKS / 8) + u;
     const int64_t jb = jb0 + jl;
@@ -41,7 +46,10 @@ __global__ void __launch_bounds__(KT_NT) kt_build_kernel(const bf16* k, int64_t 
       mx[i] = neg_inf();
       mn[i] = -neg_inf();
     }
+    bool any = false;
     for (int64_t t = t0; t < t1; ++t) {
+      if (mp && t < n_prompt && ((__ldg(mp + (t >> 5)) >> (t & 31)) & 1u) == 0) continue;
+      any = true;
       const int64_t row = ip ? min(max((int64_t)ip[t], (int64_t)0), cap - 1) : t;
       const uint2 raw = *reinterpret_cast<const uint2*>(kp + row * HD + lane * 4);
       const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x), v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
@@ -53,8 +61,8 @@ __global__ void __launch_bounds__(KT_NT) kt_build_kernel(const bf16* k, int64_t 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // values are bf16 already: the conversion back is exact
-      tmax[lane * 4 + i][jl] = __float2bfloat16_rn(mx[i]);
-      tmin[lane * 4 + i][jl] = __float2bfloat16_rn(mn[i]);
+      tmax[lane * 4 + i][jl] = __float2bfloat16_rn(any ? mx[i] : 0.f);
+      tmin[lane * 4 + i][jl] = __float2bfloat16_rn(any ? mn[i] : 0.f);
     }
   }
   __syncthreads();
@@ -189,12 +197,40 @@ __global__ void __launch_bounds__(CK_NT) compact_kt_kernel(const bf16* k, const 
 }  // namespace
 
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
-                            int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st) {
+                            int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st,
+                            const uint32_t* mask, int64_t mask_ld, int64_t n_prompt) {
   const int64_t nblk = (n + blk - 1) / blk;
   if (nblk == 0 || pairs == 0) return cudaSuccess;
   return launch_pdl(kt_build_kernel, dim3((unsigned)((nblk + KT_BLOCKS - 1) / KT_BLOCKS), pairs), dim3(KT_NT), 0, st,
                     reinterpret_cast<const bf16*>(k), cap, n, idx, idx_cap, (int)blk, reinterpret_cast<bf16*>(kt),
-                    nblk_cap);
+                    nblk_cap, mask, mask_ld, n_prompt);
+}
+
+namespace {
+
+// One CTA per pair: clear the prompt's bits, then set the bit of every kept row.
+__global__ void __launch_bounds__(256) keep_mask_kernel(const int32_t* keep, int64_t keep_ld, int64_t B1,
+                                                        int64_t n_prompt, uint32_t* mask, int64_t mask_ld) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int pair = blockIdx.x;
+  uint32_t* m = mask + (size_t)pair * mask_ld;
+  const int64_t words = (n_prompt + 31) / 32;
+  for (int64_t w = threadIdx.x; w < words; w += blockDim.x) m[w] = 0u;
+  __syncthreads();
+  const int32_t* kp = keep + (size_t)pair * keep_ld;
+  for (int64_t i = threadIdx.x; i < B1; i += blockDim.x) {
+    const int32_t r = kp[i];
+    if (r >= 0 && r < n_prompt) atomicOr(m + (r >> 5), 1u << (r & 31));
+  }
+}
+
+}  // namespace
+
+cudaError_t keep_mask_launch(const int32_t* keep, int64_t keep_ld, int64_t B1, int64_t n_prompt, uint32_t* mask,
+                             int64_t mask_ld, int32_t pairs, cudaStream_t st) {
+  if (pairs == 0) return cudaSuccess;
+  return launch_pdl(keep_mask_kernel, dim3(pairs), dim3(256), 0, st, keep, keep_ld, B1, n_prompt, mask, mask_ld);
 }
 
 cudaError_t append_launch(const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,

@@ -123,9 +123,18 @@ class Layer:
 
 
 class MTLayer:
-    """RocketKV-MT state: the full cache stays resident; stage 2 reads it through idx."""
+    """RocketKV-MT state: the full cache stays resident; stage 2 reads it through idx.
 
-    def __init__(self, wl: Workload, device="cuda"):
+    reading="candidates": stage-2 blocks run over the candidate sequence (the
+    stage-1 survivors, then the decoded tokens) read through idx.
+    reading="full_blocks": stage-2 blocks are fixed runs of blk rows of the full
+    cache; a survivor mask over the turn's prompt rows marks the candidates.
+    """
+
+    def __init__(self, wl: Workload, device="cuda", reading: str = "candidates"):
+        if reading not in ("candidates", "full_blocks"):
+            raise ValueError(reading)
+        self.reading = reading
         self.wl = wl
         self.dims = (wl.B, wl.Hq, wl.Hkv, wl.D)
         B, Hkv, D = wl.B, wl.Hkv, wl.D
@@ -136,6 +145,11 @@ class MTLayer:
         self.idx_cap = max(b.B1 for b in self.budgets) + wl.steps
         self.nblk_cap = nblk_capacity(self.idx_cap, wl.blk)
         self.idx = torch.zeros(B, Hkv, self.idx_cap, dtype=torch.int32, device=device)
+        if reading == "full_blocks":
+            self.nblk_cap = nblk_capacity(self.cap, wl.blk)
+            self.mask_ld = (self.cap + 31) // 32
+            self.mask = torch.zeros(B, Hkv, self.mask_ld, dtype=torch.int32, device=device)
+        self.n_prompt = 0
         self.kt = torch.empty(B, Hkv, 2, D, self.nblk_cap, dtype=torch.bfloat16, device=device)
         S_max = wl.turn_context(wl.n_turns - 1)
         self.ws_bytes = rkv.rkv_snap_evict_workspace(self.dims, S_max, wl.W)
@@ -166,20 +180,40 @@ class MTLayer:
                            self.scale, self.idx, self.idx_cap, None, None, 0, self.pooled, self.ws, self.ws_bytes,
                            stream)
         self.n = bud.B1
+        self.n_prompt = self.rows
+        if self.reading == "full_blocks":
+            rkv.rkv_keep_mask(self.dims, self.idx, self.idx_cap, bud.B1, self.n_prompt, self.mask, self.mask_ld,
+                              stream)
 
     def build_kt(self, stream=None):
+        if self.reading == "full_blocks":
+            rkv.rkv_build_kt_masked(self.dims, self.k, self.cap, self.rows, self.mask, self.mask_ld, self.n_prompt,
+                                    self.wl.blk, self.kt, self.nblk_cap, stream)
+            return
         rkv.rkv_build_kt(self.dims, self.k, self.cap, self.n, self.idx, self.idx_cap, self.wl.blk, self.kt,
                          self.nblk_cap, stream)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        if self.reading == "full_blocks":
+            raise RuntimeError("the full-block reading appends inside step()")
         rkv.rkv_append_kv(self.dims, k_new, v_new, self.k, self.v, self.cap, self.n, self.rows, self.idx,
                           self.idx_cap, self.kt, self.nblk_cap, self.wl.blk, stream)
         self.n += 1
         self.rows += 1
 
+    def _masked(self, q, k_new, v_new, stream):
+        wl = self.wl
+        k2 = self.budgets[self.turn].k2
+        rkv.rkv_hsa_decode_mt_masked(self.dims, q, self.k, self.v, self.cap, self.rows, self.mask, self.mask_ld,
+                                     self.n_prompt, self.kt, self.nblk_cap, wl.blk, wl.k1, k2, self.scale, self.out,
+                                     self.sel_blocks, self.sel_channels, k_new, v_new, stream)
+
     def decode(self, q: torch.Tensor, stream=None):
         wl = self.wl
         k2 = self.budgets[self.turn].k2
+        if self.reading == "full_blocks":
+            self._masked(q, None, None, stream)
+            return
         rkv.rkv_hsa_decode_mt(self.dims, q, self.k, self.v, self.cap, self.idx, self.idx_cap, self.n, self.kt,
                               self.nblk_cap, wl.blk, wl.k1, k2, self.scale, self.out, self.sel_blocks,
                               self.sel_channels, stream=stream)
@@ -188,8 +222,11 @@ class MTLayer:
         """One MT decode step with the append (full cache row + candidate index) fused in."""
         wl = self.wl
         k2 = self.budgets[self.turn].k2
-        rkv.rkv_hsa_decode_mt(self.dims, q, self.k, self.v, self.cap, self.idx, self.idx_cap, self.n, self.kt,
-                              self.nblk_cap, wl.blk, wl.k1, k2, self.scale, self.out, self.sel_blocks,
-                              self.sel_channels, k_new, v_new, self.rows, stream)
+        if self.reading == "full_blocks":
+            self._masked(q, k_new, v_new, stream)
+        else:
+            rkv.rkv_hsa_decode_mt(self.dims, q, self.k, self.v, self.cap, self.idx, self.idx_cap, self.n, self.kt,
+                                  self.nblk_cap, wl.blk, wl.k1, k2, self.scale, self.out, self.sel_blocks,
+                                  self.sel_channels, k_new, v_new, self.rows, stream)
         self.n += 1
         self.rows += 1

@@ -21,8 +21,8 @@ STATUS_NAMES = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
 # Every symbol include/rkv.h declares.
 EXPORTED = ["rkv_last_error", "rkv_abi_version", "rkv_budget_split", "rkv_snap_evict_workspace",
             "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_compact_kt_paged", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
-            "rkv_hsa_decode_ragged", "rkv_hsa_decode_paged",
-            "rkv_read_device_flags"]
+            "rkv_hsa_decode_ragged", "rkv_hsa_decode_paged", "rkv_keep_mask", "rkv_build_kt_masked",
+            "rkv_hsa_decode_mt_masked", "rkv_read_device_flags"]
 
 
 class RkvError(RuntimeError):
@@ -63,6 +63,10 @@ _SIGS = {
                                      _vp, _vp, _vp, _vp, _vp]),
     "rkv_hsa_decode_paged": (_i32, [Dims, _vp, _vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i32, _i32, _i32,
                                     _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "rkv_keep_mask": (_i32, [Dims, _vp, _i64, _i64, _i64, _vp, _i64, _vp]),
+    "rkv_build_kt_masked": (_i32, [Dims, _vp, _i64, _i64, _vp, _i64, _i64, _i32, _vp, _i64, _vp]),
+    "rkv_hsa_decode_mt_masked": (_i32, [Dims, _vp, _vp, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i32, _i32,
+                                        _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "rkv_read_device_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -188,6 +192,27 @@ def rkv_hsa_decode_paged(dims, q, k_pages, v_pages, num_pages, block_table, bt_s
                                       _ptr(block_table), bt_stride, _ptr(n_rows), n_max, _ptr(kt), nblk_cap, blk, k1,
                                       k2, scale, _ptr(out), _ptr(sel_blocks), _ptr(sel_channels), _ptr(k_new),
                                       _ptr(v_new), _stream(stream)))
+
+
+def rkv_keep_mask(dims, keep_idx, keep_ld, B1, n_prompt, mask, mask_ld, stream=None):
+    """Candidate bits of the prompt rows [0, n_prompt) from a stage-1 keep list."""
+    _check(lib().rkv_keep_mask(_dims(dims), _ptr(keep_idx), keep_ld, B1, n_prompt, _ptr(mask), mask_ld,
+                               _stream(stream)))
+
+
+def rkv_build_kt_masked(dims, k, cap, n, mask, mask_ld, n_prompt, blk, kt, nblk_cap, stream=None):
+    """KT over fixed blocks of the full cache, candidate rows only."""
+    _check(lib().rkv_build_kt_masked(_dims(dims), _ptr(k), cap, n, _ptr(mask), mask_ld, n_prompt, blk, _ptr(kt),
+                                     nblk_cap, _stream(stream)))
+
+
+def rkv_hsa_decode_mt_masked(dims, q, k, v, cap, n, mask, mask_ld, n_prompt, kt, nblk_cap, blk, k1, k2, scale, out,
+                             sel_blocks=None, sel_channels=None, k_new=None, v_new=None, stream=None):
+    """Multi-turn HSA step over fixed blocks of the full cache (candidate rows from the mask)."""
+    _check(lib().rkv_hsa_decode_mt_masked(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, n, _ptr(mask), mask_ld,
+                                          n_prompt, _ptr(kt), nblk_cap, blk, k1, k2, scale, _ptr(out),
+                                          _ptr(sel_blocks), _ptr(sel_channels), _ptr(k_new), _ptr(v_new),
+                                          _stream(stream)))
 
 
 def rkv_read_device_flags() -> int:
