@@ -231,9 +231,9 @@ def compact(X: np.ndarray, keep: np.ndarray) -> np.ndarray:
 def build_kt(Kc: np.ndarray, n: int, blk: int) -> Tuple[np.ndarray, np.ndarray]:
     """Elementwise max and min of each block of blk consecutive keys.
 
-    Kc: [>= n, D].  Returns Kmax, Kmin as [D, nblk] (channel-major, the layout
-    "aligned along the head dimension"); a partial last block uses only its
-    valid rows (READING R9).
+    Kc: [>= n, D].  Returns Kmax, Kmin as [D, nblk] (channel-major: [RKV] HSA
+    step 1 keeps the bounds per head dimension); a partial last block uses
+    only its valid rows (READING R9).
     """
     D = Kc.shape[1]
     nblk = (n + blk - 1) // blk
@@ -359,8 +359,8 @@ def hsa_decode_mt(q_group: np.ndarray, Kfull: np.ndarray, Vfull: np.ndarray, idx
 
 def candidate_rows(keep: np.ndarray, n_prompt: int, n: int) -> np.ndarray:
     """Which of the rows [0, n) stage 2 may attend: the kept prompt rows and
-    every row decoded after the prompt (the model "selects from the N input
-    tokens plus newly generated tokens")."""
+    every row decoded after the prompt (RocketKV-MT limits stage 2 to the
+    stage-1 survivors of the input and the tokens generated since)."""
     cand = np.zeros(n, dtype=bool)
     keep = np.asarray(keep, dtype=np.int64)
     cand[keep[keep < min(n_prompt, n)]] = True
