@@ -150,7 +150,10 @@ rkv_status rkv_snap_evict_noalloc(rkv_dims d, const void* q_obs, int32_t W, cons
  * compacted cache (bit for bit), in one pass over the kept rows; run
  * rkv_snap_evict in mask mode (k_out = v_out = NULL) first to get keep_idx.
  * Arguments
- *   k, v       [B, Hkv, cap, D] bf16 prompt caches (16-byte aligned).
+ *   k, v       [B, Hkv, cap, D] bf16 prompt caches (16-byte aligned), each in
+ *              device memory or in page-locked host memory: a host-resident
+ *              cache is read in place over the host link, so only its kept
+ *              rows cross it (stage 1 needs all of K but none of V).
  *   keep_idx   [B, Hkv, keep_ld] int32 rows to keep (entries are clamped into
  *              [0, cap)); keep_ld >= B1.
  *   k_out,v_out[B, Hkv, out_cap, D] bf16 compacted caches, B1 <= out_cap;
@@ -158,8 +161,9 @@ rkv_status rkv_snap_evict_noalloc(rkv_dims d, const void* q_obs, int32_t W, cons
  *   kt         [B, Hkv, 2, D, nblk_cap] bf16 (16-byte aligned), nblk_cap a
  *              multiple of 8 and >= ceil(B1 / blk); columns [0, ceil(B1/blk))
  *              are written.
- * Errors: RKV_ERR_INVALID_ARG for NULL or misaligned pointers and the size
- * rules above; RKV_ERR_CUDA if the launch fails.
+ * Errors: RKV_ERR_INVALID_ARG for NULL or misaligned pointers, k or v in
+ * memory the device cannot reach (pageable host memory included), and the
+ * size rules above; RKV_ERR_CUDA if the launch fails.
  */
 rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
                           int64_t keep_ld, int64_t B1, void* k_out, void* v_out, int64_t out_cap, int32_t blk, void* kt,
@@ -169,7 +173,8 @@ rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap,
  * rkv_compact_kt writing the compacted rows into pages: row i of batch row b
  * (for every KV head h) goes to slot i % blk of page block_table[b, i / blk]:
  *   k_pages[page, h, i % blk] = k[b, h, keep_idx[b, h, i]], likewise for v;
- * KT as rkv_compact_kt (per (b, h), logical block order).
+ * KT as rkv_compact_kt (per (b, h), logical block order); k and v as there
+ * (device or page-locked host memory).
  *   k_pages,v_pages [num_pages, Hkv, blk, D] bf16 pools (16-byte aligned).
  *   block_table     [B, bt_stride] int32 DEVICE array, bt_stride >= ceil(B1/blk);
  *                   page ids are clamped into [0, num_pages).

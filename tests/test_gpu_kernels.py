@@ -717,3 +717,39 @@ def test_hsa_decode_mt_masked_all_candidates_equals_dense():
     rkv.rkv_hsa_decode(dims, q, k, v, n + 8, n, kt2, ncap, blk, k1, k2, 0.1, o2, s2)
     torch.cuda.synchronize()
     assert torch.equal(kt1, kt2) and torch.equal(s1, s2) and torch.equal(o1, o2)
+
+
+# --------------------------------------------------- host-resident prompt V --
+
+
+def test_compact_kt_reads_page_locked_host_v():
+    """A prompt V in page-locked host memory is compacted in place (only the kept
+    rows cross the host link) with results identical to a device-resident V;
+    pageable host memory is refused on the host before any launch."""
+    B, Hq, Hkv, D, cap, B1, blk = 2, 8, 2, 128, 1500, 333, 16
+    dims = (B, Hq, Hkv, D)
+    kb, k = _rand(71, (B, Hkv, cap, D))
+    vb, v = _rand(72, (B, Hkv, cap, D))
+    rng = np.random.default_rng(73)
+    keep = np.stack([np.stack([np.sort(rng.choice(cap, B1, replace=False)) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32)
+    keep_t = torch.from_numpy(keep).to(DEV)
+    ncap = -(-(-(-B1 // blk)) // 8) * 8
+    outs = []
+    for vv in (v, v.cpu().pin_memory()):
+        ko = torch.zeros((B, Hkv, B1, D), dtype=torch.bfloat16, device=DEV)
+        vo = torch.zeros_like(ko)
+        kt = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+        rkv.rkv_compact_kt(dims, k, vv, cap, keep_t, B1, B1, ko, vo, B1, blk, kt, ncap)
+        torch.cuda.synchronize()
+        outs.append((ko, vo, kt))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    vf = bf16_bits_to_f64(vb)
+    got = t2f64(outs[1][1])
+    for b in range(B):
+        for h in range(Hkv):
+            assert np.array_equal(got[b, h], oracle.compact(vf[b, h], keep[b, h]))
+    with pytest.raises(rkv.RkvError) as e:
+        rkv.rkv_compact_kt(dims, k, v.cpu(), cap, keep_t, B1, B1, outs[0][0], outs[0][1], B1, blk, outs[0][2], ncap)
+    assert e.value.status == 1

@@ -33,6 +33,26 @@ rkv_status cuda_fail(cudaError_t e, const char* where) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The address kernels use for a source that may live in device memory or in
+// page-locked host memory (read over the host link; only the rows a kernel
+// touches cross it).  Anything else is refused rather than dereferenced.
+rkv_status device_view(const void* p, const void** out, const char* what) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RKV_ERR_INVALID_ARG, "%s: not an address the device can reach", what);
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return RKV_OK;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) {
+    *out = at.devicePointer;
+    return RKV_OK;
+  }
+  return fail(RKV_ERR_INVALID_ARG, "%s must be device memory or page-locked host memory", what);
+}
+
 rkv_status check_dims(const rkv_dims& d) {
   if (d.batch < 0 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.head_dim < 1)
     return fail(RKV_ERR_INVALID_ARG, "dims: batch=%d Hq=%d Hkv=%d D=%d", d.batch, d.n_q_heads, d.n_kv_heads,
@@ -359,6 +379,8 @@ rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap,
   if (nblk_cap % 8 != 0) return fail(RKV_ERR_INVALID_ARG, "compact_kt: nblk_cap=%lld is not a multiple of 8",
                                      (long long)nblk_cap);
   if ((B1 + blk - 1) / blk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "compact_kt: nblk_cap too small");
+  if ((s = device_view(k, &k, "compact_kt: k")) != RKV_OK || (s = device_view(v, &v, "compact_kt: v")) != RKV_OK)
+    return s;
   cudaError_t e = rkv::compact_kt_launch(k, v, cap, keep_idx, keep_ld, B1, blk, k_out, v_out, out_cap, kt, nblk_cap,
                                          d.batch * d.n_kv_heads, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "compact_kt launch");
@@ -385,6 +407,9 @@ rkv_status rkv_compact_kt_paged(rkv_dims d, const void* k, const void* v, int64_
   if (nblk_cap % 8 != 0) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: nblk_cap=%lld is not a multiple of 8",
                                      (long long)nblk_cap);
   if (nblk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "compact_kt_paged: nblk_cap too small");
+  if ((s = device_view(k, &k, "compact_kt_paged: k")) != RKV_OK ||
+      (s = device_view(v, &v, "compact_kt_paged: v")) != RKV_OK)
+    return s;
   cudaError_t e = rkv::compact_kt_launch(k, v, cap, keep_idx, keep_ld, B1, blk, k_pages, v_pages, 0, kt, nblk_cap,
                                          d.batch * d.n_kv_heads, reinterpret_cast<cudaStream_t>(stream), block_table,
                                          bt_stride, num_pages, d.n_kv_heads);
