@@ -38,6 +38,14 @@ Readings where the pages are silent or ambiguous (each marked READING below):
   R10 multi-turn: stage-2 candidates are the stage-1 survivors (ascending)
      followed by the tokens decoded since; blocks are formed over that
      compacted index sequence and K/V rows are read from the full cache.
+  R12 FP8 storage (not on the pages; a storage option of this build): the
+     compacted K and V hold e4m3 codes (1 sign, 4 exponent bits with bias 7,
+     3 mantissa bits, no infinities, S.1111.111 = NaN, largest 448) of
+     x / scale, rounded to nearest even in fp32 and saturated to +-448, with a
+     caller-given fp32 scale per (batch, KV head) for K and for V; a row's
+     value is code * scale.  The KT bounds are the max / min of the stored
+     key codes (exact), and block scores are taken on code values (the
+     positive K scale does not change their order).
   R11 multi-turn, the other reading (built beside R10): blocks are the fixed
      runs of blk rows of the full cache itself.  A row is a candidate when
      stage 1 kept it (prompt rows [0, n_prompt)) or when it was decoded after
@@ -427,6 +435,71 @@ def hsa_decode_mt_masked(q_group: np.ndarray, Kfull: np.ndarray, Vfull: np.ndarr
     tok = tok[cand[tok]]
     y = attention(q_group, Kfull[tok], Vfull[tok], scale)
     return {"y": y, "i1": i1, "i2": i2, "s": s, "tok": tok}
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) storage of the compacted cache  (READING R12)
+# ---------------------------------------------------------------------------
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Value of each e4m3 code: exponent field 0 is subnormal (m/8 * 2^-6),
+    otherwise (1 + m/8) * 2^(e - 7); S.1111.111 is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.power(2.0, e - 7))
+    val = sign * mag
+    return np.where((e == 15) & (m == 7), np.nan, val)
+
+
+_E4M3_POS = e4m3_decode(np.arange(127, dtype=np.uint8))     # codes 0..126: 0 .. 448, ascending
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code of each value (ties to the even code, i.e. even
+    mantissa), magnitudes above 448 saturated to 448, NaN -> 0x7f; the sign
+    bit follows the value's sign (a negative value that rounds to zero gives
+    0x80)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    dlo = np.abs(a - _E4M3_POS[lo])
+    dhi = np.abs(_E4M3_POS[hi] - a)
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.int64)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    return np.where(np.isnan(x), 0x7F, code).astype(np.uint8)
+
+
+def fp8_quantize(X: np.ndarray, scale: float) -> np.ndarray:
+    """Codes of X / scale, the quotient taken in fp32 (READING R12)."""
+    q = np.asarray(X, dtype=np.float32) / np.float32(scale)
+    return e4m3_encode(q.astype(np.float64))
+
+
+def build_kt_fp8(Kcodes: np.ndarray, n: int, blk: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Kmax / Kmin of the key code values of each block, [D, nblk]."""
+    return build_kt(e4m3_decode(Kcodes), n, blk)
+
+
+def hsa_decode_fp8(q_group: np.ndarray, Kcodes: np.ndarray, Vcodes: np.ndarray, n: int, kmax: np.ndarray,
+                   kmin: np.ndarray, k_scale: float, v_scale: float, blk: int, k1: int, k2: int,
+                   scale: float) -> Dict[str, np.ndarray]:
+    """HSA step over an e4m3 cache: Algorithm 1's scores on the code values
+    (kmax / kmin from build_kt_fp8), then attention over the selected rows'
+    values code * scale."""
+    nblk = (n + blk - 1) // blk
+    i1, qbar = hsa_channels(q_group, k1)
+    s = hsa_block_scores(qbar, i1, kmax[:, :nblk], kmin[:, :nblk])
+    i2 = topk_lowest_index(s, k2)
+    tok = block_tokens(i2, n, blk)
+    Kd = e4m3_decode(Kcodes[tok]) * float(np.float32(k_scale))
+    Vd = e4m3_decode(Vcodes[tok]) * float(np.float32(v_scale))
+    y = attention(q_group, Kd, Vd, scale)
+    return {"y": y, "i1": i1, "i2": i2, "s": s}
 
 
 # ---------------------------------------------------------------------------

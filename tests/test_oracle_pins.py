@@ -449,6 +449,66 @@ def test_kt_append_masked_equals_rebuild():
 
 
 # ---------------------------------------------------------------------------
+# FP8 (e4m3) storage
+# ---------------------------------------------------------------------------
+
+
+def _torch_e4m3(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_closed_forms_and_library():
+    c = np.arange(256, dtype=np.uint8)
+    d = oracle.e4m3_decode(c)
+    assert d[0x38] == 1.0 and d[0xB8] == -1.0 and d[0x7E] == 448.0 and d[0x01] == 2.0 ** -9
+    assert d[0x08] == 2.0 ** -6 and d[0x07] == 7 * 2.0 ** -9 and d[0x3C] == 1.5
+    assert np.isnan(d[0x7F]) and np.isnan(d[0xFF]) and np.isfinite(np.delete(d, [0x7F, 0xFF])).all()
+    lib = torch.from_numpy(c).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(np.nan_to_num(d, nan=7e7), np.nan_to_num(lib.astype(np.float64), nan=7e7))
+
+
+def test_e4m3_encode_vs_library_including_ties():
+    pos = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = (pos[1:] + pos[:-1]) / 2
+    x = np.concatenate([_rng(60).uniform(-464, 464, 20000), mids, -mids, pos, -pos, [464.0, -464.0]])
+    assert np.array_equal(oracle.e4m3_encode(x), _torch_e4m3(x))
+
+
+def test_e4m3_saturation_nan_and_round_trip():
+    assert oracle.e4m3_encode(np.array([1000.0, -1e9, np.nan, 449.0]).astype(np.float64)).tolist() == \
+        [0x7E, 0xFE, 0x7F, 0x7E]
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(finite)), finite)
+
+
+def test_fp8_quantize_vs_library():
+    X = _rng(61).standard_normal((64, 16)) * 8
+    for sc in (1.0, 0.0625, 0.37):
+        ref = _torch_e4m3(torch.from_numpy(X.astype(np.float32)).div(np.float32(sc)).numpy())
+        assert np.array_equal(oracle.fp8_quantize(X, sc), ref)
+
+
+def test_hsa_fp8_full_attention_and_dequantized_identity():
+    r = _rng(62)
+    G, D, n, blk = 4, 16, 150, 16
+    qg = r.standard_normal((G, D))
+    Kc = oracle.fp8_quantize(r.standard_normal((n, D)) * 3, 0.25)
+    Vc = oracle.fp8_quantize(r.standard_normal((n, D)), 0.125)
+    kmax, kmin = oracle.build_kt_fp8(Kc, n, blk)
+    Kd, Vd = oracle.e4m3_decode(Kc) * 0.25, oracle.e4m3_decode(Vc) * 0.125
+    full = oracle.hsa_decode_fp8(qg, Kc, Vc, n, kmax, kmin, 0.25, 0.125, blk, 6, 1000, 0.3)
+    np.testing.assert_allclose(full["y"], _sdpa(qg, Kd, Vd, 0.3), rtol=1e-12, atol=1e-12)
+    # a power-of-two K scale scales every score exactly: the same choices as the
+    # bf16 path on the dequantized cache
+    a = oracle.hsa_decode_fp8(qg, Kc, Vc, n, kmax, kmin, 0.25, 0.125, blk, 6, 3, 0.3)
+    dmax, dmin = oracle.build_kt(Kd, n, blk)
+    b = oracle.hsa_decode(qg, Kd, Vd, n, dmax, dmin, blk, 6, 3, 0.3)
+    assert a["i1"].tolist() == b["i1"].tolist() and a["i2"].tolist() == b["i2"].tolist()
+    np.testing.assert_allclose(a["s"] * 0.25, b["s"], rtol=1e-12)
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # Brute force of the whole pipeline on tiny inputs
 # ---------------------------------------------------------------------------
 
@@ -535,6 +595,16 @@ def test_mutation_unforced_tail_fails_brute_force(monkeypatch):
     res = ro.hsa_decode_mt_masked(qg, K, V, 100, cand, kmax, kmin, has, 8, 16, 2, 0.25)
     _, _, i2 = brute_ref.hsa_masked(qg.tolist(), K.tolist(), V.tolist(), 100, cand.tolist(), 8, 16, 2, 0.25)
     assert res["i2"].tolist() != i2
+
+
+def test_mutation_round_half_away_fails_library():
+    # rounding ties away from zero instead of to the even code must be caught
+    pos = ro.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = (pos[1:] + pos[:-1]) / 2
+    hi = np.searchsorted(pos, mids)
+    wrong = hi.astype(np.uint8)                     # every tie goes up
+    assert not np.array_equal(wrong, _torch_e4m3(mids))
+    assert np.array_equal(ro.e4m3_encode(mids), _torch_e4m3(mids))
 
 
 def test_mutation_transposed_kt_fails_library():
