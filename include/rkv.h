@@ -308,6 +308,42 @@ rkv_status rkv_hsa_decode_mt_masked(rkv_dims d, const void* q, void* k, void* v,
                                     void* stream);
 
 /*
+ * e4m3 (FP8) storage of the compacted cache.  Not on the pages: a storage
+ * option that halves the bytes of each decode step (the pages' KV-size
+ * formula counts one byte per element for FP8).  A code has 1 sign bit, 4
+ * exponent bits (bias 7) and 3 mantissa bits; there are no infinities,
+ * S.1111.111 is NaN and the largest magnitude is 448.  A stored row's value
+ * is code * scale, with fp32 scales per (b, h) that the caller chooses:
+ *   k_scale, v_scale  [B, Hkv] fp32 DEVICE arrays (4-byte aligned).
+ * rkv_compact_kt_fp8: rkv_compact_kt writing codes: k_out[b,h,i] =
+ * code(k[b,h,keep_idx[b,h,i]] / k_scale[b,h]) (the quotient in fp32, nearest
+ * even, magnitudes past 448 saturated), likewise v_out with v_scale; the KT
+ * cache holds, per block, the max / min of the key codes' values, stored as
+ * codes (exact).  k, v as rkv_compact_kt (bf16, device or page-locked host).
+ *   k_out, v_out  [B, Hkv, out_cap, D] uint8 codes (16-byte aligned).
+ *   kt            [B, Hkv, 2, D, nblk_cap] uint8 codes, nblk_cap a multiple of 16.
+ * Errors as rkv_compact_kt, plus NULL or misaligned scales.
+ */
+rkv_status rkv_compact_kt_fp8(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
+                              int64_t keep_ld, int64_t B1, const float* k_scale, const float* v_scale, void* k_out,
+                              void* v_out, int64_t out_cap, int32_t blk, void* kt, int64_t nblk_cap, void* stream);
+
+/*
+ * HSA decode step over an e4m3 cache (k, v [B, Hkv, cap, D] and kt
+ * [B, Hkv, 2, D, nblk_cap] uint8 codes from rkv_compact_kt_fp8).  Same rules
+ * and results as rkv_hsa_decode, with the block scores taken on the KT codes'
+ * values (the positive K scale does not change their order) and attention
+ * over the rows' values code * scale.  The fused append stores
+ * code(k_new / k_scale) and code(v_new / v_scale) at row n and folds the key's
+ * code into its block.  Requires blk a multiple of 8 (RKV_ERR_UNSUPPORTED
+ * otherwise) and nblk_cap a multiple of 16.
+ */
+rkv_status rkv_hsa_decode_fp8(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int64_t n,
+                              const float* k_scale, const float* v_scale, void* kt, int64_t nblk_cap, int32_t blk,
+                              int32_t k1, int32_t k2, float scale, float* out, int32_t* sel_blocks,
+                              int32_t* sel_channels, const void* k_new, const void* v_new, void* stream);
+
+/*
  * HSA decode step for a batch whose rows hold different numbers of candidates
  * (ragged batch).  [RocketKV digest, 方法细节: HSA steps 1-3 and Algorithm 1,
  * per request]  Same computation, arguments and results as rkv_hsa_decode,

@@ -112,6 +112,14 @@ D4 = (1, 32, 8, 128)
     (lambda: rkv.rkv_build_kt_masked(D4, 16, 100, 90, None, 4, 80, 16, 16, 8, stream=0), 1),
     (lambda: rkv.rkv_build_kt_masked(D4, 16, 100, 90, 16, 4, 91, 16, 16, 8, stream=0), 1),
     (lambda: rkv.rkv_build_kt_masked(D4, 16, 100, 90, 16, 2, 80, 16, 16, 8, stream=0), 1),
+    # e4m3 storage: NULL / misaligned scales, block size, KT stride
+    (lambda: rkv.rkv_hsa_decode_fp8(D4, 16, 16, 16, 100, 90, None, 16, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_fp8(D4, 16, 16, 16, 100, 90, 18, 16, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_hsa_decode_fp8(D4, 16, 16, 16, 100, 90, 16, 16, 16, 16, 12, 8, 4, 0.1, 16, stream=0), 2),
+    (lambda: rkv.rkv_hsa_decode_fp8(D4, 16, 16, 16, 100, 90, 16, 16, 16, 8, 16, 8, 4, 0.1, 16, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt_fp8(D4, 16, 16, 100, 16, 50, 50, None, 16, 16, 16, 50, 16, 16, 16, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt_fp8(D4, 16, 16, 100, 16, 50, 50, 16, 16, 16, 16, 50, 16, 16, 8, stream=0), 1),
+    (lambda: rkv.rkv_compact_kt_fp8(D4, 16, 16, 100, 16, 50, 50, 16, 16, 16, 16, 40, 16, 16, 16, stream=0), 1),
 ])
 def test_invalid_arguments_rejected_on_host(lib, call, status):
     with pytest.raises(rkv.RkvError) as e:

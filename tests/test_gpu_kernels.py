@@ -753,3 +753,134 @@ def test_compact_kt_reads_page_locked_host_v():
     with pytest.raises(rkv.RkvError) as e:
         rkv.rkv_compact_kt(dims, k, v.cpu(), cap, keep_t, B1, B1, outs[0][0], outs[0][1], B1, blk, outs[0][2], ncap)
     assert e.value.status == 1
+
+
+# ------------------------------------------------------ e4m3 (FP8) storage --
+
+
+def _fp8_case(seed, B, Hkv, cap, B1, k_mag=3.0):
+    rng = np.random.default_rng(seed)
+    kb = small_random(seed, (B, Hkv, cap, 128), k_mag)
+    vb = small_random(seed + 1, (B, Hkv, cap, 128))
+    keep = np.stack([np.stack([np.sort(rng.choice(cap, B1, replace=False)) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32)
+    # per-(b, h) scales, some small enough that the largest keys saturate
+    ks = rng.uniform(0.004, 0.05, (B, Hkv)).astype(np.float32)
+    vs = rng.uniform(0.002, 0.02, (B, Hkv)).astype(np.float32)
+    return kb, vb, keep, ks, vs
+
+
+@pytest.mark.parametrize("B1,blk", [(300, 16), (1, 16), (1000, 32), (259, 128), (77, 8)])
+def test_compact_kt_fp8_bit_exact(B1, blk):
+    """e4m3 compaction: codes of row / scale equal the oracle's bit for bit
+    (saturated and negative-zero codes included), KT bounds equal the max /
+    min of the key codes' values."""
+    B, Hq, Hkv, D, cap = 2, 8, 2, 128, 2 * B1 + 37
+    kb, vb, keep, ks, vs = _fp8_case(80 + B1, B, Hkv, cap, B1)
+    dims = (B, Hq, Hkv, D)
+    ncap = -(-(-(-B1 // blk)) // 16) * 16
+    ko = torch.zeros((B, Hkv, B1 + 3, D), dtype=torch.uint8, device=DEV)
+    vo = torch.zeros_like(ko)
+    kt = torch.full((B, Hkv, 2, D, ncap), 0x55, dtype=torch.uint8, device=DEV)
+    ks_t, vs_t = torch.from_numpy(ks).to(DEV), torch.from_numpy(vs).to(DEV)
+    rkv.rkv_compact_kt_fp8(dims, _bf16(kb), _bf16(vb), cap, torch.from_numpy(keep).to(DEV), B1, B1, ks_t, vs_t, ko,
+                           vo, B1 + 3, blk, kt, ncap)
+    torch.cuda.synchronize()
+    kog, vog, ktg = ko.cpu().numpy(), vo.cpu().numpy(), kt.cpu().numpy()
+    kf, vf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb)
+    nblk = -(-B1 // blk)
+    sat = 0
+    for b in range(B):
+        for h in range(Hkv):
+            kc = oracle.fp8_quantize(kf[b, h][keep[b, h]], ks[b, h])
+            vc = oracle.fp8_quantize(vf[b, h][keep[b, h]], vs[b, h])
+            assert np.array_equal(kog[b, h, :B1], kc), "key codes"
+            assert np.array_equal(vog[b, h, :B1], vc), "value codes"
+            sat += int(np.sum((kc & 0x7F) == 0x7E))
+            kmax, kmin = oracle.build_kt_fp8(kc, B1, blk)
+            assert np.array_equal(oracle.e4m3_decode(ktg[b, h, 0, :, :nblk]), kmax)
+            assert np.array_equal(oracle.e4m3_decode(ktg[b, h, 1, :, :nblk]), kmin)
+            assert np.all(ktg[b, h, :, :, nblk:] == 0x55)
+    assert np.all(kog[:, :, B1:] == 0)
+    if B1 >= 259:
+        assert sat > 0, "the case should exercise saturation"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,B1,blk,k1,k2", [
+    (2, 32, 8, 300, 16, 32, 5),       # G = 4, ragged tail
+    (1, 64, 8, 1000, 32, 64, 11),     # G = 8, block 32
+    (1, 32, 2, 333, 8, 128, 40),      # G = 16, block 8, all channels
+    (2, 32, 8, 130, 16, 32, 64),      # k2 >= blocks: full attention
+    (1, 32, 8, 5000, 16, 32, 30),     # several CTAs per pair, KT prefetch
+    (1, 32, 8, 20000, 16, 32, 300),   # chunked KT gather, several rounds per CTA
+])
+def test_hsa_decode_fp8_parity(B, Hq, Hkv, B1, blk, k1, k2):
+    """Decode steps over the e4m3 cache (three with the fused append, one
+    without) against the oracle on the stored codes: channels exact, blocks by
+    the tie rule, outputs within 2e-3; the appended rows' codes and the KT
+    bounds after the appends bit-exact."""
+    D, G, steps = 128, Hq // Hkv, 4
+    dims = (B, Hq, Hkv, D)
+    scale = 1 / math.sqrt(D)
+    cap_in = B1 + 57
+    kb, vb, keep, ks, vs = _fp8_case(90 + B1, B, Hkv, cap_in, B1, k_mag=1.0)
+    cap = B1 + steps + 5
+    ncap = -(-(-(-cap // blk)) // 16) * 16
+    ko = torch.zeros((B, Hkv, cap, D), dtype=torch.uint8, device=DEV)
+    vo = torch.zeros_like(ko)
+    kt = torch.zeros((B, Hkv, 2, D, ncap), dtype=torch.uint8, device=DEV)
+    ks_t, vs_t = torch.from_numpy(ks).to(DEV), torch.from_numpy(vs).to(DEV)
+    rkv.rkv_compact_kt_fp8(dims, _bf16(kb), _bf16(vb), cap_in, torch.from_numpy(keep).to(DEV), B1, B1, ks_t, vs_t,
+                           ko, vo, cap, blk, kt, ncap)
+    qb = small_random(91 + B1, (steps, B, Hq, D))
+    knb = small_random(92 + B1, (steps, B, Hkv, D))
+    vnb = small_random(93 + B1, (steps, B, Hkv, D))
+    qf, knf, vnf = bf16_bits_to_f64(qb), bf16_bits_to_f64(knb), bf16_bits_to_f64(vnb)
+    kf, vf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb)
+    state = {}
+    for b in range(B):
+        for h in range(Hkv):
+            kc = list(oracle.fp8_quantize(kf[b, h][keep[b, h]], ks[b, h]))
+            vc = list(oracle.fp8_quantize(vf[b, h][keep[b, h]], vs[b, h]))
+            kmax, kmin = oracle.build_kt_fp8(np.array(kc), B1, blk)
+            state[(b, h)] = [kc, vc, kmax, kmin]
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
+    sc = torch.full((B, Hkv, k1), -7, dtype=torch.int32, device=DEV)
+    q_t, kn_t, vn_t = _bf16(qb), _bf16(knb), _bf16(vnb)
+    n, worst, exempt = B1, 0.0, 0
+    for s in range(steps):
+        fused = s != 1
+        rkv.rkv_hsa_decode_fp8(dims, q_t[s], ko, vo, cap, n, ks_t, vs_t, kt, ncap, blk, k1, k2, scale, out, sb, sc,
+                               kn_t[s] if fused else None, vn_t[s] if fused else None)
+        torch.cuda.synchronize()
+        out_h, sb_h, sc_h = out.cpu().numpy(), sb.cpu().numpy(), sc.cpu().numpy()
+        n_att = n + (1 if fused else 0)
+        for (b, h), st in state.items():
+            if fused:
+                kcode = oracle.fp8_quantize(knf[s, b, h][None], ks[b, h])[0]
+                vcode = oracle.fp8_quantize(vnf[s, b, h][None], vs[b, h])[0]
+                st[0].append(kcode)
+                st[1].append(vcode)
+                st[2], st[3] = oracle.kt_append(st[2], st[3], n, oracle.e4m3_decode(kcode), blk)
+            Kc, Vc = np.array(st[0]), np.array(st[1])
+            qg = qf[s, b, h * G:(h + 1) * G]
+            res = oracle.hsa_decode_fp8(qg, Kc, Vc, n_att, st[2], st[3], ks[b, h], vs[b, h], blk, k1, k2, scale)
+            assert sc_h[b, h].tolist() == res["i1"].tolist(), "channel set differs"
+            k2e = min(k2, res["s"].shape[0])
+            exempt += check_topk(sb_h[b, h, :k2e], res["s"], k2, f"step {s} blocks")
+            if np.array_equal(sb_h[b, h, :k2e], res["i2"]):
+                y = res["y"]
+            else:
+                tok = oracle.block_tokens(sb_h[b, h, :k2e], n_att, blk)
+                y = oracle.attention(qg, oracle.e4m3_decode(Kc[tok]) * float(ks[b, h]),
+                                     oracle.e4m3_decode(Vc[tok]) * float(vs[b, h]), scale)
+            worst = max(worst, max_abs(out_h[b, h * G:(h + 1) * G], y))
+        n = n_att
+    kog, vog, ktg = ko.cpu().numpy(), vo.cpu().numpy(), kt.cpu().numpy()
+    for (b, h), st in state.items():
+        assert np.array_equal(kog[b, h, :n], np.array(st[0])) and np.array_equal(vog[b, h, :n], np.array(st[1]))
+        nb = st[2].shape[1]
+        assert np.array_equal(oracle.e4m3_decode(ktg[b, h, 0, :, :nb]), st[2])
+        assert np.array_equal(oracle.e4m3_decode(ktg[b, h, 1, :, :nb]), st[3])
+    assert worst <= ATOL_OUT, worst

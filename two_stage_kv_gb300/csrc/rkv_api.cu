@@ -97,16 +97,36 @@ rkv_status make_kv_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t 
   return RKV_OK;
 }
 
+// 3-D map over a [pairs, cap, 128] e4m3 code cache (128-byte rows): rows >= `rows`
+// read as zero.  Box = 128 codes x box_rows rows x 1 pair, unswizzled.
+rkv_status make_kv_map_u8(CUtensorMap* m, const void* base, int64_t pairs, int64_t cap, int64_t rows, int box_rows,
+                          const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {(cuuint64_t)rkv::HD_HOST, (cuuint64_t)rows, (cuuint64_t)pairs};
+  cuuint64_t strides[2] = {(cuuint64_t)rkv::HD_HOST, (cuuint64_t)cap * rkv::HD_HOST};
+  cuuint32_t box[3] = {(cuuint32_t)rkv::HD_HOST, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+  return RKV_OK;
+}
+
 // 2-D map over the KT cache viewed as [pairs * 2 * 128 rows, nblk_cap] bf16, box
 // box_cols blocks x 256 rows (all Kmax and Kmin rows of one pair), no swizzle.
-rkv_status make_kt_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t nblk_cap, int box_cols) {
+// (e4m3 codes: one byte per entry, box_cols a multiple of 16)
+rkv_status make_kt_map(CUtensorMap* m, const void* base, int64_t pairs, int64_t nblk_cap, int box_cols,
+                       bool f8 = false) {
   auto fn = encode_fn();
   if (!fn) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {(cuuint64_t)nblk_cap, (cuuint64_t)pairs * 2 * rkv::HD_HOST};
-  cuuint64_t strides[1] = {(cuuint64_t)nblk_cap * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)nblk_cap * (f8 ? 1 : 2)};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, 2 * rkv::HD_HOST};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                  dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(RKV_ERR_CUDA, "cuTensorMapEncodeTiled(kt) failed with %d", (int)r);
@@ -133,7 +153,9 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
                       float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
                       const void* v_new, int64_t row, void* stream, bool mt, const int32_t* n_rows = nullptr,
                       const int32_t* block_table = nullptr, int64_t bt_stride = 0, int64_t num_pages = 0,
-                      const uint32_t* mask = nullptr, int64_t mask_ld = 0, int64_t n_prompt = 0) {
+                      const uint32_t* mask = nullptr, int64_t mask_ld = 0, int64_t n_prompt = 0,
+                      const float* k_scale = nullptr, const float* v_scale = nullptr) {
+  const bool f8 = k_scale != nullptr;
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
@@ -176,6 +198,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.n = (int32_t)n; a.n_rows = n_rows; a.B = d.batch;
   a.block_table = block_table; a.bt_stride = bt_stride; a.num_pages = num_pages; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
   a.mask = mask; a.mask_ld = mask_ld; a.n_prompt = n_prompt;
+  a.k_scale = k_scale; a.v_scale = v_scale; a.f8 = f8 ? 1 : 0;
   a.blk = blk; a.k1 = k1; a.k2 = k2;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.tma_kv = (!mt && blk % 8 == 0) ? 1 : 0;
@@ -186,7 +209,10 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   std::memset(&tmV, 0, sizeof(tmV));
   std::memset(&tmKT, 0, sizeof(tmKT));
   const int64_t pairs = (int64_t)d.batch * d.n_kv_heads;
-  if (a.tma_kv && block_table) {
+  if (f8) {
+    if ((s = make_kv_map_u8(&tmK, k, pairs, cap, std::max<int64_t>(n, 1), blk, "k codes")) != RKV_OK) return s;
+    if ((s = make_kv_map_u8(&tmV, v, pairs, cap, std::max<int64_t>(n, 1), blk, "v codes")) != RKV_OK) return s;
+  } else if (a.tma_kv && block_table) {
     // one (page, KV head) slab of blk rows per box; the kernel masks rows past n
     const int64_t slabs = num_pages * d.n_kv_heads;
     if ((s = make_kv_map(&tmK, k, slabs, blk, blk, blk, "k pages")) != RKV_OK) return s;
@@ -199,7 +225,7 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
     if ((s = make_kv_map(&tmV, v, pairs, cap, extent, blk, "v")) != RKV_OK) return s;
   }
   if (a.kt_spec) {
-    if ((s = make_kt_map(&tmKT, kt, pairs, nblk_cap, a.cpr)) != RKV_OK) return s;
+    if ((s = make_kt_map(&tmKT, kt, pairs, nblk_cap, a.cpr, f8)) != RKV_OK) return s;
   }
   cudaError_t e = rkv::hsa_launch(a, &tmK, &tmV, &tmKT, mt, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "hsa_decode launch");
@@ -387,6 +413,33 @@ rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap,
   return RKV_OK;
 }
 
+rkv_status rkv_compact_kt_fp8(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
+                              int64_t keep_ld, int64_t B1, const float* k_scale, const float* v_scale, void* k_out,
+                              void* v_out, int64_t out_cap, int32_t blk, void* kt, int64_t nblk_cap, void* stream) {
+  rkv_status s = check_dims(d);
+  if (s != RKV_OK) return s;
+  if (d.batch == 0 || B1 == 0) return RKV_OK;
+  if (!k || !v || !keep_idx || !k_out || !v_out || !kt || !k_scale || !v_scale)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: NULL pointer");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out) || !aligned16(kt))
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: k, v, k_out, v_out and kt must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(k_scale) % 4 != 0 || reinterpret_cast<uintptr_t>(v_scale) % 4 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: scales must be 4-byte aligned");
+  if (cap < 1 || B1 < 0 || B1 > out_cap || keep_ld < B1)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: need cap >= 1, 0 <= B1 <= out_cap and keep_ld >= B1");
+  if (blk < 1) return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: blk < 1");
+  if (nblk_cap % 16 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: nblk_cap=%lld is not a multiple of 16", (long long)nblk_cap);
+  if ((B1 + blk - 1) / blk > nblk_cap) return fail(RKV_ERR_INVALID_ARG, "compact_kt_fp8: nblk_cap too small");
+  if ((s = device_view(k, &k, "compact_kt_fp8: k")) != RKV_OK || (s = device_view(v, &v, "compact_kt_fp8: v")) != RKV_OK)
+    return s;
+  cudaError_t e = rkv::compact_kt_fp8_launch(k, v, cap, keep_idx, keep_ld, B1, blk, k_scale, v_scale, k_out, v_out,
+                                             out_cap, kt, nblk_cap, d.batch * d.n_kv_heads,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "compact_kt_fp8 launch");
+  return RKV_OK;
+}
+
 rkv_status rkv_compact_kt_paged(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
                                 int64_t keep_ld, int64_t B1, void* k_pages, void* v_pages, int64_t num_pages,
                                 const int32_t* block_table, int64_t bt_stride, int32_t blk, void* kt,
@@ -465,6 +518,20 @@ rkv_status rkv_hsa_decode_mt_masked(rkv_dims d, const void* q, void* k, void* v,
     return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: mask_ld=%lld < ceil(n_prompt/32)", (long long)mask_ld);
   return hsa_common(d, q, k, v, cap, nullptr, 0, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks, sel_channels,
                     k_new, v_new, n, stream, false, nullptr, nullptr, 0, 0, mask, mask_ld, n_prompt);
+}
+
+rkv_status rkv_hsa_decode_fp8(rkv_dims d, const void* q, void* k, void* v, int64_t cap, int64_t n,
+                              const float* k_scale, const float* v_scale, void* kt, int64_t nblk_cap, int32_t blk,
+                              int32_t k1, int32_t k2, float scale, float* out, int32_t* sel_blocks,
+                              int32_t* sel_channels, const void* k_new, const void* v_new, void* stream) {
+  if (!k_scale || !v_scale) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_fp8: NULL k_scale or v_scale");
+  if (reinterpret_cast<uintptr_t>(k_scale) % 4 != 0 || reinterpret_cast<uintptr_t>(v_scale) % 4 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_fp8: scales must be 4-byte aligned");
+  if (blk % 8 != 0) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode_fp8: block size %d is not a multiple of 8", blk);
+  if (nblk_cap % 16 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "hsa_decode_fp8: nblk_cap=%lld is not a multiple of 16", (long long)nblk_cap);
+  return hsa_common(d, q, k, v, cap, nullptr, 0, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks, sel_channels,
+                    k_new, v_new, n, stream, false, nullptr, nullptr, 0, 0, nullptr, 0, 0, k_scale, v_scale);
 }
 
 rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, int64_t cap, const int32_t* n_rows,

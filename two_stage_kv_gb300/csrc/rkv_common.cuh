@@ -273,6 +273,31 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
 
+// e4m3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest
+// 448): two fp32 values to a code pair, nearest even, magnitudes past 448
+// saturated; `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// A code pair back to fp32 (exact: every e4m3 value is an f16 value); the low
+// byte lands in .x.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  float lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return make_float2(lo, hi);
+}
+// Code pair -> bf16x2 of the same values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
+  const float2 f = e4m3x2_to_f32(v);
+  return pack_bf16(f.x, f.y);
+}
+
 // Order-preserving map float -> uint32 (larger float -> larger key); -0 and +0
 // map to the same key.
 __device__ __forceinline__ uint32_t f2key(float f) {

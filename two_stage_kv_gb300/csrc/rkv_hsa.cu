@@ -61,7 +61,9 @@ constexpr int MEMBER_MAX = 512;         // boundary-bucket members ranked pairwi
 
 struct FixedSmem {
   bf16 qs[16][HD + 8];          // query rows (padded: conflict-free ldmatrix), rows >= G are zero
-  bf16 knew[HD];                // appended key / value of this pair
+  bf16 knew[HD];                // appended key / value of this pair (e4m3 storage: its code values)
+  uint8_t knew8[HD];            // e4m3 storage: codes of the appended key / value
+  uint8_t vnew8[HD];
   bf16 vnew[HD];
   float qsel[HD];               // group-summed q of the kept channels, ascending channel
   int32_t rowoff[HD];           // KT row (0..2*HD) of each kept channel
@@ -244,7 +246,10 @@ __device__ void bucket_topk(float* vals, int n, int k, float mn, float mx, uint8
 // of the prompt, every row decoded after it) count: bounds, blocks without a
 // candidate never chosen, the newest row's block always chosen, attention over
 // candidate rows only.
-template <bool MT, int NH, bool RAG, bool PG, bool MK = false>
+// F8: k, v and kt hold e4m3 codes (value = code * the pair's scale); the
+// bounds and scores are on code values, attention dequantizes through the
+// logit and output scales.
+template <bool MT, int NH, bool RAG, bool PG, bool MK = false, bool F8 = false>
 __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                            const __grid_constant__ CUtensorMap tmV,
                                                            const __grid_constant__ CUtensorMap tmKT,
@@ -260,6 +265,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   float* recv = reinterpret_cast<float*>(smem + a.off_recv);
   uint8_t* tK = smem + a.off_tiles;
   uint8_t* tV = tK + 2 * a.tile_half_bytes;
+  uint8_t* tV8 = smem + a.off_v8;                                      // e4m3: staged V code rows
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // KT rows do not depend on the query: with the prefetch, all 2*D rows of this
   // CTA's blocks are in flight while the channels are chosen
   if (spec && tid == 0 && jhi > jlo) {
-    mbar_arrive_expect_tx(&fs.ktbar, (uint32_t)(2 * HD * cpr * 2));
+    mbar_arrive_expect_tx(&fs.ktbar, (uint32_t)(2 * HD * cpr * (F8 ? 1 : 2)));
     tma_load_2d(kttile, &tmKT, jlo, pair * 2 * HD, &fs.ktbar);
   }
   // the CTA holding the appended key's block persists its KT column; without
@@ -349,11 +355,22 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   if (MK && own_new && !fresh_new) fresh_new = !cand_any(mrow, a.n_prompt, (int64_t)nb_new * a.blk, n_old);
   bf16 kt_old = __float2bfloat16(0.f);
   bf16* kt_col = nullptr;
+  uint8_t kt_old8 = 0;
+  uint8_t* kt_col8 = nullptr;
   if (own_new) {
     const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
-    kt_col = reinterpret_cast<bf16*>(a.kt) + ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
-    if (!spec && !fresh_new) kt_old = *kt_col;
+    const size_t o = ((size_t)pair * 2 * HD + m * HD + c) * a.nblk_cap + nb_new;
+    if (F8) {
+      kt_col8 = reinterpret_cast<uint8_t*>(a.kt) + o;
+      if (!spec && !fresh_new) kt_old8 = *kt_col8;
+    } else {
+      kt_col = reinterpret_cast<bf16*>(a.kt) + o;
+      if (!spec && !fresh_new) kt_old = *kt_col;
+    }
   }
+  // e4m3 storage: dequantization scales of this pair
+  const float k_sc = F8 ? __ldg(a.k_scale + pair) : 1.f;
+  const float v_sc = F8 ? __ldg(a.v_scale + pair) : 1.f;
 
   // ---------------------------------------------------------------- A ------
   {
@@ -369,6 +386,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     }
   }
   __syncthreads();
+  if (F8 && app) {
+    // the appended key / value as stored: codes of x / scale, and their values
+    const int c = tid & (HD - 1);
+    bf16* src = tid < HD ? fs.knew : fs.vnew;
+    const uint16_t code = e4m3x2_from_f32(__fdiv_rn(bf2f(src[c]), tid < HD ? k_sc : v_sc), 0.f);
+    (tid < HD ? fs.knew8 : fs.vnew8)[c] = (uint8_t)(code & 0xFF);
+    src[c] = __float2bfloat16_rn(e4m3x2_to_f32(code).x);   // read after the barriers of phase A
+  }
   bool inexact = false;
   if (tid < HD) {
     float sa = 0.f, sq = 0.f;
@@ -454,8 +479,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   {
     const uint32_t sbar_local = smem_u32(&fs.sbar);
     const uint32_t sval_local = smem_u32(sval);
-    const bf16* ktp = reinterpret_cast<const bf16*>(a.kt) + (size_t)pair * 2 * HD * a.nblk_cap;
-    const int bc = spec ? cpr : a.kt_chunk;          // columns per tile (multiple of 8)
+    const int bc = spec ? cpr : a.kt_chunk;          // columns per tile (multiple of 8; of 16 for e4m3)
     const int cg = tid & 3, bp = tid >> 2;           // channel group, block pair within a 128-block span
     if (MK) {
       // which of this CTA's blocks hold a candidate (read after the barrier before scoring)
@@ -471,23 +495,34 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           // fold the appended key into its block in every KT row and persist the column
           const int col = nb_new - cb0;
           const int m = tid >> 7, c = tid & (HD - 1);
-          const bf16 kv = fs.knew[c];
-          bf16& slot = kttile[(size_t)tid * bc + col];
-          if (fresh_new) {
-            slot = kv;
+          if (F8) {
+            uint8_t& slot = reinterpret_cast<uint8_t*>(kttile)[(size_t)tid * bc + col];
+            const float x = bf2f(fs.knew[c]), o = e4m3x2_to_f32(slot).x;
+            if (fresh_new || (m == 1 ? (x < o) : (x > o))) slot = fs.knew8[c];
+            *kt_col8 = slot;
           } else {
-            const float x = bf2f(kv), o = bf2f(slot);
-            if (m == 1 ? (x < o) : (x > o)) slot = kv;
+            const bf16 kv = fs.knew[c];
+            bf16& slot = kttile[(size_t)tid * bc + col];
+            if (fresh_new) {
+              slot = kv;
+            } else {
+              const float x = bf2f(kv), o = bf2f(slot);
+              if (m == 1 ? (x < o) : (x > o)) slot = kv;
+            }
+            *kt_col = slot;
           }
-          *kt_col = slot;
         }
       } else {
         if (cb0 > jlo) __syncthreads();              // the previous chunk's scores are done with the tile
-        const int n16 = (nb_here + 7) / 8;
+        // 16-byte chunks: 8 bf16 entries, or 16 e4m3 codes
+        const int per = F8 ? 16 : 8;
+        const int n16 = (nb_here + per - 1) / per;
         for (int row = warp; row < k1; row += NWARP) {
-          const bf16* src = ktp + (size_t)fs.rowoff[row] * a.nblk_cap + cb0;
-          bf16* dst = kttile + (size_t)row * bc;
-          for (int ch = lane; ch < n16; ch += 32) cp_async_16(smem_u32(dst + ch * 8), src + ch * 8);
+          const size_t eb = F8 ? 1 : 2;
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.kt) +
+                               (((size_t)pair * 2 * HD + fs.rowoff[row]) * a.nblk_cap + cb0) * eb;
+          uint8_t* dst = reinterpret_cast<uint8_t*>(kttile) + (size_t)row * bc * eb;
+          for (int ch = lane; ch < n16; ch += 32) cp_async_16(smem_u32(dst + ch * 16), src + ch * 16);
         }
         cp_async_commit();
         cp_async_wait_all();
@@ -498,12 +533,18 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           for (int i = tid; i < k1; i += NT) {
             const int ro = fs.rowoff[i];
             const bf16 kv = fs.knew[ro & (HD - 1)];
-            bf16& slot = kttile[(size_t)i * bc + col];
-            if (fresh) {
-              slot = kv;
+            if (F8) {
+              uint8_t& slot = reinterpret_cast<uint8_t*>(kttile)[(size_t)i * bc + col];
+              const float x = bf2f(kv), o = e4m3x2_to_f32(slot).x;
+              if (fresh || (ro >= HD ? (x < o) : (x > o))) slot = fs.knew8[ro & (HD - 1)];
             } else {
-              const float x = bf2f(kv), o = bf2f(slot);
-              if (ro >= HD ? (x < o) : (x > o)) slot = kv;
+              bf16& slot = kttile[(size_t)i * bc + col];
+              if (fresh) {
+                slot = kv;
+              } else {
+                const float x = bf2f(kv), o = bf2f(slot);
+                if (ro >= HD ? (x < o) : (x > o)) slot = kv;
+              }
             }
           }
         }
@@ -518,10 +559,17 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         float s0 = 0.f, s1 = 0.f;
         for (int i = cg; i < k1; i += 4) {
           const int row = spec ? fs.rowoff[i] : i;
-          const uint32_t v = tile32[(size_t)row * pitch + jpc];
           const float q = fs.qsel[i];
-          s0 = fmaf(q, bf16_lo(v), s0);
-          s1 = fmaf(q, bf16_hi(v), s1);
+          if (F8) {
+            // two blocks' codes per 16-bit word, row pitch bc bytes
+            const float2 f = e4m3x2_to_f32(reinterpret_cast<const uint16_t*>(kttile)[(size_t)row * pitch + jpc]);
+            s0 = fmaf(q, f.x, s0);
+            s1 = fmaf(q, f.y, s1);
+          } else {
+            const uint32_t v = tile32[(size_t)row * pitch + jpc];
+            s0 = fmaf(q, bf16_lo(v), s0);
+            s1 = fmaf(q, bf16_hi(v), s1);
+          }
         }
         s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
         s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
@@ -629,6 +677,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // gathered row by row with cp.async (MT candidate rows, or other block sizes)
   const bool gat = MT || a.tma_kv == 0;
 
+  const float sl2 = a.scale_log2 * k_sc;        // logits in log2 units (e4m3: times the K scale)
   for (int r0 = s_lo; r0 < s_hi; r0 += a.slots_round) {
     const int nsl = min(a.slots_round, s_hi - r0);
     const int rows = nsl * blk;
@@ -640,15 +689,28 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         // The region was last read through the generic proxy before a barrier (write
         // after read), so no proxy fence is needed.
         if (warp == 0)
-          for (int s = lane; s < nsl; s += 32) mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * 4u);
+          for (int s = lane; s < nsl; s += 32)
+            mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * (F8 ? 2u : 4u));
         __syncwarp();
-        const int part = warp & 3;                   // K lo, K hi, V lo, V hi
-        for (int s = (warp >> 2) + 2 * lane; s < nsl; s += 64) {
-          // dense: rows sel*blk.. of the pair's cache; paged: the whole (page, head) slab
-          const int y = PG ? 0 : sel[r0 + s] * blk;
-          const int z = PG ? bt_s[sel[r0 + s]] * a.Hkv + hk : pair;
-          const uint32_t off = (uint32_t)s * blk * 128u + (uint32_t)(part & 1) * half;
-          tma_load_3d(((part >> 1) ? tV : tK) + off, (part >> 1) ? &tmV : &tmK, (part & 1) * 64, y, z, &fs.mbar[s]);
+        if (F8) {
+          // code rows (128 bytes, unswizzled): K into the hi half of the K tile,
+          // converted in place by the warp that owns the rows; V into its own staging
+          const int part = warp & 1;
+          for (int s = (warp >> 1) + 4 * lane; s < nsl; s += 128) {
+            const uint32_t off = (uint32_t)s * blk * 128u;
+            tma_load_3d(part ? tV8 + off : tK + half + off, part ? &tmV : &tmK, 0, sel[r0 + s] * blk, pair,
+                        &fs.mbar[s]);
+          }
+        } else {
+          const int part = warp & 3;                   // K lo, K hi, V lo, V hi
+          for (int s = (warp >> 2) + 2 * lane; s < nsl; s += 64) {
+            // dense: rows sel*blk.. of the pair's cache; paged: the whole (page, head) slab
+            const int y = PG ? 0 : sel[r0 + s] * blk;
+            const int z = PG ? bt_s[sel[r0 + s]] * a.Hkv + hk : pair;
+            const uint32_t off = (uint32_t)s * blk * 128u + (uint32_t)(part & 1) * half;
+            tma_load_3d(((part >> 1) ? tV : tK) + off, (part >> 1) ? &tmV : &tmK, (part & 1) * 64, y, z,
+                        &fs.mbar[s]);
+          }
         }
       }
     } else {
@@ -708,10 +770,40 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         const int sa = c0 / blk, sb = min((c0 + 15) / blk, nsl - 1);
         for (int s = sa; s <= sb; ++s)
           if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
+        if (F8) {
+          // this warp's 16 key rows: codes (row r at byte r*128 of the hi half) to
+          // bf16 code values in the swizzled tile, in place (all reads first)
+          uint4 cv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int q = lane + 32 * i, r = c0 + (q >> 3), cb = q & 7;
+            cv[i] = r < rows ? *reinterpret_cast<const uint4*>(tK + half + (uint32_t)r * 128u + cb * 16)
+                             : make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int q = lane + 32 * i, r = c0 + (q >> 3), cb = q & 7;
+            if (r >= rows) continue;
+            const uint32_t w[4] = {cv[i].x, cv[i].y, cv[i].z, cv[i].w};
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int ch8 = 2 * cb + hh;               // 8 channels per bf16 chunk
+              const uint4 o = make_uint4(e4m3x2_to_bf16x2((uint16_t)(w[2 * hh] & 0xFFFF)),
+                                         e4m3x2_to_bf16x2((uint16_t)(w[2 * hh] >> 16)),
+                                         e4m3x2_to_bf16x2((uint16_t)(w[2 * hh + 1] & 0xFFFF)),
+                                         e4m3x2_to_bf16x2((uint16_t)(w[2 * hh + 1] >> 16)));
+              *reinterpret_cast<uint4*>(tK + (uint32_t)(ch8 >> 3) * half + swz128(r, ch8 & 7)) = o;
+            }
+          }
+          __syncwarp();
+        }
         if (app) {
           // the appended token lies past the tensor map's extent (read as zero): write it in
+          // (e4m3: the key here, the value by the V conversion below)
           for (int s = sa; s <= sb; ++s) {
             if (sel[r0 + s] != nb_new) continue;
+            if (F8 && lane >= 16) continue;
             const int r = s * blk + (n_old - nb_new * blk);
             const int ch = lane & 15;
             const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
@@ -749,7 +841,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float sv = (st[ht][0][e] + st[ht][1][e]) * a.scale_log2;
+          const float sv = (st[ht][0][e] + st[ht][1][e]) * sl2;
           x[ht][e] = ((e < 2) ? va : vb) ? sv : neg_inf();
         }
     }
@@ -828,6 +920,32 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       acc[ht][2] *= corr[ht][0];
       acc[ht][3] *= corr[ht][1];
     }
+    if (F8) {
+      // this warp's 16 value channels of every staged row: codes to bf16 code
+      // values (the appended token's from its stored codes, rows past the round zero)
+      for (int s = 0; s < nsl; ++s)
+        if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
+      const int r_app = app ? (n_old - nb_new * blk) : -1;   // the appended token's row within its block
+      for (int r = lane; r < rows16; r += 32) {
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+        if (r < rows) {
+          if (r_app >= 0 && r % blk == r_app && sel[r0 + r / blk] == nb_new) {
+            o0 = *reinterpret_cast<const uint4*>(fs.vnew + 16 * warp);
+            o1 = *reinterpret_cast<const uint4*>(fs.vnew + 16 * warp + 8);
+          } else {
+            const uint4 cv = *reinterpret_cast<const uint4*>(tV8 + (uint32_t)r * 128u + 16 * warp);
+            o0 = make_uint4(e4m3x2_to_bf16x2((uint16_t)(cv.x & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.x >> 16)),
+                            e4m3x2_to_bf16x2((uint16_t)(cv.y & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.y >> 16)));
+            o1 = make_uint4(e4m3x2_to_bf16x2((uint16_t)(cv.z & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.z >> 16)),
+                            e4m3x2_to_bf16x2((uint16_t)(cv.w & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.w >> 16)));
+          }
+        }
+        const int ch8 = 2 * warp;
+        *reinterpret_cast<uint4*>(tV + (uint32_t)(ch8 >> 3) * half + swz128(r, ch8 & 7)) = o0;
+        *reinterpret_cast<uint4*>(tV + (uint32_t)((ch8 + 1) >> 3) * half + swz128(r, (ch8 + 1) & 7)) = o1;
+      }
+      __syncwarp();
+    }
     // --- O^T (dims 16*warp .. +15) += V^T P^T over every 16-token step of the round
     for (int cs = 0; cs < nsteps; ++cs) {
       const int r = cs * 16 + (lane & 7) + (lane >> 4) * 8;
@@ -903,13 +1021,16 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         A = fmaf(f, vr[r], A);
         L = fmaf(f, lr[r], L);
       }
-      a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = A / L;
+      a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = F8 ? (A / L) * v_sc : A / L;
     }
   }
   if (own_new && !spec) {
     const int m = tid >> 7, c = tid & (HD - 1);    // 256 threads = {max, min} x 128 channels
     const bf16 kv = fs.knew[c];
-    if (fresh_new) {
+    if (F8) {
+      const float x = bf2f(kv), o = e4m3x2_to_f32(kt_old8).x;
+      if (fresh_new || (m == 1 ? (x < o) : (x > o))) *kt_col8 = fs.knew8[c];
+    } else if (fresh_new) {
       *kt_col = kv;
     } else {
       const float x = bf2f(kv), o = bf2f(kt_old);
@@ -922,7 +1043,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     }
     if (app) {
       // persist the appended token: cache row and candidate index (MT)
-      if (tid < 32) {
+      if (F8 && tid < 16) {
+        // 128 code bytes per row: lanes 0-7 the key, 8-15 the value
+        uint8_t* dst = (tid < 8 ? reinterpret_cast<uint8_t*>(a.k) : reinterpret_cast<uint8_t*>(a.v)) +
+                       ((size_t)pair * a.cap + (size_t)n_old) * HD + (tid & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 8 ? fs.knew8 : fs.vnew8) + (tid & 7) * 16);
+      } else if (!F8 && tid < 32) {
         bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
                     (PG ? (((size_t)bt_s[nb_new] * a.Hkv + hk) * blk + (size_t)(n_old % blk))
                         : (size_t)pair * a.cap + (MT ? a.row : (int64_t)n_old)) * HD + (tid & 15) * 8;
@@ -961,12 +1087,15 @@ bool hsa_plan(HsaArgs& a) {
   // blocks scored per CTA; with at most HSA_SPEC_MAX_COLS of them every KT row of
   // the CTA's blocks is prefetched at launch, otherwise the chosen rows are
   // gathered in chunks after the channel choice
-  a.cpr = std::max(8, (((a.nblk + a.ns - 1) / a.ns) + 7) & ~7);
+  // (e4m3 codes: 16 blocks per 16-byte KT chunk)
+  const int cq = a.f8 ? 16 : 8;
+  const uint32_t eb = a.f8 ? 1u : 2u;
+  a.cpr = std::max(cq, (((a.nblk + a.ns - 1) / a.ns) + cq - 1) / cq * cq);
   a.kt_spec = a.cpr <= HSA_SPEC_MAX_COLS ? 1 : 0;
   int bc = a.cpr;
-  if ((uint32_t)a.k1 * bc * 2u > KT_TILE_BUDGET) bc = std::max(8, (int)(KT_TILE_BUDGET / (2u * a.k1)) & ~7);
+  if ((uint32_t)a.k1 * bc * eb > KT_TILE_BUDGET) bc = std::max(cq, (int)(KT_TILE_BUDGET / (eb * a.k1)) / cq * cq);
   a.kt_chunk = bc;
-  const uint32_t kt_tile_bytes = a.kt_spec ? 2u * HD * a.cpr * 2u : 2u * a.k1 * bc;
+  const uint32_t kt_tile_bytes = a.kt_spec ? 2u * HD * a.cpr * eb : eb * a.k1 * bc;
   const int gown = (a.G + a.ns - 1) / a.ns;
   auto al = [](uint32_t x, uint32_t q) { return (x + q - 1) / q * q; };
   uint32_t off = al(sizeof(FixedSmem), 128);
@@ -984,7 +1113,8 @@ bool hsa_plan(HsaArgs& a) {
   a.off_tiles = off;                       // K/V tiles; the KT gather tile shares this region
   const uint32_t rows16 = al((uint32_t)(a.slots_round * a.blk), 16);
   a.tile_half_bytes = rows16 * 128u;
-  off += std::max(4u * a.tile_half_bytes, al(kt_tile_bytes, 16));
+  a.off_v8 = off + 4u * a.tile_half_bytes;    // e4m3: V code rows (rows16 x 128 bytes)
+  off += std::max(4u * a.tile_half_bytes + (a.f8 ? a.tile_half_bytes : 0u), al(kt_tile_bytes, 16));
   a.smem_bytes = off + 1024u;   // room to align the base to 1024 bytes
   return a.smem_bytes <= 227u * 1024u;
 }
@@ -994,7 +1124,9 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    const void* ks[10] = {
+    const void* ks[12] = {
+        (const void*)hsa_decode_kernel<false, 1, false, false, false, true>,
+        (const void*)hsa_decode_kernel<false, 2, false, false, false, true>,
         (const void*)hsa_decode_kernel<false, 1, false, false, true>,
         (const void*)hsa_decode_kernel<false, 2, false, false, true>,
         (const void*)hsa_decode_kernel<false, 1, false, false>, (const void*)hsa_decode_kernel<false, 2, false, false>,
@@ -1025,6 +1157,8 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   // kernels keep every length a launch constant
   const bool wide = a.G > 8;
   auto kern = mt ? (wide ? hsa_decode_kernel<true, 2, false, false> : hsa_decode_kernel<true, 1, false, false>)
+          : a.f8 ? (wide ? hsa_decode_kernel<false, 2, false, false, false, true>
+                         : hsa_decode_kernel<false, 1, false, false, false, true>)
           : a.mask ? (wide ? hsa_decode_kernel<false, 2, false, false, true>
                            : hsa_decode_kernel<false, 1, false, false, true>)
           : a.block_table ? (wide ? hsa_decode_kernel<false, 2, true, true> : hsa_decode_kernel<false, 1, true, true>)

@@ -33,6 +33,9 @@ struct HsaArgs {
   int64_t bt_stride, num_pages;  // paged: K/V pools are [num_pages, Hkv, blk, D]
   const uint32_t* mask;  // masked MT: [B, Hkv, mask_ld] bit r = prompt row r kept by stage 1, else nullptr
   int64_t mask_ld, n_prompt;     // rows >= n_prompt (decoded after the prompt) are always candidates
+  const float* k_scale;  // e4m3 storage: [B, Hkv] value = code * scale for K and V (k, v, kt hold codes)
+  const float* v_scale;
+  int32_t f8;           // 1: k, v and kt hold e4m3 codes
   int32_t nblk;         // blocks over the attended candidates
   int32_t k2e;          // min(k2, nblk)
   int32_t ns;           // CTAs per cluster (one cluster per (b, kv head))
@@ -45,6 +48,7 @@ struct HsaArgs {
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared-memory layout (bytes)
   uint32_t off_x, off_scores, off_flags, off_sel, off_bt, off_recv, off_tiles, tile_half_bytes, smem_bytes;
+  uint32_t off_v8;      // e4m3: V code rows staged by TMA before conversion (K codes land in the K tile's hi half)
 };
 
 // Computes ns/chunk/slots_round and the shared-memory layout.  Returns false if
@@ -81,6 +85,9 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
                             int32_t blk, void* kt, int64_t nblk_cap, int32_t pairs, cudaStream_t st,
                             const uint32_t* mask = nullptr, int64_t mask_ld = 0, int64_t n_prompt = 0);
+cudaError_t compact_kt_fp8_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
+                                  int64_t B1, int blk, const float* k_scale, const float* v_scale, void* ko, void* vo,
+                                  int64_t out_cap, void* kt, int64_t nblk_cap, int pairs, cudaStream_t st);
 cudaError_t keep_mask_launch(const int32_t* keep, int64_t keep_ld, int64_t B1, int64_t n_prompt, uint32_t* mask,
                              int64_t mask_ld, int32_t pairs, cudaStream_t st);
 cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,

@@ -194,6 +194,95 @@ __global__ void __launch_bounds__(CK_NT) compact_kt_kernel(const bf16* k, const 
   }
 }
 
+// 8 bf16 (one 16-byte chunk) / scale -> 8 e4m3 codes (8 bytes); the codes'
+// values are folded into mx / mn.
+__device__ __forceinline__ uint2 quantize8(const uint4& r, float scale, float* mx, float* mn) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  uint16_t c[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    c[q] = e4m3x2_from_f32(__fdiv_rn(bf16_lo(w[q]), scale), __fdiv_rn(bf16_hi(w[q]), scale));
+    if (mx) {
+      const float2 v = e4m3x2_to_f32(c[q]);
+      mx[2 * q] = fmaxf(mx[2 * q], v.x);
+      mn[2 * q] = fminf(mn[2 * q], v.x);
+      mx[2 * q + 1] = fmaxf(mx[2 * q + 1], v.y);
+      mn[2 * q + 1] = fminf(mn[2 * q + 1], v.y);
+    }
+  }
+  return make_uint2((uint32_t)c[0] | ((uint32_t)c[1] << 16), (uint32_t)c[2] | ((uint32_t)c[3] << 16));
+}
+
+// compact_kt_kernel storing e4m3 codes: K_c[i] = code(K[keep[i]] / k_scale),
+// V_c[i] = code(V[keep[i]] / v_scale) (fp32 quotient, nearest even, saturated),
+// and the KT cache as the max / min of the key codes' values, stored as codes
+// (exact).  Rows are 128 bytes; the KT row stride nblk_cap is a multiple of 16.
+__global__ void __launch_bounds__(CK_NT) compact_kt_fp8_kernel(const bf16* k, const bf16* v, int64_t cap,
+                                                               const int32_t* keep, int64_t keep_ld, int64_t B1,
+                                                               int blk, const float* ksc, const float* vsc,
+                                                               uint8_t* ko, uint8_t* vo, int64_t out_cap, uint8_t* kt,
+                                                               int64_t nblk_cap) {
+  __shared__ __align__(16) uint8_t tile[2 * HD][CK_BLOCKS];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int pair = blockIdx.y;
+  const int ch = threadIdx.x & 15, bl = threadIdx.x >> 4;
+  const int64_t nblk = (B1 + blk - 1) / blk;
+  const int64_t jb0 = (int64_t)blockIdx.x * CK_BLOCKS;
+  const int64_t jb = jb0 + bl;
+  const float sk = __ldg(ksc + pair), sv = __ldg(vsc + pair);
+  float mx[8], mn[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mx[e] = neg_inf();
+    mn[e] = -neg_inf();
+  }
+  if (jb < nblk) {
+    const int64_t t0 = jb * blk, t1 = min(B1, t0 + blk);
+    const int32_t* kp = keep + (size_t)pair * keep_ld;
+    const bf16* ks = k + (size_t)pair * cap * HD + ch * 8;
+    const bf16* vs = v + (size_t)pair * cap * HD + ch * 8;
+    uint8_t* kd = ko + (size_t)pair * out_cap * HD + ch * 8;
+    uint8_t* vd = vo + (size_t)pair * out_cap * HD + ch * 8;
+    for (int64_t tb = t0; tb < t1; tb += 4) {
+      uint4 kr[4], vr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {            // four rows in flight
+        if (tb + u < t1) {
+          const int64_t src = min(max((int64_t)kp[tb + u], (int64_t)0), cap - 1);
+          kr[u] = *reinterpret_cast<const uint4*>(ks + src * HD);
+          vr[u] = *reinterpret_cast<const uint4*>(vs + src * HD);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (tb + u < t1) {
+          *reinterpret_cast<uint2*>(kd + (tb + u) * HD) = quantize8(kr[u], sk, mx, mn);
+          *reinterpret_cast<uint2*>(vd + (tb + u) * HD) = quantize8(vr[u], sv, nullptr, nullptr);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    // the bounds are code values already: re-encoding them is exact
+    const uint16_t hx = e4m3x2_from_f32(mx[e], mx[e + 1]), hn = e4m3x2_from_f32(mn[e], mn[e + 1]);
+    tile[ch * 8 + e][bl] = (uint8_t)(hx & 0xFF);
+    tile[ch * 8 + e + 1][bl] = (uint8_t)(hx >> 8);
+    tile[HD + ch * 8 + e][bl] = (uint8_t)(hn & 0xFF);
+    tile[HD + ch * 8 + e + 1][bl] = (uint8_t)(hn >> 8);
+  }
+  __syncthreads();
+  const int row = threadIdx.x;                   // KT row m*HD + c
+  const int nb = (int)min((int64_t)CK_BLOCKS, nblk - jb0);
+  uint8_t* dst = kt + ((size_t)pair * 2 * HD + row) * nblk_cap + jb0;   // 16-byte aligned: nblk_cap % 16 == 0
+  if (nb == CK_BLOCKS) {
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[row][0]);
+  } else {
+    for (int i = 0; i < nb; ++i) dst[i] = tile[row][i];
+  }
+}
+
 }  // namespace
 
 cudaError_t kt_build_launch(const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
@@ -251,6 +340,16 @@ cudaError_t compact_kt_launch(const void* k, const void* v, int64_t cap, const i
                     reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v), cap, keep, keep_ld, B1, blk,
                     reinterpret_cast<bf16*>(ko), reinterpret_cast<bf16*>(vo), out_cap, reinterpret_cast<bf16*>(kt),
                     nblk_cap, bt, bt_stride, num_pages, Hkv);
+}
+
+cudaError_t compact_kt_fp8_launch(const void* k, const void* v, int64_t cap, const int32_t* keep, int64_t keep_ld,
+                                  int64_t B1, int blk, const float* k_scale, const float* v_scale, void* ko, void* vo,
+                                  int64_t out_cap, void* kt, int64_t nblk_cap, int pairs, cudaStream_t st) {
+  const int64_t nblk = (B1 + blk - 1) / blk;
+  return launch_pdl(compact_kt_fp8_kernel, dim3((unsigned)((nblk + CK_BLOCKS - 1) / CK_BLOCKS), pairs), dim3(CK_NT),
+                    0, st, reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v), cap, keep, keep_ld, B1,
+                    blk, k_scale, v_scale, reinterpret_cast<uint8_t*>(ko), reinterpret_cast<uint8_t*>(vo), out_cap,
+                    reinterpret_cast<uint8_t*>(kt), nblk_cap);
 }
 
 }  // namespace rkv
