@@ -771,19 +771,21 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         for (int s = sa; s <= sb; ++s)
           if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
         if (F8) {
-          // this warp's 16 key rows: codes (row r at byte r*128 of the hi half) to
-          // bf16 code values in the swizzled tile, in place (all reads first)
-          uint4 cv[4];
+          // this warp's 16 key and value rows: codes to bf16 code values in the
+          // swizzled tiles (key codes sit in the K tile's hi half: all reads
+          // first); other warps read the value rows only after the barriers
+          // before the PV step
+          uint4 cv[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int q = lane + 32 * i, r = c0 + (q >> 3), cb = q & 7;
-            cv[i] = r < rows ? *reinterpret_cast<const uint4*>(tK + half + (uint32_t)r * 128u + cb * 16)
-                             : make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < 8; ++i) {
+            const int q = lane + 32 * (i & 3), r = c0 + (q >> 3), cb = q & 7;
+            const uint8_t* src = (i < 4 ? tK + half : tV8) + (uint32_t)r * 128u + cb * 16;
+            cv[i] = r < rows ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int q = lane + 32 * i, r = c0 + (q >> 3), cb = q & 7;
+          for (int i = 0; i < 8; ++i) {
+            const int q = lane + 32 * (i & 3), r = c0 + (q >> 3), cb = q & 7;
             if (r >= rows) continue;
             const uint32_t w[4] = {cv[i].x, cv[i].y, cv[i].z, cv[i].w};
 #pragma unroll
@@ -793,17 +795,15 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
                                          e4m3x2_to_bf16x2((uint16_t)(w[2 * hh] >> 16)),
                                          e4m3x2_to_bf16x2((uint16_t)(w[2 * hh + 1] & 0xFFFF)),
                                          e4m3x2_to_bf16x2((uint16_t)(w[2 * hh + 1] >> 16)));
-              *reinterpret_cast<uint4*>(tK + (uint32_t)(ch8 >> 3) * half + swz128(r, ch8 & 7)) = o;
+              *reinterpret_cast<uint4*>((i < 4 ? tK : tV) + (uint32_t)(ch8 >> 3) * half + swz128(r, ch8 & 7)) = o;
             }
           }
           __syncwarp();
         }
         if (app) {
           // the appended token lies past the tensor map's extent (read as zero): write it in
-          // (e4m3: the key here, the value by the V conversion below)
           for (int s = sa; s <= sb; ++s) {
             if (sel[r0 + s] != nb_new) continue;
-            if (F8 && lane >= 16) continue;
             const int r = s * blk + (n_old - nb_new * blk);
             const int ch = lane & 15;
             const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
@@ -919,32 +919,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       acc[ht][1] *= corr[ht][1];
       acc[ht][2] *= corr[ht][0];
       acc[ht][3] *= corr[ht][1];
-    }
-    if (F8) {
-      // this warp's 16 value channels of every staged row: codes to bf16 code
-      // values (the appended token's from its stored codes, rows past the round zero)
-      for (int s = 0; s < nsl; ++s)
-        if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
-      const int r_app = app ? (n_old - nb_new * blk) : -1;   // the appended token's row within its block
-      for (int r = lane; r < rows16; r += 32) {
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-        if (r < rows) {
-          if (r_app >= 0 && r % blk == r_app && sel[r0 + r / blk] == nb_new) {
-            o0 = *reinterpret_cast<const uint4*>(fs.vnew + 16 * warp);
-            o1 = *reinterpret_cast<const uint4*>(fs.vnew + 16 * warp + 8);
-          } else {
-            const uint4 cv = *reinterpret_cast<const uint4*>(tV8 + (uint32_t)r * 128u + 16 * warp);
-            o0 = make_uint4(e4m3x2_to_bf16x2((uint16_t)(cv.x & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.x >> 16)),
-                            e4m3x2_to_bf16x2((uint16_t)(cv.y & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.y >> 16)));
-            o1 = make_uint4(e4m3x2_to_bf16x2((uint16_t)(cv.z & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.z >> 16)),
-                            e4m3x2_to_bf16x2((uint16_t)(cv.w & 0xFFFF)), e4m3x2_to_bf16x2((uint16_t)(cv.w >> 16)));
-          }
-        }
-        const int ch8 = 2 * warp;
-        *reinterpret_cast<uint4*>(tV + (uint32_t)(ch8 >> 3) * half + swz128(r, ch8 & 7)) = o0;
-        *reinterpret_cast<uint4*>(tV + (uint32_t)((ch8 + 1) >> 3) * half + swz128(r, (ch8 + 1) & 7)) = o1;
-      }
-      __syncwarp();
     }
     // --- O^T (dims 16*warp .. +15) += V^T P^T over every 16-token step of the round
     for (int cs = 0; cs < nsteps; ++cs) {

@@ -117,6 +117,35 @@ class Layer:
                            k_new, v_new, stream)
         self.n += 1
 
+    # -- e4m3 (FP8) storage of the compacted cache -------------------------------
+
+    def enable_fp8(self, k_scale: torch.Tensor, v_scale: torch.Tensor):
+        """Allocate e4m3 code caches; k_scale / v_scale are [B, Hkv] fp32 (value = code * scale)."""
+        wl = self.wl
+        B, Hkv, D = wl.B, wl.Hkv, wl.D
+        dev = self.kc.device
+        self.k_scale, self.v_scale = k_scale, v_scale
+        self.nblk_cap8 = -(-nblk_capacity(self.cap, wl.blk) // 16) * 16
+        self.kc8 = torch.empty(B, Hkv, self.cap, D, dtype=torch.uint8, device=dev)
+        self.vc8 = torch.empty_like(self.kc8)
+        self.kt8 = torch.empty(B, Hkv, 2, D, self.nblk_cap8, dtype=torch.uint8, device=dev)
+
+    def compact_kt_fp8(self, stream=None):
+        rkv.rkv_compact_kt_fp8(self.dims, self.k, self.v, self.cap_in, self.keep, self.bud.B1, self.bud.B1,
+                               self.k_scale, self.v_scale, self.kc8, self.vc8, self.cap, self.wl.blk, self.kt8,
+                               self.nblk_cap8, stream)
+        self.n = self.bud.B1
+
+    def step_fp8(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, stream=None,
+                 selections: bool = True, out: Optional[torch.Tensor] = None):
+        """One decode step over the e4m3 cache with the append fused in."""
+        wl = self.wl
+        rkv.rkv_hsa_decode_fp8(self.dims, q, self.kc8, self.vc8, self.cap, self.n, self.k_scale, self.v_scale,
+                               self.kt8, self.nblk_cap8, wl.blk, wl.k1, self.bud.k2, self.scale,
+                               self.out if out is None else out, self.sel_blocks if selections else None,
+                               self.sel_channels if selections else None, k_new, v_new, stream)
+        self.n += 1
+
     def reset_decode(self):
         """Forget appended tokens (the next stage1() re-creates the compacted caches)."""
         self.n = self.bud.B1
