@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   float* recv = reinterpret_cast<float*>(smem + a.off_recv);
   uint8_t* tK = smem + a.off_tiles;
   uint8_t* tV = tK + 2 * a.tile_half_bytes;
-  uint8_t* tV8 = smem + a.off_v8;                                      // e4m3: staged V code rows
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -693,13 +692,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
             mbar_arrive_expect_tx(&fs.mbar[s], (uint32_t)blk * 128u * (F8 ? 2u : 4u));
         __syncwarp();
         if (F8) {
-          // code rows (128 bytes, unswizzled): K into the hi half of the K tile,
-          // converted in place by the warp that owns the rows; V into its own staging
+          // code rows (128 bytes, unswizzled) into the hi half of the K and V
+          // tiles, converted in place by the warp that owns the rows
           const int part = warp & 1;
           for (int s = (warp >> 1) + 4 * lane; s < nsl; s += 128) {
             const uint32_t off = (uint32_t)s * blk * 128u;
-            tma_load_3d(part ? tV8 + off : tK + half + off, part ? &tmV : &tmK, 0, sel[r0 + s] * blk, pair,
-                        &fs.mbar[s]);
+            tma_load_3d((part ? tV : tK) + half + off, part ? &tmV : &tmK, 0, sel[r0 + s] * blk, pair, &fs.mbar[s]);
           }
         } else {
           const int part = warp & 3;                   // K lo, K hi, V lo, V hi
@@ -771,15 +769,15 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         for (int s = sa; s <= sb; ++s)
           if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
         if (F8) {
-          // this warp's 16 key and value rows: codes to bf16 code values in the
-          // swizzled tiles (key codes sit in the K tile's hi half: all reads
-          // first); other warps read the value rows only after the barriers
-          // before the PV step
+          // this warp's 16 key and value rows: codes (row r at byte r*128 of each
+          // tile's hi half) to bf16 code values in the swizzled tiles, in place
+          // (all reads first); other warps read the value rows only after the
+          // barriers before the PV step
           uint4 cv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int q = lane + 32 * (i & 3), r = c0 + (q >> 3), cb = q & 7;
-            const uint8_t* src = (i < 4 ? tK + half : tV8) + (uint32_t)r * 128u + cb * 16;
+            const uint8_t* src = (i < 4 ? tK : tV) + half + (uint32_t)r * 128u + cb * 16;
             cv[i] = r < rows ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
@@ -1087,8 +1085,7 @@ bool hsa_plan(HsaArgs& a) {
   a.off_tiles = off;                       // K/V tiles; the KT gather tile shares this region
   const uint32_t rows16 = al((uint32_t)(a.slots_round * a.blk), 16);
   a.tile_half_bytes = rows16 * 128u;
-  a.off_v8 = off + 4u * a.tile_half_bytes;    // e4m3: V code rows (rows16 x 128 bytes)
-  off += std::max(4u * a.tile_half_bytes + (a.f8 ? a.tile_half_bytes : 0u), al(kt_tile_bytes, 16));
+  off += std::max(4u * a.tile_half_bytes, al(kt_tile_bytes, 16));
   a.smem_bytes = off + 1024u;   // room to align the base to 1024 bytes
   return a.smem_bytes <= 227u * 1024u;
 }

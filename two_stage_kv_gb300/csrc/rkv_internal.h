@@ -48,7 +48,6 @@ struct HsaArgs {
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared-memory layout (bytes)
   uint32_t off_x, off_scores, off_flags, off_sel, off_bt, off_recv, off_tiles, tile_half_bytes, smem_bytes;
-  uint32_t off_v8;      // e4m3: V code rows staged by TMA before conversion (K codes land in the K tile's hi half)
 };
 
 // Computes ns/chunk/slots_round and the shared-memory layout.  Returns false if
