@@ -173,69 +173,126 @@ __device__ void radix_topk(const uint32_t* keys, int n, int k, uint8_t* flag, Fi
   __syncthreads();
 }
 
-// Exact top-k (0 < k < n) of vals[0, n): flag[j] = 1 for the k largest values,
-// equal values taken in ascending index order.  mn / mx are the minimum and
-// maximum of vals.  The fallback overwrites vals with order-preserving keys.
-// fs.hist must be zero on entry and is zero again on return.
-__device__ void bucket_topk(float* vals, int n, int k, float mn, float mx, uint8_t* flag, FixedSmem& fs) {
+// Exact top-k (0 < k < n) of vals[0, n), listed: sel[0, k) = the indices of
+// the k largest values in ascending order, equal values taken in ascending
+// index order.  mn / mx are the minimum and maximum of vals.
+//
+// A 256-bucket histogram over [mn, mx] locates the bucket holding the k-th
+// value; every warp reads the whole histogram and finds that bucket on its
+// own (no block barrier for the search).  Usually that bucket is taken whole
+// and the chosen values are simply those in it or above; otherwise its
+// members are ranked pairwise.  Degenerate value sets (equal, non-finite
+// range, a crowded boundary bucket) go to a radix select on order-preserving
+// keys, which overwrites vals.  fs.hist must be zero on entry and fs.misc[3]
+// zero; both are left dirty (one call per launch).
+__device__ void topk_list(float* vals, int n, int k, float mn, float mx, uint8_t* flag, int32_t* sel, FixedSmem& fs) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float width = mx - mn;
   bool fallback = !(width > 0.f) || !isfinite(width);
   const float inv = fallback ? 0.f : (float)NBUCKET / width;
   // (clamped at both ends: -inf / +inf entries of the masked multi-turn reading)
   auto bucket = [&](float s) { return max(0, min(NBUCKET - 1, (int)((s - mn) * inv))); };
+  int bb = 0, need = 0, m = 0;
   if (!fallback) {
     for (int j = tid; j < n; j += NT) atomicAdd(&fs.hist[bucket(vals[j])], 1);
     __syncthreads();
-    const int c = fs.hist[tid];
-    int incl = c;   // this thread's bucket and every higher bucket of its warp
+    // lane l holds buckets 8l .. 8l+7; counts from the top bucket down
+    const int4 h0 = *reinterpret_cast<const int4*>(&fs.hist[8 * lane]);
+    const int4 h1 = *reinterpret_cast<const int4*>(&fs.hist[8 * lane + 4]);
+    const int cnt[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    int s = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += cnt[u];
+    int incl = s;   // this lane's buckets and every higher lane's
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_down_sync(0xffffffffu, incl, o);
       if (lane + o < 32) incl += t;
     }
-    if (lane == 0) fs.wsum[warp] = incl;
-    fs.hist[tid] = 0;                 // leave the histogram zeroed for the next caller
-    __syncthreads();
-    int above = incl - c;
-    for (int w = warp + 1; w < NWARP; ++w) above += fs.wsum[w];
-    if (above < k && above + c >= k) {
-      fs.misc[0] = tid;               // boundary bucket
-      fs.misc[1] = k - above;         // its members to take
-      fs.misc[2] = c;                 // its size
-      fs.misc[3] = 0;
+    int above = incl - s;
+    int found = -1, fneed = 0, fm = 0;
+#pragma unroll
+    for (int u = 7; u >= 0; --u) {
+      if (above < k && above + cnt[u] >= k) {
+        found = 8 * lane + u;
+        fneed = k - above;
+        fm = cnt[u];
+      }
+      above += cnt[u];
     }
-    __syncthreads();
-    fallback = fs.misc[2] > MEMBER_MAX;
+    const int src = __ffs(__ballot_sync(0xffffffffu, found >= 0)) - 1;   // exactly one lane
+    bb = __shfl_sync(0xffffffffu, found, src);
+    need = __shfl_sync(0xffffffffu, fneed, src);
+    m = __shfl_sync(0xffffffffu, fm, src);
+    fallback = m > MEMBER_MAX;                      // the same in every warp
   }
   if (!fallback) {
-    const int bb = fs.misc[0], need = fs.misc[1], m = fs.misc[2];
-    for (int j = tid; j < n; j += NT) {
-      const int bk = bucket(vals[j]);
-      flag[j] = bk > bb;
-      if (bk == bb) fs.members[atomicAdd(&fs.misc[3], 1)] = j;
-    }
-    __syncthreads();
-    for (int i = tid; i < m; i += NT) {
-      const int j = fs.members[i];
-      const float s = vals[j];
-      int rk = 0;
-      for (int i2 = 0; i2 < m; ++i2) {
-        const int j2 = fs.members[i2];
-        const float s2 = vals[j2];
-        rk += (s2 > s) || (s2 == s && j2 < j);
+    if (need < m) {
+      // the boundary bucket is split: rank its members
+      for (int j = tid; j < n; j += NT)
+        if (bucket(vals[j]) == bb) fs.members[atomicAdd(&fs.misc[3], 1)] = j;
+      __syncthreads();
+      for (int i = tid; i < m; i += NT) {
+        const int j = fs.members[i];
+        const float sv = vals[j];
+        int rk = 0;
+        for (int i2 = 0; i2 < m; ++i2) {
+          const int j2 = fs.members[i2];
+          const float s2 = vals[j2];
+          rk += (s2 > sv) || (s2 == sv && j2 < j);
+        }
+        flag[j] = rk < need ? 1 : 0;
       }
-      if (rk < need) flag[j] = 1;
+      __syncthreads();
     }
-    __syncthreads();
+    auto chosen = [&](int j) -> bool {
+      if (j >= n) return false;
+      const int bk = bucket(vals[j]);
+      return bk > bb || (bk == bb && (need == m || flag[j] != 0));
+    };
+    if (n <= 2 * NT) {
+      // thread t lists blocks 2t and 2t+1: one block-wide scan
+      const bool f0 = chosen(2 * tid), f1 = chosen(2 * tid + 1);
+      const int cnt = (int)f0 + (int)f1;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) fs.wsum[warp] = incl;
+      __syncthreads();
+      int pre = incl - cnt;
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) pre += w < warp ? fs.wsum[w] : 0;
+      if (f0 && pre < k) sel[pre] = 2 * tid;
+      if (f1 && pre + (int)f0 < k) sel[pre + (int)f0] = 2 * tid + 1;
+    } else {
+      int out = 0;
+      for (int base = 0; base < n; base += NT) {
+        const int j = base + tid;
+        const bool f = chosen(j);
+        int tot;
+        const int pre = scan1(f, fs.wsum, tot);
+        if (f && out + pre < k) sel[out + pre] = j;
+        out += tot;
+      }
+    }
   } else {
     uint32_t* keys = reinterpret_cast<uint32_t*>(vals);
     __syncthreads();
     for (int j = tid; j < n; j += NT) keys[j] = f2key(vals[j]);
     __syncthreads();
     radix_topk(keys, n, k, flag, fs);
-    for (int i = tid; i < 4 * 256; i += NT) fs.hist[i] = 0;
-    __syncthreads();
+    int out = 0;
+    for (int base = 0; base < n; base += NT) {
+      const int j = base + tid;
+      const bool f = j < n && flag[j];
+      int tot;
+      const int pre = scan1(f, fs.wsum, tot);
+      if (f && out + pre < k) sel[out + pre] = j;
+      out += tot;
+    }
   }
 }
 
@@ -305,6 +362,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     if (spec) prefetch_tmap(&tmKT);
   }
   for (int i = tid; i < 4 * 256; i += NT) fs.hist[i] = 0;
+  if (tid == 0) fs.misc[3] = 0;
   if (tid < 16) {
     fs.mrun[tid] = neg_inf();
     fs.lrun[tid] = 0.f;
@@ -410,22 +468,29 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // Top-k1 channels by rank: channel c = tid / 2 is taken when fewer than k1
   // channels have a larger sum, or an equal sum and a lower index.  The two
   // threads of a channel count the even and the odd groups of four channels.
+  // Both CTAs of an SM run this count at once, so it is kept to one compare
+  // per channel: the sums are >= +0, so "v >= mine" is "v > below" with below
+  // the next float under mine, and a group of four channels wholly below c
+  // compares against below (equal sums count), any other group against mine;
+  // the group holding c then adds its lower-index ties on its own.
   const int c = tid >> 1, hc = tid & 1;
   int rk = 0;
   if (!use64) {
     if (a.k1 < HD) {
       const float mine = fs.asum[c];
+      const int mbits = __float_as_int(mine);
+      const float below = mbits > 0 ? __int_as_float(mbits - 1) : -1.f;
       const float4* a4 = reinterpret_cast<const float4*>(fs.asum);
 #pragma unroll
       for (int i = 0; i < HD / 8; ++i) {
         const int q4 = 2 * i + hc;                 // the two halves hit different banks
         const float4 v = a4[q4];
-        const int j = 4 * q4;
-        rk += (int)(v.x > mine) + (int)((v.x == mine) & (j < c));
-        rk += (int)(v.y > mine) + (int)((v.y == mine) & (j + 1 < c));
-        rk += (int)(v.z > mine) + (int)((v.z == mine) & (j + 2 < c));
-        rk += (int)(v.w > mine) + (int)((v.w == mine) & (j + 3 < c));
+        const float t = (4 * q4 + 3 < c) ? below : mine;
+        rk += (int)(v.x > t) + (int)(v.y > t) + (int)(v.z > t) + (int)(v.w > t);
       }
+      const int qc = c >> 2;
+      if ((qc & 1) == hc)
+        for (int j = 4 * qc; j < c; ++j) rk += (int)(fs.asum[j] == mine);
     }
   } else {
     // rare: some group sum needs more than fp32's 24 bits; redo every channel in fp64
@@ -458,9 +523,19 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     int pos = __popc(bal & ((1u << lane) - 1u));
     for (int w = 0; w < warp; ++w) pos += fs.wsum[w];
     if (take) {
-      const double qb = use64 ? fs.qbar64[c] : (double)fs.qbar32[c];
-      fs.qsel[pos] = (float)qb;
-      fs.rowoff[pos] = (qb >= 0.0 ? 0 : HD) + c;     // Kmax when the group sum is >= 0
+      // (fp64 only on the rare inexact path: this GPU's fp64 rate is low)
+      float qf;
+      bool nonneg;
+      if (use64) {
+        const double qb = fs.qbar64[c];
+        qf = (float)qb;
+        nonneg = qb >= 0.0;
+      } else {
+        qf = fs.qbar32[c];
+        nonneg = qf >= 0.f;
+      }
+      fs.qsel[pos] = qf;
+      fs.rowoff[pos] = (nonneg ? 0 : HD) + c;     // Kmax when the group sum is >= 0
       if (rank == 0 && a.sel_channels) a.sel_channels[(size_t)pair * a.k1 + pos] = c;
     }
   }
@@ -631,21 +706,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // ---------------------------------------------------------------- C ------
   const int k2e = RAG ? min(a.k2, nblk) : a.k2e;
   if (k2e >= nblk) {
-    for (int j = tid; j < nblk; j += NT) flag[j] = 1;
+    for (int j = tid; j < nblk; j += NT) sel[j] = j;
   } else {
-    bucket_topk(sval, nblk, k2e, smn, smx, flag, fs);
-  }
-  __syncthreads();
-  {
-    int out = 0;
-    for (int base = 0; base < nblk; base += NT) {
-      const int j = base + tid;
-      const bool f = j < nblk && flag[j];
-      int tot;
-      const int pre = scan1(f, fs.wsum, tot);
-      if (f && out + pre < k2e) sel[out + pre] = j;
-      out += tot;
-    }
+    topk_list(sval, nblk, k2e, smn, smx, flag, sel, fs);
   }
   __syncthreads();
 
