@@ -67,14 +67,14 @@ struct FixedSmem {
   bf16 vnew[HD];
   float qsel[HD];               // group-summed q of the kept channels, ascending channel
   int32_t rowoff[HD];           // KT row (0..2*HD) of each kept channel
-  float asum[HD];               // sum_g |q_g| per channel (fp32, exact)
+  alignas(16) float asum[HD];   // sum_g |q_g| per channel (fp32, exact)
   float qbar32[HD];
   uint64_t akey64[HD];          // fp64 fallback
   double qbar64[HD];
-  int32_t hist[4 * 256];        // bucket histogram; the radix fallback uses 4 x 256
+  alignas(16) int32_t hist[4 * 256];   // bucket histogram; the radix fallback uses 4 x 256
   int32_t members[MEMBER_MAX];
   float wmin[NWARP], wmax[NWARP];
-  int32_t wsum[2 * NWARP];
+  alignas(16) int32_t wsum[2 * NWARP];
   int32_t misc[8];
   float wmaxh[NWARP][16];       // per-warp head maxima of a round
   float wsumh[NWARP][16];       // per-warp head probability sums of a round
@@ -472,7 +472,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // per channel: the sums are >= +0, so "v >= mine" is "v > below" with below
   // the next float under mine, and a group of four channels wholly below c
   // compares against below (equal sums count), any other group against mine;
-  // the group holding c then adds its lower-index ties on its own.
+  // the group holding c then adds its lower-index ties on its own.  The
+  // counts are kept in fp32 (exact up to 2^24): a compare feeding a float
+  // select and add issues far faster here than one turned into an integer.
   const int c = tid >> 1, hc = tid & 1;
   int rk = 0;
   if (!use64) {
@@ -481,16 +483,19 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       const int mbits = __float_as_int(mine);
       const float below = mbits > 0 ? __int_as_float(mbits - 1) : -1.f;
       const float4* a4 = reinterpret_cast<const float4*>(fs.asum);
+      float f0 = 0.f, f1 = 0.f;
 #pragma unroll
       for (int i = 0; i < HD / 8; ++i) {
         const int q4 = 2 * i + hc;                 // the two halves hit different banks
         const float4 v = a4[q4];
         const float t = (4 * q4 + 3 < c) ? below : mine;
-        rk += (int)(v.x > t) + (int)(v.y > t) + (int)(v.z > t) + (int)(v.w > t);
+        f0 += (v.x > t ? 1.f : 0.f) + (v.y > t ? 1.f : 0.f);
+        f1 += (v.z > t ? 1.f : 0.f) + (v.w > t ? 1.f : 0.f);
       }
       const int qc = c >> 2;
       if ((qc & 1) == hc)
-        for (int j = 4 * qc; j < c; ++j) rk += (int)(fs.asum[j] == mine);
+        for (int j = 4 * qc; j < c; ++j) f0 += fs.asum[j] == mine ? 1.f : 0.f;
+      rk = (int)(f0 + f1);
     }
   } else {
     // rare: some group sum needs more than fp32's 24 bits; redo every channel in fp64
@@ -521,7 +526,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     if (lane == 0) fs.wsum[warp] = __popc(bal);
     __syncthreads();
     int pos = __popc(bal & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) pos += fs.wsum[w];
+    {
+      const int4 w0 = *reinterpret_cast<const int4*>(&fs.wsum[0]);
+      const int4 w1 = *reinterpret_cast<const int4*>(&fs.wsum[4]);
+      pos += (warp > 0 ? w0.x : 0) + (warp > 1 ? w0.y : 0) + (warp > 2 ? w0.z : 0) + (warp > 3 ? w0.w : 0) +
+             (warp > 4 ? w1.x : 0) + (warp > 5 ? w1.y : 0) + (warp > 6 ? w1.z : 0);
+    }
     if (take) {
       // (fp64 only on the rare inexact path: this GPU's fp64 rate is low)
       float qf;
@@ -555,6 +565,19 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     const uint32_t sval_local = smem_u32(sval);
     const int bc = spec ? cpr : a.kt_chunk;          // columns per tile (multiple of 8; of 16 for e4m3)
     const int cg = tid & 3, bp = tid >> 2;           // channel group, block pair within a 128-block span
+    // with k1 <= 32 each thread's channels (i = cg + 4u) are read into registers
+    // now, so the tile reads below do not wait on them one by one
+    constexpr int KC = 8;
+    const bool kfast = k1 <= 4 * KC;
+    int rowv[KC];
+    float qv[KC];
+#pragma unroll
+    for (int u = 0; u < KC; ++u) {
+      const int i = cg + 4 * u;
+      const bool ok = kfast && i < k1;
+      rowv[u] = ok ? (spec ? fs.rowoff[i] : i) : 0;   // row 0 with weight 0 adds +0
+      qv[u] = ok ? fs.qsel[i] : 0.f;
+    }
     if (MK) {
       // which of this CTA's blocks hold a candidate (read after the barrier before scoring)
       for (int j = jlo + tid; j < jhi; j += NT)
@@ -631,18 +654,33 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         const bool live = 2 * jp < nb_here;
         const int jpc = live ? jp : 0;
         float s0 = 0.f, s1 = 0.f;
-        for (int i = cg; i < k1; i += 4) {
-          const int row = spec ? fs.rowoff[i] : i;
-          const float q = fs.qsel[i];
-          if (F8) {
-            // two blocks' codes per 16-bit word, row pitch bc bytes
-            const float2 f = e4m3x2_to_f32(reinterpret_cast<const uint16_t*>(kttile)[(size_t)row * pitch + jpc]);
-            s0 = fmaf(q, f.x, s0);
-            s1 = fmaf(q, f.y, s1);
-          } else {
-            const uint32_t v = tile32[(size_t)row * pitch + jpc];
-            s0 = fmaf(q, bf16_lo(v), s0);
-            s1 = fmaf(q, bf16_hi(v), s1);
+        if (kfast) {
+#pragma unroll
+          for (int u = 0; u < KC; ++u) {
+            if (F8) {
+              // two blocks' codes per 16-bit word, row pitch bc bytes
+              const float2 f = e4m3x2_to_f32(reinterpret_cast<const uint16_t*>(kttile)[rowv[u] * pitch + jpc]);
+              s0 = fmaf(qv[u], f.x, s0);
+              s1 = fmaf(qv[u], f.y, s1);
+            } else {
+              const uint32_t v = tile32[rowv[u] * pitch + jpc];
+              s0 = fmaf(qv[u], bf16_lo(v), s0);
+              s1 = fmaf(qv[u], bf16_hi(v), s1);
+            }
+          }
+        } else {
+          for (int i = cg; i < k1; i += 4) {
+            const int row = spec ? fs.rowoff[i] : i;
+            const float q = fs.qsel[i];
+            if (F8) {
+              const float2 f = e4m3x2_to_f32(reinterpret_cast<const uint16_t*>(kttile)[(size_t)row * pitch + jpc]);
+              s0 = fmaf(q, f.x, s0);
+              s1 = fmaf(q, f.y, s1);
+            } else {
+              const uint32_t v = tile32[(size_t)row * pitch + jpc];
+              s0 = fmaf(q, bf16_lo(v), s0);
+              s1 = fmaf(q, bf16_hi(v), s1);
+            }
           }
         }
         s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
@@ -723,9 +761,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
               qb[ht][2 * j + 1][0], qb[ht][2 * j + 1][1]);
   // O^T accumulator of this warp's 16 output dimensions: dims 16*warp + lane/4 (+8),
   // heads 8*ht + 2*(lane%4) + {0, 1}
-  float acc[NH][4];
+  // (the narrow-group kernel keeps the lo part of P in its own accumulator,
+  // halving the chain of dependent mma in the PV step)
+  constexpr bool SPLIT = NH == 1;
+  float acc[NH][4], accl[NH][4];
 #pragma unroll
-  for (int ht = 0; ht < NH; ++ht) acc[ht][0] = acc[ht][1] = acc[ht][2] = acc[ht][3] = 0.f;
+  for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[ht][e] = accl[ht][e] = 0.f;
 
   const int chunk = RAG ? (k2e + ns - 1) / ns : a.chunk;   // blocks per CTA (at most the plan's chunk)
   const int s_lo = (int)rank * chunk;
@@ -875,11 +918,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           __syncwarp();
         }
       }
-      float st[NH][2][4];
+      // NC independent accumulator chains over the 8 k-steps (a dependent mma
+      // costs ~35 cycles here); two for the wide-group kernel (register room)
+      constexpr int NC = NH == 1 ? 4 : 2;
+      float st[NH][NC][4];
 #pragma unroll
       for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) st[ht][u][0] = st[ht][u][1] = st[ht][u][2] = st[ht][u][3] = 0.f;
+        for (int u = 0; u < NC; ++u) st[ht][u][0] = st[ht][u][1] = st[ht][u][2] = st[ht][u][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const int r = c0 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -887,7 +933,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         uint32_t ka[4];
         ldsm_x4(smem_u32(tK) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), ka[0], ka[1], ka[2], ka[3]);
 #pragma unroll
-        for (int ht = 0; ht < NH; ++ht) mma_bf16(st[ht][ks & 1], ka, qb[ht][ks][0], qb[ht][ks][1]);
+        for (int ht = 0; ht < NH; ++ht) mma_bf16(st[ht][ks % NC], ka, qb[ht][ks][0], qb[ht][ks][1]);
       }
       // this lane: tokens c0 + lane/4 (e = 0, 1) and + 8 (e = 2, 3); heads 2(lane%4) + (e & 1)
       const int ta = c0 + g4, tb = ta + 8;
@@ -902,7 +948,8 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float sv = (st[ht][0][e] + st[ht][1][e]) * sl2;
+          const float sv = (NC == 4 ? (st[ht][0][e] + st[ht][1][e]) + (st[ht][2][NC == 4 ? e : 0] + st[ht][3 % NC][e])
+                                    : st[ht][0][e] + st[ht][1][e]) * sl2;
           x[ht][e] = ((e < 2) ? va : vb) ? sv : neg_inf();
         }
     }
@@ -980,6 +1027,12 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       acc[ht][1] *= corr[ht][1];
       acc[ht][2] *= corr[ht][0];
       acc[ht][3] *= corr[ht][1];
+      if (SPLIT) {
+        accl[ht][0] *= corr[ht][0];
+        accl[ht][1] *= corr[ht][1];
+        accl[ht][2] *= corr[ht][0];
+        accl[ht][3] *= corr[ht][1];
+      }
     }
     // --- O^T (dims 16*warp .. +15) += V^T P^T over every 16-token step of the round
     for (int cs = 0; cs < nsteps; ++cs) {
@@ -991,13 +1044,19 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       for (int ht = 0; ht < NH; ++ht) {
         const uint32_t* pf = &fs.pfrag[cs][ht][0][0];
         mma_bf16(acc[ht], va4, pf[0 * 32 + lane], pf[1 * 32 + lane]);
-        mma_bf16(acc[ht], va4, pf[2 * 32 + lane], pf[3 * 32 + lane]);
+        mma_bf16(SPLIT ? accl[ht] : acc[ht], va4, pf[2 * 32 + lane], pf[3 * 32 + lane]);
       }
     }
     phase ^= 1u;
     if (r0 + a.slots_round < s_hi) __syncthreads();   // tiles and fragments are reused by the next round
   }
 
+  if (SPLIT) {
+#pragma unroll
+    for (int ht = 0; ht < NH; ++ht)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[ht][e] += accl[ht][e];
+  }
   // ---------------------------------------------------------------- E ------
   // Partials go to the owner of each head (head g: CTA g % ns) with st.async,
   // which counts their bytes on the owner's ebar; only owners wait.
