@@ -465,6 +465,25 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     fs.qbar32[tid] = sq;
   }
   const bool use64 = __syncthreads_or(inexact) != 0;
+  if (app && rank == 0) {
+    // Persist the appended token now (cache row, MT candidate index): this launch
+    // never reads that row from memory (its tiles take the token from shared
+    // memory, TMA reads past the old length return zero, gathers stop below it),
+    // so the store leaves the tail of the launch.
+    if (F8 && tid < 16) {
+      // 128 code bytes per row: threads 0-7 the key, 8-15 the value
+      uint8_t* dst = (tid < 8 ? reinterpret_cast<uint8_t*>(a.k) : reinterpret_cast<uint8_t*>(a.v)) +
+                     ((size_t)pair * a.cap + (size_t)n_old) * HD + (tid & 7) * 16;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 8 ? fs.knew8 : fs.vnew8) + (tid & 7) * 16);
+    } else if (!F8 && tid < 32) {
+      bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
+                  (PG ? (((size_t)bt_s[nb_new] * a.Hkv + hk) * a.blk + (size_t)(n_old % a.blk))
+                      : (size_t)pair * a.cap + (MT ? a.row : (int64_t)n_old)) * HD + (tid & 15) * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 16 ? fs.knew : fs.vnew) +
+                                                                        (tid & 15) * 8);
+    }
+    if (MT && tid == 32) a.idx_w[(size_t)pair * a.idx_cap + n_old] = (int32_t)a.row;
+  }
   // Top-k1 channels by rank: channel c = tid / 2 is taken when fewer than k1
   // channels have a larger sum, or an equal sum and a lower index.  The two
   // threads of a channel count the even and the odd groups of four channels.
@@ -775,6 +794,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   const int s_hi = min(k2e, s_lo + chunk);
   const uint32_t half = a.tile_half_bytes;
   const int blk = a.blk;
+  const int bsh = a.blk_shift;
+  // x / blk for x >= 0 (a shift for power-of-two blocks: this sits on the chain)
+  auto divb = [bsh, blk](int x) { return bsh >= 0 ? x >> bsh : x / blk; };
   uint32_t phase = 0;
   unsigned int* err = &g_hsa_err;
   const int g4 = lane >> 2, t4 = lane & 3;
@@ -871,7 +893,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     for (int ht = 0; ht < NH; ++ht) x[ht][0] = x[ht][1] = x[ht][2] = x[ht][3] = neg_inf();
     if (has_step) {
       if (!gat) {
-        const int sa = c0 / blk, sb = min((c0 + 15) / blk, nsl - 1);
+        const int sa = divb(c0), sb = min(divb(c0 + 15), nsl - 1);
         for (int s = sa; s <= sb; ++s)
           if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
         if (F8) {
@@ -937,7 +959,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       }
       // this lane: tokens c0 + lane/4 (e = 0, 1) and + 8 (e = 2, 3); heads 2(lane%4) + (e & 1)
       const int ta = c0 + g4, tb = ta + 8;
-      const int sla = ta / blk, slb = tb / blk;
+      const int sla = divb(ta), slb = divb(tb);
       bool va = ta < rows && sel[r0 + sla] * blk + (ta - sla * blk) < n_tot;
       bool vb = tb < rows && sel[r0 + slb] * blk + (tb - slb * blk) < n_tot;
       if (MK) {
@@ -1135,22 +1157,6 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     if (a.sel_blocks) {
       for (int j = tid; j < a.k2; j += NT) a.sel_blocks[(size_t)pair * a.k2 + j] = j < k2e ? sel[j] : -1;
     }
-    if (app) {
-      // persist the appended token: cache row and candidate index (MT)
-      if (F8 && tid < 16) {
-        // 128 code bytes per row: lanes 0-7 the key, 8-15 the value
-        uint8_t* dst = (tid < 8 ? reinterpret_cast<uint8_t*>(a.k) : reinterpret_cast<uint8_t*>(a.v)) +
-                       ((size_t)pair * a.cap + (size_t)n_old) * HD + (tid & 7) * 16;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 8 ? fs.knew8 : fs.vnew8) + (tid & 7) * 16);
-      } else if (!F8 && tid < 32) {
-        bf16* dst = (tid < 16 ? reinterpret_cast<bf16*>(a.k) : reinterpret_cast<bf16*>(a.v)) +
-                    (PG ? (((size_t)bt_s[nb_new] * a.Hkv + hk) * blk + (size_t)(n_old % blk))
-                        : (size_t)pair * a.cap + (MT ? a.row : (int64_t)n_old)) * HD + (tid & 15) * 8;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>((tid < 16 ? fs.knew : fs.vnew) +
-                                                                          (tid & 15) * 8);
-      }
-      if (MT && tid == 32) a.idx_w[(size_t)pair * a.idx_cap + n_old] = (int32_t)a.row;
-    }
   }
 }
 
@@ -1169,6 +1175,7 @@ bool hsa_plan(HsaArgs& a) {
   const int n_tot = a.n + (a.k_new ? 1 : 0);
   a.nblk = (n_tot + a.blk - 1) / a.blk;
   a.k2e = std::min(a.k2, a.nblk);
+  a.blk_shift = (a.blk & (a.blk - 1)) == 0 ? __builtin_ctz((unsigned)a.blk) : -1;
   const int pairs = a.B * a.Hkv;
   // one wave at two CTAs per SM, at most 8 CTAs per cluster, no more CTAs than blocks
   int ns = std::max(1, (2 * g_num_sms) / std::max(1, pairs));
