@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   const uint32_t* mrow = MK ? a.mask + (size_t)pair * a.mask_ld : nullptr;
   // the appended key starts its block's bounds when the block holds no earlier
   // candidate, and widens them otherwise
-  bool fresh_new = (n_old % a.blk) == 0;
+  bool fresh_new = (a.blk_shift >= 0 ? (n_old & (a.blk - 1)) : n_old % a.blk) == 0;
   if (MK && own_new && !fresh_new) fresh_new = !cand_any(mrow, a.n_prompt, (int64_t)nb_new * a.blk, n_old);
   bf16 kt_old = __float2bfloat16(0.f);
   bf16* kt_col = nullptr;
@@ -1082,7 +1082,11 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   // ---------------------------------------------------------------- E ------
   // Partials go to the owner of each head (head g: CTA g % ns) with st.async,
   // which counts their bytes on the owner's ebar; only owners wait.
-  const int gown = (G + ns - 1) / ns;
+  // owner CTA and slot of head g (shifts for a power-of-two cluster: this is the tail)
+  const int nsh = a.ns_shift;
+  auto own_of = [nsh, ns](int g) { return nsh >= 0 ? g & (ns - 1) : g % ns; };
+  auto slot_of = [nsh, ns](int g) { return nsh >= 0 ? g >> nsh : g / ns; };
+  const int gown = slot_of(G + ns - 1);
   {
     const uint32_t ebar_local = smem_u32(&fs.ebar);
 #pragma unroll
@@ -1091,7 +1095,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       for (int hh = 0; hh < 2; ++hh) {
         const int g = 8 * ht + 2 * t4 + hh;
         if (g < G) {
-          const int owner = g % ns, gl = g / ns;
+          const int owner = own_of(g), gl = slot_of(g);
           const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
           const uint32_t bar = mapa(ebar_local, owner);
           st_async_f32(base + 4u * (16 * warp + g4), acc[ht][hh], bar);
@@ -1100,7 +1104,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       }
     }
     if (tid < G) {
-      const int owner = tid % ns, gl = tid / ns;
+      const int owner = own_of(tid), gl = slot_of(tid);
       const uint32_t base = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
       st_async_v2f32(base + 4u * HD, fs.mrun[tid], fs.lrun[tid], mapa(ebar_local, owner));
     }
@@ -1182,6 +1186,7 @@ bool hsa_plan(HsaArgs& a) {
   ns = std::min(ns, 8);
   ns = std::min(ns, a.k2e);
   a.ns = std::max(ns, 1);
+  a.ns_shift = (a.ns & (a.ns - 1)) == 0 ? __builtin_ctz((unsigned)a.ns) : -1;
   a.chunk = (a.k2e + a.ns - 1) / a.ns;
   a.slots_round = std::max(1, std::min(a.chunk, MAX_ROUND_ROWS / a.blk));
   const int nblk8 = (a.nblk + 7) & ~7;
