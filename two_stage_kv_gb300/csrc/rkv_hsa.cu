@@ -251,20 +251,18 @@ __device__ void topk_list(float* vals, int n, int k, float mn, float mx, uint8_t
       return bk > bb || (bk == bb && (need == m || flag[j] != 0));
     };
     if (n <= 2 * NT) {
-      // thread t lists blocks 2t and 2t+1: one block-wide scan
+      // thread t lists blocks 2t and 2t+1: in-warp positions from two ballots,
+      // warp offsets from one exchange
       const bool f0 = chosen(2 * tid), f1 = chosen(2 * tid + 1);
-      const int cnt = (int)f0 + (int)f1;
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (lane == 31) fs.wsum[warp] = incl;
+      const unsigned b0 = __ballot_sync(0xffffffffu, f0), b1 = __ballot_sync(0xffffffffu, f1);
+      const unsigned lt = (1u << lane) - 1u;
+      if (lane == 0) fs.wsum[warp] = __popc(b0) + __popc(b1);
       __syncthreads();
-      int pre = incl - cnt;
-#pragma unroll
-      for (int w = 0; w < NWARP; ++w) pre += w < warp ? fs.wsum[w] : 0;
+      const int4 w0 = *reinterpret_cast<const int4*>(&fs.wsum[0]);
+      const int4 w1 = *reinterpret_cast<const int4*>(&fs.wsum[4]);
+      const int pre = __popc(b0 & lt) + __popc(b1 & lt) + (warp > 0 ? w0.x : 0) + (warp > 1 ? w0.y : 0) +
+                      (warp > 2 ? w0.z : 0) + (warp > 3 ? w0.w : 0) + (warp > 4 ? w1.x : 0) + (warp > 5 ? w1.y : 0) +
+                      (warp > 6 ? w1.z : 0);
       if (f0 && pre < k) sel[pre] = 2 * tid;
       if (f1 && pre + (int)f0 < k) sel[pre + (int)f0] = 2 * tid + 1;
     } else {
