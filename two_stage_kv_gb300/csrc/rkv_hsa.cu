@@ -189,12 +189,21 @@ __device__ void topk_list(float* vals, int n, int k, float mn, float mx, uint8_t
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float width = mx - mn;
   bool fallback = !(width > 0.f) || !isfinite(width);
-  const float inv = fallback ? 0.f : (float)NBUCKET / width;
+  // (any monotone map of the scores to buckets gives the same exact selection,
+  // so the scale need not be correctly rounded)
+  const float inv = fallback ? 0.f : __fdividef((float)NBUCKET, width);
   // (clamped at both ends: -inf / +inf entries of the masked multi-turn reading)
   auto bucket = [&](float s) { return max(0, min(NBUCKET - 1, (int)((s - mn) * inv))); };
   int bb = 0, need = 0, m = 0;
   if (!fallback) {
-    for (int j = tid; j < n; j += NT) atomicAdd(&fs.hist[bucket(vals[j])], 1);
+    if (n <= 2 * NT) {
+      // both of this thread's scores read before either count is added
+      const float v0 = tid < n ? vals[tid] : 0.f, v1 = tid + NT < n ? vals[tid + NT] : 0.f;
+      if (tid < n) atomicAdd(&fs.hist[bucket(v0)], 1);
+      if (tid + NT < n) atomicAdd(&fs.hist[bucket(v1)], 1);
+    } else {
+      for (int j = tid; j < n; j += NT) atomicAdd(&fs.hist[bucket(vals[j])], 1);
+    }
     __syncthreads();
     // lane l holds buckets 8l .. 8l+7; counts from the top bucket down
     const int4 h0 = *reinterpret_cast<const int4*>(&fs.hist[8 * lane]);
