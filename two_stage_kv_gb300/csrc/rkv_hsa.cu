@@ -1148,7 +1148,10 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         A = fmaf(f, vr[r], A);
         L = fmaf(f, lr[r], L);
       }
-      a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = F8 ? (A / L) * v_sc : A / L;
+      // (L >= 1: the partial holding the maximum contributes exp2(0); a fast
+      // divide is within 2 ulp and keeps the IEEE divide off the launch's tail)
+      const float y = __fdividef(A, L);
+      a.out[((size_t)b * a.Hq + (size_t)hk * G + g) * HD + tid] = F8 ? y * v_sc : y;
     }
   }
   if (own_new && !spec) {
