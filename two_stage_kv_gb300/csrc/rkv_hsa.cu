@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     fs.lrun[tid] = 0.f;
   }
   // every CTA of the cluster must have started before a DSMEM store reaches it;
-  // the matching wait precedes the first remote store (phase E)
+  // the matching wait (start of phase B) precedes the first remote store (phase B)
   cluster_arrive_relaxed();
   pdl_wait();
   pdl_launch_dependents();
