@@ -9,7 +9,7 @@ import torch
 import oracle
 from parity_util import ATOL_OUT, check_topk, max_abs, t2bits, t2f64
 from two_stage_kv_gb300 import rkv
-from two_stage_kv_gb300.synth import bf16_bits_to_f64, small_random
+from two_stage_kv_gb300.synth import bf16_bits_to_f32, bf16_bits_to_f64, f32_to_bf16_bits, small_random
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -222,6 +222,35 @@ def test_hsa_decode_crowded_boundary_bucket():
         kb[:, :, :16, :] = 0x42C8            # bf16 100.0
         return kb
     _hsa_case(12, 1, 32, 8, 700 * 16, 16, 32, 50, k_scale=1e-3, kmod=kmod)
+
+
+@pytest.mark.parametrize("Hq,k1", [(32, 32), (32, 20), (64, 64)])
+def test_hsa_decode_channel_partial_ties(Hq, k1):
+    """Queries drawn from {-2, ..., 2}: the group sums of |q| fall in a few values,
+    so large groups of channels tie across the k1-th place (the lower channel
+    index must win), and some group sums of q are exactly zero (the sign rule
+    picks Kmax).  The channel set must equal the oracle's exactly."""
+    def qmod(qb):
+        r = np.random.default_rng(5 + Hq + k1)
+        return f32_to_bf16_bits(r.integers(-2, 3, qb.shape).astype(np.float32))
+    _hsa_case(13 + k1, 2, Hq, 8, 900, 16, k1, 12, qmod=qmod)
+
+
+def test_hsa_decode_split_boundary_bucket():
+    """Blocks 10-19 hold the same large keys, so their scores tie exactly and are
+    the ten largest, alone in the top histogram bucket; k2 = 5 takes half of that
+    bucket, which sends the selection through the pairwise ranking of its
+    members.  Ties must go to the lower block index: no tie-band exemption."""
+    blk = 16
+
+    def kmod(kb):
+        kb = kb.copy()
+        big = f32_to_bf16_bits(bf16_bits_to_f32(kb[:, :, 3 * blk:4 * blk, :]) * np.float32(4))
+        for j in range(10, 20):
+            kb[:, :, j * blk:(j + 1) * blk, :] = big
+        return kb
+    _, exempt = _hsa_case(14, 1, 32, 8, 700, blk, 32, 5, kmod=kmod)
+    assert exempt == 0
 
 
 @pytest.mark.parametrize("append", [False, True])
