@@ -633,8 +633,23 @@ __global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled
 // memory.  Same result as snap_pool + snap_select.
 constexpr int PS_NT = 1024;
 constexpr int PS_MAX_WORDS = 54 * 1024;        // padded shared words (216 KB)
+constexpr int PS_NB = 1024;                     // buckets of the bucket select
+constexpr int PS_MAXM = 1024;                   // members of a split bucket ranked pairwise
 
 __device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }   // one pad word per 32: no bank conflicts
+
+// shared words of the padded keys for prefix length L and half window h
+__host__ __device__ inline int ps_key_words(int64_t L, int h) {
+  const int E = h + 1;
+  const int64_t nq = (L + E - 1) / E;
+  const int64_t U = nq * E + 2 * E;
+  return (int)(((U + U / 32 + 1) + 3) & ~3);
+}
+// extra words of the bucket select: counters, taken-bit map, (key, position) members
+__host__ __device__ inline int ps_bucket_words(int64_t L) {
+  const int64_t bm = (L + 31) >> 5;
+  return (int)(PS_NB + ((bm + 1) & ~1) + 2 * PS_MAXM);
+}
 
 // shared words needed for prefix length L and half window h (0 if the fused path does not apply)
 int pool_select_words(int64_t L, int h) {
@@ -644,7 +659,10 @@ int pool_select_words(int64_t L, int h) {
   if (nq > PS_NT) return 0;
   const int64_t U = nq * E + 2 * E;
   const int64_t words = U + U / 32 + 1;
-  return words <= PS_MAX_WORDS ? (int)words : 0;
+  if (words > PS_MAX_WORDS) return 0;
+  // room for the bucket select past the keys when it fits (the kernel checks)
+  const int64_t with_bucket = (int64_t)ps_key_words(L, h) + ps_bucket_words(L);
+  return with_bucket <= PS_MAX_WORDS ? (int)with_bucket : (int)words;
 }
 
 __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float* scores, int RG, int64_t L64,
@@ -654,8 +672,9 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
   extern __shared__ __align__(16) uint32_t xs[];
   __shared__ int hist[256];
   __shared__ int wsum[PS_NT / 32];
+  __shared__ uint32_t wmin_s[PS_NT / 32], wmax_s[PS_NT / 32];
   __shared__ uint32_t sh_digit;
-  __shared__ int sh_k;
+  __shared__ int sh_k, sh_bb, sh_need, sh_m, sh_cnt;
   pdl_wait();
   pdl_launch_dependents();
   const int pair = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -726,12 +745,19 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
   }
   __syncthreads();
   // keys of the candidates [n_sink, L) replace the scores; 0 elsewhere
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
   if (mine) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (i < E) {
         const int j = a + i;
-        xs[ps_pad(j)] = (j >= n_sink && j < L) ? f2key(pv[i]) : 0u;
+        const bool cand = j >= n_sink && j < L;
+        const uint32_t key = cand ? f2key(pv[i]) : 0u;
+        xs[ps_pad(j)] = key;
+        if (cand) {
+          kmn = min(kmn, key);
+          kmx = max(kmx, key);
+        }
       }
     }
   }
@@ -740,11 +766,150 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
     for (int j = n_sink + tid; j < L; j += PS_NT) out[j] = j;
     return;
   }
+
+  // Bucket select.  The candidates' pooled log2 scores span [vlo, vhi];
+  // bucket = floor((v - vlo) * PS_NB / (vhi - vlo)), clamped: a monotone map of
+  // the value, so of the key.  One histogram finds the bucket that
+  // holds the ntop-th largest key; the buckets above it are taken, and that
+  // bucket's members are ranked pairwise (larger key first, equal keys by
+  // position) only when it is split.  Pooled scores form plateaus, so each
+  // thread counts runs of equal buckets along its own positions.  The counters,
+  // a taken-bit map and the members sit past the keys in the dynamic shared
+  // words when the launch gave room for them; otherwise, or when the split
+  // bucket has more than PS_MAXM members, the radix select below runs.
+  const int kwords = ps_key_words(L, h);
+  const int bm_words = (L + 31) >> 5;
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  bool use_radix = (uint32_t)(kwords + ps_bucket_words(L)) * 4u > dyn_bytes;
+  int k = (int)ntop;
+  if (!use_radix) {
+    uint32_t* hist_b = xs + kwords;                            // PS_NB counters
+    uint32_t* taken = hist_b + PS_NB;                          // bit j: position j of the split bucket is taken
+    uint2* memb = reinterpret_cast<uint2*>(taken + ((bm_words + 1) & ~1));   // (key, position) of its members
+    kmn = __reduce_min_sync(0xffffffffu, kmn);
+    kmx = __reduce_max_sync(0xffffffffu, kmx);
+    if (lane == 0) {
+      wmin_s[warp] = kmn;
+      wmax_s[warp] = kmx;
+    }
+    for (int i = tid; i < PS_NB + bm_words; i += PS_NT) hist_b[i] = 0u;
+    if (tid == 0) sh_cnt = 0;
+    __syncthreads();
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int w = 0; w < PS_NT / 32; ++w) {
+      lo = min(lo, wmin_s[w]);
+      hi = max(hi, wmax_s[w]);
+    }
+    // the value of a key (inverse of f2key); equal or non-finite ranges take the radix path
+    auto kval = [](uint32_t key) { return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key); };
+    const float vlo = kval(lo), width = kval(hi) - vlo;
+    const float inv = (width > 0.f && isfinite(width)) ? __fdividef((float)PS_NB, width) : 0.f;
+    auto bucket = [&](uint32_t key) { return max(0, min(PS_NB - 1, (int)((kval(key) - vlo) * inv))); };
+    if (inv == 0.f) use_radix = true;                          // the same in every thread
+    const int cnt_i = mine ? max(0, min(E, L - a)) : 0;       // this thread's positions [a, a + cnt_i)
+    const int i_lo = mine ? max(0, n_sink - a) : 0;           // candidates start at n_sink
+    if (!use_radix) {
+    // histogram: one count per run of equal buckets along this thread's positions
+    {
+      int prev = -1, run = 0;
+      for (int i = i_lo; i < cnt_i; ++i) {
+        const int bk = bucket(xs[ps_pad(a + i)]);
+        if (bk == prev) {
+          ++run;
+        } else {
+          if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
+          prev = bk;
+          run = 1;
+        }
+      }
+      if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds buckets 32l .. 32l+31; counts from the top bucket down
+      const uint4* h4 = reinterpret_cast<const uint4*>(&hist_b[32 * lane]);
+      uint32_t sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = h4[q];
+        sum += v.x + v.y + v.z + v.w;
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      uint32_t above = incl - sum;
+      if (above < (uint32_t)k && incl >= (uint32_t)k) {
+        // the crossing is in this lane's buckets (exactly one lane)
+        for (int q = 7; q >= 0; --q) {
+          const uint4 v = h4[q];
+          const uint32_t c4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int u = 3; u >= 0; --u) {
+            if (above < (uint32_t)k && above + c4[u] >= (uint32_t)k) {
+              sh_bb = 32 * lane + 4 * q + u;
+              sh_need = (int)((uint32_t)k - above);
+              sh_m = (int)c4[u];
+            }
+            above += c4[u];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const int bb = sh_bb, need = sh_need, m = sh_m;
+    if (need < m && m > PS_MAXM) use_radix = true;           // the same in every thread
+    if (!use_radix) {
+      if (need < m) {
+        // collect and rank the split bucket's members; the taken ones set their bit
+        for (int i = i_lo; i < cnt_i; ++i) {
+          const uint32_t key = xs[ps_pad(a + i)];
+          if (bucket(key) == bb) memb[atomicAdd(&sh_cnt, 1)] = make_uint2(key, (uint32_t)(a + i));
+        }
+        __syncthreads();
+        for (int t = tid; t < m; t += PS_NT) {
+          const uint2 me = memb[t];
+          int rk = 0;
+          for (int u = 0; u < m; ++u) {
+            const uint2 o = memb[u];
+            rk += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+          }
+          if (rk < need) atomicOr(&taken[me.y >> 5], 1u << (me.y & 31));
+        }
+        __syncthreads();
+      }
+      // ascending write-out of the taken positions
+      uint32_t tk = 0;
+      for (int i = i_lo; i < cnt_i; ++i) {
+        const int j = a + i;
+        const int bk = bucket(xs[ps_pad(j)]);
+        if (bk > bb || (bk == bb && (need == m || ((taken[j >> 5] >> (j & 31)) & 1u)))) tk |= 1u << i;
+      }
+      const uint32_t cnt = (uint32_t)__popc(tk);
+      uint32_t inc = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (lane == 31) wsum[warp] = (int)inc;
+      __syncthreads();
+      int pos = n_sink + (int)(inc - cnt);
+      for (int w = 0; w < warp; ++w) pos += wsum[w];
+      for (uint32_t bits = tk; bits; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
+      return;
+    }
+    }
+  }
   __syncthreads();
 
   // radix select of the ntop-th largest key, 8 bits at a time from the top
   uint32_t prefix = 0, mask = 0;
-  int k = (int)ntop;
+  k = (int)ntop;
   for (int shift = 24; shift >= 0; shift -= 8) {
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
