@@ -549,6 +549,13 @@ def test_snap_evict_parity(B, Hq, Hkv, S, W, P, B1, sink):
     _snap_case(500 + S, B, Hq, Hkv, S, W, P, B1, sink)
 
 
+def test_snap_evict_all_scores_tied():
+    """Zero window queries: every prefix key gets the same score, so the pooled
+    scores have an empty range and the select takes its radix path; the kept
+    prefix positions must be the lowest ones (no tie-band exemption)."""
+    assert _snap_case(31, 2, 32, 8, 5000, 32, 63, 700, q_scale=0.0) == 0
+
+
 def test_snap_evict_mask_mode_and_peaked():
     _snap_case(9, 1, 32, 8, 3000, 32, 63, 400, compact=False, q_scale=4.0)
 
