@@ -491,7 +491,7 @@ def test_hsa_decode_deterministic():
 # ----------------------------------------------------------------- stage 1 --
 
 
-def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0, compact=True):
+def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0, compact=True, qmod=None):
     D = 128
     G = Hq // Hkv
     dims = (B, Hq, Hkv, D)
@@ -500,6 +500,9 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
     kb, k = _rand(seed, (B, Hkv, cap, D))
     vb, v = _rand(seed + 1, (B, Hkv, cap, D))
     qb, q = _rand(seed + 2, (B, Hq, W, D), q_scale)
+    if qmod is not None:
+        qb = qmod(qb, kb)
+        q = _bf16(qb)
     keep = torch.full((B, Hkv, B1 + 2), -5, dtype=torch.int32, device=DEV)
     ko = torch.empty((B, Hkv, B1 + 1, D), dtype=torch.bfloat16, device=DEV) if compact else None
     vo = torch.empty_like(ko) if compact else None
@@ -554,6 +557,22 @@ def test_snap_evict_all_scores_tied():
     scores have an empty range and the select takes its radix path; the kept
     prefix positions must be the lowest ones (no tie-band exemption)."""
     assert _snap_case(31, 2, 32, 8, 5000, 32, 63, 700, q_scale=0.0) == 0
+
+
+def test_snap_evict_crowded_boundary_bucket():
+    """Window queries zero except one row per group, twice key 5: that key's
+    score spans the range and every other pooled score lies within a sliver
+    of the minimum, so the 1024-bucket histogram puts thousands of candidates
+    in the boundary bucket and the select falls back to its radix path."""
+    G = 32 // 8
+
+    def qmod(qb, kb):
+        qb = np.zeros_like(qb)
+        for b in range(qb.shape[0]):
+            for h in range(8):
+                qb[b, h * G, 0] = f32_to_bf16_bits(bf16_bits_to_f32(kb[b, h, 5]) * np.float32(2.0))
+        return qb
+    _snap_case(41, 1, 32, 8, 5000, 32, 63, 700, qmod=qmod)
 
 
 def test_snap_evict_mask_mode_and_peaked():
