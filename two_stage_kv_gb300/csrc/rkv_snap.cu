@@ -811,98 +811,98 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
     const int cnt_i = mine ? max(0, min(E, L - a)) : 0;       // this thread's positions [a, a + cnt_i)
     const int i_lo = mine ? max(0, n_sink - a) : 0;           // candidates start at n_sink
     if (!use_radix) {
-    // histogram: one count per run of equal buckets along this thread's positions
-    {
-      int prev = -1, run = 0;
-      for (int i = i_lo; i < cnt_i; ++i) {
-        const int bk = bucket(xs[ps_pad(a + i)]);
-        if (bk == prev) {
-          ++run;
-        } else {
-          if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
-          prev = bk;
-          run = 1;
-        }
-      }
-      if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l holds buckets 32l .. 32l+31; counts from the top bucket down
-      const uint4* h4 = reinterpret_cast<const uint4*>(&hist_b[32 * lane]);
-      uint32_t sum = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 v = h4[q];
-        sum += v.x + v.y + v.z + v.w;
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += t;
-      }
-      uint32_t above = incl - sum;
-      if (above < (uint32_t)k && incl >= (uint32_t)k) {
-        // the crossing is in this lane's buckets (exactly one lane)
-        for (int q = 7; q >= 0; --q) {
-          const uint4 v = h4[q];
-          const uint32_t c4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int u = 3; u >= 0; --u) {
-            if (above < (uint32_t)k && above + c4[u] >= (uint32_t)k) {
-              sh_bb = 32 * lane + 4 * q + u;
-              sh_need = (int)((uint32_t)k - above);
-              sh_m = (int)c4[u];
-            }
-            above += c4[u];
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int bb = sh_bb, need = sh_need, m = sh_m;
-    if (need < m && m > PS_MAXM) use_radix = true;           // the same in every thread
-    if (!use_radix) {
-      if (need < m) {
-        // collect and rank the split bucket's members; the taken ones set their bit
+      // histogram: one count per run of equal buckets along this thread's positions
+      {
+        int prev = -1, run = 0;
         for (int i = i_lo; i < cnt_i; ++i) {
-          const uint32_t key = xs[ps_pad(a + i)];
-          if (bucket(key) == bb) memb[atomicAdd(&sh_cnt, 1)] = make_uint2(key, (uint32_t)(a + i));
-        }
-        __syncthreads();
-        for (int t = tid; t < m; t += PS_NT) {
-          const uint2 me = memb[t];
-          int rk = 0;
-          for (int u = 0; u < m; ++u) {
-            const uint2 o = memb[u];
-            rk += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+          const int bk = bucket(xs[ps_pad(a + i)]);
+          if (bk == prev) {
+            ++run;
+          } else {
+            if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
+            prev = bk;
+            run = 1;
           }
-          if (rk < need) atomicOr(&taken[me.y >> 5], 1u << (me.y & 31));
         }
-        __syncthreads();
+        if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
       }
-      // ascending write-out of the taken positions
-      uint32_t tk = 0;
-      for (int i = i_lo; i < cnt_i; ++i) {
-        const int j = a + i;
-        const int bk = bucket(xs[ps_pad(j)]);
-        if (bk > bb || (bk == bb && (need == m || ((taken[j >> 5] >> (j & 31)) & 1u)))) tk |= 1u << i;
-      }
-      const uint32_t cnt = (uint32_t)__popc(tk);
-      uint32_t inc = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += t;
-      }
-      if (lane == 31) wsum[warp] = (int)inc;
       __syncthreads();
-      int pos = n_sink + (int)(inc - cnt);
-      for (int w = 0; w < warp; ++w) pos += wsum[w];
-      for (uint32_t bits = tk; bits; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
-      return;
-    }
+      if (warp == 0) {
+        // lane l holds buckets 32l .. 32l+31; counts from the top bucket down
+        const uint4* h4 = reinterpret_cast<const uint4*>(&hist_b[32 * lane]);
+        uint32_t sum = 0;
+  #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = h4[q];
+          sum += v.x + v.y + v.z + v.w;
+        }
+        uint32_t incl = sum;
+  #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
+          if (lane + o < 32) incl += t;
+        }
+        uint32_t above = incl - sum;
+        if (above < (uint32_t)k && incl >= (uint32_t)k) {
+          // the crossing is in this lane's buckets (exactly one lane)
+          for (int q = 7; q >= 0; --q) {
+            const uint4 v = h4[q];
+            const uint32_t c4[4] = {v.x, v.y, v.z, v.w};
+  #pragma unroll
+            for (int u = 3; u >= 0; --u) {
+              if (above < (uint32_t)k && above + c4[u] >= (uint32_t)k) {
+                sh_bb = 32 * lane + 4 * q + u;
+                sh_need = (int)((uint32_t)k - above);
+                sh_m = (int)c4[u];
+              }
+              above += c4[u];
+            }
+          }
+        }
+      }
+      __syncthreads();
+      const int bb = sh_bb, need = sh_need, m = sh_m;
+      if (need < m && m > PS_MAXM) use_radix = true;           // the same in every thread
+      if (!use_radix) {
+        if (need < m) {
+          // collect and rank the split bucket's members; the taken ones set their bit
+          for (int i = i_lo; i < cnt_i; ++i) {
+            const uint32_t key = xs[ps_pad(a + i)];
+            if (bucket(key) == bb) memb[atomicAdd(&sh_cnt, 1)] = make_uint2(key, (uint32_t)(a + i));
+          }
+          __syncthreads();
+          for (int t = tid; t < m; t += PS_NT) {
+            const uint2 me = memb[t];
+            int rk = 0;
+            for (int u = 0; u < m; ++u) {
+              const uint2 o = memb[u];
+              rk += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+            }
+            if (rk < need) atomicOr(&taken[me.y >> 5], 1u << (me.y & 31));
+          }
+          __syncthreads();
+        }
+        // ascending write-out of the taken positions
+        uint32_t tk = 0;
+        for (int i = i_lo; i < cnt_i; ++i) {
+          const int j = a + i;
+          const int bk = bucket(xs[ps_pad(j)]);
+          if (bk > bb || (bk == bb && (need == m || ((taken[j >> 5] >> (j & 31)) & 1u)))) tk |= 1u << i;
+        }
+        const uint32_t cnt = (uint32_t)__popc(tk);
+        uint32_t inc = cnt;
+  #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += t;
+        }
+        if (lane == 31) wsum[warp] = (int)inc;
+        __syncthreads();
+        int pos = n_sink + (int)(inc - cnt);
+        for (int w = 0; w < warp; ++w) pos += wsum[w];
+        for (uint32_t bits = tk; bits; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
+        return;
+      }
     }
   }
   __syncthreads();
