@@ -313,7 +313,7 @@ __device__ void topk_list(float* vals, int n, int k, float mn, float mx, uint8_t
 // F8: k, v and kt hold e4m3 codes (value = code * the pair's scale); the
 // bounds and scores are on code values, attention dequantizes through the
 // logit and output scales.
-template <bool MT, int NH, bool RAG, bool PG, bool MK = false, bool F8 = false>
+template <bool MT, int NH, bool RAG, bool PG, bool MK = false, bool F8 = false, bool WF = false>
 __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                            const __grid_constant__ CUtensorMap tmV,
                                                            const __grid_constant__ CUtensorMap tmKT,
@@ -795,6 +795,17 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   for (int ht = 0; ht < NH; ++ht)
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[ht][e] = accl[ht][e] = 0.f;
+  // With several staging rounds per CTA (WF, narrow groups) every warp instead
+  // runs its own online softmax over its own 16-token steps and accumulates O^T
+  // over all 128 dimensions (acc8[dt]: dims 16*dt + lane/4 (+8), heads
+  // 2*(lane%4) + {0, 1}); the CTA merges the eight warp partials once, after the
+  // last round, so a round needs only its closing barrier.  Each warp reads only
+  // its own K and V rows.
+  constexpr bool WARP_FLASH = WF && NH == 1;
+  float acc8[WARP_FLASH ? 8 : 1][4];
+  float wm[2] = {neg_inf(), neg_inf()}, wl[2] = {0.f, 0.f};   // this warp's heads 2*(lane%4) + {0, 1}
+#pragma unroll
+  for (int i = 0; i < (WARP_FLASH ? 8 : 1); ++i) acc8[i][0] = acc8[i][1] = acc8[i][2] = acc8[i][3] = 0.f;
 
   const int chunk = RAG ? (k2e + ns - 1) / ns : a.chunk;   // blocks per CTA (at most the plan's chunk)
   const int s_lo = (int)rank * chunk;
@@ -982,98 +993,149 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           x[ht][e] = ((e < 2) ? va : vb) ? sv : neg_inf();
         }
     }
-    // --- CTA-wide head maxima of this round
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht) {
-      float m0 = fmaxf(x[ht][0], x[ht][2]), m1 = fmaxf(x[ht][1], x[ht][3]);
+    if constexpr (WARP_FLASH) {
+      // --- this warp's head maxima and probability sums (x = -inf off its step)
+      float m0 = fmaxf(x[0][0], x[0][2]), m1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
         m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
       }
-      if (g4 == 0) {
-        fs.wmaxh[warp][8 * ht + 2 * t4] = m0;
-        fs.wmaxh[warp][8 * ht + 2 * t4 + 1] = m1;
-      }
-    }
-    __syncthreads();
-    float mnew[NH][2], corr[NH][2];
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int h = 8 * ht + 2 * t4 + hh;
-        float m = fs.mrun[h];
-#pragma unroll
-        for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][h]);
-        const float mo = fs.mrun[h];
-        mnew[ht][hh] = m;
-        corr[ht][hh] = (mo == neg_inf()) ? 0.f : exp2f(mo - m);
-      }
-    // --- probabilities, their head sums, and P^T fragments for every warp
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht) {
+      const float mn0 = fmaxf(wm[0], m0), mn1 = fmaxf(wm[1], m1);
+      const float cr0 = (wm[0] == neg_inf()) ? 0.f : exp2f(wm[0] - mn0);
+      const float cr1 = (wm[1] == neg_inf()) ? 0.f : exp2f(wm[1] - mn1);
       float p[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) p[e] = (x[ht][e] == neg_inf()) ? 0.f : exp2f(x[ht][e] - mnew[ht][e & 1]);
+      for (int e = 0; e < 4; ++e) p[e] = (x[0][e] == neg_inf()) ? 0.f : exp2f(x[0][e] - ((e & 1) ? mn1 : mn0));
       float s0 = p[0] + p[2], s1 = p[1] + p[3];
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         s0 += __shfl_xor_sync(0xffffffffu, s0, o);
         s1 += __shfl_xor_sync(0xffffffffu, s1, o);
       }
-      if (g4 == 0) {
-        fs.wsumh[warp][8 * ht + 2 * t4] = s0;
-        fs.wsumh[warp][8 * ht + 2 * t4 + 1] = s1;
+      wl[0] = wl[0] * cr0 + s0;
+      wl[1] = wl[1] * cr1 + s1;
+      wm[0] = mn0;
+      wm[1] = mn1;
+#pragma unroll
+      for (int dt = 0; dt < 8; ++dt) {
+        acc8[dt][0] *= cr0;
+        acc8[dt][1] *= cr1;
+        acc8[dt][2] *= cr0;
+        acc8[dt][3] *= cr1;
       }
       if (has_step) {
+        // --- O^T (all 128 dims) += V^T P^T over this warp's 16 tokens; P^T as the
+        // B operand straight from registers (hi + lo bf16 parts)
         const uint32_t h0 = pack_bf16(p[0], p[1]), h1 = pack_bf16(p[2], p[3]);
         const uint32_t l0 = pack_bf16(p[0] - bf16_lo(h0), p[1] - bf16_hi(h0));
         const uint32_t l1 = pack_bf16(p[2] - bf16_lo(h1), p[3] - bf16_hi(h1));
-        uint32_t* pf = &fs.pfrag[warp][ht][0][0];
-        pf[0 * 32 + lane] = movmatrix_trans(h0);
-        pf[1 * 32 + lane] = movmatrix_trans(h1);
-        pf[2 * 32 + lane] = movmatrix_trans(l0);
-        pf[3 * 32 + lane] = movmatrix_trans(l1);
+        const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
+        const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+        const int r = c0 + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+          const int ch = 2 * dt + ((lane >> 3) & 1);
+          uint32_t va4[4];
+          ldsm_x4_t(smem_u32(tV) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), va4[0], va4[1], va4[2], va4[3]);
+          mma_bf16(acc8[dt], va4, bh0, bh1);
+          mma_bf16(acc8[dt], va4, bl0, bl1);
+        }
       }
-    }
-    __syncthreads();
-    // --- running max / sum (threads < 16 keep the CTA copy) and rescale
-    if (tid < 16) {
-      float m = fs.mrun[tid];
-#pragma unroll
-      for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][tid]);
-      const float c = (fs.mrun[tid] == neg_inf()) ? 0.f : exp2f(fs.mrun[tid] - m);
-      float l = fs.lrun[tid] * c;
-#pragma unroll
-      for (int w = 0; w < NWARP; ++w) l += fs.wsumh[w][tid];
-      fs.lrun[tid] = l;
-      fs.mrun[tid] = m;
-    }
-#pragma unroll
-    for (int ht = 0; ht < NH; ++ht) {
-      acc[ht][0] *= corr[ht][0];
-      acc[ht][1] *= corr[ht][1];
-      acc[ht][2] *= corr[ht][0];
-      acc[ht][3] *= corr[ht][1];
-      if (SPLIT) {
-        accl[ht][0] *= corr[ht][0];
-        accl[ht][1] *= corr[ht][1];
-        accl[ht][2] *= corr[ht][0];
-        accl[ht][3] *= corr[ht][1];
-      }
-    }
-    // --- O^T (dims 16*warp .. +15) += V^T P^T over every 16-token step of the round
-    for (int cs = 0; cs < nsteps; ++cs) {
-      const int r = cs * 16 + (lane & 7) + (lane >> 4) * 8;
-      const int ch = 2 * warp + ((lane >> 3) & 1);
-      uint32_t va4[4];
-      ldsm_x4_t(smem_u32(tV) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), va4[0], va4[1], va4[2], va4[3]);
-#pragma unroll
+    } else {
+      // --- CTA-wide head maxima of this round
+  #pragma unroll
       for (int ht = 0; ht < NH; ++ht) {
-        const uint32_t* pf = &fs.pfrag[cs][ht][0][0];
-        mma_bf16(acc[ht], va4, pf[0 * 32 + lane], pf[1 * 32 + lane]);
-        mma_bf16(SPLIT ? accl[ht] : acc[ht], va4, pf[2 * 32 + lane], pf[3 * 32 + lane]);
+        float m0 = fmaxf(x[ht][0], x[ht][2]), m1 = fmaxf(x[ht][1], x[ht][3]);
+  #pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        }
+        if (g4 == 0) {
+          fs.wmaxh[warp][8 * ht + 2 * t4] = m0;
+          fs.wmaxh[warp][8 * ht + 2 * t4 + 1] = m1;
+        }
+      }
+      __syncthreads();
+      float mnew[NH][2], corr[NH][2];
+  #pragma unroll
+      for (int ht = 0; ht < NH; ++ht)
+  #pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = 8 * ht + 2 * t4 + hh;
+          float m = fs.mrun[h];
+  #pragma unroll
+          for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][h]);
+          const float mo = fs.mrun[h];
+          mnew[ht][hh] = m;
+          corr[ht][hh] = (mo == neg_inf()) ? 0.f : exp2f(mo - m);
+        }
+      // --- probabilities, their head sums, and P^T fragments for every warp
+  #pragma unroll
+      for (int ht = 0; ht < NH; ++ht) {
+        float p[4];
+  #pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = (x[ht][e] == neg_inf()) ? 0.f : exp2f(x[ht][e] - mnew[ht][e & 1]);
+        float s0 = p[0] + p[2], s1 = p[1] + p[3];
+  #pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (g4 == 0) {
+          fs.wsumh[warp][8 * ht + 2 * t4] = s0;
+          fs.wsumh[warp][8 * ht + 2 * t4 + 1] = s1;
+        }
+        if (has_step) {
+          const uint32_t h0 = pack_bf16(p[0], p[1]), h1 = pack_bf16(p[2], p[3]);
+          const uint32_t l0 = pack_bf16(p[0] - bf16_lo(h0), p[1] - bf16_hi(h0));
+          const uint32_t l1 = pack_bf16(p[2] - bf16_lo(h1), p[3] - bf16_hi(h1));
+          uint32_t* pf = &fs.pfrag[warp][ht][0][0];
+          pf[0 * 32 + lane] = movmatrix_trans(h0);
+          pf[1 * 32 + lane] = movmatrix_trans(h1);
+          pf[2 * 32 + lane] = movmatrix_trans(l0);
+          pf[3 * 32 + lane] = movmatrix_trans(l1);
+        }
+      }
+      __syncthreads();
+      // --- running max / sum (threads < 16 keep the CTA copy) and rescale
+      if (tid < 16) {
+        float m = fs.mrun[tid];
+  #pragma unroll
+        for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][tid]);
+        const float c = (fs.mrun[tid] == neg_inf()) ? 0.f : exp2f(fs.mrun[tid] - m);
+        float l = fs.lrun[tid] * c;
+  #pragma unroll
+        for (int w = 0; w < NWARP; ++w) l += fs.wsumh[w][tid];
+        fs.lrun[tid] = l;
+        fs.mrun[tid] = m;
+      }
+  #pragma unroll
+      for (int ht = 0; ht < NH; ++ht) {
+        acc[ht][0] *= corr[ht][0];
+        acc[ht][1] *= corr[ht][1];
+        acc[ht][2] *= corr[ht][0];
+        acc[ht][3] *= corr[ht][1];
+        if (SPLIT) {
+          accl[ht][0] *= corr[ht][0];
+          accl[ht][1] *= corr[ht][1];
+          accl[ht][2] *= corr[ht][0];
+          accl[ht][3] *= corr[ht][1];
+        }
+      }
+      // --- O^T (dims 16*warp .. +15) += V^T P^T over every 16-token step of the round
+      for (int cs = 0; cs < nsteps; ++cs) {
+        const int r = cs * 16 + (lane & 7) + (lane >> 4) * 8;
+        const int ch = 2 * warp + ((lane >> 3) & 1);
+        uint32_t va4[4];
+        ldsm_x4_t(smem_u32(tV) + (uint32_t)(ch >> 3) * half + swz128(r, ch & 7), va4[0], va4[1], va4[2], va4[3]);
+  #pragma unroll
+        for (int ht = 0; ht < NH; ++ht) {
+          const uint32_t* pf = &fs.pfrag[cs][ht][0][0];
+          mma_bf16(acc[ht], va4, pf[0 * 32 + lane], pf[1 * 32 + lane]);
+          mma_bf16(SPLIT ? accl[ht] : acc[ht], va4, pf[2 * 32 + lane], pf[3 * 32 + lane]);
+        }
       }
     }
     phase ^= 1u;
@@ -1094,7 +1156,66 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   auto own_of = [nsh, ns](int g) { return nsh >= 0 ? g & (ns - 1) : g % ns; };
   auto slot_of = [nsh, ns](int g) { return nsh >= 0 ? g >> nsh : g / ns; };
   const int gown = slot_of(G + ns - 1);
-  {
+  if constexpr (WARP_FLASH) {
+    // Warp w leaves its O^T in its own K rows (bytes [2048 w, 2048 w + 2048) of
+    // the lo half for dims 0-63, of the hi half for dims 64-127; no other warp
+    // reads those rows after the last round) as [dim][G] floats, so a lane's two
+    // heads are one 8-byte store and the merge reads consecutive words; its
+    // (max, sum) per head go to wmaxh / wsumh.
+    {
+      const int g0 = 2 * t4;
+#pragma unroll
+      for (int dt = 0; dt < 8; ++dt) {
+        float* rg = reinterpret_cast<float*>(tK + (dt < 4 ? 0u : half) + (uint32_t)warp * 2048u);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float* dst = rg + ((16 * dt + g4 + 8 * u) & 63) * G + g0;
+          if ((G & 1) == 0 && g0 + 1 < G) {
+            *reinterpret_cast<float2*>(dst) = make_float2(acc8[dt][2 * u], acc8[dt][2 * u + 1]);
+          } else {
+            if (g0 < G) dst[0] = acc8[dt][2 * u];
+            if (g0 + 1 < G) dst[1] = acc8[dt][2 * u + 1];
+          }
+        }
+      }
+      if (g4 == 0) {
+        fs.wmaxh[warp][2 * t4] = wm[0];
+        fs.wmaxh[warp][2 * t4 + 1] = wm[1];
+        fs.wsumh[warp][2 * t4] = wl[0];
+        fs.wsumh[warp][2 * t4 + 1] = wl[1];
+      }
+    }
+    __syncthreads();
+    const uint32_t ebar_local = smem_u32(&fs.ebar);
+    // thread t merges head g = t % G over dims t / G, t / G + NT / G, ...: the
+    // head's owner, remote address and warp weights are worked out once
+    const int gstep = NT / G;
+    if (tid < gstep * G) {
+      const int g = tid % G;
+      float fw[NWARP], M = neg_inf(), L = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) {
+        fw[w] = fs.wmaxh[w][g];
+        M = fmaxf(M, fw[w]);
+      }
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) {
+        fw[w] = fw[w] == neg_inf() ? 0.f : exp2f(fw[w] - M);   // a warp with no token of head g weighs 0
+        L = fmaf(fw[w], fs.wsumh[w][g], L);
+      }
+      const int owner = own_of(g), gl = slot_of(g);
+      const uint32_t rbase = mapa(smem_u32(recv + ((size_t)gl * ns + rank) * PART_STRIDE), owner);
+      const uint32_t rbar = mapa(ebar_local, owner);
+      for (int d = tid / G; d < HD; d += gstep) {
+        const float* og = reinterpret_cast<const float*>(tK + (d < 64 ? 0u : half)) + (d & 63) * G + g;
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) O = fmaf(fw[w], og[w * 512], O);
+        st_async_f32(rbase + 4u * d, O, rbar);
+      }
+      if (tid < G) st_async_v2f32(rbase + 4u * HD, M, L, rbar);
+    }
+  } else {
     const uint32_t ebar_local = smem_u32(&fs.ebar);
 #pragma unroll
     for (int ht = 0; ht < NH; ++ht) {
@@ -1199,6 +1320,10 @@ bool hsa_plan(HsaArgs& a) {
   a.ns_shift = (a.ns & (a.ns - 1)) == 0 ? __builtin_ctz((unsigned)a.ns) : -1;
   a.chunk = (a.k2e + a.ns - 1) / a.ns;
   a.slots_round = std::max(1, std::min(a.chunk, MAX_ROUND_ROWS / a.blk));
+  // several staging rounds per CTA on the plain streamed path with narrow groups:
+  // per-warp online softmax (one barrier per round instead of three)
+  a.wflash = (a.tma_kv && !a.f8 && !a.mask && !a.block_table && !a.n_rows && a.G <= 8 &&
+              a.chunk * a.blk > MAX_ROUND_ROWS) ? 1 : 0;
   const int nblk8 = (a.nblk + 7) & ~7;
   // blocks scored per CTA; with at most HSA_SPEC_MAX_COLS of them every KT row of
   // the CTA's blocks is prefetched at launch, otherwise the chosen rows are
@@ -1228,7 +1353,8 @@ bool hsa_plan(HsaArgs& a) {
   off = al(off + 4u * gown * a.ns * PART_STRIDE, 1024);
   a.off_tiles = off;                       // K/V tiles; the KT gather tile shares this region
   const uint32_t rows16 = al((uint32_t)(a.slots_round * a.blk), 16);
-  a.tile_half_bytes = rows16 * 128u;
+  // (per-warp softmax: every warp owns 16 rows of each half tile for its partial)
+  a.tile_half_bytes = a.wflash ? (uint32_t)MAX_ROUND_ROWS * 128u : rows16 * 128u;
   off += std::max(4u * a.tile_half_bytes, al(kt_tile_bytes, 16));
   a.smem_bytes = off + 1024u;   // room to align the base to 1024 bytes
   return a.smem_bytes <= 227u * 1024u;
@@ -1239,7 +1365,8 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    const void* ks[12] = {
+    const void* ks[13] = {
+        (const void*)hsa_decode_kernel<false, 1, false, false, false, false, true>,
         (const void*)hsa_decode_kernel<false, 1, false, false, false, true>,
         (const void*)hsa_decode_kernel<false, 2, false, false, false, true>,
         (const void*)hsa_decode_kernel<false, 1, false, false, true>,
@@ -1278,6 +1405,7 @@ cudaError_t hsa_launch(const HsaArgs& a, const CUtensorMap* tmK, const CUtensorM
                            : hsa_decode_kernel<false, 1, false, false, true>)
           : a.block_table ? (wide ? hsa_decode_kernel<false, 2, true, true> : hsa_decode_kernel<false, 1, true, true>)
           : a.n_rows ? (wide ? hsa_decode_kernel<false, 2, true, false> : hsa_decode_kernel<false, 1, true, false>)
+          : a.wflash ? hsa_decode_kernel<false, 1, false, false, false, false, true>
                      : (wide ? hsa_decode_kernel<false, 2, false, false> : hsa_decode_kernel<false, 1, false, false>);
   return cudaLaunchKernelEx(&cfg, kern, *tmK, *tmV, *tmKT, a);
 }

@@ -46,6 +46,7 @@ struct HsaArgs {
   int32_t kt_spec;      // 1: each CTA prefetches all 2*D KT rows of its blocks with one TMA box at launch
   int32_t blk_shift;    // log2(blk) when blk is a power of two, else -1
   int32_t ns_shift;     // log2(ns) when ns is a power of two, else -1
+  int32_t wflash;       // 1: per-warp online softmax (several staging rounds per CTA, narrow groups)
   int32_t tma_kv;       // 1: K/V block rows by TMA (blk a multiple of 8, no idx); 0: gathered rows
   float scale_log2;     // softmax scale * log2(e)
   // dynamic shared-memory layout (bytes)
