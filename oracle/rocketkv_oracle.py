@@ -30,9 +30,12 @@ Readings where the pages are silent or ambiguous (each marked READING below):
      returned index sets are sorted ascending.
   R6 B1 = floor(S * c**-r) clamped to [min(W+1, S), S]; k2 = floor((t/2)/blk)
      blocks, at least 1 (the even step-2 / step-3 split of the budget).
-  R7 sign at zero: a zero group sum takes Kmax (Algorithm 1 tests g_i >= 0).
-  R8 block score = sum over the kept channels of (group-summed q) times the
-     sign-selected Kmax/Kmin entry; no scale or softmax is applied to it.
+  R7 sign at zero: a zero group sum takes Kmax (Algorithm 1 tests g_i >= 0);
+     with the box form of R8 the choice cannot change a score.
+  R8 block score = the maximum of the kept-channel part of qbar . x over the
+     block's box Kmin <= x <= Kmax (qbar = group-summed q), i.e. per channel
+     the larger of qbar_c * Kmax_c and qbar_c * Kmin_c; no scale or softmax is
+     applied to it.
   R9 a partial last block uses only its valid tokens, for both the bounds and
      attention, and competes like any other block.
   R10 multi-turn: stage-2 candidates are the stage-1 survivors (ascending)
@@ -289,16 +292,19 @@ def hsa_channels(q_group: np.ndarray, k1: int) -> Tuple[np.ndarray, np.ndarray]:
 
 
 def hsa_block_scores(qbar: np.ndarray, i1: np.ndarray, kmax: np.ndarray, kmin: np.ndarray) -> np.ndarray:
-    """Approximate block scores of Algorithm 1 (READING R7, R8).
+    """Block scores of HSA step 2 (READING R8): for block b, the largest value
+    that the linear form  sum_{c in i1} qbar_c * x_c  takes over the block's
+    bounding box  Kmin[c, b] <= x_c <= Kmax[c, b].
 
-    For each kept channel c the sign of the group-summed q picks Kmax (g_c >= 0)
-    or Kmin (g_c < 0); the score of block b is sum_c qbar_c * P[c, b].  This is
-    max(q*Kmax, q*Kmin) channel by channel: an upper bound of q.k (restricted to
-    the kept channels) for every key in the block.
+    The box holds every key of the block, so the score bounds qbar . k (kept
+    channels only) from above for each of them ([RKV] HSA step 2: the
+    Kmax/Kmin bound of the attention score).  A linear form over a box is
+    maximised channel by channel, each channel at whichever end of its
+    interval gives the larger product; at qbar_c = 0 both ends give 0, so the
+    sign convention of Algorithm 1 (READING R7) cannot change a score.
     """
-    g = qbar[i1]
-    Psel = np.where((g >= 0)[:, None], kmax[i1, :], kmin[i1, :])   # [k1, nblk]
-    return g @ Psel
+    g = qbar[i1][:, None]                                      # [k1, 1]
+    return np.maximum(g * kmax[i1, :], g * kmin[i1, :]).sum(axis=0)
 
 
 def attention(q_group: np.ndarray, Ks: np.ndarray, Vs: np.ndarray, scale: float) -> np.ndarray:
@@ -319,10 +325,12 @@ def block_tokens(i2: np.ndarray, n: int, blk: int) -> np.ndarray:
 
 def hsa_decode(q_group: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, n: int, kmax: np.ndarray,
                kmin: np.ndarray, blk: int, k1: int, k2: int, scale: float) -> Dict[str, np.ndarray]:
-    """One HSA decode step of one GQA group over the first n compacted tokens.
+    """One HSA decode step of one GQA group over the first n compacted tokens
+    ([RKV] HSA steps 2-3, Algorithm 1).
 
-    Follows Algorithm 1: channel top-k1 of sum|q|, sign of sum q, sign-selected
-    Kmax/Kmin block scores, block top-k2, exact attention over those blocks.
+    The kept channels i1 carry the largest group mass sum_g |q_g|; each block
+    is scored by its box bound (hsa_block_scores); the k2 best blocks i2 are
+    kept; each head then attends exactly to the valid tokens of those blocks.
     Returns y [G, D] plus the intermediate selections and scores.
     """
     nblk = (n + blk - 1) // blk

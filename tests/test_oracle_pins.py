@@ -314,6 +314,26 @@ def test_sign_at_zero_takes_kmax():
     assert s.tolist() == [0.0 * 5 + 3 * 0 + (-2) * (-1) + 2 * 0]
 
 
+def test_block_score_is_box_maximum_by_corners():
+    # The score of a block is the largest value of sum_{c in i1} qbar_c x_c over
+    # the box Kmin <= x <= Kmax.  A linear form over a box peaks at a corner, so
+    # enumerating all 2^k1 corners gives the score with no per-channel argument.
+    r = _rng(13)
+    for G, D, n, blk, k1 in [(4, 12, 70, 8, 6), (2, 8, 33, 4, 8), (3, 10, 20, 20, 5)]:
+        qg = r.standard_normal((G, D))
+        qg[:, 0] = 0.0                                          # one zero group sum
+        K = r.standard_normal((n, D))
+        kmax, kmin = oracle.build_kt(K, n, blk)
+        i1, qbar = oracle.hsa_channels(qg, k1)
+        s = oracle.hsa_block_scores(qbar, i1, kmax, kmin)
+        for b in range(s.shape[0]):
+            best = -np.inf
+            for corner in range(1 << k1):
+                x = [kmax[c, b] if (corner >> u) & 1 else kmin[c, b] for u, c in enumerate(i1)]
+                best = max(best, float(np.dot(qbar[i1], x)))
+            assert abs(s[b] - best) <= 1e-12 * (1 + abs(best))
+
+
 # ---------------------------------------------------------------------------
 # Multi-turn identity
 # ---------------------------------------------------------------------------
