@@ -58,6 +58,9 @@ def dist_env():
     return rank, world, local
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -296,7 +299,11 @@ def run_ours(args, rank, world, local):
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
                 "fallback 6.8 TB/s", "bytes_per_launch": int(bytes_avg), "avg_launch_us": round(hsa_avg_us, 3),
                 "timing": "decode-phase events of the last timed pass / 64 launches (gaps included)",
-                "l2": "warm within a pass: inputs > L2 but the 190 MB compacted cache is re-read each step"}
+                "l2": "warm within a pass: inputs > L2 but the 190 MB compacted cache is re-read each step",
+                # the same achieved rate against GB300's nominal HBM3e rate, and the
+                # target fraction this kernel is held to (not met while frac < target)
+                "peak_nominal": NOMINAL_HBM_GBS, "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                "target_frac": 0.70, "target_met": bool(achieved / peak >= 0.70)}
 
     # e4m3 storage of the compacted cache (a storage option; the headline stays
     # bf16): the same pass with rkv_compact_kt_fp8 and rkv_hsa_decode_fp8, fixed
