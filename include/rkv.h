@@ -109,6 +109,10 @@ size_t rkv_snap_evict_workspace(rkv_dims d, int64_t S, int32_t W);
  *              fp32 range (written here as 0) still rank exactly.
  *   ws         workspace of rkv_snap_evict_workspace() bytes.
  * k/v and k_out/v_out must not overlap.
+ * Errors: RKV_ERR_INVALID_ARG for NULL or misaligned pointers, a pointer that
+ * is not device memory (q_obs, k, keep_idx, ws, the outputs, and v when the
+ * call compacts) and the size rules above; RKV_ERR_WORKSPACE for a missing or
+ * short workspace; RKV_ERR_CUDA if a launch fails.
  */
 rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v,
                           int64_t cap, int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1,
@@ -117,9 +121,10 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
 
 /*
  * Stage-1 eviction for callers that cannot allocate device memory.  The
- * paper has no counterpart to this entry point; it exists for engines whose
- * memory pool owns all device memory, plugin hooks that must not call
- * cudaMalloc, and code running while a stream is captured into a CUDA graph.
+ * paper has no counterpart to this entry point; it exists for serving
+ * engines whose memory pool owns all device memory and for plugin hooks that
+ * run inside another framework's step, where a cudaMalloc can fail or
+ * synchronise the device.
  * Same operation, arguments and results as rkv_snap_evict, minus ws/ws_bytes:
  * the scratch is a fixed 32 MiB array of device memory inside this library,
  * held on every GPU that loads the library's device code until the process
@@ -127,10 +132,12 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
  * RKV_ERR_WORKSPACE with a message giving both sizes.  It calls no cudaMalloc
  * or cudaFree.  The first call on a device, made with that device current,
  * looks up the array's device address (cudaGetSymbolAddress); make that first
- * call before any stream capture.  Every call uses the same array, so calls
- * that can overlap on the GPU (different streams, or devices sharing the
- * address) race and must be serialised by the caller.  No part of the scratch
- * needs to start at zero: each call writes all it reads.
+ * call before any stream capture.  Devices 0-63 are served (others get
+ * RKV_ERR_UNSUPPORTED).  Each device has its own copy of the array, so calls
+ * on different devices are independent; every call on one device uses that
+ * device's copy, so calls on one device that can overlap (different streams,
+ * or several host threads) race, and the caller must serialise them.  No
+ * part of the scratch needs to start at zero: each call writes all it reads.
  */
 rkv_status rkv_snap_evict_noalloc(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v,
                                   int64_t cap, int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1,

@@ -1,7 +1,6 @@
 """GPU test of rkv_snap_evict_noalloc, the stage-1 entry point for callers that
 cannot allocate device memory (an engine whose pool owns all device memory, a
-plugin hook that must not call cudaMalloc, code running under stream
-capture).  It must give the same keep set, compacted caches and pooled scores
+plugin hook that must not call cudaMalloc).  It must give the same keep set, compacted caches and pooled scores
 as rkv_snap_evict with a caller-allocated workspace, on consecutive calls that
 reuse the library's fixed scratch, and reject shapes whose scratch would not
 fit.  Collected last so a failure here comes after every other test ran.
@@ -61,9 +60,19 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_rejects_oversized_scratch():
-    dims = (64, 32, 8, 128)     # about 70 MB of scratch for a 32K prompt
-    assert rkv.rkv_snap_evict_workspace(dims, 32768, 32) > 32 << 20
+    # 16 rows of a 32K prompt need about 34 MiB of scratch.  Every tensor is a
+    # real allocation of the full shape, so the call would stay in bounds even
+    # if the size check did not come first.
+    B, Hq, Hkv, D, S, W, B1 = 16, 32, 8, 128, 32768, 32, 4000
+    dims = (B, Hq, Hkv, D)
+    assert rkv.rkv_snap_evict_workspace(dims, S, W) > 32 << 20
+    q = torch.zeros((B, Hq, W, D), dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros((B, Hkv, S, D), dtype=torch.bfloat16, device=DEV)
+    v = torch.zeros_like(k)
+    keep = torch.zeros((B, Hkv, B1), dtype=torch.int32, device=DEV)
+    ko = torch.zeros((B, Hkv, B1, D), dtype=torch.bfloat16, device=DEV)
+    vo = torch.zeros_like(ko)
     with pytest.raises(rkv.RkvError) as e:
-        rkv.rkv_snap_evict_noalloc(dims, 16, 32, 16, 16, 32768, 32768, 63, 0, 4000, 0.1, 16, 4000, 16, 16, 4000,
-                                   None)
+        rkv.rkv_snap_evict_noalloc(dims, q, W, k, v, S, S, 63, 0, B1, 0.1, keep, B1, ko, vo, B1, None)
     assert e.value.status == 3 and "fixed scratch" in str(e.value)
+    torch.cuda.synchronize()

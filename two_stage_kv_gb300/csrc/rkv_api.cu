@@ -53,6 +53,18 @@ rkv_status device_view(const void* p, const void** out, const char* what) {
   return fail(RKV_ERR_INVALID_ARG, "%s must be device memory or page-locked host memory", what);
 }
 
+// Refuses a pointer that is not device (or managed) memory of the current
+// context: a made-up or host address must never reach a kernel.
+rkv_status require_device(const void* p, const char* what) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RKV_ERR_INVALID_ARG, "%s: not an address the device can reach", what);
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return RKV_OK;
+  return fail(RKV_ERR_INVALID_ARG, "%s must be device memory", what);
+}
+
 rkv_status check_dims(const rkv_dims& d) {
   if (d.batch < 0 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.head_dim < 1)
     return fail(RKV_ERR_INVALID_ARG, "dims: batch=%d Hq=%d Hkv=%d D=%d", d.batch, d.n_q_heads, d.n_kv_heads,
@@ -307,6 +319,15 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
     return fail(RKV_ERR_WORKSPACE, "snap_evict: workspace %zu bytes < %zu required", ws_bytes, need);
   if (!keep_all && (reinterpret_cast<uintptr_t>(ws) & 255u))
     return fail(RKV_ERR_INVALID_ARG, "snap_evict: workspace must be 256-byte aligned");
+  {
+    // (v is read only when the call compacts)
+    const void* ptrs[8] = {q_obs, k, k_out ? v : nullptr, keep_idx, k_out, v_out, pooled_out,
+                           keep_all ? nullptr : ws};
+    const char* names[8] = {"snap_evict: q_obs", "snap_evict: k", "snap_evict: v", "snap_evict: keep_idx",
+                            "snap_evict: k_out", "snap_evict: v_out", "snap_evict: pooled_out", "snap_evict: ws"};
+    for (int i = 0; i < 8; ++i)
+      if (ptrs[i] && (s = require_device(ptrs[i], names[i])) != RKV_OK) return s;
+  }
 
   rkv::SnapArgs a = {};
   a.q_obs = q_obs; a.k = k; a.v = v; a.cap = cap; a.S = S; a.out_cap = out_cap; a.B1 = B1;

@@ -2,11 +2,11 @@
 //
 // rkv_snap_evict needs device scratch (softmax statistics, score partials and
 // pooled scores) that its caller allocates.  Some callers cannot allocate:
-// serving engines whose memory pool already owns all device memory, plugin or
-// callback hooks that must not call cudaMalloc, and code running while a
-// stream is being captured into a CUDA graph (cudaMalloc is not allowed
-// then).  rkv_snap_evict_noalloc serves them from one fixed array of device
-// memory that belongs to this library.
+// serving engines whose memory pool already owns all device memory (a
+// cudaMalloc beside the pool can fail or fragment it), and plugin or callback
+// hooks that run inside another framework's step and must not call cudaMalloc
+// (it can synchronise the device).  rkv_snap_evict_noalloc serves them from
+// one fixed array of device memory that belongs to this library.
 #include <cstdio>
 #include <mutex>
 
@@ -42,10 +42,16 @@ extern "C" rkv_status rkv_snap_evict_noalloc(rkv_dims d, const void* q_obs, int3
   }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess) {
     snprintf(msg, sizeof(msg), "snap_evict_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
     rkv::set_last_error(msg);
     return RKV_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(msg, sizeof(msg), "snap_evict_noalloc: device ordinal %d is past the %d devices this entry point serves",
+             dev, kMaxDevices);
+    rkv::set_last_error(msg);
+    return RKV_ERR_UNSUPPORTED;
   }
   void* scratch = nullptr;
   {
