@@ -409,6 +409,127 @@ def test_hsa_decode_paged_equals_dense(blk, append):
             assert torch.equal(vp[bt[b, n // blk], :, n % blk], v[b, :, n])
 
 
+def _kt_bits(Kc, n, blk, ncap):
+    """The oracle's Kmax / Kmin of Kc[:n] as bf16 bits [2, D, ncap] (exact: max and
+    min of bf16 values are bf16 values); columns past the last block are zero."""
+    kmax, kmin = oracle.build_kt(Kc, n, blk)
+    out = np.zeros((2, Kc.shape[1], ncap), dtype=np.uint16)
+    out[0, :, :kmax.shape[1]] = f32_to_bf16_bits(kmax.astype(np.float32))
+    out[1, :, :kmin.shape[1]] = f32_to_bf16_bits(kmin.astype(np.float32))
+    return out
+
+
+@pytest.mark.parametrize("blk,append,n_rows", [
+    (16, False, [300, 611, 57, 4000]),
+    (16, True, [300, 611, 57, 4000]),
+    (4, False, [300, 611, 57, 1500]),
+    (4, True, [301, 612, 58, 1500]),
+    (32, True, [2047, 31, 5000, 64]),
+])
+def test_hsa_decode_paged_oracle(blk, append, n_rows):
+    """Paged pools against the oracle directly: each batch row's logical sequence
+    (rows 0 .. n_b-1, plus the appended token) is scattered into pages of blk rows
+    through a shuffled block table; the KT cache comes from the oracle; every
+    unused page slot holds large random rows, so a wrong page or slot would
+    change the result.  i1 exact, i2 within the tie band, outputs within 2e-3,
+    the appended row in slot n % blk of its page and its KT column bit-exact."""
+    B, Hq, Hkv, D, k1, k2 = len(n_rows), 32, 8, 128, 32, 12
+    G = Hq // Hkv
+    n_max = max(n_rows)
+    nblk_row = -(-(n_max + 1) // blk)
+    dims = (B, Hq, Hkv, D)
+    kb = small_random(121 + blk, (B, Hkv, nblk_row * blk, D))
+    vb = small_random(122 + blk, (B, Hkv, nblk_row * blk, D))
+    qb, q = _rand(123 + blk, (B, Hq, D))
+    knb, knew = _rand(124 + blk, (B, Hkv, D))
+    vnb, vnew = _rand(125 + blk, (B, Hkv, D))
+    rng = np.random.default_rng(13 + blk)
+    bt, num_pages = _page_table(rng, B, nblk_row, 7)
+    kpb = small_random(126 + blk, (num_pages, Hkv, blk, D), 50.0)     # garbage everywhere first
+    vpb = small_random(127 + blk, (num_pages, Hkv, blk, D), 50.0)
+    for b in range(B):
+        for j in range(-(-n_rows[b] // blk)):
+            r = min(blk, n_rows[b] - j * blk)
+            kpb[bt[b, j], :, :r] = kb[b, :, j * blk:j * blk + r]
+            vpb[bt[b, j], :, :r] = vb[b, :, j * blk:j * blk + r]
+    kp, vp = _bf16(kpb), _bf16(vpb)
+    ncap = -(-nblk_row // 8) * 8
+    kf, vf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), bf16_bits_to_f64(qb)
+    ktb = np.stack([np.stack([_kt_bits(kf[b, h], n_rows[b], blk, ncap) for h in range(Hkv)]) for b in range(B)])
+    kt = _bf16(ktb)
+    n_dev = torch.tensor(n_rows, dtype=torch.int32, device=DEV)
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
+    sc = torch.full((B, Hkv, k1), -7, dtype=torch.int32, device=DEV)
+    scale = 1 / math.sqrt(D)
+    rkv.rkv_hsa_decode_paged(dims, q, kp, vp, num_pages, torch.from_numpy(bt).to(DEV), nblk_row, n_dev, n_max, kt,
+                             ncap, blk, k1, k2, scale, out, sb, sc, knew if append else None,
+                             vnew if append else None)
+    torch.cuda.synchronize()
+    assert rkv.rkv_read_device_flags() == 0
+    out_h, sb_h, sc_h, kt_h = out.cpu().numpy(), sb.cpu().numpy(), sc.cpu().numpy(), t2f64(kt)
+    kp_h, vp_h = t2bits(kp), t2bits(vp)
+    worst = 0.0
+    for b in range(B):
+        n = n_rows[b] + (1 if append else 0)
+        for h in range(Hkv):
+            Kc, Vc = kf[b, h, :n].copy(), vf[b, h, :n].copy()
+            if append:
+                Kc[-1] = bf16_bits_to_f64(knb)[b, h]
+                Vc[-1] = bf16_bits_to_f64(vnb)[b, h]
+                pg, sl = bt[b, n_rows[b] // blk], n_rows[b] % blk
+                assert np.array_equal(kp_h[pg, h, sl], knb[b, h]) and np.array_equal(vp_h[pg, h, sl], vnb[b, h])
+            kmax, kmin = oracle.build_kt(Kc, n, blk)
+            nblk = kmax.shape[1]
+            assert np.array_equal(kt_h[b, h, 0, :, :nblk], kmax) and np.array_equal(kt_h[b, h, 1, :, :nblk], kmin)
+            qg = qf[b, h * G:(h + 1) * G]
+            res = oracle.hsa_decode(qg, Kc, Vc, n, kmax, kmin, blk, k1, k2, scale)
+            assert sc_h[b, h].tolist() == res["i1"].tolist(), f"row {b} head {h}: channel set differs"
+            k2e = min(k2, nblk)
+            check_topk(sb_h[b, h, :k2e], res["s"], k2, f"row {b} head {h} blocks")
+            assert np.all(sb_h[b, h, k2e:] == -1)
+            y = res["y"] if np.array_equal(sb_h[b, h, :k2e], res["i2"]) else \
+                oracle.attention_over_blocks(qg, Kc, Vc, n, sb_h[b, h, :k2e], blk, scale)
+            worst = max(worst, max_abs(out_h[b, h * G:(h + 1) * G], y))
+    assert worst <= ATOL_OUT, worst
+
+
+@pytest.mark.parametrize("blk,B1", [(16, 333), (4, 333), (32, 2500)])
+def test_compact_kt_paged_oracle(blk, B1):
+    """Paged compaction against the oracle: page block_table[b, i / blk] slot i % blk
+    holds k[b, h, keep[b, h, i]] (bit for bit), the KT cache equals the oracle's
+    Kmax / Kmin of the compacted keys, and pages outside the table keep their
+    canary contents."""
+    B, Hq, Hkv, D, cap = 2, 8, 2, 128, 3000
+    dims = (B, Hq, Hkv, D)
+    kb, k = _rand(131 + blk, (B, Hkv, cap, D))
+    vb, v = _rand(132 + blk, (B, Hkv, cap, D))
+    rng = np.random.default_rng(17 + blk)
+    keep = np.stack([np.stack([np.sort(rng.choice(cap, B1, replace=False)) for _ in range(Hkv)])
+                     for _ in range(B)]).astype(np.int32)
+    nblk = -(-B1 // blk)
+    ncap = -(-(nblk + 1) // 8) * 8
+    bt, num_pages = _page_table(rng, B, nblk, 5)
+    kp = torch.full((num_pages, Hkv, blk, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vp = torch.full_like(kp, float("nan"))
+    kt = torch.full((B, Hkv, 2, D, ncap), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_compact_kt_paged(dims, k, v, cap, torch.from_numpy(keep).to(DEV), B1, B1, kp, vp, num_pages,
+                             torch.from_numpy(bt).to(DEV), nblk, blk, kt, ncap)
+    torch.cuda.synchronize()
+    kp_h, vp_h, kt_h = t2bits(kp), t2bits(vp), t2f64(kt)
+    kf = bf16_bits_to_f64(kb)
+    for b in range(B):
+        for h in range(Hkv):
+            kc, vc = oracle.compact(kb[b, h], keep[b, h]), oracle.compact(vb[b, h], keep[b, h])
+            for i in range(B1):
+                assert np.array_equal(kp_h[bt[b, i // blk], h, i % blk], kc[i])
+                assert np.array_equal(vp_h[bt[b, i // blk], h, i % blk], vc[i])
+            kmax, kmin = oracle.build_kt(oracle.compact(kf[b, h], keep[b, h]), B1, blk)
+            assert np.array_equal(kt_h[b, h, 0, :, :nblk], kmax) and np.array_equal(kt_h[b, h, 1, :, :nblk], kmin)
+    unused = np.setdiff1d(np.arange(num_pages), bt.reshape(-1))
+    assert torch.isnan(kp[torch.from_numpy(unused).to(DEV)].float()).all()
+
+
 def test_hsa_decode_exact_topk_pin():
     """k1 = D and block 1: the block score is qbar . k_j exactly, so the chosen tokens
     are the plain top-k2 of qbar . k (lowest index on ties) and the output is

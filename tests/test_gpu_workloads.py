@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import oracle
+import workload_check
 from parity_util import ATOL_OUT, check_topk, max_abs, t2bits, t2f64
 from two_stage_kv_gb300 import pipeline, synth
 from two_stage_kv_gb300.synth import WORKLOADS, bf16_bits_to_f64 as f64, scaled
@@ -37,110 +38,61 @@ def _pairs(wl, max_pairs):
     return [allp[i] for i in sorted(pick)]
 
 
-def _needle_recall(wl, needles, keep, sel, k2, pairs):
-    """Fraction of (needle i, (batch row, KV head) in pairs) whose token survives
-    stage 1 (keep[(b, h)]) and whose block is selected (sel[step][(b, h)]) at the
-    decode step that queries it."""
-    hit = tot = 0
-    for (b, h) in pairs:
-        kp = keep[(b, h)]
-        for i, p in enumerate(needles[b]):
-            tot += 1
-            pos = np.searchsorted(kp, p)
-            if pos < len(kp) and kp[pos] == p:
-                hit += int((pos // wl.blk) in set(np.asarray(sel[synth.needle_step(wl, i)][(b, h)])[:k2].tolist()))
-    return hit / max(tot, 1)
-
-
 def run_single_turn(wl, layer=0, max_pairs=64, steps=None, fused=True):
     """fused: stage 1 in mask mode + rkv_compact_kt and decode steps with the append
     fused in; otherwise stage 1 with its own compaction, rkv_build_kt, and separate
-    append and decode calls."""
+    append and decode calls.  The GPU run records every pair's results; the
+    oracle then checks the sampled pairs (workload_check.check_pair), spread over
+    host processes when there are many."""
+    assert steps is None or steps == wl.steps
     li = synth.layer_inputs(wl, layer)
-    G, D, blk, k1 = wl.G, wl.D, wl.blk, wl.k1
-    scale = 1 / math.sqrt(D)
+    G = wl.G
     L = pipeline.Layer(wl, _t(li.k), _t(li.v), _t(li.q_obs), device=DEV)
     bud = L.bud
     if fused:
-        # stage 1 in mask mode, then compaction with the KT cache built on the way
         L.stage1_select()
         L.compact_kt()
     else:
         L.stage1()
-    torch.cuda.synchronize()
-    keep = L.keep.cpu().numpy()
-    pairs = _pairs(wl, max_pairs)
-    exempt = 0
-    states = {}
-    ref_keep = {}
-    for (b, h) in pairs:
-        qo = f64(li.q_obs[b, h * G:(h + 1) * G])
-        K = f64(li.k[b, h])
-        ref, pooled = oracle.snap_keep(qo, K, bud.B1, wl.W, wl.P, scale)
-        ref_keep[(b, h)] = ref
-        pg = L.pooled[b, h, :wl.S - wl.W].cpu().numpy().astype(np.float64)
-        assert np.max(np.abs(pg - pooled) / np.maximum(np.abs(pooled), 1e-30)) < 1e-4
-        got = keep[b, h]
-        assert got[-wl.W:].tolist() == list(range(wl.S - wl.W, wl.S))
-        exempt += check_topk(got[:bud.B1 - wl.W], pooled, bud.B1 - wl.W, f"keep {b},{h}")
-        assert np.array_equal(t2bits(L.kc[b, h, :bud.B1]), li.k[b, h][got])
-        assert np.array_equal(t2bits(L.vc[b, h, :bud.B1]), li.v[b, h][got])
-        Kc = np.zeros((L.cap, D))
-        Vc = np.zeros((L.cap, D))
-        Kc[:bud.B1] = K[got]
-        Vc[:bud.B1] = f64(li.v[b, h])[got]
-        states[(b, h)] = [Kc, Vc]
-    if not fused:
         L.build_kt()
     torch.cuda.synchronize()
-    for (b, h), st in states.items():
-        kmax, kmin = oracle.build_kt(st[0], bud.B1, blk)
-        ktg = t2f64(L.kt[b, h])
-        assert np.array_equal(ktg[0, :, :kmax.shape[1]], kmax) and np.array_equal(ktg[1, :, :kmin.shape[1]], kmin)
-        st += [kmax, kmin]
-    n = bud.B1
-    worst = 0.0
-    sel_steps, ref_steps = [], []
-    nsteps = wl.steps if steps is None else steps
-    for s in range(nsteps):
+    keep = L.keep.cpu().numpy()
+    pooled = L.pooled.cpu().numpy()
+    kt0 = t2bits(L.kt)
+    kc, vc = t2bits(L.kc[:, :, :bud.B1]), t2bits(L.vc[:, :, :bud.B1])
+    outs, sbs, scs = [], [], []
+    for s in range(wl.steps):
         if fused:
             L.step(_t(li.q_dec[s]), _t(li.k_new[s]), _t(li.v_new[s]))
         else:
             L.append(_t(li.k_new[s]), _t(li.v_new[s]))
             L.decode(_t(li.q_dec[s]))
-        torch.cuda.synchronize()
-        out = L.out.cpu().numpy()
-        sb = L.sel_blocks.cpu().numpy()
-        sc = L.sel_channels.cpu().numpy()
-        sel_steps.append({(b, h): sb[b, h] for (b, h) in pairs})
-        ref_steps.append({})
-        for (b, h), st in states.items():
-            Kc, Vc, kmax, kmin = st
-            Kc[n] = f64(li.k_new[s, b, h])
-            Vc[n] = f64(li.v_new[s, b, h])
-            kmax, kmin = oracle.kt_append(kmax, kmin, n, Kc[n], blk)
-            st[2], st[3] = kmax, kmin
-            qg = f64(li.q_dec[s, b, h * G:(h + 1) * G])
-            res = oracle.hsa_decode(qg, Kc, Vc, n + 1, kmax, kmin, blk, k1, bud.k2, scale)
-            ref_steps[-1][(b, h)] = res["i2"]
-            assert sc[b, h].tolist() == res["i1"].tolist(), f"step {s} pair {b},{h}: channels"
-            k2e = min(bud.k2, res["s"].shape[0])
-            exempt += check_topk(sb[b, h, :k2e], res["s"], bud.k2, f"step {s} blocks {b},{h}")
-            y = res["y"] if np.array_equal(sb[b, h, :k2e], res["i2"]) else \
-                oracle.attention_over_blocks(qg, Kc, Vc, n + 1, sb[b, h, :k2e], blk, scale)
-            worst = max(worst, max_abs(out[b, h * G:(h + 1) * G], y))
-        n += 1
-    assert worst <= ATOL_OUT, worst
-    for (b, h), st in states.items():
-        ktg = t2f64(L.kt[b, h])
-        nb = st[2].shape[1]
-        assert np.array_equal(ktg[0, :, :nb], st[2]) and np.array_equal(ktg[1, :, :nb], st[3])
+        outs.append(L.out.cpu().numpy())
+        sbs.append(L.sel_blocks.cpu().numpy())
+        scs.append(L.sel_channels.cpu().numpy())
+    torch.cuda.synchronize()
+    kt_final = t2bits(L.kt)
+    out, sb, sc = np.stack(outs), np.stack(sbs), np.stack(scs)
+    pairs = _pairs(wl, max_pairs)
+    tasks = []
+    for (b, h) in pairs:
+        # compaction is a copy: the kept rows, bit for bit
+        assert np.array_equal(kc[b, h], li.k[b, h][keep[b, h]]) and np.array_equal(vc[b, h], li.v[b, h][keep[b, h]])
+        tasks.append({"wl": wl, "layer": layer, "b": b, "h": h, "B1": bud.B1, "k2": bud.k2,
+                      "keep": keep[b, h].copy(), "pooled": pooled[b, h, :wl.S - wl.W].copy(),
+                      "kt0": kt0[b, h].copy(), "kt_final": kt_final[b, h].copy(),
+                      "out": out[:, b, h * G:(h + 1) * G].copy(), "sb": sb[:, b, h].copy(),
+                      "sc": sc[:, b, h].copy()})
+    res = workload_check.check_pairs(tasks)
+    worst = max(r["worst"] for r in res)
+    exempt = sum(r["exempt"] for r in res)
     recall = recall_oracle = None
     if wl.n_needles:
-        # the GPU's survivors and blocks, and the oracle's (its blocks computed on the
-        # GPU's survivors, which equal the oracle's own when nothing was tie-exempt)
-        recall = _needle_recall(wl, li.needles, {p: keep[p[0], p[1]] for p in pairs}, sel_steps, bud.k2, pairs)
-        recall_oracle = _needle_recall(wl, li.needles, ref_keep, ref_steps, bud.k2, pairs)
+        hits = [x for r in res for x in r["hits"]]
+        hits_o = [x for r in res for x in r["hits_oracle"]]
+        recall, recall_oracle = sum(hits) / len(hits), sum(hits_o) / len(hits_o)
+        # (the oracle's blocks are computed on the GPU's survivors, which equal the
+        # oracle's own when nothing was tie-exempt)
         if exempt == 0:
             assert recall == recall_oracle, (recall, recall_oracle)
     return {"worst": worst, "exempt": exempt, "recall": recall, "recall_oracle": recall_oracle,
@@ -345,7 +297,9 @@ def test_full_needle_b1_4k():
 
 
 def test_full_b8_32k():
-    print("b8_32k", run_single_turn(WORKLOADS["b8_32k"], max_pairs=16))
+    r = run_single_turn(WORKLOADS["b8_32k"], max_pairs=64)
+    print("b8_32k", r)
+    assert r["pairs"] == 64
 
 
 def test_full_needle_b1_109k():
@@ -355,7 +309,9 @@ def test_full_needle_b1_109k():
 
 @pytest.mark.parametrize("layer", [0, 1, 2, 3])
 def test_full_l70b_b32_32k(layer):
-    print("l70b_b32_32k layer", layer, run_single_turn(WORKLOADS["l70b_b32_32k"], layer=layer, max_pairs=6))
+    r = run_single_turn(WORKLOADS["l70b_b32_32k"], layer=layer, max_pairs=64)
+    print("l70b_b32_32k layer", layer, r)
+    assert r["pairs"] == 64
 
 
 def test_full_mt_b4_16k():
