@@ -395,6 +395,18 @@ rkv_status rkv_hsa_decode_paged(rkv_dims d, const void* q, void* k_pages, void* 
                                 const void* v_new, void* stream);
 
 /*
+ * Diagnostics for the bounded waits of the HSA decode kernels (every
+ * rkv_hsa_decode* call made after it, from any host thread).  limit_ns > 0
+ * shortens each bounded wait from 1 s to limit_ns (at least 1000); extra_bytes
+ * (at most 4096) is added to the byte count that each CTA's block-score
+ * barrier expects, bytes that no copy ever delivers, so that wait runs out
+ * while every real copy still completes: the kernel then goes on with the
+ * scores it has received, finishes, and sets bit 0 of the device error word.
+ * rkv_debug_set_wait(0, 0) restores normal operation.  Host only.
+ */
+rkv_status rkv_debug_set_wait(uint64_t limit_ns, uint32_t extra_bytes);
+
+/*
  * Read and clear the library's device error word (synchronises the device).
  * Bit 0: a bounded wait for an asynchronous copy gave up in some kernel.
  * Bit 1: a per-row length or page id read from device memory was out of range.

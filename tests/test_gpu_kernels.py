@@ -197,6 +197,12 @@ def _hsa_case(seed, B, Hq, Hkv, n, blk, k1, k2, cap_extra=3, q_scale=1.0, mt=Fal
     (2, 32, 8, 500, 4, 32, 10),       # block 4, gathered rows
     (1, 64, 8, 333, 12, 64, 7),       # block 12 (not a multiple of 8), G = 8
     (1, 32, 8, 300, 1, 128, 20),      # k1 = D and block 1: exact top-k of qbar . k (Exact-TopK)
+    # several staging rounds per CTA (per-warp online softmax, merged once)
+    (1, 8, 8, 6000, 16, 16, 300),     # G = 1
+    (1, 24, 8, 6000, 16, 32, 300),    # G = 3 (odd group: scalar partial stores)
+    (1, 64, 8, 6000, 16, 64, 300),    # G = 8
+    (1, 32, 8, 8000, 24, 32, 250),    # block 24: 120-row rounds, zero-filled tail rows
+    (2, 40, 8, 8000, 40, 32, 150),    # block 40, G = 5
 ])
 def test_hsa_decode_parity(B, Hq, Hkv, n, blk, k1, k2):
     _hsa_case(100 + n, B, Hq, Hkv, n, blk, k1, k2)
@@ -407,6 +413,48 @@ def test_hsa_decode_paged_equals_dense(blk, append):
             n = n_rows[b]
             assert torch.equal(kp[bt[b, n // blk], :, n % blk], k[b, :, n])
             assert torch.equal(vp[bt[b, n // blk], :, n % blk], v[b, :, n])
+
+
+def test_hsa_decode_bounded_wait_runs_out():
+    """The timeout path of the bounded waits, without a fault: the block-score
+    barrier of every CTA is told to expect 16 bytes that no copy delivers and
+    each wait is shortened to 20 us.  The wait runs out, the kernel goes on
+    with the scores it received (all of them arrived), finishes, and reports
+    bit 0 of the device error word; the results equal a normal run's, and the
+    next normal launch on the same context is clean."""
+    B, Hq, Hkv, D, n, blk, k1, k2 = 2, 32, 8, 128, 3000, 16, 32, 8
+    dims = (B, Hq, Hkv, D)
+    _, k = _rand(141, (B, Hkv, n, D))
+    _, v = _rand(142, (B, Hkv, n, D))
+    _, q = _rand(143, (B, Hq, D))
+    ncap = -(-(-(-n // blk)) // 8) * 8
+    kt = torch.empty((B, Hkv, 2, D, ncap), dtype=torch.bfloat16, device=DEV)
+    rkv.rkv_build_kt(dims, k, n, n, None, 0, blk, kt, ncap)
+    scale = 1 / math.sqrt(D)
+
+    def run():
+        out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+        sb = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=DEV)
+        rkv.rkv_hsa_decode(dims, q, k, v, n, n, kt, ncap, blk, k1, k2, scale, out, sb, None)
+        torch.cuda.synchronize()
+        return out, sb
+
+    assert rkv.rkv_read_device_flags() == 0
+    ref_out, ref_sb = run()
+    assert rkv.rkv_read_device_flags() == 0
+    rkv.rkv_debug_set_wait(20_000, 16)
+    try:
+        out, sb = run()
+        with pytest.raises(rkv.RkvError) as e:
+            rkv.rkv_read_device_flags()
+        assert e.value.status == 5 and "0x1" in str(e.value)
+    finally:
+        rkv.rkv_debug_set_wait(0, 0)
+    assert torch.isfinite(out).all()
+    assert torch.equal(sb, ref_sb) and torch.equal(out, ref_out)
+    out2, sb2 = run()
+    assert rkv.rkv_read_device_flags() == 0
+    assert torch.equal(out2, ref_out) and torch.equal(sb2, ref_sb)
 
 
 def _kt_bits(Kc, n, blk, ncap):

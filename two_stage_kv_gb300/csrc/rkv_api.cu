@@ -2,11 +2,13 @@
 // TMA descriptor encoding and kernel launches.  Every entry point validates its
 // arguments before any launch and returns a status; no exception escapes.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -16,6 +18,10 @@
 namespace {
 
 thread_local std::string g_last_error;
+
+// Bounded-wait test setting (rkv_debug_set_wait): 0 = normal operation.
+std::atomic<uint64_t> g_test_wait_ns{0};
+std::atomic<uint32_t> g_test_extra_tx{0};
 
 rkv_status fail(rkv_status s, const char* fmt, ...) {
   char buf[512];
@@ -30,6 +36,16 @@ rkv_status fail(rkv_status s, const char* fmt, ...) {
 rkv_status cuda_fail(cudaError_t e, const char* where) {
   return fail(RKV_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
+
+// One NVTX range per entry point call (its name), so a profiler timeline shows
+// each library call around the kernels it launched; without a profiler
+// attached a push / pop costs a few nanoseconds.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -213,6 +229,11 @@ rkv_status hsa_common(const rkv_dims& d, const void* q, void* k, void* v, int64_
   a.k_scale = k_scale; a.v_scale = v_scale; a.f8 = f8 ? 1 : 0;
   a.blk = blk; a.k1 = k1; a.k2 = k2;
   a.scale_log2 = scale * 1.4426950408889634f;
+  {
+    const uint64_t w = g_test_wait_ns.load(std::memory_order_relaxed);
+    a.wait_ns = w ? w : rkv::WAIT_LIMIT_NS_HOST;
+    a.sbar_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
+  }
   a.tma_kv = (!mt && blk % 8 == 0) ? 1 : 0;
   if (!rkv::hsa_plan(a)) return fail(RKV_ERR_UNSUPPORTED, "hsa_decode: shared memory plan does not fit");
 
@@ -285,6 +306,7 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
                           int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1, float scale, int32_t* keep_idx,
                           int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out, void* ws, size_t ws_bytes,
                           void* stream) {
+  TraceRange trace("rkv_snap_evict");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
@@ -355,6 +377,7 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
 
 rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,
                         int32_t blk, void* kt, int64_t nblk_cap, void* stream) {
+  TraceRange trace("rkv_build_kt");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0 || n == 0) return RKV_OK;
@@ -372,6 +395,7 @@ rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const
 
 rkv_status rkv_keep_mask(rkv_dims d, const int32_t* keep_idx, int64_t keep_ld, int64_t B1, int64_t n_prompt,
                          uint32_t* mask, int64_t mask_ld, void* stream) {
+  TraceRange trace("rkv_keep_mask");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0 || n_prompt == 0) return RKV_OK;
@@ -391,6 +415,7 @@ rkv_status rkv_keep_mask(rkv_dims d, const int32_t* keep_idx, int64_t keep_ld, i
 rkv_status rkv_build_kt_masked(rkv_dims d, const void* k, int64_t cap, int64_t n, const uint32_t* mask,
                                int64_t mask_ld, int64_t n_prompt, int32_t blk, void* kt, int64_t nblk_cap,
                                void* stream) {
+  TraceRange trace("rkv_build_kt_masked");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0 || n == 0) return RKV_OK;
@@ -414,6 +439,7 @@ rkv_status rkv_build_kt_masked(rkv_dims d, const void* k, int64_t cap, int64_t n
 rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
                           int64_t keep_ld, int64_t B1, void* k_out, void* v_out, int64_t out_cap, int32_t blk, void* kt,
                           int64_t nblk_cap, void* stream) {
+  TraceRange trace("rkv_compact_kt");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0 || B1 == 0) return RKV_OK;
@@ -437,6 +463,7 @@ rkv_status rkv_compact_kt(rkv_dims d, const void* k, const void* v, int64_t cap,
 rkv_status rkv_compact_kt_fp8(rkv_dims d, const void* k, const void* v, int64_t cap, const int32_t* keep_idx,
                               int64_t keep_ld, int64_t B1, const float* k_scale, const float* v_scale, void* k_out,
                               void* v_out, int64_t out_cap, int32_t blk, void* kt, int64_t nblk_cap, void* stream) {
+  TraceRange trace("rkv_compact_kt_fp8");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0 || B1 == 0) return RKV_OK;
@@ -465,6 +492,7 @@ rkv_status rkv_compact_kt_paged(rkv_dims d, const void* k, const void* v, int64_
                                 int64_t keep_ld, int64_t B1, void* k_pages, void* v_pages, int64_t num_pages,
                                 const int32_t* block_table, int64_t bt_stride, int32_t blk, void* kt,
                                 int64_t nblk_cap, void* stream) {
+  TraceRange trace("rkv_compact_kt_paged");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0 || B1 == 0) return RKV_OK;
@@ -494,6 +522,7 @@ rkv_status rkv_compact_kt_paged(rkv_dims d, const void* k, const void* v, int64_
 rkv_status rkv_append_kv(rkv_dims d, const void* k_new, const void* v_new, void* k, void* v, int64_t cap, int64_t n,
                          int64_t row, int32_t* idx, int64_t idx_cap, void* kt, int64_t nblk_cap, int32_t blk,
                          void* stream) {
+  TraceRange trace("rkv_append_kv");
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
@@ -512,6 +541,7 @@ rkv_status rkv_hsa_decode(rkv_dims d, const void* q, void* k, void* v, int64_t c
                           int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale, float* out,
                           int32_t* sel_blocks, int32_t* sel_channels, const void* k_new, const void* v_new,
                           void* stream) {
+  TraceRange trace("rkv_hsa_decode");
   return hsa_common(d, q, k, v, cap, nullptr, 0, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks, sel_channels,
                     k_new, v_new, n, stream, false);
 }
@@ -520,6 +550,7 @@ rkv_status rkv_hsa_decode_mt(rkv_dims d, const void* q, void* k, void* v, int64_
                              int64_t n, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
                              float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
                              const void* v_new, int64_t row, void* stream) {
+  TraceRange trace("rkv_hsa_decode_mt");
   return hsa_common(d, q, k, v, cap, idx, idx_cap, n, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
                     sel_channels, k_new, v_new, row, stream, true);
 }
@@ -529,6 +560,7 @@ rkv_status rkv_hsa_decode_mt_masked(rkv_dims d, const void* q, void* k, void* v,
                                     int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale, float* out,
                                     int32_t* sel_blocks, int32_t* sel_channels, const void* k_new, const void* v_new,
                                     void* stream) {
+  TraceRange trace("rkv_hsa_decode_mt_masked");
   if (!mask) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: mask is NULL");
   if (reinterpret_cast<uintptr_t>(mask) % 4 != 0)
     return fail(RKV_ERR_INVALID_ARG, "hsa_decode_mt_masked: mask must be 4-byte aligned");
@@ -545,6 +577,7 @@ rkv_status rkv_hsa_decode_fp8(rkv_dims d, const void* q, void* k, void* v, int64
                               const float* k_scale, const float* v_scale, void* kt, int64_t nblk_cap, int32_t blk,
                               int32_t k1, int32_t k2, float scale, float* out, int32_t* sel_blocks,
                               int32_t* sel_channels, const void* k_new, const void* v_new, void* stream) {
+  TraceRange trace("rkv_hsa_decode_fp8");
   if (!k_scale || !v_scale) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_fp8: NULL k_scale or v_scale");
   if (reinterpret_cast<uintptr_t>(k_scale) % 4 != 0 || reinterpret_cast<uintptr_t>(v_scale) % 4 != 0)
     return fail(RKV_ERR_INVALID_ARG, "hsa_decode_fp8: scales must be 4-byte aligned");
@@ -559,6 +592,7 @@ rkv_status rkv_hsa_decode_ragged(rkv_dims d, const void* q, void* k, void* v, in
                                  int64_t n_max, void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2,
                                  float scale, float* out, int32_t* sel_blocks, int32_t* sel_channels,
                                  const void* k_new, const void* v_new, void* stream) {
+  TraceRange trace("rkv_hsa_decode_ragged");
   if (d.batch > 0 && !n_rows) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_ragged: n_rows is NULL");
   if (n_max < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_ragged: n_max=%lld < 1", (long long)n_max);
   return hsa_common(d, q, k, v, cap, nullptr, 0, n_max, kt, nblk_cap, blk, k1, k2, scale, out, sel_blocks,
@@ -570,6 +604,7 @@ rkv_status rkv_hsa_decode_paged(rkv_dims d, const void* q, void* k_pages, void* 
                                 void* kt, int64_t nblk_cap, int32_t blk, int32_t k1, int32_t k2, float scale,
                                 float* out, int32_t* sel_blocks, int32_t* sel_channels, const void* k_new,
                                 const void* v_new, void* stream) {
+  TraceRange trace("rkv_hsa_decode_paged");
   if (d.batch > 0 && !block_table) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_paged: block_table is NULL");
   if (n_max < 1) return fail(RKV_ERR_INVALID_ARG, "hsa_decode_paged: n_max=%lld < 1", (long long)n_max);
   if (num_pages < 1 || num_pages * (int64_t)d.n_kv_heads * blk >= ((int64_t)1 << 31))
@@ -583,7 +618,17 @@ rkv_status rkv_hsa_decode_paged(rkv_dims d, const void* q, void* k_pages, void* 
                     num_pages);
 }
 
+rkv_status rkv_debug_set_wait(uint64_t limit_ns, uint32_t extra_bytes) {
+  if (extra_bytes > 4096) return fail(RKV_ERR_INVALID_ARG, "debug_set_wait: extra_bytes above 4096");
+  if (limit_ns != 0 && limit_ns < 1000)
+    return fail(RKV_ERR_INVALID_ARG, "debug_set_wait: limit below 1 us");
+  g_test_wait_ns.store(limit_ns, std::memory_order_relaxed);
+  g_test_extra_tx.store(extra_bytes, std::memory_order_relaxed);
+  return RKV_OK;
+}
+
 rkv_status rkv_read_device_flags(uint32_t* flags) {
+  TraceRange trace("rkv_read_device_flags");
   if (!flags) return fail(RKV_ERR_INVALID_ARG, "read_device_flags: NULL");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "read_device_flags");

@@ -56,14 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete, at most WAIT_LIMIT_NS.
+// Waits for the phase with the given parity to complete, at most limit_ns
+// (WAIT_LIMIT_NS unless a kernel was given a shorter limit for testing).
 // Returns false (and records ERR_WAIT_TIMEOUT in *err) if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(err, ERR_WAIT_TIMEOUT);
       return false;
     }
@@ -89,6 +91,12 @@ __device__ __forceinline__ bool cand_any(const uint32_t* m, int64_t n_prompt, in
   if (hi <= lo) return false;
   if (hi > n_prompt) return true;
   return mask_any(m, lo, hi);
+}
+
+// Ask L2 for `bytes` (a multiple of 16) at a 16-byte aligned global address;
+// nothing is read into the CTA.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {

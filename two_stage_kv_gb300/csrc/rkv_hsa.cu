@@ -303,6 +303,145 @@ __device__ void topk_list(float* vals, int n, int k, float mn, float mx, uint8_t
   }
 }
 
+// Exact top-k (0 < k < n <= 2 * NT) of vals[0, n), listed: sel[0, k) = the
+// indices of the k largest values in ascending order, equal values taken in
+// ascending index order.  mn < mx are the finite minimum and maximum of the
+// finite values (infinite values clamp to the end buckets).  Thread t owns
+// blocks 2t and 2t+1 for the whole selection.
+//   1. a 256-bucket histogram over [mn, mx] (any monotone map keeps the exact
+//      order between buckets); every warp then finds the bucket holding the
+//      k-th value on its own;
+//   2. blocks above that bucket are chosen; when the bucket is split, each
+//      warp lists its members (in block order) in shared memory;
+//   3. every warp ranks all members itself (at most 64: one or two per lane),
+//      so each thread knows the list position of its blocks without another
+//      exchange, and writes them.
+// Returns true when the list was written (three CTA barriers in all, the last
+// one left to the caller).  Returns false for a split bucket of more than 64
+// members, having written nothing and left fs.hist zero for the general select.
+// fs.hist must be zero on entry.
+__device__ bool topk_small(const float* vals, int n, int k, float mn, float mx, int32_t* sel, FixedSmem& fs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // (any monotone map of the scores to buckets gives the same exact selection)
+  const float inv = __fdividef((float)NBUCKET, mx - mn);
+  const int j0 = 2 * tid;
+  const bool ok0 = j0 < n, ok1 = j0 + 1 < n;
+  float2 v = make_float2(0.f, 0.f);
+  // (the score array holds n rounded up to 8 entries: the pair word stays inside it)
+  if (ok0) v = *reinterpret_cast<const float2*>(vals + j0);
+  const int b0 = ok0 ? max(0, min(NBUCKET - 1, (int)((v.x - mn) * inv))) : -1;
+  const int b1 = ok1 ? max(0, min(NBUCKET - 1, (int)((v.y - mn) * inv))) : -1;
+  if (ok0) atomicAdd(&fs.hist[b0], 1);
+  if (ok1) atomicAdd(&fs.hist[b1], 1);
+  __syncthreads();
+  int bb, need, m;
+  {
+    // lane l holds buckets 8l .. 8l+7; counts from the top bucket down
+    const int4 h0 = *reinterpret_cast<const int4*>(&fs.hist[8 * lane]);
+    const int4 h1 = *reinterpret_cast<const int4*>(&fs.hist[8 * lane + 4]);
+    const int cnt[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    int tot = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) tot += cnt[u];
+    int incl = tot;   // this lane's buckets and every higher lane's
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += t;
+    }
+    int above = incl - tot;
+    int found = -1, fneed = 0, fm = 0;
+#pragma unroll
+    for (int u = 7; u >= 0; --u) {
+      if (above < k && above + cnt[u] >= k) {
+        found = 8 * lane + u;
+        fneed = k - above;
+        fm = cnt[u];
+      }
+      above += cnt[u];
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, found >= 0)) - 1;   // exactly one lane
+    bb = __shfl_sync(0xffffffffu, found, src);
+    need = __shfl_sync(0xffffffffu, fneed, src);
+    m = __shfl_sync(0xffffffffu, fm, src);
+  }
+  const bool split = need < m;             // the same in every warp
+  if (split && m > 64) {
+    __syncthreads();                       // every warp has read the histogram
+    fs.hist[tid] = 0;
+    __syncthreads();
+    return false;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  const bool c0 = b0 > bb || (b0 == bb && !split), c1 = b1 > bb || (b1 == bb && !split);
+  const unsigned bc0 = __ballot_sync(0xffffffffu, c0), bc1 = __ballot_sync(0xffffffffu, c1);
+  const bool m0 = split && b0 == bb, m1 = split && b1 == bb;
+  int mp = 0;                              // this warp's members in lower lanes
+  if (split) {
+    const unsigned bm0 = __ballot_sync(0xffffffffu, m0), bm1 = __ballot_sync(0xffffffffu, m1);
+    mp = __popc(bm0 & lt) + __popc(bm1 & lt);
+    if (m0) fs.members[warp * 64 + mp] = j0;
+    if (m1) fs.members[warp * 64 + mp + (m0 ? 1 : 0)] = j0 + 1;
+    if (lane == 0) fs.wsum[NWARP + warp] = __popc(bm0) + __popc(bm1);
+  }
+  if (lane == 0) fs.wsum[warp] = __popc(bc0) + __popc(bc1);
+  __syncthreads();
+  int pre = __popc(bc0 & lt) + __popc(bc1 & lt);
+  {
+    const int4 w0 = *reinterpret_cast<const int4*>(&fs.wsum[0]);
+    const int4 w1 = *reinterpret_cast<const int4*>(&fs.wsum[4]);
+    pre += (warp > 0 ? w0.x : 0) + (warp > 1 ? w0.y : 0) + (warp > 2 ? w0.z : 0) + (warp > 3 ? w0.w : 0) +
+           (warp > 4 ? w1.x : 0) + (warp > 5 ? w1.y : 0) + (warp > 6 ? w1.z : 0);
+  }
+  bool f0 = c0, f1 = c1;
+  if (split) {
+    // members in block order: warp w's list starts at ms[w]
+    const int4 q0 = *reinterpret_cast<const int4*>(&fs.wsum[NWARP]);
+    const int4 q1 = *reinterpret_cast<const int4*>(&fs.wsum[NWARP + 4]);
+    const int mc[NWARP] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    int ms[NWARP];
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) {
+      ms[w] = acc;
+      acc += mc[w];
+    }
+    // lane l ranks members l and l + 32 against every member
+    int jm[2];
+    float sm[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      int w = 0;
+#pragma unroll
+      for (int u = 1; u < NWARP; ++u) w = i >= ms[u] ? u : w;
+      jm[h] = i < m ? fs.members[w * 64 + (i - ms[w])] : 0x7fffffff;
+      sm[h] = i < m ? vals[jm[h]] : 0.f;
+    }
+    int rk[2] = {0, 0};
+    for (int i2 = 0; i2 < m; ++i2) {
+      const int sl = i2 & 31;
+      const float s2 = __shfl_sync(0xffffffffu, i2 < 32 ? sm[0] : sm[1], sl);
+      const int j2 = __shfl_sync(0xffffffffu, i2 < 32 ? jm[0] : jm[1], sl);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) rk[h] += (s2 > sm[h]) || (s2 == sm[h] && j2 < jm[h]);
+    }
+    const unsigned win0 = __ballot_sync(0xffffffffu, lane < m && rk[0] < need);
+    const unsigned win1 = __ballot_sync(0xffffffffu, lane + 32 < m && rk[1] < need);
+    // chosen members before this thread's blocks (global member index < g)
+    const int g = ms[warp] + mp;
+    const int below = g <= 32 ? __popc(g == 32 ? win0 : (win0 & ((1u << g) - 1u)))
+                              : __popc(win0) + __popc(g == 64 ? win1 : (win1 & ((1u << (g - 32)) - 1u)));
+    pre += below;
+    auto won = [&](int gi) { return gi < 32 ? ((win0 >> gi) & 1u) != 0 : ((win1 >> (gi - 32)) & 1u) != 0; };
+    if (m0) f0 = won(g);
+    if (m1) f1 = won(g + (m0 ? 1 : 0));
+  }
+  if (f0 && pre < k) sel[pre] = j0;
+  if (f1 && pre + (int)f0 < k) sel[pre + (int)f0] = j0 + 1;
+  return true;
+}
+
 // RAG: lengths read after the dependency wait (n_rows, or the call's n when
 // n_rows is NULL); PG: K/V in pages of blk rows, [num_pages, Hkv, blk, D], found
 // through a per-row block table (implies RAG); MK: the multi-turn reading over
@@ -358,7 +497,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     fence_mbar_init();
     // every CTA of the cluster sends its scores and its warps' score bounds to every
     // CTA (per-row lengths are only known after the dependency wait: armed below)
-    if (!RAG) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(a.nblk * 4 + ns * NWARP * 8));
+    if (!RAG) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(a.nblk * 4 + ns * NWARP * 8) + a.sbar_extra_tx);
     // every CTA of the cluster sends its (O, max, sum) of each head this CTA owns
     const int gmine = (int)rank < G ? (G - (int)rank + ns - 1) / ns : 0;
     if (gmine > 0) mbar_arrive_expect_tx(&fs.ebar, (uint32_t)(gmine * ns * PART_STRIDE * 4));
@@ -373,6 +512,17 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   if (tid < 16) {
     fs.mrun[tid] = neg_inf();
     fs.lrun[tid] = 0.f;
+  }
+  // The group's query rows and the appended key / value are read first after
+  // the dependency wait: ask L2 for them now (a prefetch brings nothing into
+  // the CTA, so it may run while the previous kernel still writes them).
+  if (tid == 32) {
+    prefetch_l2_bulk(reinterpret_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)hk * G) * HD,
+                     (uint32_t)(G * HD * 2));
+    if (app) {
+      prefetch_l2_bulk(a.k_new + (size_t)pair * HD, HD * 2);
+      prefetch_l2_bulk(a.v_new + (size_t)pair * HD, HD * 2);
+    }
   }
   // every CTA of the cluster must have started before a DSMEM store reaches it;
   // the matching wait (start of phase B) precedes the first remote store (phase B)
@@ -391,7 +541,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     jhi = min(nblk, jlo + cpr);
     own_new = app && nb_new >= jlo && nb_new < jhi;
     // (a remote byte count arriving before this arrival is fine: the phase needs both)
-    if (tid == 0) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(nblk * 4 + ns * NWARP * 8));
+    if (tid == 0) mbar_arrive_expect_tx(&fs.sbar, (uint32_t)(nblk * 4 + ns * NWARP * 8) + a.sbar_extra_tx);
   }
   if (PG) {
     // this row's block table (published by the barriers of phase A); a page id out
@@ -613,7 +763,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     for (int cb0 = jlo; cb0 < jhi; cb0 += bc) {
       const int nb_here = min(bc, jhi - cb0);
       if (spec) {
-        if (!mbar_wait(&fs.ktbar, 0, &g_hsa_err)) mbar_wait(&fs.ktbar, 0, &g_hsa_err);
+        if (!mbar_wait(&fs.ktbar, 0, &g_hsa_err, a.wait_ns)) mbar_wait(&fs.ktbar, 0, &g_hsa_err, a.wait_ns);
         if (own_new) {
           // fold the appended key into its block in every KT row and persist the column
           const int col = nb_new - cb0;
@@ -751,7 +901,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       const uint32_t off = smem_u32(&fs.rbound[(int)rank * NWARP + warp]);
       st_async_v2f32(mapa(off, lane), smn, smx, mapa(sbar_local, lane));
     }
-    if (!mbar_wait(&fs.sbar, 0, &g_hsa_err)) mbar_wait(&fs.sbar, 0, &g_hsa_err);
+    if (!mbar_wait(&fs.sbar, 0, &g_hsa_err, a.wait_ns)) mbar_wait(&fs.sbar, 0, &g_hsa_err, a.wait_ns);
     {
       // every warp combines the ns * NWARP (<= 64) bounds, two per lane
       const int nb = ns * NWARP;
@@ -772,7 +922,9 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
   if (k2e >= nblk) {
     for (int j = tid; j < nblk; j += NT) sel[j] = j;
   } else {
-    topk_list(sval, nblk, k2e, smn, smx, flag, sel, fs);
+    const bool done = nblk <= 2 * NT && smx > smn && isfinite(smx - smn) &&
+                      topk_small(sval, nblk, k2e, smn, smx, sel, fs);
+    if (!done) topk_list(sval, nblk, k2e, smn, smx, flag, sel, fs);
   }
   __syncthreads();
 
@@ -913,7 +1065,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       if (!gat) {
         const int sa = divb(c0), sb = min(divb(c0 + 15), nsl - 1);
         for (int s = sa; s <= sb; ++s)
-          if (!mbar_wait(&fs.mbar[s], phase, err)) mbar_wait(&fs.mbar[s], phase, err);
+          if (!mbar_wait(&fs.mbar[s], phase, err, a.wait_ns)) mbar_wait(&fs.mbar[s], phase, err, a.wait_ns);
         if (F8) {
           // this warp's 16 key and value rows: codes (row r at byte r*128 of each
           // tile's hi half) to bf16 code values in the swizzled tiles, in place
@@ -1238,7 +1390,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
     }
   }
   if ((int)rank < G) {
-    if (!mbar_wait(&fs.ebar, 0, err)) mbar_wait(&fs.ebar, 0, err);
+    if (!mbar_wait(&fs.ebar, 0, err, a.wait_ns)) mbar_wait(&fs.ebar, 0, err, a.wait_ns);
   }
   for (int gl = 0; gl < gown; ++gl) {
     const int g = gl * ns + (int)rank;

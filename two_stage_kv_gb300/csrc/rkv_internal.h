@@ -11,6 +11,7 @@
 namespace rkv {
 
 constexpr int HD_HOST = 128;   // head dimension of the implemented path
+constexpr uint64_t WAIT_LIMIT_NS_HOST = 1000000000ull;   // limit of a bounded device wait (1 s)
 
 // ------------------------------------------------------------ HSA decode ---
 struct HsaArgs {
@@ -49,6 +50,8 @@ struct HsaArgs {
   int32_t wflash;       // 1: per-warp online softmax (several staging rounds per CTA, narrow groups)
   int32_t tma_kv;       // 1: K/V block rows by TMA (blk a multiple of 8, no idx); 0: gathered rows
   float scale_log2;     // softmax scale * log2(e)
+  uint64_t wait_ns;     // limit of each bounded wait (WAIT_LIMIT_NS unless shortened for a test)
+  uint32_t sbar_extra_tx;   // test only: bytes the block-score barrier expects that no copy delivers
   // dynamic shared-memory layout (bytes)
   uint32_t off_x, off_scores, off_flags, off_sel, off_bt, off_recv, off_tiles, tile_half_bytes, smem_bytes;
 };

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
 EXPORTED = ["rkv_last_error", "rkv_abi_version", "rkv_budget_split", "rkv_snap_evict_workspace",
             "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_compact_kt_paged", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
             "rkv_hsa_decode_ragged", "rkv_hsa_decode_paged", "rkv_keep_mask", "rkv_build_kt_masked",
-            "rkv_hsa_decode_mt_masked", "rkv_compact_kt_fp8", "rkv_hsa_decode_fp8", "rkv_read_device_flags"]
+            "rkv_hsa_decode_mt_masked", "rkv_compact_kt_fp8", "rkv_hsa_decode_fp8", "rkv_debug_set_wait",
+            "rkv_read_device_flags"]
 
 
 class RkvError(RuntimeError):
@@ -71,6 +72,7 @@ _SIGS = {
                                   _vp]),
     "rkv_hsa_decode_fp8": (_i32, [Dims, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _f32, _vp,
                                   _vp, _vp, _vp, _vp, _vp]),
+    "rkv_debug_set_wait": (_i32, [ctypes.c_uint64, ctypes.c_uint32]),
     "rkv_read_device_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -233,6 +235,10 @@ def rkv_hsa_decode_fp8(dims, q, k, v, cap, n, k_scale, v_scale, kt, nblk_cap, bl
     _check(lib().rkv_hsa_decode_fp8(_dims(dims), _ptr(q), _ptr(k), _ptr(v), cap, n, _ptr(k_scale), _ptr(v_scale),
                                     _ptr(kt), nblk_cap, blk, k1, k2, scale, _ptr(out), _ptr(sel_blocks),
                                     _ptr(sel_channels), _ptr(k_new), _ptr(v_new), _stream(stream)))
+
+
+def rkv_debug_set_wait(limit_ns: int, extra_bytes: int) -> None:
+    _check(lib().rkv_debug_set_wait(limit_ns, extra_bytes))
 
 
 def rkv_read_device_flags() -> int:
