@@ -88,6 +88,11 @@ struct FixedSmem {
   uint32_t relig[MAX_ROUND_ROWS / 32];  // masked MT: candidate rows of the staged round
 };
 
+// Inverse of f2key.
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Block-wide exclusive scan of a flag.  Returns the prefix, writes the total.
 __device__ __forceinline__ int scan1(bool f, int32_t* wsum, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -892,11 +897,8 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      smn = fminf(smn, __shfl_xor_sync(0xffffffffu, smn, o));
-      smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, o));
-    }
+    smn = key2f(__reduce_min_sync(0xffffffffu, f2key(smn)));
+    smx = key2f(__reduce_max_sync(0xffffffffu, f2key(smx)));
     if (lane < ns) {
       const uint32_t off = smem_u32(&fs.rbound[(int)rank * NWARP + warp]);
       st_async_v2f32(mapa(off, lane), smn, smx, mapa(sbar_local, lane));
@@ -909,11 +911,8 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       const float2 r1 = lane + 32 < nb ? fs.rbound[lane + 32] : make_float2(__int_as_float(0x7f800000), neg_inf());
       smn = fminf(r0.x, r1.x);
       smx = fmaxf(r0.y, r1.y);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        smn = fminf(smn, __shfl_xor_sync(0xffffffffu, smn, o));
-        smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, o));
-      }
+      smn = key2f(__reduce_min_sync(0xffffffffu, f2key(smn)));
+      smx = key2f(__reduce_max_sync(0xffffffffu, f2key(smx)));
     }
   }
 
