@@ -71,10 +71,23 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the source the HSA launch depends on: the kernel file, the device
+    helpers, the HsaArgs structure and the host function that plans and launches it."""
+    csrc = os.path.join(ROOT, "two_stage_kv_gb300", "csrc")
+
+    def read(f):
+        with open(os.path.join(csrc, f)) as fh:
+            return fh.read()
+
+    def between(text, start, end):
+        i = text.index(start)
+        return text[i:text.index(end, i)]
+
     h = hashlib.sha256()
-    for f in ["rkv_hsa.cu", "rkv_common.cuh", "rkv_internal.h", "rkv_api.cu"]:
-        with open(os.path.join(ROOT, "two_stage_kv_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    h.update(read("rkv_hsa.cu").encode())
+    h.update(read("rkv_common.cuh").encode())
+    h.update(between(read("rkv_internal.h"), "struct HsaArgs {", "};").encode())
+    h.update(between(read("rkv_api.cu"), "rkv_status hsa_common(", "\n}\n").encode())
     return h.hexdigest()[:16]
 
 
