@@ -120,6 +120,58 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
                           float* pooled_out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Stage 1 for a batch whose rows hold prompts of different lengths, each with
+ * its own keep count (ragged batch).  [RocketKV digest, 方法细节: SnapKV in
+ * stage 1, GQA group-level token selection, pooling kernel size 63, per
+ * request]  Same computation, arguments and results as rkv_snap_evict for
+ * every batch row b on its own prompt of S_b tokens and keep count B1_b:
+ * window = the row's last W tokens (q_obs[b] holds their queries), prefix
+ * [0, S_b - W), keep[b, h, 0:B1_b] ascending, compacted rows [0, B1_b).  A row
+ * with S_b <= W, or B1_b >= S_b, keeps all its S_b tokens.
+ *   S_rows   [B] int32 DEVICE array of prompt lengths; S_max >= every entry
+ *            sizes the launch (entries are clamped into [1, S_max]).
+ *   B1_rows  [B] int32 DEVICE array of keep counts; B1_max >= every entry
+ *            (entries are clamped into [min(W + sinks, hi), hi] with hi =
+ *            min(S_b, B1_max)); B1_max >= min(S_max, W + n_sink + 1).
+ *   k, v     [B, Hkv, cap, D] with S_max <= cap; row b's tokens are rows [0, S_b).
+ *   pooled_out optional [B, Hkv, S_max - W] fp32: entries [0, S_b - W) of row b
+ *            (not written for a row that keeps all its tokens).
+ *   ws       rkv_snap_evict_workspace(d, S_max, W) bytes.
+ * keep_ld and out_cap bound B1_max as in rkv_snap_evict; entries of keep and
+ * of the compacted caches past a row's B1_b are not written.  A clamped
+ * length or keep count sets bit 1 of the device error word.
+ */
+rkv_status rkv_snap_evict_ragged(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v,
+                                 int64_t cap, const int32_t* S_rows, int64_t S_max, int32_t pool_kernel,
+                                 int32_t n_sink, const int32_t* B1_rows, int64_t B1_max, float scale,
+                                 int32_t* keep_idx, int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap,
+                                 float* pooled_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stage 1 over a paged prompt cache.  [RocketKV digest, 方法细节: SnapKV in
+ * stage 1, per request, over a cache held in pages]  Same computation and
+ * results as rkv_snap_evict_ragged, with each batch row's prompt K/V rows held
+ * in pages of `page` rows shared by the whole batch:
+ *   k_pages,v_pages [num_pages, Hkv, page, D] bf16 (16-byte aligned);
+ *   block_table     [B, bt_stride] int32 DEVICE array: prompt rows
+ *                   j*page .. j*page + page-1 of batch row b (every KV head)
+ *                   are page block_table[b, j]; bt_stride * page >= S_max;
+ *                   page ids are clamped into [0, num_pages) and a clamped id
+ *                   sets bit 1 of the device error word;
+ *   page            rows per page: a power of two in [8, 128];
+ *   S_rows, B1_rows per-row prompt lengths and keep counts as in
+ *                   rkv_snap_evict_ragged, or NULL: every row has S_max / B1_max.
+ * The compacted caches k_out / v_out (when set) are dense [B, Hkv, out_cap, D]:
+ * rkv_compact_kt_paged can move them into pages of the decode pool.
+ */
+rkv_status rkv_snap_evict_paged(rkv_dims d, const void* q_obs, int32_t W, const void* k_pages, const void* v_pages,
+                                int64_t num_pages, int32_t page, const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* S_rows, int64_t S_max, int32_t pool_kernel, int32_t n_sink,
+                                const int32_t* B1_rows, int64_t B1_max, float scale, int32_t* keep_idx,
+                                int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Stage-1 eviction for callers that cannot allocate device memory.  The
  * paper has no counterpart to this entry point; it exists for serving
  * engines whose memory pool owns all device memory and for plugin hooks that
@@ -409,7 +461,8 @@ rkv_status rkv_debug_set_wait(uint64_t limit_ns, uint32_t extra_bytes);
 /*
  * Read and clear the library's device error word (synchronises the device).
  * Bit 0: a bounded wait for an asynchronous copy gave up in some kernel.
- * Bit 1: a per-row length or page id read from device memory was out of range.
+ * Bit 1: a per-row length, keep count or page id read from device memory was
+ *        out of range (it was clamped).
  * Returns RKV_ERR_TIMEOUT if any bit was set, RKV_OK otherwise.
  */
 rkv_status rkv_read_device_flags(uint32_t* flags);

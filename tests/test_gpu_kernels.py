@@ -748,6 +748,166 @@ def test_snap_evict_mask_mode_and_peaked():
     _snap_case(9, 1, 32, 8, 3000, 32, 63, 400, compact=False, q_scale=4.0)
 
 
+@pytest.mark.parametrize("S_rows,B1_rows,Hq,n_sink,compact", [
+    ([2500, 6000, 1111, 4097], [400, 900, 200, 700], 32, 0, True),     # lengths off the 2048-key chunk and W
+    ([3000, 20, 5000], [300, 20, 5000], 32, 0, False),                 # a row shorter than W, a row keeping all
+    ([7000, 2049, 3333], [1000, 300, 600], 64, 4, True),                # G = 8, sinks
+])
+def test_snap_evict_ragged_parity(S_rows, B1_rows, Hq, n_sink, compact):
+    """Per-row prompt lengths and keep counts in one launch: every row matches
+    the oracle's stage 1 on its own prefix (pooled scores within 1e-4, keep set
+    under the tie rule, window and sinks kept, compaction bit-exact), and no
+    keep entry or compacted row past a row's own count is written."""
+    B, Hkv, D, W, P = len(S_rows), 8, 128, 32, 63
+    G = Hq // Hkv
+    dims = (B, Hq, Hkv, D)
+    S_max, B1_max = max(S_rows), max(B1_rows)
+    cap = S_max + 7
+    scale = 1 / math.sqrt(D)
+    kb, k = _rand(701, (B, Hkv, cap, D))
+    vb, v = _rand(702, (B, Hkv, cap, D))
+    qb, q = _rand(703, (B, Hq, W, D))
+    keep = torch.full((B, Hkv, B1_max + 3), -5, dtype=torch.int32, device=DEV)
+    ko = torch.full((B, Hkv, B1_max + 1, D), float("nan"), dtype=torch.bfloat16, device=DEV) if compact else None
+    vo = torch.full_like(ko, float("nan")) if compact else None
+    Lmax = max(S_max - W, 1)
+    pooled = torch.full((B, Hkv, Lmax), float("nan"), dtype=torch.float32, device=DEV)
+    ws_bytes = rkv.rkv_snap_evict_workspace(dims, S_max, W)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=DEV)
+    S_dev = torch.tensor(S_rows, dtype=torch.int32, device=DEV)
+    B1_dev = torch.tensor(B1_rows, dtype=torch.int32, device=DEV)
+    rkv.rkv_snap_evict_ragged(dims, q, W, k, v, cap, S_dev, S_max, P, n_sink, B1_dev, B1_max, scale, keep,
+                              B1_max + 3, ko, vo, B1_max + 1, pooled, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert rkv.rkv_read_device_flags() == 0
+    keep_h = keep.cpu().numpy()
+    kf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(qb)
+    for b in range(B):
+        S, B1 = S_rows[b], min(B1_rows[b], S_rows[b])
+        L = max(S - W, 0)
+        for h in range(Hkv):
+            got = keep_h[b, h, :B1]
+            assert np.all(keep_h[b, h, B1:] == -5), f"row {b}: keep written past B1_b"
+            if compact:
+                assert torch.isnan(ko[b, h, B1:].float()).all() and torch.isnan(vo[b, h, B1:].float()).all()
+            if B1 >= S or L == 0:
+                assert got.tolist() == list(range(S))
+            else:
+                ref, pooled_o = oracle.snap_keep(qf[b, h * G:(h + 1) * G], kf[b, h, :S], B1, W, P, scale, n_sink)
+                pg = pooled[b, h, :L].cpu().numpy().astype(np.float64)
+                assert np.max(np.abs(pg - pooled_o) / np.maximum(np.abs(pooled_o), 1e-30)) < 1e-4, f"row {b} pooled"
+                ns = min(n_sink, L)
+                assert got[:ns].tolist() == list(range(ns))
+                assert got[B1 - W:].tolist() == list(range(S - W, S))
+                check_topk(got[ns:B1 - W] - ns, pooled_o[ns:], B1 - W - ns, f"row {b} keep")
+            if compact:
+                assert np.array_equal(t2bits(ko[b, h, :B1]), kb[b, h][got])
+                assert np.array_equal(t2bits(vo[b, h, :B1]), vb[b, h][got])
+
+
+@pytest.mark.parametrize("page,S_rows,B1_rows,compact", [
+    (16, [2500, 6000, 1111], [400, 900, 200], True),
+    (64, [4097, 3000], [700, 3000], True),          # the second row keeps everything
+    (128, [5000, 2049, 777], [600, 300, 120], False),
+])
+def test_snap_evict_paged_parity(page, S_rows, B1_rows, compact):
+    """Stage 1 reading its prompt K/V through a block table: each row's prompt is
+    scattered over a shuffled set of pages (unused page slots hold large random
+    rows).  Every row matches the oracle on its own prefix (pooled scores within
+    1e-4, keep set under the tie rule, compaction bit-exact), and the keep lists
+    and pooled scores equal rkv_snap_evict_ragged's over the same rows held
+    densely."""
+    B, Hq, Hkv, D, W, P = len(S_rows), 32, 8, 128, 32, 63
+    G = Hq // Hkv
+    dims = (B, Hq, Hkv, D)
+    S_max, B1_max = max(S_rows), max(B1_rows)
+    npg_row = -(-S_max // page)
+    scale = 1 / math.sqrt(D)
+    kb = small_random(721 + page, (B, Hkv, npg_row * page, D))
+    vb = small_random(722 + page, (B, Hkv, npg_row * page, D))
+    qb, q = _rand(723 + page, (B, Hq, W, D))
+    rng = np.random.default_rng(page)
+    bt, num_pages = _page_table(rng, B, npg_row, 5)
+    kpb = small_random(724 + page, (num_pages, Hkv, page, D), 50.0)
+    vpb = small_random(725 + page, (num_pages, Hkv, page, D), 50.0)
+    for b in range(B):
+        for j in range(-(-S_rows[b] // page)):
+            r = min(page, S_rows[b] - j * page)
+            kpb[bt[b, j], :, :r] = kb[b, :, j * page:j * page + r]
+            vpb[bt[b, j], :, :r] = vb[b, :, j * page:j * page + r]
+    S_dev = torch.tensor(S_rows, dtype=torch.int32, device=DEV)
+    B1_dev = torch.tensor(B1_rows, dtype=torch.int32, device=DEV)
+    ws_bytes = rkv.rkv_snap_evict_workspace(dims, S_max, W)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=DEV)
+    Lmax = S_max - W
+
+    def run(paged):
+        keep = torch.full((B, Hkv, B1_max + 2), -5, dtype=torch.int32, device=DEV)
+        ko = torch.full((B, Hkv, B1_max, D), float("nan"), dtype=torch.bfloat16, device=DEV) if compact else None
+        vo = torch.full_like(ko, float("nan")) if compact else None
+        pooled = torch.full((B, Hkv, Lmax), float("nan"), dtype=torch.float32, device=DEV)
+        if paged:
+            rkv.rkv_snap_evict_paged(dims, q, W, _bf16(kpb), _bf16(vpb), num_pages, page,
+                                     torch.from_numpy(bt).to(DEV), npg_row, S_dev, S_max, P, 0, B1_dev, B1_max, scale,
+                                     keep, B1_max + 2, ko, vo, B1_max, pooled, ws, ws_bytes)
+        else:
+            rkv.rkv_snap_evict_ragged(dims, q, W, _bf16(kb), _bf16(vb), npg_row * page, S_dev, S_max, P, 0, B1_dev,
+                                      B1_max, scale, keep, B1_max + 2, ko, vo, B1_max, pooled, ws, ws_bytes)
+        torch.cuda.synchronize()
+        assert rkv.rkv_read_device_flags() == 0
+        return keep, ko, vo, pooled
+
+    keep, ko, vo, pooled = run(True)
+    keep_d, _, _, pooled_d = run(False)
+    assert torch.equal(keep, keep_d)
+    for b in range(B):
+        L = max(S_rows[b] - W, 0)
+        if B1_rows[b] < S_rows[b]:              # (a row that keeps everything scores nothing)
+            assert torch.equal(pooled[b, :, :L], pooled_d[b, :, :L])
+    keep_h = keep.cpu().numpy()
+    kf, qf = bf16_bits_to_f64(kb), bf16_bits_to_f64(qb)
+    for b in range(B):
+        S, B1 = S_rows[b], min(B1_rows[b], S_rows[b])
+        L = S - W
+        for h in range(Hkv):
+            got = keep_h[b, h, :B1]
+            assert np.all(keep_h[b, h, B1:] == -5)
+            if B1 >= S:
+                assert got.tolist() == list(range(S))
+            else:
+                ref, pooled_o = oracle.snap_keep(qf[b, h * G:(h + 1) * G], kf[b, h, :S], B1, W, P, scale)
+                pg = pooled[b, h, :L].cpu().numpy().astype(np.float64)
+                assert np.max(np.abs(pg - pooled_o) / np.maximum(np.abs(pooled_o), 1e-30)) < 1e-4
+                assert got[B1 - W:].tolist() == list(range(S - W, S))
+                check_topk(got[:B1 - W], pooled_o, B1 - W, f"row {b} keep")
+            if compact:
+                assert np.array_equal(t2bits(ko[b, h, :B1]), kb[b, h][got])
+                assert np.array_equal(t2bits(vo[b, h, :B1]), vb[b, h][got])
+
+
+def test_snap_evict_ragged_out_of_range_flagged():
+    """A prompt length past S_max and a keep count below the window are clamped
+    (row 0 to S_max, row 1 to W + 0) and set bit 1 of the device error word."""
+    B, Hq, Hkv, D, W, P = 2, 32, 8, 128, 32, 63
+    dims = (B, Hq, Hkv, D)
+    S_max, B1_max = 3000, 500
+    cap = S_max
+    _, k = _rand(711, (B, Hkv, cap, D))
+    _, q = _rand(712, (B, Hq, W, D))
+    keep = torch.full((B, Hkv, B1_max), -5, dtype=torch.int32, device=DEV)
+    ws_bytes = rkv.rkv_snap_evict_workspace(dims, S_max, W)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    rkv.rkv_snap_evict_ragged(dims, q, W, k, None, cap, torch.tensor([9000, 2000], dtype=torch.int32, device=DEV),
+                              S_max, P, 0, torch.tensor([400, 3], dtype=torch.int32, device=DEV), B1_max, 0.1, keep,
+                              B1_max, None, None, 0, None, ws, ws_bytes)
+    with pytest.raises(rkv.RkvError) as e:
+        rkv.rkv_read_device_flags()
+    assert "0x2" in str(e.value)
+    keep_h = keep.cpu().numpy()
+    assert keep_h[0, :, 400 - W:400].tolist() == [list(range(S_max - W, S_max))] * Hkv
+    assert keep_h[1, :, :W].tolist() == [list(range(2000 - W, 2000))] * Hkv and np.all(keep_h[1, :, W:] == -5)
+
+
 # ------------------------------------------------------------- fused append --
 
 

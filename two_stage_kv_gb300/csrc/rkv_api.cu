@@ -302,69 +302,107 @@ size_t rkv_snap_evict_workspace(rkv_dims d, int64_t S, int32_t W) {
   return rkv::snap_workspace_bytes(d.batch, d.n_q_heads, d.n_kv_heads, S, (int32_t)w);
 }
 
-rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v, int64_t cap,
-                          int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1, float scale, int32_t* keep_idx,
-                          int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out, void* ws, size_t ws_bytes,
-                          void* stream) {
-  TraceRange trace("rkv_snap_evict");
+}  // extern "C"
+
+namespace {
+
+// Stage 1 for both entry points: S / B1 are the call's lengths, or with
+// per-row arrays their maxima.
+rkv_status snap_common(const char* who, rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v,
+                       int64_t cap, int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1, float scale,
+                       int32_t* keep_idx, int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out,
+                       void* ws, size_t ws_bytes, void* stream, const int32_t* S_rows, const int32_t* B1_rows,
+                       bool per_row, const int32_t* bt = nullptr, int64_t bt_stride = 0, int64_t num_pages = 0,
+                       int32_t page = 0) {
   rkv_status s = check_dims(d);
   if (s != RKV_OK) return s;
   if (d.batch == 0) return RKV_OK;
-  if (!q_obs || !k || !keep_idx) return fail(RKV_ERR_INVALID_ARG, "snap_evict: NULL q_obs, k or keep_idx");
+  const bool ragged = per_row;
+  if (!q_obs || !k || !keep_idx) return fail(RKV_ERR_INVALID_ARG, "%s: NULL q_obs, k or keep_idx", who);
   if ((k_out == nullptr) != (v_out == nullptr))
-    return fail(RKV_ERR_INVALID_ARG, "snap_evict: k_out and v_out must both be set or both be NULL");
-  if (k_out && !v) return fail(RKV_ERR_INVALID_ARG, "snap_evict: v is NULL but compaction was requested");
+    return fail(RKV_ERR_INVALID_ARG, "%s: k_out and v_out must both be set or both be NULL", who);
+  if (k_out && !v) return fail(RKV_ERR_INVALID_ARG, "%s: v is NULL but compaction was requested", who);
   if (!aligned16(q_obs) || !aligned16(k) || (v && !aligned16(v)) || (k_out && (!aligned16(k_out) || !aligned16(v_out))))
-    return fail(RKV_ERR_INVALID_ARG, "snap_evict: tensors must be 16-byte aligned");
-  if (W < 1) return fail(RKV_ERR_INVALID_ARG, "snap_evict: W=%d < 1", W);
-  if (S < 1 || S > cap) return fail(RKV_ERR_INVALID_ARG, "snap_evict: S=%lld outside [1, cap=%lld]", (long long)S,
+    return fail(RKV_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", who);
+  if ((reinterpret_cast<uintptr_t>(S_rows) & 3u) || (reinterpret_cast<uintptr_t>(B1_rows) & 3u) ||
+      (reinterpret_cast<uintptr_t>(bt) & 3u))
+    return fail(RKV_ERR_INVALID_ARG, "%s: S_rows, B1_rows and block_table must be 4-byte aligned", who);
+  int32_t page_shift = 0;
+  if (bt) {
+    if (page < 8 || page > 128 || (page & (page - 1)) != 0)
+      return fail(RKV_ERR_UNSUPPORTED, "%s: page of %d rows (a power of two in [8, 128] is required)", who, page);
+    page_shift = __builtin_ctz((unsigned)page);
+    if (num_pages < 1 || num_pages * d.n_kv_heads >= ((int64_t)1 << 31))
+      return fail(RKV_ERR_INVALID_ARG, "%s: num_pages=%lld out of range", who, (long long)num_pages);
+    if (bt_stride * page < S)
+      return fail(RKV_ERR_INVALID_ARG, "%s: bt_stride=%lld pages cover fewer than S_max=%lld rows", who,
+                  (long long)bt_stride, (long long)S);
+    cap = bt_stride * page;       // rows a batch row's pages cover
+  }
+  if (W < 1) return fail(RKV_ERR_INVALID_ARG, "%s: W=%d < 1", who, W);
+  if (S < 1 || S > cap) return fail(RKV_ERR_INVALID_ARG, "%s: S=%lld outside [1, cap=%lld]", who, (long long)S,
                                     (long long)cap);
-  if (cap >= (int64_t)1 << 31) return fail(RKV_ERR_UNSUPPORTED, "snap_evict: cap >= 2^31");
+  if (ragged && B1 > S) B1 = S;       // (a keep count past the longest prompt keeps it whole)
+  if (cap >= (int64_t)1 << 31) return fail(RKV_ERR_UNSUPPORTED, "%s: cap >= 2^31", who);
   if (pool_kernel < 1 || pool_kernel % 2 == 0 || pool_kernel > 1025)
-    return fail(RKV_ERR_INVALID_ARG, "snap_evict: pool kernel %d must be odd in [1, 1025]", pool_kernel);
-  if (n_sink < 0) return fail(RKV_ERR_INVALID_ARG, "snap_evict: n_sink < 0");
-  const int64_t w = std::min<int64_t>(W, S);
-  const int64_t L = S - w;
+    return fail(RKV_ERR_INVALID_ARG, "%s: pool kernel %d must be odd in [1, 1025]", who, pool_kernel);
+  if (n_sink < 0) return fail(RKV_ERR_INVALID_ARG, "%s: n_sink < 0", who);
+  const int64_t w = ragged ? W : std::min<int64_t>(W, S);
+  const int64_t L = std::max<int64_t>(S - w, 0);
   const int64_t sinks = std::min<int64_t>(n_sink, L);
-  const bool keep_all = B1 >= S || L <= 0;
-  if (keep_all && B1 != S)
-    return fail(RKV_ERR_INVALID_ARG, "snap_evict: B1=%lld must equal S=%lld when nothing is evicted",
-                (long long)B1, (long long)S);
-  if (!keep_all && B1 < w + sinks)
-    return fail(RKV_ERR_INVALID_ARG, "snap_evict: B1=%lld < window %lld + sinks %lld", (long long)B1, (long long)w,
-                (long long)sinks);
-  if (keep_ld < B1) return fail(RKV_ERR_INVALID_ARG, "snap_evict: keep_ld=%lld < B1", (long long)keep_ld);
-  if (k_out && out_cap < B1) return fail(RKV_ERR_INVALID_ARG, "snap_evict: out_cap=%lld < B1", (long long)out_cap);
-  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "snap_evict: bad scale");
+  const bool keep_all = !ragged && (B1 >= S || L <= 0);
+  if (ragged) {
+    // every row's window and sinks must fit the longest keep list
+    if (B1 < 1 || B1 < std::min<int64_t>(S, (int64_t)W + n_sink + 1))
+      return fail(RKV_ERR_INVALID_ARG, "%s: B1_max=%lld < min(S_max, W + n_sink + 1)", who, (long long)B1);
+  } else {
+    if (keep_all && B1 != S)
+      return fail(RKV_ERR_INVALID_ARG, "%s: B1=%lld must equal S=%lld when nothing is evicted", who, (long long)B1,
+                  (long long)S);
+    if (!keep_all && B1 < w + sinks)
+      return fail(RKV_ERR_INVALID_ARG, "%s: B1=%lld < window %lld + sinks %lld", who, (long long)B1, (long long)w,
+                  (long long)sinks);
+  }
+  if (keep_ld < B1) return fail(RKV_ERR_INVALID_ARG, "%s: keep_ld=%lld < B1", who, (long long)keep_ld);
+  if (k_out && out_cap < B1) return fail(RKV_ERR_INVALID_ARG, "%s: out_cap=%lld < B1", who, (long long)out_cap);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "%s: bad scale", who);
+  const bool scored = !keep_all && L > 0;
   const size_t need = rkv::snap_workspace_bytes(d.batch, d.n_q_heads, d.n_kv_heads, S, (int32_t)w);
-  if (!keep_all && (ws == nullptr || ws_bytes < need))
-    return fail(RKV_ERR_WORKSPACE, "snap_evict: workspace %zu bytes < %zu required", ws_bytes, need);
-  if (!keep_all && (reinterpret_cast<uintptr_t>(ws) & 255u))
-    return fail(RKV_ERR_INVALID_ARG, "snap_evict: workspace must be 256-byte aligned");
+  if (scored && (ws == nullptr || ws_bytes < need))
+    return fail(RKV_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required", who, ws_bytes, need);
+  if (scored && (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(RKV_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
   {
     // (v is read only when the call compacts)
-    const void* ptrs[8] = {q_obs, k, k_out ? v : nullptr, keep_idx, k_out, v_out, pooled_out,
-                           keep_all ? nullptr : ws};
-    const char* names[8] = {"snap_evict: q_obs", "snap_evict: k", "snap_evict: v", "snap_evict: keep_idx",
-                            "snap_evict: k_out", "snap_evict: v_out", "snap_evict: pooled_out", "snap_evict: ws"};
-    for (int i = 0; i < 8; ++i)
+    const void* ptrs[11] = {q_obs, k, k_out ? v : nullptr, keep_idx, k_out, v_out, pooled_out,
+                            scored ? ws : nullptr, S_rows, B1_rows, bt};
+    const char* names[11] = {"q_obs", "k", "v", "keep_idx", "k_out", "v_out", "pooled_out", "ws", "S_rows",
+                             "B1_rows", "block_table"};
+    for (int i = 0; i < 11; ++i)
       if (ptrs[i] && (s = require_device(ptrs[i], names[i])) != RKV_OK) return s;
   }
 
   rkv::SnapArgs a = {};
   a.q_obs = q_obs; a.k = k; a.v = v; a.cap = cap; a.S = S; a.out_cap = out_cap; a.B1 = B1;
   a.B = d.batch; a.Hq = d.n_q_heads; a.Hkv = d.n_kv_heads; a.G = d.n_q_heads / d.n_kv_heads;
-  a.W = (int32_t)w; a.pool = pool_kernel; a.n_sink = (int32_t)sinks;
+  a.W = ragged ? W : (int32_t)w; a.pool = pool_kernel; a.n_sink = ragged ? n_sink : (int32_t)sinks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.keep = keep_idx; a.keep_ld = keep_ld; a.k_out = k_out; a.v_out = v_out; a.pooled_out = pooled_out;
+  a.S_rows = S_rows; a.B1_rows = B1_rows;
+  a.bt = bt; a.bt_stride = bt_stride; a.num_pages = num_pages; a.page_shift = page_shift;
   a.ws = ws; a.ws_bytes = ws_bytes;
   CUtensorMap tmK, tmQ1, tmQ2;
   std::memset(&tmK, 0, sizeof(tmK));
   std::memset(&tmQ1, 0, sizeof(tmQ1));
   std::memset(&tmQ2, 0, sizeof(tmQ2));
-  if (!keep_all) {
+  if (scored) {
     const int64_t qrows = (int64_t)d.batch * d.n_q_heads * W;
-    if ((s = make_kv_map(&tmK, k, (int64_t)d.batch * d.n_kv_heads, cap, S, 128, "k")) != RKV_OK) return s;
+    if (bt) {
+      // one (page, KV head) slab of `page` rows per box
+      if ((s = make_kv_map(&tmK, k, num_pages * d.n_kv_heads, page, page, page, "k pages")) != RKV_OK) return s;
+    } else if ((s = make_kv_map(&tmK, k, (int64_t)d.batch * d.n_kv_heads, cap, S, 128, "k")) != RKV_OK) {
+      return s;
+    }
     if ((s = make_q_map(&tmQ1, q_obs, qrows, 128)) != RKV_OK) return s;
     if ((s = make_q_map(&tmQ2, q_obs, qrows, rkv::snap_pass2_rows(d.n_q_heads / d.n_kv_heads, (int32_t)w))) !=
         RKV_OK)
@@ -373,6 +411,44 @@ rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* 
   cudaError_t e = rkv::snap_launch(a, &tmK, &tmQ1, &tmQ2, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "snap_evict launch");
   return RKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rkv_status rkv_snap_evict(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v, int64_t cap,
+                          int64_t S, int32_t pool_kernel, int32_t n_sink, int64_t B1, float scale, int32_t* keep_idx,
+                          int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out, void* ws,
+                          size_t ws_bytes, void* stream) {
+  TraceRange trace("rkv_snap_evict");
+  return snap_common("snap_evict", d, q_obs, W, k, v, cap, S, pool_kernel, n_sink, B1, scale, keep_idx, keep_ld, k_out,
+                     v_out, out_cap, pooled_out, ws, ws_bytes, stream, nullptr, nullptr, false);
+}
+
+rkv_status rkv_snap_evict_ragged(rkv_dims d, const void* q_obs, int32_t W, const void* k, const void* v, int64_t cap,
+                                 const int32_t* S_rows, int64_t S_max, int32_t pool_kernel, int32_t n_sink,
+                                 const int32_t* B1_rows, int64_t B1_max, float scale, int32_t* keep_idx,
+                                 int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  TraceRange trace("rkv_snap_evict_ragged");
+  if (d.batch > 0 && (!S_rows || !B1_rows))
+    return fail(RKV_ERR_INVALID_ARG, "snap_evict_ragged: S_rows and B1_rows are required");
+  return snap_common("snap_evict_ragged", d, q_obs, W, k, v, cap, S_max, pool_kernel, n_sink, B1_max, scale, keep_idx,
+                     keep_ld, k_out, v_out, out_cap, pooled_out, ws, ws_bytes, stream, S_rows, B1_rows, true);
+}
+
+rkv_status rkv_snap_evict_paged(rkv_dims d, const void* q_obs, int32_t W, const void* k_pages, const void* v_pages,
+                                int64_t num_pages, int32_t page, const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* S_rows, int64_t S_max, int32_t pool_kernel, int32_t n_sink,
+                                const int32_t* B1_rows, int64_t B1_max, float scale, int32_t* keep_idx,
+                                int64_t keep_ld, void* k_out, void* v_out, int64_t out_cap, float* pooled_out,
+                                void* ws, size_t ws_bytes, void* stream) {
+  TraceRange trace("rkv_snap_evict_paged");
+  if (d.batch > 0 && !block_table) return fail(RKV_ERR_INVALID_ARG, "snap_evict_paged: block_table is NULL");
+  return snap_common("snap_evict_paged", d, q_obs, W, k_pages, v_pages, 0, S_max, pool_kernel, n_sink, B1_max, scale,
+                     keep_idx, keep_ld, k_out, v_out, out_cap, pooled_out, ws, ws_bytes, stream, S_rows, B1_rows,
+                     true, block_table, bt_stride, num_pages, page);
 }
 
 rkv_status rkv_build_kt(rkv_dims d, const void* k, int64_t cap, int64_t n, const int32_t* idx, int64_t idx_cap,

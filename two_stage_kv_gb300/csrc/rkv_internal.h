@@ -76,6 +76,11 @@ struct SnapArgs {
   void* k_out;          // [B, Hkv, out_cap, D] or nullptr (mask mode)
   void* v_out;
   float* pooled_out;    // [B, Hkv, S-W] or nullptr
+  const int32_t* S_rows;    // [B] per-row prompt lengths (S is their maximum), or nullptr
+  const int32_t* B1_rows;   // [B] per-row keep counts (B1 is their maximum), or nullptr
+  const int32_t* bt;        // paged prompt cache: k, v are [num_pages, Hkv, page, D] pools and bt [B, bt_stride]
+  int64_t bt_stride, num_pages;   // the page of each logical page of a row; nullptr = dense [B, Hkv, cap, D]
+  int32_t page_shift;       // log2 of the rows per page
   // workspace carve-up
   void* ws;
   size_t ws_bytes;

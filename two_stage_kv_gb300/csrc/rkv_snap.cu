@@ -53,7 +53,11 @@ constexpr uint32_t T_KTILE = T_KEYS * 256;        // 32 KB: two 16 KB k-blocks
 constexpr uint32_t T_QMAX = P2_ROWS * 256;        // 64 KB
 
 struct PassArgs {
-  int64_t S, L;                    // L = S - W prefix keys
+  int64_t S, L;                    // L = S - W prefix keys (per-row lengths: the maxima)
+  const int32_t* S_rows;           // [B] prompt length of each batch row, or nullptr (all rows S)
+  const int32_t* bt;               // paged prompt cache: [B, bt_stride] page of each logical page, or nullptr
+  int64_t bt_stride, num_pages;
+  int32_t page_shift;              // log2 of the rows per page (pages hold 8 .. 128 rows)
   int32_t Hq, Hkv, G, W, R, RG1, RG2, nchunk1, nq2;
   int32_t pairs, nchunk2;
   float scale_log2;
@@ -93,6 +97,49 @@ __device__ __forceinline__ bool epi_any(bool p) {
   return r != 0;
 }
 
+// One batch row's stage-1 lengths.  Without per-row arrays they are the
+// call's own S and B1.  Per-row entries are clamped into range: S_b into
+// [1, S_max]; B1_b into [min(W + sinks, hi), hi] with hi = min(S_b, B1_max)
+// (an entry at or past S_b keeps the whole row and is no error).  `bad` marks
+// a clamped entry.
+struct RowPlan {
+  int S, L, sinks, B1;
+  int64_t ntop;                    // prefix positions chosen by the top-k
+  bool all, bad;                   // every token kept; an entry was out of range
+};
+__device__ __forceinline__ RowPlan row_plan(const int32_t* S_rows, const int32_t* B1_rows, int b, int64_t S_max,
+                                            int64_t B1_max, int W, int n_sink) {
+  RowPlan p;
+  p.bad = false;
+  int64_t S = S_max;
+  if (S_rows) {
+    const int64_t r = S_rows[b];
+    S = min(max(r, (int64_t)1), S_max);
+    p.bad |= S != r;
+  }
+  const int w = (int)min((int64_t)W, S);
+  p.S = (int)S;
+  p.L = (int)(S - w);
+  p.sinks = min(n_sink, p.L);
+  int64_t B1 = B1_max;
+  if (B1_rows) {
+    const int64_t r = B1_rows[b];
+    const int64_t hi = min(S, B1_max), lo = min((int64_t)w + p.sinks, hi);
+    B1 = min(max(r, lo), hi);
+    p.bad |= B1 != r && !(r >= S && B1 == S);
+  }
+  p.all = B1 >= S || p.L <= 0;
+  if (p.all) B1 = S;
+  p.B1 = (int)B1;
+  p.ntop = max((int64_t)0, B1 - w - p.sinks);
+  return p;
+}
+
+// Prompt length of pair `pair`'s batch row.
+__device__ __forceinline__ int64_t pair_S(const PassArgs& a, int pair) {
+  return a.S_rows ? min(max((int64_t)a.S_rows[pair / a.Hkv], (int64_t)1), a.S) : a.S;
+}
+
 // One work item = (pair, row group, key chunk of P_CHUNK keys).  The grid is
 // persistent: CTA c takes the contiguous items [c*n/grid, (c+1)*n/grid), so
 // the K stream, the MMAs and the epilogue run across item boundaries without
@@ -110,10 +157,12 @@ __device__ __forceinline__ PassItem pass_item(const PassArgs& a, int item) {
   const int t2 = item / nchunk;
   it.rg = t2 % RGp;
   it.pair = t2 / RGp;
-  const int64_t kend = (PASS == 1) ? a.S : a.L;
+  // (a batch row shorter than the longest has empty items past its own length)
+  const int64_t Sp = pair_S(a, it.pair);
+  const int64_t kend = (PASS == 1) ? Sp : max(Sp - (int64_t)a.W, (int64_t)0);
   it.j0 = (int64_t)it.chunk * P_CHUNK;
   const int64_t j1 = min(kend, it.j0 + (int64_t)P_CHUNK);
-  it.ntiles = (int)((j1 - it.j0 + T_KEYS - 1) / T_KEYS);
+  it.ntiles = j1 > it.j0 ? (int)((j1 - it.j0 + T_KEYS - 1) / T_KEYS) : 0;
   return it;
 }
 
@@ -198,8 +247,25 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
           if (T >= T_NST && !tc_wait(&ts.empty[s], ((T / T_NST) & 1) ^ 1, abort_flag, err)) break;
           mbar_arrive_expect_tx(&ts.full[s], T_KTILE);
           const int y = (int)(it.j0 + (int64_t)t * T_KEYS);
-          tma_load_3d(sK + s * T_KTILE, &tmK, 0, y, it.pair, &ts.full[s]);
-          tma_load_3d(sK + s * T_KTILE + T_KTILE / 2, &tmK, 64, y, it.pair, &ts.full[s]);
+          if (a.bt) {
+            // paged prompt: one box per page of the tile (a (page, KV head) slab of
+            // the pool), each channel half; rows of the swizzled tile continue across pages
+            const int b = it.pair / a.Hkv, hk = it.pair - b * a.Hkv;
+            const int lp0 = y >> a.page_shift, npg = T_KEYS >> a.page_shift;
+            const int32_t* btr = a.bt + (size_t)b * a.bt_stride;
+            for (int i = 0; i < npg; ++i) {
+              const int lp = lp0 + i;
+              const int id = lp < a.bt_stride ? __ldg(btr + lp) : 0;
+              const int idc = min(max(id, 0), (int)a.num_pages - 1);
+              if (idc != id && lp < a.bt_stride) atomicOr(err, ERR_BAD_LENGTH);
+              const uint32_t off = ((uint32_t)i << a.page_shift) * 128u;
+              tma_load_3d(sK + s * T_KTILE + off, &tmK, 0, 0, idc * a.Hkv + hk, &ts.full[s]);
+              tma_load_3d(sK + s * T_KTILE + T_KTILE / 2 + off, &tmK, 64, 0, idc * a.Hkv + hk, &ts.full[s]);
+            }
+          } else {
+            tma_load_3d(sK + s * T_KTILE, &tmK, 0, y, it.pair, &ts.full[s]);
+            tma_load_3d(sK + s * T_KTILE + T_KTILE / 2, &tmK, 64, y, it.pair, &ts.full[s]);
+          }
         }
       }
       // every load issued has landed before the CTA can leave (bounded)
@@ -252,12 +318,12 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
     const int r_loc = 32 * quad + lane;              // TMEM lane of this thread
     const int etid = (warp - 2) * 32 + lane;         // 0 .. 255 over both sets
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16) + (uint32_t)(eset * ncols);
-    const int S32 = (int)a.S, L32 = (int)a.L;
     int T0 = 0, key = -1;                            // first tile of the item in the CTA's stream
     for (int ii = ib; ii < ie; ++ii) {
       const PassItem it = pass_item<PASS>(a, item_at<PASS>(ib, ie, ii));
       const int j032 = (int)it.j0;
       const int pair = it.pair;
+      const int S32 = (int)pair_S(a, pair), L32 = max(S32 - a.W, 0);   // this row's prompt and prefix
       const int row0 = it.rg * (PASS == 1 ? P1_ROWS : P2_ROWS);
       const int tfirst = (T0 & 1) == eset ? 0 : 1;   // this set's first tile of the item
       if (PASS == 1) {
@@ -490,20 +556,24 @@ __device__ __forceinline__ float log2_add(float a, float b) {
 constexpr int POOL_TILE = 1024;
 constexpr int POOL_MAX_HALF = 512;
 
-__global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int RG, int64_t L, int half,
-                                                        float* pooled_log, float* pooled_out) {
+__global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int RG, int64_t Ls, int half,
+                                                        float* pooled_log, float* pooled_out, const int32_t* S_rows,
+                                                        int64_t S_max, int Hkv, int W) {
   __shared__ float tile[POOL_TILE + 2 * POOL_MAX_HALF];
   pdl_wait();
   pdl_launch_dependents();
   const int pair = blockIdx.y;
+  // Ls: row stride of the score arrays (the longest prefix); L: this row's prefix
+  const int64_t Sp = S_rows ? min(max((int64_t)S_rows[pair / Hkv], (int64_t)1), S_max) : S_max;
+  const int64_t L = max(Sp - (int64_t)W, (int64_t)0);
   const int64_t j0 = (int64_t)blockIdx.x * POOL_TILE;
   const int span = POOL_TILE + 2 * half;
   for (int i = threadIdx.x; i < span; i += blockDim.x) {
     const int64_t j = j0 - half + i;
     float v = neg_inf();
     if (j >= 0 && j < L) {
-      v = scores[((size_t)pair * RG) * L + j];
-      for (int r = 1; r < RG; ++r) v = log2_add(v, scores[((size_t)pair * RG + r) * L + j]);
+      v = scores[((size_t)pair * RG) * Ls + j];
+      for (int r = 1; r < RG; ++r) v = log2_add(v, scores[((size_t)pair * RG + r) * Ls + j]);
     }
     tile[i] = v;
   }
@@ -513,8 +583,8 @@ __global__ void __launch_bounds__(256) snap_pool_kernel(const float* scores, int
     if (j >= L) break;
     float m = tile[i];
     for (int t = 1; t <= 2 * half; ++t) m = fmaxf(m, tile[i + t]);
-    pooled_log[(size_t)pair * L + j] = m;
-    if (pooled_out) pooled_out[(size_t)pair * L + j] = exp2f(m);
+    pooled_log[(size_t)pair * Ls + j] = m;
+    if (pooled_out) pooled_out[(size_t)pair * Ls + j] = exp2f(m);
   }
 }
 
@@ -545,9 +615,10 @@ __device__ __forceinline__ int block_excl_scan(bool flag, int* wsum, int& total)
   return r;
 }
 
-__global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled, int64_t L, int64_t S, int W,
-                                                             int n_sink, int64_t ntop, int64_t B1,
-                                                             int32_t* keep, int64_t keep_ld) {
+__global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled, int64_t Ls, int64_t S_max,
+                                                             int W0, int n_sink0, int64_t B1_max,
+                                                             int32_t* keep, int64_t keep_ld, const int32_t* S_rows,
+                                                             const int32_t* B1_rows, int Hkv) {
   __shared__ int hist[256];
   __shared__ int wsum[72];
   __shared__ uint32_t sh_digit;
@@ -555,8 +626,18 @@ __global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled
   pdl_wait();
   pdl_launch_dependents();
   const int pair = blockIdx.x, tid = threadIdx.x;
-  const float* p = pooled + (size_t)pair * L;
+  // this row's lengths (Ls: row stride of the pooled scores)
+  const RowPlan rp = row_plan(S_rows, B1_rows, pair / Hkv, S_max, B1_max, W0, n_sink0);
+  if (rp.bad && tid == 0) atomicOr(&g_snap_err, ERR_BAD_LENGTH);
+  const int64_t L = rp.L, S = rp.S, B1 = rp.B1;
+  const int W = (int)(S - L), n_sink = rp.sinks;
+  const int64_t ntop = rp.ntop;
+  const float* p = pooled + (size_t)pair * Ls;
   int32_t* out = keep + (size_t)pair * keep_ld;
+  if (rp.all) {
+    for (int64_t i = tid; i < S; i += SEL_NT) out[i] = (int32_t)i;
+    return;
+  }
   for (int i = tid; i < n_sink; i += SEL_NT) out[i] = i;
   for (int i = tid; i < W; i += SEL_NT) out[B1 - W + i] = (int32_t)(S - W + i);
   if (ntop <= 0) return;
@@ -665,10 +746,11 @@ int pool_select_words(int64_t L, int h) {
   return with_bucket <= PS_MAX_WORDS ? (int)with_bucket : (int)words;
 }
 
-__global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float* scores, int RG, int64_t L64,
-                                                                    int h, int64_t S, int W, int n_sink,
-                                                                    int64_t ntop, int64_t B1, int32_t* keep,
-                                                                    int64_t keep_ld, float* pooled_out) {
+__global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float* scores, int RG, int64_t Ls,
+                                                                    int h, int64_t S_max, int W0, int n_sink0,
+                                                                    int64_t B1_max, int32_t* keep, int64_t keep_ld,
+                                                                    float* pooled_out, const int32_t* S_rows,
+                                                                    const int32_t* B1_rows, int Hkv) {
   extern __shared__ __align__(16) uint32_t xs[];
   __shared__ int hist[256];
   __shared__ int wsum[PS_NT / 32];
@@ -678,16 +760,25 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
   pdl_wait();
   pdl_launch_dependents();
   const int pair = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int L = (int)L64;
+  // this row's lengths (Ls: row stride of the score arrays)
+  const RowPlan rp = row_plan(S_rows, B1_rows, pair / Hkv, S_max, B1_max, W0, n_sink0);
+  if (rp.bad && tid == 0) atomicOr(&g_snap_err, ERR_BAD_LENGTH);
+  const int L = rp.L, S = rp.S, B1 = rp.B1, W = rp.S - rp.L, n_sink = rp.sinks;
+  const int64_t ntop = rp.ntop;
   const int E = h + 1;
   const int nq = (L + E - 1) / E;
   const int U = nq * E + 2 * E;
   int32_t* out = keep + (size_t)pair * keep_ld;
+  if (rp.all) {
+    for (int i = tid; i < S; i += PS_NT) out[i] = i;
+    return;
+  }
   for (int i = tid; i < n_sink; i += PS_NT) out[i] = i;
   for (int i = tid; i < W; i += PS_NT) out[B1 - W + i] = (int32_t)(S - W + i);
+  if (ntop <= 0 && !pooled_out) return;        // only the window and the sinks are kept
 
   // scores of position j = u - h at u (minus infinity outside [0, L))
-  const float* sc = scores + (size_t)pair * RG * L;
+  const float* sc = scores + (size_t)pair * RG * Ls;
   for (int u0 = tid; u0 < U; u0 += 8 * PS_NT) {
     float v[8];                                  // eight independent loads in flight per thread
 #pragma unroll
@@ -699,7 +790,7 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         const int j = u0 + t * PS_NT - h;
-        if (j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * L + j));
+        if (j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * Ls + j));
       }
     }
 #pragma unroll
@@ -737,7 +828,7 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
       }
     }
     if (pooled_out) {
-      float* po = pooled_out + (size_t)pair * L;
+      float* po = pooled_out + (size_t)pair * Ls;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (i < E && a + i < L) po[a + i] = exp2f(pv[i]);
@@ -762,6 +853,7 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
     }
   }
   const int ncand = L - n_sink;
+  if (ntop <= 0) return;                         // (the pooled scores were written above)
   if (ntop >= ncand) {
     for (int j = n_sink + tid; j < L; j += PS_NT) out[j] = j;
     return;
@@ -900,7 +992,8 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
         __syncthreads();
         int pos = n_sink + (int)(inc - cnt);
         for (int w = 0; w < warp; ++w) pos += wsum[w];
-        for (uint32_t bits = tk; bits; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
+        const int pend = n_sink + (int)ntop;        // (exactly ntop are taken; the bound guards the row)
+        for (uint32_t bits = tk; bits && pos < pend; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
         return;
       }
     }
@@ -985,7 +1078,8 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
   const int gt_before = (int)(before & 0xffffu), eq_before = (int)(before >> 16);
   int pos = n_sink + gt_before + min(k, eq_before);
   int eq_seen = eq_before;
-  for (uint32_t bits = gt | eq; bits; bits &= bits - 1u) {
+  const int pend = n_sink + (int)ntop;          // (exactly ntop are taken; the bound guards the row)
+  for (uint32_t bits = gt | eq; bits && pos < pend; bits &= bits - 1u) {
     const int i = __ffs(bits) - 1;
     const bool is_eq = (eq >> i) & 1;
     if (!is_eq || eq_seen < k) out[pos++] = a + i;
@@ -995,18 +1089,31 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
 
 // K_c[i] = K[keep[i]], V_c[i] = V[keep[i]].
 __global__ void __launch_bounds__(256) snap_compact_kernel(const bf16* k, const bf16* v, int64_t cap,
-                                                           const int32_t* keep, int64_t keep_ld, int64_t B1,
-                                                           bf16* ko, bf16* vo, int64_t out_cap) {
+                                                           const int32_t* keep, int64_t keep_ld, int64_t B1_max,
+                                                           bf16* ko, bf16* vo, int64_t out_cap, const int32_t* S_rows,
+                                                           const int32_t* B1_rows, int64_t S_max, int Hkv, int W,
+                                                           int n_sink, const int32_t* bt, int64_t bt_stride,
+                                                           int64_t num_pages, int page_shift) {
   pdl_wait();
   pdl_launch_dependents();
   const int pair = blockIdx.y;
+  const int64_t B1 = row_plan(S_rows, B1_rows, pair / Hkv, S_max, B1_max, W, n_sink).B1;
+  const int b = pair / Hkv, hk = pair - b * Hkv;
   for (int i = threadIdx.x; i < 32 * 16; i += blockDim.x) {
     const int64_t row = (int64_t)blockIdx.x * 32 + i / 16;
     const int ch = i % 16;
     if (row >= B1) break;
     const int64_t src = min(max((int64_t)keep[(size_t)pair * keep_ld + row], (int64_t)0), cap - 1);
-    const uint4 kv = *reinterpret_cast<const uint4*>(k + ((size_t)pair * cap + src) * HD + ch * 8);
-    const uint4 vv = *reinterpret_cast<const uint4*>(v + ((size_t)pair * cap + src) * HD + ch * 8);
+    // dense: row src of the pair; paged: slot src % page of page bt[b, src / page] (cap = rows a row's pages cover)
+    size_t e;
+    if (bt) {
+      const int64_t pg = min(max((int64_t)bt[(size_t)b * bt_stride + (src >> page_shift)], (int64_t)0), num_pages - 1);
+      e = (((size_t)pg * Hkv + hk) << page_shift) + (size_t)(src & ((1 << page_shift) - 1));
+    } else {
+      e = (size_t)pair * cap + src;
+    }
+    const uint4 kv = *reinterpret_cast<const uint4*>(k + e * HD + ch * 8);
+    const uint4 vv = *reinterpret_cast<const uint4*>(v + e * HD + ch * 8);
     *reinterpret_cast<uint4*>(ko + ((size_t)pair * out_cap + row) * HD + ch * 8) = kv;
     *reinterpret_cast<uint4*>(vo + ((size_t)pair * out_cap + row) * HD + ch * 8) = vv;
   }
@@ -1054,13 +1161,21 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int pairs = a.B * a.Hkv;
-  const int W = (int)std::min<int64_t>(a.W, a.S);
-  const int64_t L = a.S - W;
-  const bool keep_all = a.B1 >= a.S || L <= 0;
-  if (!keep_all) {
+  // (per-row lengths: S and B1 are the maxima, W the window of rows longer than it)
+  const bool ragged = a.S_rows != nullptr || a.B1_rows != nullptr || a.bt != nullptr;
+  const int W = ragged ? a.W : (int)std::min<int64_t>(a.W, a.S);
+  const int64_t L = std::max<int64_t>(a.S - W, 0);
+  const bool keep_all = !ragged && (a.B1 >= a.S || L <= 0);
+  const int n_sink = (int)std::max<int64_t>(0, std::min<int64_t>(a.n_sink, L));
+  if (!keep_all && L > 0) {
     PassArgs p;
     p.S = a.S;
     p.L = L;
+    p.S_rows = a.S_rows;
+    p.bt = a.bt;
+    p.bt_stride = a.bt_stride;
+    p.num_pages = a.num_pages;
+    p.page_shift = a.page_shift;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.G = a.G;
@@ -1088,34 +1203,37 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     e = launch_pdl(snap_pass_kernel<2>, dim3((unsigned)std::min(items2, snap_num_sms())), dim3(T_NT), T_SMEM, st,
                    *tmK, *tmQ2, p);
     if (e != cudaSuccess) return e;
-    const int n_sink = (int)std::max<int64_t>(0, std::min<int64_t>(a.n_sink, L));
-    const int64_t ntop = std::max<int64_t>(0, a.B1 - W - n_sink);
     const int half = (int)(a.pool / 2);
     const int ps_words = pool_select_words(L, half);
     if (ps_words > 0 && ps_attr_err == cudaSuccess) {
       e = launch_pdl(snap_pool_select_kernel, dim3(pairs), dim3(PS_NT), (size_t)ps_words * 4u, st,
-                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, (int64_t)a.S, (int)W, (int)n_sink,
-                     (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.pooled_out);
+                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, (int64_t)a.S, (int)W, (int)a.n_sink,
+                     (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.pooled_out, a.S_rows, a.B1_rows, (int)a.Hkv);
       if (e != cudaSuccess) return e;
     } else {
       e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
-                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, pooled_log, a.pooled_out);
+                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, pooled_log, a.pooled_out, a.S_rows,
+                     (int64_t)a.S, (int)a.Hkv, (int)W);
       if (e != cudaSuccess) return e;
       e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)pooled_log, (int64_t)L,
-                     (int64_t)a.S, (int)W, (int)n_sink, (int64_t)ntop, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
+                     (int64_t)a.S, (int)W, (int)a.n_sink, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.S_rows,
+                     a.B1_rows, (int)a.Hkv);
       if (e != cudaSuccess) return e;
     }
   } else {
-    // every token kept: keep = 0..S-1 (B1 == S enforced by the caller)
+    // every token of every row kept: keep = 0..S_b-1
     cudaError_t e = launch_pdl(snap_select_kernel, dim3(pairs), dim3(SEL_NT), 0, st, (const float*)nullptr, (int64_t)0,
-                               (int64_t)a.S, (int)a.S, 0, (int64_t)0, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld);
+                               (int64_t)a.S, (int)W, n_sink, (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.S_rows,
+                               a.B1_rows, (int)a.Hkv);
     if (e != cudaSuccess) return e;
   }
   if (a.k_out) {
     cudaError_t e = launch_pdl(snap_compact_kernel, dim3((unsigned)((a.B1 + 31) / 32), pairs), dim3(256), 0, st,
                                reinterpret_cast<const bf16*>(a.k), reinterpret_cast<const bf16*>(a.v), (int64_t)a.cap,
                                (const int32_t*)a.keep, (int64_t)a.keep_ld, (int64_t)a.B1,
-                               reinterpret_cast<bf16*>(a.k_out), reinterpret_cast<bf16*>(a.v_out), (int64_t)a.out_cap);
+                               reinterpret_cast<bf16*>(a.k_out), reinterpret_cast<bf16*>(a.v_out), (int64_t)a.out_cap,
+                               a.S_rows, a.B1_rows, (int64_t)a.S, (int)a.Hkv, (int)W, (int)a.n_sink, a.bt,
+                               (int64_t)a.bt_stride, (int64_t)a.num_pages, (int)a.page_shift);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

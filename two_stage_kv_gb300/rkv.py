@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "RKV_OK", 1: "RKV_ERR_INVALID_ARG", 2: "RKV_ERR_UNSUPPORTED",
 
 # Every symbol include/rkv.h declares.
 EXPORTED = ["rkv_last_error", "rkv_abi_version", "rkv_budget_split", "rkv_snap_evict_workspace",
-            "rkv_snap_evict", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_compact_kt_paged", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
+            "rkv_snap_evict", "rkv_snap_evict_ragged", "rkv_snap_evict_paged", "rkv_snap_evict_noalloc", "rkv_compact_kt", "rkv_compact_kt_paged", "rkv_build_kt", "rkv_append_kv", "rkv_hsa_decode", "rkv_hsa_decode_mt",
             "rkv_hsa_decode_ragged", "rkv_hsa_decode_paged", "rkv_keep_mask", "rkv_build_kt_masked",
             "rkv_hsa_decode_mt_masked", "rkv_compact_kt_fp8", "rkv_hsa_decode_fp8", "rkv_debug_set_wait",
             "rkv_read_device_flags"]
@@ -49,6 +49,10 @@ _SIGS = {
     "rkv_snap_evict_workspace": (_sz, [Dims, _i64, _i32]),
     "rkv_snap_evict": (_i32, [Dims, _vp, _i32, _vp, _vp, _i64, _i64, _i32, _i32, _i64, _f32, _vp, _i64, _vp, _vp,
                               _i64, _vp, _vp, _sz, _vp]),
+    "rkv_snap_evict_ragged": (_i32, [Dims, _vp, _i32, _vp, _vp, _i64, _vp, _i64, _i32, _i32, _vp, _i64, _f32, _vp,
+                                     _i64, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "rkv_snap_evict_paged": (_i32, [Dims, _vp, _i32, _vp, _vp, _i64, _i32, _vp, _i64, _vp, _i64, _i32, _i32, _vp,
+                                    _i64, _f32, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "rkv_snap_evict_noalloc": (_i32, [Dims, _vp, _i32, _vp, _vp, _i64, _i64, _i32, _i32, _i64, _f32, _vp, _i64, _vp,
                                       _vp, _i64, _vp, _vp]),
     "rkv_compact_kt": (_i32, [Dims, _vp, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _vp]),
@@ -135,6 +139,23 @@ def rkv_snap_evict(dims, q_obs, W, k, v, cap, S, pool_kernel, n_sink, B1, scale,
     _check(lib().rkv_snap_evict(_dims(dims), _ptr(q_obs), W, _ptr(k), _ptr(v), cap, S, pool_kernel, n_sink, B1,
                                 scale, _ptr(keep_idx), keep_ld, _ptr(k_out), _ptr(v_out), out_cap, _ptr(pooled_out),
                                 _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def rkv_snap_evict_ragged(dims, q_obs, W, k, v, cap, S_rows, S_max, pool_kernel, n_sink, B1_rows, B1_max, scale,
+                          keep_idx, keep_ld, k_out, v_out, out_cap, pooled_out, ws, ws_bytes, stream=None):
+    _check(lib().rkv_snap_evict_ragged(_dims(dims), _ptr(q_obs), W, _ptr(k), _ptr(v), cap, _ptr(S_rows), S_max,
+                                       pool_kernel, n_sink, _ptr(B1_rows), B1_max, scale, _ptr(keep_idx), keep_ld,
+                                       _ptr(k_out), _ptr(v_out), out_cap, _ptr(pooled_out), _ptr(ws), ws_bytes,
+                                       _stream(stream)))
+
+
+def rkv_snap_evict_paged(dims, q_obs, W, k_pages, v_pages, num_pages, page, block_table, bt_stride, S_rows, S_max,
+                         pool_kernel, n_sink, B1_rows, B1_max, scale, keep_idx, keep_ld, k_out, v_out, out_cap,
+                         pooled_out, ws, ws_bytes, stream=None):
+    _check(lib().rkv_snap_evict_paged(_dims(dims), _ptr(q_obs), W, _ptr(k_pages), _ptr(v_pages), num_pages, page,
+                                      _ptr(block_table), bt_stride, _ptr(S_rows), S_max, pool_kernel, n_sink,
+                                      _ptr(B1_rows), B1_max, scale, _ptr(keep_idx), keep_ld, _ptr(k_out), _ptr(v_out),
+                                      out_cap, _ptr(pooled_out), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def rkv_snap_evict_noalloc(dims, q_obs, W, k, v, cap, S, pool_kernel, n_sink, B1, scale, keep_idx, keep_ld, k_out,
