@@ -254,12 +254,12 @@ def run_ours(args, rank, world, local):
         if record:
             ev["d1"].record()
 
-    # two score passes, the fused pool + select (or pool and select apart for long
-    # prefixes), compaction with the KT build, and the fused append + HSA steps
+    # two score passes, the fused pool + select (one CTA, or a cluster of up to 8
+    # for prefixes of up to 2048 pooling groups; pool and select apart beyond),
+    # compaction with the KT build, and the fused append + HSA steps
     E_pool, L_pref = wl.P // 2 + 1, wl.S - wl.W
     nq_pool = -(-L_pref // E_pool)
-    U_pool = nq_pool * E_pool + 2 * E_pool
-    fused_ps = E_pool <= 32 and nq_pool <= 1024 and U_pool + U_pool // 32 + 1 <= 54 * 1024
+    fused_ps = E_pool <= 32 and nq_pool <= 8 * 256
     launches_per_pass = 2 + (1 if fused_ps else 2) + 1 + wl.steps
     with torch.cuda.stream(stream):
         one_pass(record=False)          # sets kernel attributes outside capture

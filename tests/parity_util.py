@@ -36,6 +36,8 @@ def check_topk(gpu_idx, scores, k, what="", rel=REL_TIE):
     scores = np.asarray(scores, dtype=np.float64)
     k = min(k, scores.shape[0])
     assert gpu_idx.shape[0] == k, f"{what}: {gpu_idx.shape[0]} indices, expected {k}"
+    if k == 0:
+        return 0
     assert np.all(np.diff(gpu_idx) > 0), f"{what}: indices not strictly ascending"
     assert gpu_idx.min() >= 0 and gpu_idx.max() < scores.shape[0], f"{what}: index out of range"
     ref = topk_lowest_index(scores, k)

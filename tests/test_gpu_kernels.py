@@ -716,19 +716,26 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
     (1, 32, 8, 200, 32, 63, 200, 0),        # B1 == S: keep all
     (1, 32, 8, 20, 32, 63, 20, 0),          # prompt shorter than the window
     (1, 32, 8, 70000, 32, 63, 900, 0),      # long prompt, many chunks
+    (1, 32, 8, 32768, 32, 63, 1024, 0),     # the 32K batch-8 workload's rows: pool + select over a cluster of 4
+    (2, 32, 8, 20000, 32, 63, 700, 4),      # cluster of 3, sinks, ragged last CTA
+    (1, 32, 8, 12000, 32, 63, 36, 4),       # cluster, keep count with no prefix slot (window and sinks only)
+    (1, 32, 8, 65000, 32, 63, 2000, 0),     # cluster of 8
 ])
 def test_snap_evict_parity(B, Hq, Hkv, S, W, P, B1, sink):
     _snap_case(500 + S, B, Hq, Hkv, S, W, P, B1, sink)
 
 
-def test_snap_evict_all_scores_tied():
+@pytest.mark.parametrize("S", [5000, 20000])
+def test_snap_evict_all_scores_tied(S):
     """Zero window queries: every prefix key gets the same score, so the pooled
-    scores have an empty range and the select takes its radix path; the kept
-    prefix positions must be the lowest ones (no tie-band exemption)."""
-    assert _snap_case(31, 2, 32, 8, 5000, 32, 63, 700, q_scale=0.0) == 0
+    scores have an empty range and the select takes its radix path (in one CTA,
+    or over a cluster for the longer prompt); the kept prefix positions must be
+    the lowest ones (no tie-band exemption)."""
+    assert _snap_case(31, 2, 32, 8, S, 32, 63, 700, q_scale=0.0) == 0
 
 
-def test_snap_evict_crowded_boundary_bucket():
+@pytest.mark.parametrize("S", [5000, 20000])
+def test_snap_evict_crowded_boundary_bucket(S):
     """Window queries zero except one row per group, twice key 5: that key's
     score spans the range and every other pooled score lies within a sliver
     of the minimum, so the 1024-bucket histogram puts thousands of candidates
@@ -741,7 +748,7 @@ def test_snap_evict_crowded_boundary_bucket():
             for h in range(8):
                 qb[b, h * G, 0] = f32_to_bf16_bits(bf16_bits_to_f32(kb[b, h, 5]) * np.float32(2.0))
         return qb
-    _snap_case(41, 1, 32, 8, 5000, 32, 63, 700, qmod=qmod)
+    _snap_case(41, 1, 32, 8, S, 32, 63, 700, qmod=qmod)
 
 
 def test_snap_evict_mask_mode_and_peaked():
@@ -752,6 +759,8 @@ def test_snap_evict_mask_mode_and_peaked():
     ([2500, 6000, 1111, 4097], [400, 900, 200, 700], 32, 0, True),     # lengths off the 2048-key chunk and W
     ([3000, 20, 5000], [300, 20, 5000], 32, 0, False),                 # a row shorter than W, a row keeping all
     ([7000, 2049, 3333], [1000, 300, 600], 64, 4, True),                # G = 8, sinks
+    ([9000, 30000, 300, 16500], [800, 1024, 100, 700], 32, 4, True),   # pool + select over clusters of 4; a
+                                                                        # short row leaves CTAs without positions
 ])
 def test_snap_evict_ragged_parity(S_rows, B1_rows, Hq, n_sink, compact):
     """Per-row prompt lengths and keep counts in one launch: every row matches
@@ -809,6 +818,7 @@ def test_snap_evict_ragged_parity(S_rows, B1_rows, Hq, n_sink, compact):
     (16, [2500, 6000, 1111], [400, 900, 200], True),
     (64, [4097, 3000], [700, 3000], True),          # the second row keeps everything
     (128, [5000, 2049, 777], [600, 300, 120], False),
+    (64, [12000, 3000], [900, 400], True),           # pool + select over a cluster of 2
 ])
 def test_snap_evict_paged_parity(page, S_rows, B1_rows, compact):
     """Stage 1 reading its prompt K/V through a block table: each row's prompt is

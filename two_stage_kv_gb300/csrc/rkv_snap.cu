@@ -32,6 +32,30 @@ namespace rkv {
 
 static __device__ unsigned int g_snap_err = 0;
 
+// Full cluster barrier: release this CTA's prior writes (shared and global
+// memory) to every CTA of the cluster, and acquire theirs.
+// 4-byte asynchronous copy global -> shared (no register staging)
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Loads from another CTA's shared memory (an address from mapa).
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 namespace {
 
 // Score passes on the 5th-generation tensor core.  One CTA = one (pair, row
@@ -1087,6 +1111,502 @@ __global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float*
   }
 }
 
+// Pool + select for one pair over a cluster of NC CTAs (prefixes of up to
+// 8 x 256 x (h + 1) positions).  CTA r pools positions [r*PC, r*PC + PC),
+// PC = 256 (h + 1), each thread h + 1 consecutive outputs from a van Herk
+// split of its window (as snap_pool_select_kernel does for a whole prefix).
+// The pooled scores form runs of equal values, and the passes after pooling
+// walk a thread's runs (keys are order-preserving integers of the pooled log2
+// scores).  The bucket select then runs
+// over the cluster with four cluster barriers: the key range; the 1024-bucket
+// histograms (every CTA sums all of them); the counts of certainly taken
+// positions and the members of a split boundary bucket (which every CTA ranks
+// itself); and one before leaving, so no CTA exits while another reads its
+// shared memory.  Each CTA writes its own taken positions at their places in
+// the ascending keep list.  An equal or non-finite key range, or a split
+// bucket of more than CL_MAXM members, sends the keys to global scratch, where
+// CTA 0 runs a radix select over them.
+constexpr int CL_NT = 256;
+constexpr int CL_MAXM = 512;
+constexpr int CL_MAXNC = 8;
+
+// shared words of one cluster CTA's padded window of CL_NT (h + 1) + 2 (h + 1)
+// scores; its CL_NT (h + 1) pooled scores follow (cl_smem_words in all)
+__host__ __device__ inline int cl_key_words(int h) {
+  const int U = (CL_NT + 2) * (h + 1);
+  return ((U + U / 32 + 1) + 3) & ~3;
+}
+__host__ __device__ inline int cl_smem_words(int h) {
+  const int P = CL_NT * (h + 1);
+  return cl_key_words(h) + (((P + P / 32 + 1) + 3) & ~3);
+}
+
+struct __align__(16) ClSmem {
+  uint32_t hist[PS_NB];            // this CTA's bucket counts
+  uint32_t ghist[PS_NB];           // the cluster's (radix fallback: 256-digit counts)
+  uint2 memb[CL_MAXM];             // this CTA's members of the split bucket (key, position)
+  uint2 allm[CL_MAXM];             // every member of the cluster, in CTA order
+  uint32_t taken[CL_NT];           // taken bits of this CTA's positions (at most CL_NT * 32)
+  uint32_t mm[2];                  // this CTA's (min, max) candidate key
+  uint32_t cnt[2];                 // this CTA's (certainly taken positions, members)
+  uint32_t ctk[CL_MAXNC];          // taken members of each CTA
+  uint32_t wsum[CL_NT / 32], wmin[CL_NT / 32], wmax[CL_NT / 32];
+  int32_t sh[8];
+};
+
+// Exclusive prefix of a flag over the CTA's CL_NT threads; writes the total.
+__device__ __forceinline__ int cl_excl_scan(bool f, uint32_t* wsum, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, f);
+  if (lane == 0) wsum[warp] = __popc(bal);
+  __syncthreads();
+  int pre = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < CL_NT / 32; ++w) {
+    const int v = (int)wsum[w];
+    if (w < warp) pre += v;
+    tot += v;
+  }
+  __syncthreads();
+  total = tot;
+  return pre + __popc(bal & ((1u << lane) - 1u));
+}
+
+__global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float* scores, int RG, int64_t Ls, int h,
+                                                                     int64_t S_max, int W0, int n_sink0,
+                                                                     int64_t B1_max, int32_t* keep, int64_t keep_ld,
+                                                                     float* pooled_out, const int32_t* S_rows,
+                                                                     const int32_t* B1_rows, int Hkv, int NC,
+                                                                     uint32_t* key_scratch) {
+  extern __shared__ __align__(16) uint32_t xs[];
+  __shared__ ClSmem cs;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int rank = (int)cluster_ctarank();
+  const int pair = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const RowPlan rp = row_plan(S_rows, B1_rows, pair / Hkv, S_max, B1_max, W0, n_sink0);
+  if (rp.bad && tid == 0 && rank == 0) atomicOr(&g_snap_err, ERR_BAD_LENGTH);
+  const int L = rp.L, S = rp.S, B1 = rp.B1, W = rp.S - rp.L, n_sink = rp.sinks;
+  const int ntop = (int)rp.ntop;
+  const int E = h + 1, PC = CL_NT * E;
+  const int p0 = rank * PC;                       // this CTA's first position
+  int32_t* out = keep + (size_t)pair * keep_ld;
+  // (every decision below up to the select is the same in every CTA of the cluster)
+  if (rp.all) {
+    for (int i = rank * CL_NT + tid; i < S; i += NC * CL_NT) out[i] = i;
+    return;
+  }
+  if (rank == 0) {
+    for (int i = tid; i < n_sink; i += CL_NT) out[i] = i;
+    for (int i = tid; i < W; i += CL_NT) out[B1 - W + i] = (int32_t)(S - W + i);
+  }
+  if (ntop <= 0 && !pooled_out) return;
+
+  // This CTA's window of the row-group sums: padded coordinate u holds position
+  // p0 + u - h, at ps_pad(u).  The per-thread phases below are loops over a
+  // thread's E positions, kept rolled: straight-line code of this length does
+  // not stay in the instruction cache, and every warp runs it once.
+  const int Uloc = PC + 2 * E;
+  {
+    const float* sc = scores + (size_t)pair * RG * Ls;
+    if (RG == 1) {
+      // one asynchronous 4-byte copy per entry: every copy of a thread in flight at once
+      for (int u = tid; u < Uloc; u += CL_NT) {
+        const int j = p0 + u - h;
+        if (j >= 0 && j < L) cp_async_4(smem_u32(&xs[ps_pad(u)]), sc + j);
+        else xs[ps_pad(u)] = __float_as_uint(neg_inf());
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+    }
+    for (int u0 = RG == 1 ? Uloc : tid; u0 < Uloc; u0 += 8 * CL_NT) {
+      float v[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int j = p0 + u0 + t * CL_NT - h;
+        v[t] = (u0 + t * CL_NT < Uloc && j >= 0 && j < L) ? __ldg(sc + j) : neg_inf();
+      }
+      for (int r = 1; r < RG; ++r) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int j = p0 + u0 + t * CL_NT - h;
+          if (u0 + t * CL_NT < Uloc && j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * Ls + j));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int u = u0 + t * CL_NT;
+        if (u < Uloc) xs[ps_pad(u)] = __float_as_uint(v[t]);
+      }
+    }
+  }
+  __syncthreads();
+
+  // max-pool of outputs [a, a + E) (van Herk split of the window, as in
+  // snap_pool_select_kernel; the right prefix maxima wait in ko, the pooled
+  // values replace them), and the runs of equal pooled values among this
+  // thread's candidates (positions >= n_sink): a max-pool this wide leaves about
+  // two runs per 32 positions, so the passes below walk runs, not positions
+  const int al = tid * E, a = p0 + al;
+  const bool mine = a < L;
+  const int cnt_i = mine ? min(E, L - a) : 0;       // this thread's positions [a, a + cnt_i)
+  const int i_lo = mine ? max(0, n_sink - a) : 0;   // its candidates start here
+  // the pooled log2 score of position a + i sits at kr[kx(i)] (a padded run of ko)
+  uint32_t* ko = xs + cl_key_words(h);
+  uint32_t* kr = ko + ps_pad(al);
+  const int alo = al & 31;
+  auto kx = [alo](int i) { return i + ((alo + i) >> 5); };
+  uint32_t runs = 0u;                               // bit i: candidate position a + i starts a run of equal values
+  if (mine) {
+    float m;
+    float l = neg_inf();
+    if (E == 32) {
+      // blocks of 32 window entries are padded rows of 33 words: the left block
+      // is row tid (entries 0-30), the middle row tid's entry 31 and row tid + 1
+      // (0-30), the right row tid + 1's entry 31 and row tid + 2 (0-29)
+      const uint32_t* r0 = xs + 33 * tid;
+      const uint32_t* r1 = r0 + 33;
+      const uint32_t* r2 = r0 + 66;
+      float m0 = __uint_as_float(r0[31]), m1 = neg_inf();
+      for (int k = 0; k < 30; k += 2) {
+        m0 = fmaxf(m0, __uint_as_float(r1[k]));
+        m1 = fmaxf(m1, __uint_as_float(r1[k + 1]));
+      }
+      m = fmax3(m0, m1, __uint_as_float(r1[30]));
+      float r = __uint_as_float(r1[31]);
+      kr[0] = __float_as_uint(neg_inf());
+      for (int i = 1; i < 32; ++i) {
+        kr[i] = __float_as_uint(r);
+        r = fmaxf(r, __uint_as_float(r2[i - 1]));
+      }
+      uint32_t pnext = 0u;                          // pooled value bits of position i + 1
+      for (int i = 31; i >= 0; --i) {
+        const uint32_t pb = __float_as_uint(fmax3(__uint_as_float(kr[i]), l, m));
+        kr[i] = pb;
+        runs |= (pb != pnext ? 2u : 0u) << i;       // position i + 1 starts a run
+        pnext = pb;
+        if (i > 0) l = fmaxf(l, __uint_as_float(r0[i - 1]));
+      }
+    } else {
+      auto X = [&](int u) { return __uint_as_float(xs[ps_pad(u)]); };
+      float m0 = neg_inf(), m1 = neg_inf();
+      for (int i = 0; i < E; i += 2) {
+        m0 = fmaxf(m0, X(al + E - 1 + i));
+        if (i + 1 < E) m1 = fmaxf(m1, X(al + E + i));
+      }
+      m = fmaxf(m0, m1);
+      float r = neg_inf();
+      for (int i = 0; i < E; ++i) {
+        kr[kx(i)] = __float_as_uint(r);
+        r = fmaxf(r, X(al + 2 * E - 1 + i));
+      }
+      uint32_t pnext = 0u;
+      for (int i = E - 1; i >= 0; --i) {
+        const uint32_t pb = __float_as_uint(fmax3(__uint_as_float(kr[kx(i)]), l, m));
+        kr[kx(i)] = pb;
+        runs |= (pb != pnext ? 2u : 0u) << i;
+        pnext = pb;
+        if (i > 0) l = fmaxf(l, X(al + i - 1));
+      }
+    }
+  }
+  if (pooled_out && mine) {
+    float* po = pooled_out + (size_t)pair * Ls;
+    for (int i = 0; i < cnt_i; ++i) po[a + i] = exp2f(__uint_as_float(kr[kx(i)]));
+  }
+  // runs within [i_lo, cnt_i), the first one starting at i_lo
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  {
+    const uint32_t span = i_lo >= cnt_i ? 0u : (cnt_i >= 32 ? 0xffffffffu : ((1u << cnt_i) - 1u)) & ~((1u << i_lo) - 1u);
+    runs = (runs | (i_lo < cnt_i ? 1u << i_lo : 0u)) & span;
+    for (uint32_t rb = runs; rb; rb &= rb - 1u) {
+      const uint32_t key = f2key(__uint_as_float(kr[kx(__ffs(rb) - 1)]));
+      kmn = min(kmn, key);
+      kmx = max(kmx, key);
+    }
+  }
+  // the order-preserving key of position a + i
+  auto key_at = [&](int i) { return f2key(__uint_as_float(kr[kx(i)])); };
+  // the run starting at bit i of `rb` (lowest set bit) ends at the next set bit, or at cnt_i
+  auto run_end = [&](uint32_t rest) { return rest ? __ffs(rest) - 1 : cnt_i; };
+  if (ntop <= 0) return;                            // (the pooled scores were written above)
+  if (ntop >= L - n_sink) {
+    for (int i = i_lo; i < cnt_i; ++i) out[a + i] = a + i;
+    return;
+  }
+
+  // ---- key range of the cluster
+  kmn = __reduce_min_sync(0xffffffffu, kmn);
+  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  if (lane == 0) {
+    cs.wmin[warp] = kmn;
+    cs.wmax[warp] = kmx;
+  }
+  for (int i = tid; i < PS_NB; i += CL_NT) cs.hist[i] = 0u;
+  cs.taken[tid] = 0u;
+  if (tid < CL_MAXNC) cs.ctk[tid] = 0u;
+  if (tid == 0) cs.sh[3] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int w = 0; w < CL_NT / 32; ++w) {
+      lo = min(lo, cs.wmin[w]);
+      hi = max(hi, cs.wmax[w]);
+    }
+    cs.mm[0] = lo;
+    cs.mm[1] = hi;
+  }
+  cluster_sync();                                   // (1) every CTA's range is published
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int c = 0; c < NC; ++c) {
+    lo = min(lo, ld_cluster_u32(mapa(smem_u32(&cs.mm[0]), (uint32_t)c)));
+    hi = max(hi, ld_cluster_u32(mapa(smem_u32(&cs.mm[1]), (uint32_t)c)));
+  }
+  auto kval = [](uint32_t key) { return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key); };
+  const float vlo = kval(lo), width = kval(hi) - vlo;
+  const float inv = (width > 0.f && isfinite(width)) ? __fdividef((float)PS_NB, width) : 0.f;
+  auto bucket = [&](uint32_t key) { return max(0, min(PS_NB - 1, (int)((kval(key) - vlo) * inv))); };
+  bool use_radix = inv == 0.f;
+  int bb = 0, need = 0, m = 0;
+  if (!use_radix) {
+    // ---- histogram: one count per run of equal buckets along this thread's positions
+    {
+      for (uint32_t rb = runs; rb;) {
+        const int i = __ffs(rb) - 1;
+        rb &= rb - 1u;
+        atomicAdd(&cs.hist[bucket(key_at(i))], (uint32_t)(run_end(rb) - i));
+      }
+    }
+    __syncthreads();
+    cluster_sync();                                 // (2) every CTA's histogram is complete
+    for (int q = tid; q < PS_NB / 4; q += CL_NT) {
+      uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < NC; ++c) {
+        const uint4 v = ld_cluster_v4(mapa(smem_u32(&cs.hist[4 * q]), (uint32_t)c));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      *reinterpret_cast<uint4*>(&cs.ghist[4 * q]) = acc;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds buckets 32l .. 32l+31; counts from the top bucket down
+      const uint4* h4 = reinterpret_cast<const uint4*>(&cs.ghist[32 * lane]);
+      uint32_t sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = h4[q];
+        sum += v.x + v.y + v.z + v.w;
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      uint32_t above = incl - sum;
+      if (above < (uint32_t)ntop && incl >= (uint32_t)ntop) {
+        for (int q = 7; q >= 0; --q) {
+          const uint4 v = h4[q];
+          const uint32_t c4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int u = 3; u >= 0; --u) {
+            if (above < (uint32_t)ntop && above + c4[u] >= (uint32_t)ntop) {
+              cs.sh[0] = 32 * lane + 4 * q + u;
+              cs.sh[1] = (int)((uint32_t)ntop - above);
+              cs.sh[2] = (int)c4[u];
+            }
+            above += c4[u];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    bb = cs.sh[0];
+    need = cs.sh[1];
+    m = cs.sh[2];
+    if (need < m && m > CL_MAXM) use_radix = true;   // the same in every CTA
+  }
+  if (!use_radix) {
+    // ---- this CTA's certainly taken positions and its members of a split bucket
+    const bool split = need < m;
+    uint32_t cert = 0u;
+    for (uint32_t rb = runs; rb;) {
+      const int i = __ffs(rb) - 1;
+      rb &= rb - 1u;
+      const int e = run_end(rb);                    // positions [a + i, a + e) share one key
+      const uint32_t key = key_at(i);
+      const int bk = bucket(key);
+      if (bk > bb || (bk == bb && !split)) {
+        cert |= (e - i >= 32 ? 0xffffffffu : ((1u << (e - i)) - 1u)) << i;
+      } else if (bk == bb) {
+        const int base = atomicAdd(&cs.sh[3], e - i);
+        for (int t = i; t < e; ++t) cs.memb[base + t - i] = make_uint2(key, (uint32_t)(a + t));
+      }
+    }
+    const uint32_t wc = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(cert));
+    if (lane == 0) cs.wsum[warp] = wc;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int w = 0; w < CL_NT / 32; ++w) c += cs.wsum[w];
+      cs.cnt[0] = c;
+      cs.cnt[1] = (uint32_t)cs.sh[3];
+    }
+    cluster_sync();                                 // (3) counts and member lists are published
+    uint32_t certc[CL_MAXNC], ms[CL_MAXNC];
+    uint32_t mtot = 0;
+#pragma unroll
+    for (int c = 0; c < CL_MAXNC; ++c) {
+      certc[c] = c < NC ? ld_cluster_u32(mapa(smem_u32(&cs.cnt[0]), (uint32_t)c)) : 0u;
+      const uint32_t mc = c < NC ? ld_cluster_u32(mapa(smem_u32(&cs.cnt[1]), (uint32_t)c)) : 0u;
+      ms[c] = mtot;
+      mtot += mc;
+    }
+    auto cta_of = [&](uint32_t i) {
+      int c = 0;
+#pragma unroll
+      for (int u = 1; u < CL_MAXNC; ++u) c = (u < NC && i >= ms[u]) ? u : c;
+      return c;
+    };
+    // a taken member of the split bucket counts for its CTA, and marks its bit here
+    auto take = [&](uint32_t i, uint32_t pos) {
+      const int c = cta_of(i);
+      atomicAdd(&cs.ctk[c], 1u);
+      if (c == rank) {
+        const int lp = (int)pos - p0;               // this CTA's local position
+        atomicOr(&cs.taken[lp >> 5], 1u << (lp & 31));
+      }
+    };
+    if (split) {
+      // every member of the cluster, in CTA order, then each one's rank among them
+      // (larger key first, equal keys by position)
+      for (uint32_t i = tid; i < mtot; i += CL_NT) {
+        const int c = cta_of(i);
+        const uint32_t ad = mapa(smem_u32(&cs.memb[i - ms[c]]), (uint32_t)c);
+        cs.allm[i] = make_uint2(ld_cluster_u32(ad), ld_cluster_u32(ad + 4u));
+      }
+      __syncthreads();
+      if (mtot <= CL_NT / 4) {
+        // four threads per member, each against a quarter of the others
+        const uint32_t i = (uint32_t)tid >> 2, qd = (uint32_t)tid & 3u;
+        uint2 me = make_uint2(0u, 0u);
+        int rk = 0;
+        if (i < mtot) {
+          me = cs.allm[i];
+          for (uint32_t u = qd; u < mtot; u += 4) {
+            const uint2 o = cs.allm[u];
+            rk += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+          }
+        }
+        rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+        rk += __shfl_xor_sync(0xffffffffu, rk, 2);
+        if (i < mtot && qd == 0 && rk < need) take(i, me.y);
+      } else {
+        for (uint32_t i = tid; i < mtot; i += CL_NT) {
+          const uint2 me = cs.allm[i];
+          int rk = 0;
+          for (uint32_t u = 0; u < mtot; ++u) {
+            const uint2 o = cs.allm[u];
+            rk += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+          }
+          if (rk < need) take(i, me.y);
+        }
+      }
+      __syncthreads();
+    }
+    // taken positions of the CTAs before this one, then this CTA's in ascending order
+    int pos = n_sink;
+    for (int c = 0; c < rank; ++c) pos += (int)certc[c] + (split ? (int)cs.ctk[c] : 0);
+    uint32_t tk = cert;
+    if (split && cnt_i > 0) {
+      // bits [al, al + E) of the taken map (at most two words)
+      const uint64_t w2 = ((uint64_t)cs.taken[min((al >> 5) + 1, CL_NT - 1)] << 32) | cs.taken[al >> 5];
+      tk |= (uint32_t)(w2 >> (al & 31)) & (E == 32 ? 0xffffffffu : ((1u << E) - 1u));
+    }
+    const uint32_t cnt = (uint32_t)__popc(tk);
+    uint32_t inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) cs.wsum[warp] = inc;
+    __syncthreads();
+    pos += (int)(inc - cnt);
+    for (int w = 0; w < warp; ++w) pos += (int)cs.wsum[w];
+    const int pend = n_sink + ntop;                 // (exactly ntop are taken; the bound guards the row)
+    for (uint32_t bits = tk; bits && pos < pend; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
+    cluster_sync();                                 // (4) no CTA leaves while another reads its shared memory
+    return;
+  }
+
+  // ---- radix fallback: the keys in global scratch, CTA 0 selects over them
+  uint32_t* ks = key_scratch + (size_t)pair * Ls;
+  for (int i = i_lo; i < cnt_i; ++i) ks[a + i] = key_at(i);
+  cluster_sync();                                   // keys visible; every remote read done
+  if (rank != 0) return;
+  uint32_t prefix = 0, mask = 0;
+  int k = ntop;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    cs.ghist[tid] = 0u;                             // (CL_NT == 256 digits)
+    __syncthreads();
+    for (int j = n_sink + tid; j < L; j += CL_NT) {
+      const uint32_t key = ks[j];
+      if ((key & mask) == prefix) atomicAdd(&cs.ghist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int c[8];
+      int sum = 0;
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        c[u] = (int)cs.ghist[lane * 8 + u];
+        sum += c[u];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += t;
+      }
+      int above = incl - sum;
+#pragma unroll
+      for (int u = 7; u >= 0; --u) {
+        if (above < k && above + c[u] >= k) {
+          cs.sh[4] = lane * 8 + u;
+          cs.sh[5] = k - above;
+        }
+        above += c[u];
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)cs.sh[4] << shift;
+    mask |= 255u << shift;
+    k = cs.sh[5];
+    __syncthreads();
+  }
+  // keys > T are taken, and the first k keys equal to T in position order
+  const uint32_t T = prefix;
+  int pos = n_sink, eq_taken = 0;
+  for (int base = n_sink; base < L; base += CL_NT) {
+    const int j = base + tid;
+    const uint32_t key = j < L ? ks[j] : 0u;
+    const bool gt = j < L && key > T, eq = j < L && key == T;
+    int eq_tot, take_tot;
+    const int eq_before = cl_excl_scan(eq, cs.wsum, eq_tot);
+    const bool take = gt || (eq && eq_taken + eq_before < k);
+    const int tpos = cl_excl_scan(take, cs.wsum, take_tot);
+    if (take && pos + tpos < n_sink + ntop) out[pos + tpos] = j;
+    pos += take_tot;
+    eq_taken += eq_tot;
+  }
+}
+
 // K_c[i] = K[keep[i]], V_c[i] = V[keep[i]].
 __global__ void __launch_bounds__(256) snap_compact_kernel(const bf16* k, const bf16* v, int64_t cap,
                                                            const int32_t* keep, int64_t keep_ld, int64_t B1_max,
@@ -1148,16 +1668,52 @@ size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32
 
 int snap_pass2_rows(int32_t G, int32_t W) { return std::min(P2_ROWS, (G * W + 31) & ~31); }
 
+// CTAs of the cluster pool + select for prefix length L and half window h:
+// 2..CL_MAXNC when it applies (the single-CTA kernel takes up to CL_NT outputs
+// of h + 1 positions, the separate pool + select what exceeds the cluster)
+int pool_select_cl_ctas(int64_t L, int h) {
+  const int E = h + 1;
+  if (L <= 0 || E > 32) return 0;
+  const int64_t nq = (L + E - 1) / E;
+  const int64_t nc = (nq + CL_NT - 1) / CL_NT;
+  return (nc >= 2 && nc <= CL_MAXNC) ? (int)nc : 0;
+}
+
+
+// Launch as clusters of nc CTAs along x, with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, unsigned nc,
+                               cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = nc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmQ1, const CUtensorMap* tmQ2,
                         cudaStream_t st) {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess, ps_attr_err = cudaSuccess;
+  static cudaError_t attr_err = cudaSuccess, ps_attr_err = cudaSuccess, cl_attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     ps_attr_err = cudaFuncSetAttribute(snap_pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PS_MAX_WORDS * 4);
+    // (the window and keys of half width 31 plus the static select state pass the default 48 KB)
+    cl_attr_err = cudaFuncSetAttribute(snap_pool_select_cl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       cl_smem_words(31) * 4);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int pairs = a.B * a.Hkv;
@@ -1205,7 +1761,15 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     if (e != cudaSuccess) return e;
     const int half = (int)(a.pool / 2);
     const int ps_words = pool_select_words(L, half);
-    if (ps_words > 0 && ps_attr_err == cudaSuccess) {
+    const int cl_nc = cl_attr_err == cudaSuccess ? pool_select_cl_ctas(L, half) : 0;
+    if (cl_nc > 0) {
+      e = launch_cluster_pdl(snap_pool_select_cl_kernel, dim3((unsigned)cl_nc, pairs), dim3(CL_NT),
+                             (size_t)cl_smem_words(half) * 4u, (unsigned)cl_nc, st, (const float*)p.scores, (int)p.RG2,
+                             (int64_t)L, half, (int64_t)a.S, (int)W, (int)a.n_sink, (int64_t)a.B1, a.keep,
+                             (int64_t)a.keep_ld, a.pooled_out, a.S_rows, a.B1_rows, (int)a.Hkv, cl_nc,
+                             reinterpret_cast<uint32_t*>(pooled_log));
+      if (e != cudaSuccess) return e;
+    } else if (ps_words > 0 && ps_attr_err == cudaSuccess) {
       e = launch_pdl(snap_pool_select_kernel, dim3(pairs), dim3(PS_NT), (size_t)ps_words * 4u, st,
                      (const float*)p.scores, (int)p.RG2, (int64_t)L, half, (int64_t)a.S, (int)W, (int)a.n_sink,
                      (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.pooled_out, a.S_rows, a.B1_rows, (int)a.Hkv);
