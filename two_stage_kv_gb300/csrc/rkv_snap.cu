@@ -730,391 +730,18 @@ __global__ void __launch_bounds__(SEL_NT) snap_select_kernel(const float* pooled
   }
 }
 
-// Fused pool + select for prompts whose prefix fits one CTA: the row-group
-// sums of one pair go to shared memory once, each thread max-pools E = h + 1
-// consecutive positions (window 2h + 1) from a van Herk split of the window
-// around its own range, the order-preserving keys replace the scores in
-// place, and the radix select plus the ascending write-out run on shared
-// memory.  Same result as snap_pool + snap_select.
-constexpr int PS_NT = 1024;
-constexpr int PS_MAX_WORDS = 54 * 1024;        // padded shared words (216 KB)
-constexpr int PS_NB = 1024;                     // buckets of the bucket select
-constexpr int PS_MAXM = 1024;                   // members of a split bucket ranked pairwise
-
-__device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }   // one pad word per 32: no bank conflicts
-
-// shared words of the padded keys for prefix length L and half window h
-__host__ __device__ inline int ps_key_words(int64_t L, int h) {
-  const int E = h + 1;
-  const int64_t nq = (L + E - 1) / E;
-  const int64_t U = nq * E + 2 * E;
-  return (int)(((U + U / 32 + 1) + 3) & ~3);
-}
-// extra words of the bucket select: counters, taken-bit map, (key, position) members
-__host__ __device__ inline int ps_bucket_words(int64_t L) {
-  const int64_t bm = (L + 31) >> 5;
-  return (int)(PS_NB + ((bm + 1) & ~1) + 2 * PS_MAXM);
-}
-
-// shared words needed for prefix length L and half window h (0 if the fused path does not apply)
-int pool_select_words(int64_t L, int h) {
-  const int E = h + 1;
-  if (L <= 0 || E > 32) return 0;
-  const int64_t nq = (L + E - 1) / E;
-  if (nq > PS_NT) return 0;
-  const int64_t U = nq * E + 2 * E;
-  const int64_t words = U + U / 32 + 1;
-  if (words > PS_MAX_WORDS) return 0;
-  // room for the bucket select past the keys when it fits (the kernel checks)
-  const int64_t with_bucket = (int64_t)ps_key_words(L, h) + ps_bucket_words(L);
-  return with_bucket <= PS_MAX_WORDS ? (int)with_bucket : (int)words;
-}
-
-__global__ void __launch_bounds__(PS_NT, 1) snap_pool_select_kernel(const float* scores, int RG, int64_t Ls,
-                                                                    int h, int64_t S_max, int W0, int n_sink0,
-                                                                    int64_t B1_max, int32_t* keep, int64_t keep_ld,
-                                                                    float* pooled_out, const int32_t* S_rows,
-                                                                    const int32_t* B1_rows, int Hkv) {
-  extern __shared__ __align__(16) uint32_t xs[];
-  __shared__ int hist[256];
-  __shared__ int wsum[PS_NT / 32];
-  __shared__ uint32_t wmin_s[PS_NT / 32], wmax_s[PS_NT / 32];
-  __shared__ uint32_t sh_digit;
-  __shared__ int sh_k, sh_bb, sh_need, sh_m, sh_cnt;
-  pdl_wait();
-  pdl_launch_dependents();
-  const int pair = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // this row's lengths (Ls: row stride of the score arrays)
-  const RowPlan rp = row_plan(S_rows, B1_rows, pair / Hkv, S_max, B1_max, W0, n_sink0);
-  if (rp.bad && tid == 0) atomicOr(&g_snap_err, ERR_BAD_LENGTH);
-  const int L = rp.L, S = rp.S, B1 = rp.B1, W = rp.S - rp.L, n_sink = rp.sinks;
-  const int64_t ntop = rp.ntop;
-  const int E = h + 1;
-  const int nq = (L + E - 1) / E;
-  const int U = nq * E + 2 * E;
-  int32_t* out = keep + (size_t)pair * keep_ld;
-  if (rp.all) {
-    for (int i = tid; i < S; i += PS_NT) out[i] = i;
-    return;
-  }
-  for (int i = tid; i < n_sink; i += PS_NT) out[i] = i;
-  for (int i = tid; i < W; i += PS_NT) out[B1 - W + i] = (int32_t)(S - W + i);
-  if (ntop <= 0 && !pooled_out) return;        // only the window and the sinks are kept
-
-  // scores of position j = u - h at u (minus infinity outside [0, L))
-  const float* sc = scores + (size_t)pair * RG * Ls;
-  for (int u0 = tid; u0 < U; u0 += 8 * PS_NT) {
-    float v[8];                                  // eight independent loads in flight per thread
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int j = u0 + t * PS_NT - h;
-      v[t] = (j >= 0 && j < L) ? __ldg(sc + j) : neg_inf();
-    }
-    for (int r = 1; r < RG; ++r) {              // row-group partials, log2 domain
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int j = u0 + t * PS_NT - h;
-        if (j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * Ls + j));
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int u = u0 + t * PS_NT;
-      if (u < U) xs[ps_pad(u)] = __float_as_uint(v[t]);
-    }
-  }
-  __syncthreads();
-
-  // max-pool of outputs [a, a + E): the window of output a + i is u in [a+i, a+i+2h];
-  // [a+E-1, a+2E-2] is common to all of them, the rest is a suffix of
-  // [a, a+E-2] and a prefix of [a+2E-1, a+3E-3]
-  float pv[32];
-  const int a = tid * E;
-  const bool mine = tid < nq;
-  if (mine) {
-    auto X = [&](int u) { return __uint_as_float(xs[ps_pad(u)]); };
-    float m = neg_inf();
-    for (int i = 0; i < E; ++i) m = fmaxf(m, X(a + E - 1 + i));
-    float r = neg_inf();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i < E) {
-        pv[i] = r;
-        r = fmaxf(r, X(a + 2 * E - 1 + i));
-      }
-    }
-    float l = neg_inf();
-#pragma unroll
-    for (int i = 31; i >= 0; --i) {
-      if (i < E) {
-        pv[i] = fmax3(pv[i], l, m);
-        if (i > 0) l = fmaxf(l, X(a + i - 1));
-      }
-    }
-    if (pooled_out) {
-      float* po = pooled_out + (size_t)pair * Ls;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < E && a + i < L) po[a + i] = exp2f(pv[i]);
-    }
-  }
-  __syncthreads();
-  // keys of the candidates [n_sink, L) replace the scores; 0 elsewhere
-  uint32_t kmn = 0xffffffffu, kmx = 0u;
-  if (mine) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i < E) {
-        const int j = a + i;
-        const bool cand = j >= n_sink && j < L;
-        const uint32_t key = cand ? f2key(pv[i]) : 0u;
-        xs[ps_pad(j)] = key;
-        if (cand) {
-          kmn = min(kmn, key);
-          kmx = max(kmx, key);
-        }
-      }
-    }
-  }
-  const int ncand = L - n_sink;
-  if (ntop <= 0) return;                         // (the pooled scores were written above)
-  if (ntop >= ncand) {
-    for (int j = n_sink + tid; j < L; j += PS_NT) out[j] = j;
-    return;
-  }
-
-  // Bucket select.  The candidates' pooled log2 scores span [vlo, vhi];
-  // bucket = floor((v - vlo) * PS_NB / (vhi - vlo)), clamped: a monotone map of
-  // the value, so of the key.  One histogram finds the bucket that
-  // holds the ntop-th largest key; the buckets above it are taken, and that
-  // bucket's members are ranked pairwise (larger key first, equal keys by
-  // position) only when it is split.  Pooled scores form plateaus, so each
-  // thread counts runs of equal buckets along its own positions.  The counters,
-  // a taken-bit map and the members sit past the keys in the dynamic shared
-  // words when the launch gave room for them; otherwise, or when the split
-  // bucket has more than PS_MAXM members, the radix select below runs.
-  const int kwords = ps_key_words(L, h);
-  const int bm_words = (L + 31) >> 5;
-  uint32_t dyn_bytes;
-  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
-  bool use_radix = (uint32_t)(kwords + ps_bucket_words(L)) * 4u > dyn_bytes;
-  int k = (int)ntop;
-  if (!use_radix) {
-    uint32_t* hist_b = xs + kwords;                            // PS_NB counters
-    uint32_t* taken = hist_b + PS_NB;                          // bit j: position j of the split bucket is taken
-    uint2* memb = reinterpret_cast<uint2*>(taken + ((bm_words + 1) & ~1));   // (key, position) of its members
-    kmn = __reduce_min_sync(0xffffffffu, kmn);
-    kmx = __reduce_max_sync(0xffffffffu, kmx);
-    if (lane == 0) {
-      wmin_s[warp] = kmn;
-      wmax_s[warp] = kmx;
-    }
-    for (int i = tid; i < PS_NB + bm_words; i += PS_NT) hist_b[i] = 0u;
-    if (tid == 0) sh_cnt = 0;
-    __syncthreads();
-    uint32_t lo = 0xffffffffu, hi = 0u;
-#pragma unroll
-    for (int w = 0; w < PS_NT / 32; ++w) {
-      lo = min(lo, wmin_s[w]);
-      hi = max(hi, wmax_s[w]);
-    }
-    // the value of a key (inverse of f2key); equal or non-finite ranges take the radix path
-    auto kval = [](uint32_t key) { return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key); };
-    const float vlo = kval(lo), width = kval(hi) - vlo;
-    const float inv = (width > 0.f && isfinite(width)) ? __fdividef((float)PS_NB, width) : 0.f;
-    auto bucket = [&](uint32_t key) { return max(0, min(PS_NB - 1, (int)((kval(key) - vlo) * inv))); };
-    if (inv == 0.f) use_radix = true;                          // the same in every thread
-    const int cnt_i = mine ? max(0, min(E, L - a)) : 0;       // this thread's positions [a, a + cnt_i)
-    const int i_lo = mine ? max(0, n_sink - a) : 0;           // candidates start at n_sink
-    if (!use_radix) {
-      // histogram: one count per run of equal buckets along this thread's positions
-      {
-        int prev = -1, run = 0;
-        for (int i = i_lo; i < cnt_i; ++i) {
-          const int bk = bucket(xs[ps_pad(a + i)]);
-          if (bk == prev) {
-            ++run;
-          } else {
-            if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
-            prev = bk;
-            run = 1;
-          }
-        }
-        if (run) atomicAdd(&hist_b[prev], (uint32_t)run);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // lane l holds buckets 32l .. 32l+31; counts from the top bucket down
-        const uint4* h4 = reinterpret_cast<const uint4*>(&hist_b[32 * lane]);
-        uint32_t sum = 0;
-  #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = h4[q];
-          sum += v.x + v.y + v.z + v.w;
-        }
-        uint32_t incl = sum;
-  #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
-          if (lane + o < 32) incl += t;
-        }
-        uint32_t above = incl - sum;
-        if (above < (uint32_t)k && incl >= (uint32_t)k) {
-          // the crossing is in this lane's buckets (exactly one lane)
-          for (int q = 7; q >= 0; --q) {
-            const uint4 v = h4[q];
-            const uint32_t c4[4] = {v.x, v.y, v.z, v.w};
-  #pragma unroll
-            for (int u = 3; u >= 0; --u) {
-              if (above < (uint32_t)k && above + c4[u] >= (uint32_t)k) {
-                sh_bb = 32 * lane + 4 * q + u;
-                sh_need = (int)((uint32_t)k - above);
-                sh_m = (int)c4[u];
-              }
-              above += c4[u];
-            }
-          }
-        }
-      }
-      __syncthreads();
-      const int bb = sh_bb, need = sh_need, m = sh_m;
-      if (need < m && m > PS_MAXM) use_radix = true;           // the same in every thread
-      if (!use_radix) {
-        if (need < m) {
-          // collect and rank the split bucket's members; the taken ones set their bit
-          for (int i = i_lo; i < cnt_i; ++i) {
-            const uint32_t key = xs[ps_pad(a + i)];
-            if (bucket(key) == bb) memb[atomicAdd(&sh_cnt, 1)] = make_uint2(key, (uint32_t)(a + i));
-          }
-          __syncthreads();
-          for (int t = tid; t < m; t += PS_NT) {
-            const uint2 me = memb[t];
-            int rk = 0;
-            for (int u = 0; u < m; ++u) {
-              const uint2 o = memb[u];
-              rk += (o.x > me.x) || (o.x == me.x && o.y < me.y);
-            }
-            if (rk < need) atomicOr(&taken[me.y >> 5], 1u << (me.y & 31));
-          }
-          __syncthreads();
-        }
-        // ascending write-out of the taken positions
-        uint32_t tk = 0;
-        for (int i = i_lo; i < cnt_i; ++i) {
-          const int j = a + i;
-          const int bk = bucket(xs[ps_pad(j)]);
-          if (bk > bb || (bk == bb && (need == m || ((taken[j >> 5] >> (j & 31)) & 1u)))) tk |= 1u << i;
-        }
-        const uint32_t cnt = (uint32_t)__popc(tk);
-        uint32_t inc = cnt;
-  #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += t;
-        }
-        if (lane == 31) wsum[warp] = (int)inc;
-        __syncthreads();
-        int pos = n_sink + (int)(inc - cnt);
-        for (int w = 0; w < warp; ++w) pos += wsum[w];
-        const int pend = n_sink + (int)ntop;        // (exactly ntop are taken; the bound guards the row)
-        for (uint32_t bits = tk; bits && pos < pend; bits &= bits - 1u) out[pos++] = a + (__ffs(bits) - 1);
-        return;
-      }
-    }
-  }
-  __syncthreads();
-
-  // radix select of the ntop-th largest key, 8 bits at a time from the top
-  uint32_t prefix = 0, mask = 0;
-  k = (int)ntop;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) hist[tid] = 0;
-    __syncthreads();
-    for (int j = n_sink + tid; j - tid < L; j += PS_NT) {
-      const bool in = j < L;
-      const uint32_t key = in ? xs[ps_pad(j)] : 0u;
-      const bool act = in && (key & mask) == prefix;
-      const unsigned am = __ballot_sync(0xffffffffu, act);
-      if (act) {
-        const unsigned d = (key >> shift) & 255u;
-        const unsigned mm = __match_any_sync(am, d);
-        if (lane == __ffs(mm) - 1) atomicAdd(&hist[d], __popc(mm));
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int c[8];
-      int sum = 0;
-#pragma unroll
-      for (int u = 7; u >= 0; --u) {
-        c[u] = hist[lane * 8 + u];
-        sum += c[u];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += t;
-      }
-      int above = incl - sum;
-#pragma unroll
-      for (int u = 7; u >= 0; --u) {
-        if (above < k && above + c[u] >= k) {
-          sh_digit = (uint32_t)(lane * 8 + u);
-          sh_k = k - above;
-        }
-        above += c[u];
-      }
-    }
-    __syncthreads();
-    prefix |= sh_digit << shift;
-    mask |= 255u << shift;
-    k = sh_k;
-  }
-  // keys > T are taken, and the first k keys equal to T in index order
-  const uint32_t T = prefix;
-  uint32_t gt = 0, eq = 0;
-  if (mine) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i < E) {
-        const int j = a + i;
-        if (j >= n_sink && j < L) {
-          const uint32_t key = xs[ps_pad(j)];
-          gt |= (uint32_t)(key > T) << i;
-          eq |= (uint32_t)(key == T) << i;
-        }
-      }
-    }
-  }
-  // exclusive prefix over threads of (count > T, count == T), packed 16 + 16 bits
-  const uint32_t packed = (uint32_t)__popc(gt) | ((uint32_t)__popc(eq) << 16);   // each total <= 32768
-  uint32_t incl = packed;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) wsum[warp] = (int)incl;
-  __syncthreads();
-  uint32_t before = incl - packed;
-  for (int w = 0; w < warp; ++w) before += (uint32_t)wsum[w];
-  const int gt_before = (int)(before & 0xffffu), eq_before = (int)(before >> 16);
-  int pos = n_sink + gt_before + min(k, eq_before);
-  int eq_seen = eq_before;
-  const int pend = n_sink + (int)ntop;          // (exactly ntop are taken; the bound guards the row)
-  for (uint32_t bits = gt | eq; bits && pos < pend; bits &= bits - 1u) {
-    const int i = __ffs(bits) - 1;
-    const bool is_eq = (eq >> i) & 1;
-    if (!is_eq || eq_seen < k) out[pos++] = a + i;
-    if (is_eq) ++eq_seen;
-  }
-}
+// Buckets of the bucket select, and the padded shared-memory index of entry u
+// (one pad word per 32: threads reading entries 32 apart hit distinct banks).
+constexpr int PS_NB = 1024;
+__device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }
 
 // Pool + select for one pair over a cluster of NC CTAs (prefixes of up to
-// 8 x 256 x (h + 1) positions).  CTA r pools positions [r*PC, r*PC + PC),
-// PC = 256 (h + 1), each thread h + 1 consecutive outputs from a van Herk
-// split of its window (as snap_pool_select_kernel does for a whole prefix).
+// 8 x 256 x (h + 1) positions; one CTA for up to 256 (h + 1)).  CTA r pools
+// positions [r*PC, r*PC + PC), PC = 256 (h + 1), each thread E = h + 1
+// consecutive outputs: the window of output a + i is window entries
+// [a + i, a + i + 2h], of which [a + E - 1, a + 2E - 2] is common to all E
+// outputs, the rest a suffix of [a, a + E - 2] and a prefix of
+// [a + 2E - 1, a + 3E - 3] (the van Herk / Gil-Werman split).
 // The pooled scores form runs of equal values, and the passes after pooling
 // walk a thread's runs (keys are order-preserving integers of the pooled log2
 // scores).  The bucket select then runs
@@ -1242,9 +869,8 @@ __global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float*
   }
   __syncthreads();
 
-  // max-pool of outputs [a, a + E) (van Herk split of the window, as in
-  // snap_pool_select_kernel; the right prefix maxima wait in ko, the pooled
-  // values replace them), and the runs of equal pooled values among this
+  // max-pool of outputs [a, a + E) (the right prefix maxima wait in ko, the
+  // pooled values replace them), and the runs of equal pooled values among this
   // thread's candidates (positions >= n_sink): a max-pool this wide leaves about
   // two runs per 32 positions, so the passes below walk runs, not positions
   const int al = tid * E, a = p0 + al;
@@ -1393,7 +1019,9 @@ __global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float*
     }
     __syncthreads();
     if (warp == 0) {
-      // lane l holds buckets 32l .. 32l+31; counts from the top bucket down
+      // lane l holds buckets 32l .. 32l+31; counts from the top bucket down find the
+      // lane holding the ntop-th largest key (exactly one: ntop < the candidates),
+      // then suffix sums over that lane's 32 buckets, one per lane, the bucket
       const uint4* h4 = reinterpret_cast<const uint4*>(&cs.ghist[32 * lane]);
       uint32_t sum = 0;
 #pragma unroll
@@ -1407,21 +1035,22 @@ __global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float*
         const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
         if (lane + o < 32) incl += t;
       }
-      uint32_t above = incl - sum;
-      if (above < (uint32_t)ntop && incl >= (uint32_t)ntop) {
-        for (int q = 7; q >= 0; --q) {
-          const uint4 v = h4[q];
-          const uint32_t c4[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t above = incl - sum;
+      const unsigned cross = __ballot_sync(0xffffffffu, above < (uint32_t)ntop && incl >= (uint32_t)ntop);
+      const int lx = __ffs(cross) - 1;
+      const uint32_t above_x = __shfl_sync(0xffffffffu, above, lx);
+      const uint32_t ck = cs.ghist[32 * lx + lane];
+      uint32_t sk = ck;
 #pragma unroll
-          for (int u = 3; u >= 0; --u) {
-            if (above < (uint32_t)ntop && above + c4[u] >= (uint32_t)ntop) {
-              cs.sh[0] = 32 * lane + 4 * q + u;
-              cs.sh[1] = (int)((uint32_t)ntop - above);
-              cs.sh[2] = (int)c4[u];
-            }
-            above += c4[u];
-          }
-        }
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, sk, o);
+        if (lane + o < 32) sk += t;
+      }
+      const uint32_t abv = above_x + sk - ck;
+      if (abv < (uint32_t)ntop && abv + ck >= (uint32_t)ntop) {
+        cs.sh[0] = 32 * lx + lane;
+        cs.sh[1] = (int)((uint32_t)ntop - abv);
+        cs.sh[2] = (int)ck;
       }
     }
     __syncthreads();
@@ -1669,14 +1298,14 @@ size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32
 int snap_pass2_rows(int32_t G, int32_t W) { return std::min(P2_ROWS, (G * W + 31) & ~31); }
 
 // CTAs of the cluster pool + select for prefix length L and half window h:
-// 2..CL_MAXNC when it applies (the single-CTA kernel takes up to CL_NT outputs
-// of h + 1 positions, the separate pool + select what exceeds the cluster)
+// 1..CL_MAXNC when it applies (the separate pool + select takes longer prefixes
+// and windows wider than 63)
 int pool_select_cl_ctas(int64_t L, int h) {
   const int E = h + 1;
   if (L <= 0 || E > 32) return 0;
   const int64_t nq = (L + E - 1) / E;
   const int64_t nc = (nq + CL_NT - 1) / CL_NT;
-  return (nc >= 2 && nc <= CL_MAXNC) ? (int)nc : 0;
+  return nc <= CL_MAXNC ? (int)nc : 0;
 }
 
 
@@ -1704,13 +1333,11 @@ cudaError_t launch_cluster_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, si
 cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmQ1, const CUtensorMap* tmQ2,
                         cudaStream_t st) {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess, ps_attr_err = cudaSuccess, cl_attr_err = cudaSuccess;
+  static cudaError_t attr_err = cudaSuccess, cl_attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
-    ps_attr_err = cudaFuncSetAttribute(snap_pool_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PS_MAX_WORDS * 4);
     // (the window and keys of half width 31 plus the static select state pass the default 48 KB)
     cl_attr_err = cudaFuncSetAttribute(snap_pool_select_cl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        cl_smem_words(31) * 4);
@@ -1760,7 +1387,6 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
                    *tmK, *tmQ2, p);
     if (e != cudaSuccess) return e;
     const int half = (int)(a.pool / 2);
-    const int ps_words = pool_select_words(L, half);
     const int cl_nc = cl_attr_err == cudaSuccess ? pool_select_cl_ctas(L, half) : 0;
     if (cl_nc > 0) {
       e = launch_cluster_pdl(snap_pool_select_cl_kernel, dim3((unsigned)cl_nc, pairs), dim3(CL_NT),
@@ -1768,11 +1394,6 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
                              (int64_t)L, half, (int64_t)a.S, (int)W, (int)a.n_sink, (int64_t)a.B1, a.keep,
                              (int64_t)a.keep_ld, a.pooled_out, a.S_rows, a.B1_rows, (int)a.Hkv, cl_nc,
                              reinterpret_cast<uint32_t*>(pooled_log));
-      if (e != cudaSuccess) return e;
-    } else if (ps_words > 0 && ps_attr_err == cudaSuccess) {
-      e = launch_pdl(snap_pool_select_kernel, dim3(pairs), dim3(PS_NT), (size_t)ps_words * 4u, st,
-                     (const float*)p.scores, (int)p.RG2, (int64_t)L, half, (int64_t)a.S, (int)W, (int)a.n_sink,
-                     (int64_t)a.B1, a.keep, (int64_t)a.keep_ld, a.pooled_out, a.S_rows, a.B1_rows, (int)a.Hkv);
       if (e != cudaSuccess) return e;
     } else {
       e = launch_pdl(snap_pool_kernel, dim3((unsigned)((L + POOL_TILE - 1) / POOL_TILE), pairs), dim3(256), 0, st,
