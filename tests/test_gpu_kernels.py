@@ -720,6 +720,8 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
     (2, 32, 8, 20000, 32, 63, 700, 4),      # cluster of 3, sinks, ragged last CTA
     (1, 32, 8, 12000, 32, 63, 36, 4),       # cluster, keep count with no prefix slot (window and sinks only)
     (1, 32, 8, 65000, 32, 63, 2000, 0),     # cluster of 8
+    (1, 32, 8, 100000, 32, 63, 1500, 4),    # cluster of 13 where the GPU allows more than 8, else pool and select apart
+    (1, 32, 8, 5000, 32, 65, 700, 0),       # pool 65: pool and select as separate kernels
 ])
 def test_snap_evict_parity(B, Hq, Hkv, S, W, P, B1, sink):
     _snap_case(500 + S, B, Hq, Hkv, S, W, P, B1, sink)

@@ -736,7 +736,7 @@ constexpr int PS_NB = 1024;
 __device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }
 
 // Pool + select for one pair over a cluster of NC CTAs (prefixes of up to
-// 8 x 256 x (h + 1) positions; one CTA for up to 256 (h + 1)).  CTA r pools
+// 16 x 256 x (h + 1) positions; one CTA for up to 256 (h + 1)).  CTA r pools
 // positions [r*PC, r*PC + PC), PC = 256 (h + 1), each thread E = h + 1
 // consecutive outputs: the window of output a + i is window entries
 // [a + i, a + i + 2h], of which [a + E - 1, a + 2E - 2] is common to all E
@@ -755,7 +755,7 @@ __device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }
 // CTA 0 runs a radix select over them.
 constexpr int CL_NT = 256;
 constexpr int CL_MAXM = 512;
-constexpr int CL_MAXNC = 8;
+constexpr int CL_MAXNC = 16;                    // (beyond 8 CTAs: where the GPU schedules such clusters)
 
 // shared words of one cluster CTA's padded window of CL_NT (h + 1) + 2 (h + 1)
 // scores; its CL_NT (h + 1) pooled scores follow (cl_smem_words in all)
@@ -777,6 +777,8 @@ struct __align__(16) ClSmem {
   uint32_t mm[2];                  // this CTA's (min, max) candidate key
   uint32_t cnt[2];                 // this CTA's (certainly taken positions, members)
   uint32_t ctk[CL_MAXNC];          // taken members of each CTA
+  uint32_t certv[CL_MAXNC];        // certainly taken positions of each CTA
+  uint32_t msv[CL_MAXNC + 1];      // where each CTA's members start among all (the total last)
   uint32_t wsum[CL_NT / 32], wmin[CL_NT / 32], wmax[CL_NT / 32];
   int32_t sh[8];
 };
@@ -1087,19 +1089,31 @@ __global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float*
       cs.cnt[1] = (uint32_t)cs.sh[3];
     }
     cluster_sync();                                 // (3) counts and member lists are published
-    uint32_t certc[CL_MAXNC], ms[CL_MAXNC];
-    uint32_t mtot = 0;
+    if (warp == 0) {
+      // lane c < NC fetches CTA c's counts; the members' start in CTA order by a scan
+      uint32_t cc = 0u, mc = 0u;
+      if (lane < NC) {
+        cc = ld_cluster_u32(mapa(smem_u32(&cs.cnt[0]), (uint32_t)lane));
+        mc = ld_cluster_u32(mapa(smem_u32(&cs.cnt[1]), (uint32_t)lane));
+      }
+      uint32_t inc = mc;
 #pragma unroll
-    for (int c = 0; c < CL_MAXNC; ++c) {
-      certc[c] = c < NC ? ld_cluster_u32(mapa(smem_u32(&cs.cnt[0]), (uint32_t)c)) : 0u;
-      const uint32_t mc = c < NC ? ld_cluster_u32(mapa(smem_u32(&cs.cnt[1]), (uint32_t)c)) : 0u;
-      ms[c] = mtot;
-      mtot += mc;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (lane < NC) {
+        cs.msv[lane] = inc - mc;
+        cs.certv[lane] = cc;
+      }
+      if (lane == 31) cs.msv[CL_MAXNC] = inc;     // every member of the cluster
     }
+    __syncthreads();
+    const uint32_t mtot = cs.msv[CL_MAXNC];
+    const uint32_t* ms = cs.msv;
     auto cta_of = [&](uint32_t i) {
       int c = 0;
-#pragma unroll
-      for (int u = 1; u < CL_MAXNC; ++u) c = (u < NC && i >= ms[u]) ? u : c;
+      for (int u = 1; u < NC; ++u) c = i >= ms[u] ? u : c;
       return c;
     };
     // a taken member of the split bucket counts for its CTA, and marks its bit here
@@ -1150,7 +1164,7 @@ __global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float*
     }
     // taken positions of the CTAs before this one, then this CTA's in ascending order
     int pos = n_sink;
-    for (int c = 0; c < rank; ++c) pos += (int)certc[c] + (split ? (int)cs.ctk[c] : 0);
+    for (int c = 0; c < rank; ++c) pos += (int)cs.certv[c] + (split ? (int)cs.ctk[c] : 0);
     uint32_t tk = cert;
     if (split && cnt_i > 0) {
       // bits [al, al + E) of the taken map (at most two words)
@@ -1298,14 +1312,14 @@ size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32
 int snap_pass2_rows(int32_t G, int32_t W) { return std::min(P2_ROWS, (G * W + 31) & ~31); }
 
 // CTAs of the cluster pool + select for prefix length L and half window h:
-// 1..CL_MAXNC when it applies (the separate pool + select takes longer prefixes
+// 1..max_nc when it applies (the separate pool + select takes longer prefixes
 // and windows wider than 63)
-int pool_select_cl_ctas(int64_t L, int h) {
+int pool_select_cl_ctas(int64_t L, int h, int max_nc) {
   const int E = h + 1;
   if (L <= 0 || E > 32) return 0;
   const int64_t nq = (L + E - 1) / E;
   const int64_t nc = (nq + CL_NT - 1) / CL_NT;
-  return nc <= CL_MAXNC ? (int)nc : 0;
+  return nc <= max_nc ? (int)nc : 0;
 }
 
 
@@ -1334,6 +1348,7 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
                         cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess, cl_attr_err = cudaSuccess;
+  static int cl_max = 8;                          // largest cluster of the pool + select
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     if (attr_err == cudaSuccess)
@@ -1341,6 +1356,23 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     // (the window and keys of half width 31 plus the static select state pass the default 48 KB)
     cl_attr_err = cudaFuncSetAttribute(snap_pool_select_cl_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        cl_smem_words(31) * 4);
+    // clusters of up to 16 CTAs where the GPU schedules them (prefixes of up to
+    // 4096 pooling groups in one kernel), else the portable 8
+    if (cl_attr_err == cudaSuccess &&
+        cudaFuncSetAttribute(snap_pool_select_cl_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(CL_MAXNC, 1, 1);
+      cfg.blockDim = dim3(CL_NT, 1, 1);
+      cfg.dynamicSmemBytes = (size_t)cl_smem_words(31) * 4u;
+      int cmax = 0;
+      if (cudaOccupancyMaxPotentialClusterSize(&cmax, snap_pool_select_cl_kernel, &cfg) == cudaSuccess)
+        cl_max = std::max(8, std::min(cmax, CL_MAXNC));
+      else
+        cudaGetLastError();                       // (a refused query leaves no error behind)
+    } else if (cl_attr_err == cudaSuccess) {
+      cudaGetLastError();
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int pairs = a.B * a.Hkv;
@@ -1387,7 +1419,7 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
                    *tmK, *tmQ2, p);
     if (e != cudaSuccess) return e;
     const int half = (int)(a.pool / 2);
-    const int cl_nc = cl_attr_err == cudaSuccess ? pool_select_cl_ctas(L, half) : 0;
+    const int cl_nc = cl_attr_err == cudaSuccess ? pool_select_cl_ctas(L, half, cl_max) : 0;
     if (cl_nc > 0) {
       e = launch_cluster_pdl(snap_pool_select_cl_kernel, dim3((unsigned)cl_nc, pairs), dim3(CL_NT),
                              (size_t)cl_smem_words(half) * 4u, (unsigned)cl_nc, st, (const float*)p.scores, (int)p.RG2,
