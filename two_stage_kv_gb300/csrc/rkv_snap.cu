@@ -744,15 +744,14 @@ __device__ __forceinline__ int ps_pad(int u) { return u + (u >> 5); }
 // [a + 2E - 1, a + 3E - 3] (the van Herk / Gil-Werman split).
 // The pooled scores form runs of equal values, and the passes after pooling
 // walk a thread's runs (keys are order-preserving integers of the pooled log2
-// scores).  The bucket select then runs
-// over the cluster with four cluster barriers: the key range; the 1024-bucket
-// histograms (every CTA sums all of them); the counts of certainly taken
-// positions and the members of a split boundary bucket (which every CTA ranks
-// itself); and one before leaving, so no CTA exits while another reads its
-// shared memory.  Each CTA writes its own taken positions at their places in
-// the ascending keep list.  An equal or non-finite key range, or a split
-// bucket of more than CL_MAXM members, sends the keys to global scratch, where
-// CTA 0 runs a radix select over them.
+// scores).  The bucket select then runs over the cluster with four cluster
+// barriers: the key range; the 1024-bucket histograms (every CTA sums all of
+// them); the counts of certainly taken positions and the members of a split
+// boundary bucket (which every CTA ranks itself); and one before leaving, so
+// no CTA exits while another reads its shared memory.  Each CTA writes its own
+// taken positions at their places in the ascending keep list.  An equal or
+// non-finite key range, or a split bucket of more than CL_MAXM members, sends
+// the keys to global scratch, where CTA 0 runs a radix select over them.
 constexpr int CL_NT = 256;
 constexpr int CL_MAXM = 512;
 constexpr int CL_MAXNC = 16;                    // (beyond 8 CTAs: where the GPU schedules such clusters)
