@@ -403,7 +403,9 @@ rkv_status snap_common(const char* who, rkv_dims d, const void* q_obs, int32_t W
     } else if ((s = make_kv_map(&tmK, k, (int64_t)d.batch * d.n_kv_heads, cap, S, 128, "k")) != RKV_OK) {
       return s;
     }
-    if ((s = make_q_map(&tmQ1, q_obs, qrows, 128)) != RKV_OK) return s;
+    if ((s = make_q_map(&tmQ1, q_obs, qrows, rkv::snap_pass1_rows(d.n_q_heads / d.n_kv_heads, (int32_t)w))) !=
+        RKV_OK)
+      return s;
     if ((s = make_q_map(&tmQ2, q_obs, qrows, rkv::snap_pass2_rows(d.n_q_heads / d.n_kv_heads, (int32_t)w))) !=
         RKV_OK)
       return s;

@@ -88,6 +88,7 @@ struct SnapArgs {
 size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t W);
 // Query rows per pass-2 CTA (the MMA N of the key-major pass) for a group of G*W rows.
 int snap_pass2_rows(int32_t G, int32_t W);
+int snap_pass1_rows(int32_t G, int32_t W);
 cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmQ1, const CUtensorMap* tmQ2,
                         cudaStream_t st);
 

@@ -65,13 +65,17 @@ namespace {
 // TMEM lane quadrant) drain the accumulators.
 //   pass 1: D[128 query rows x 128 keys] = Q K^T; each epilogue thread owns a
 //           query row and keeps its online softmax (max, sum) over the keys.
+//           Groups of more than 128 window rows take 256 per CTA (two MMAs per
+//           key tile into the two halves of a 256-column buffer, each epilogue
+//           set draining one half of every tile), so the keys are read once per
+//           256 rows instead of once per 128.
 //   pass 2: D[128 keys x Ng query rows] = K Q^T; each epilogue thread owns a
 //           key and sums exp2(logit - lse(row)) over the rows in registers.
 constexpr int T_KEYS = 128;                       // keys per tile
 constexpr int T_NST = 3;                          // smem ring depth
 constexpr int T_NT = 320;                         // producer, MMA, two sets of 4 epilogue warps
 constexpr int P_CHUNK = 2048;                     // keys per CTA
-constexpr int P1_ROWS = 128;                      // query rows per pass-1 CTA (MMA M)
+constexpr int P1_ROWS = 128;                      // query rows per pass-1 MMA (M); a CTA takes one or two
 constexpr int P2_ROWS = 256;                      // query rows per pass-2 CTA (MMA N, max)
 constexpr uint32_t T_KTILE = T_KEYS * 256;        // 32 KB: two 16 KB k-blocks
 constexpr uint32_t T_QMAX = P2_ROWS * 256;        // 64 KB
@@ -83,6 +87,7 @@ struct PassArgs {
   int64_t bt_stride, num_pages;
   int32_t page_shift;              // log2 of the rows per page (pages hold 8 .. 128 rows)
   int32_t Hq, Hkv, G, W, R, RG1, RG2, nchunk1, nq2;
+  int32_t p1rows;                  // query rows per pass-1 CTA: 128, or 256 for groups of more than 128 rows
   int32_t pairs, nchunk2;
   float scale_log2;
   float2* stats;                   // [pairs][R][nchunk1]
@@ -197,7 +202,7 @@ __device__ __forceinline__ int item_at(int ib, int ie, int ii) {
   return PASS == 2 ? ie - 1 - (ii - ib) : ii;
 }
 
-template <int PASS>
+template <int PASS, bool WIDE = false>
 __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constant__ CUtensorMap tmK,
                                                             const __grid_constant__ CUtensorMap tmQ,
                                                             const PassArgs a) {
@@ -208,9 +213,11 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
   TcSmem& ts = *reinterpret_cast<TcSmem*>(smem + T_QMAX + T_NST * T_KTILE);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nq = PASS == 1 ? P1_ROWS : a.nq2;          // MMA M (pass 1) / N (pass 2) query rows
-  const int ncols = PASS == 1 ? T_KEYS : nq;                            // accumulator columns per buffer
-  const uint32_t tcols = PASS == 1 ? 256u : (nq <= 64 ? 128u : (nq <= 128 ? 256u : 512u));
+  constexpr bool wide = PASS == 1 && WIDE;             // pass 1 with two 128-row MMAs per tile (256 rows)
+  const int nq = PASS == 1 ? (wide ? 2 * P1_ROWS : P1_ROWS) : a.nq2;   // Q tile rows (pass 2: MMA N)
+  const int ncols = PASS == 1 ? T_KEYS : nq;                            // accumulator columns per MMA
+  const int bcols = wide ? 2 * T_KEYS : ncols;                          // columns per buffer
+  const uint32_t tcols = PASS == 1 ? (wide ? 512u : 256u) : (nq <= 64 ? 128u : (nq <= 128 ? 256u : 512u));
   const int nitems = a.pairs * (PASS == 1 ? a.RG1 * a.nchunk1 : a.RG2 * a.nchunk2);
   const int ib = (int)((int64_t)blockIdx.x * nitems / gridDim.x);
   const int ie = (int)((int64_t)(blockIdx.x + 1) * nitems / gridDim.x);
@@ -226,7 +233,7 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ts.tfull[i], 1);
-      mbar_init(&ts.tempty[i], 128);
+      mbar_init(&ts.tempty[i], wide ? 256 : 128);   // (wide pass 1: both epilogue sets drain every buffer)
     }
     mbar_init(&ts.qbar, 1);
     mbar_init(&ts.qfree, 1);
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
           // the MMAs of the previous Q tile have completed before it is overwritten
           if (nload > 0 && !tc_wait(&ts.qfree, (nload - 1) & 1, abort_flag, err)) break;
           const int b = it.pair / a.Hkv, hk = it.pair % a.Hkv;
-          const int qrow = (b * a.Hq + hk * a.G) * a.W + it.rg * (PASS == 1 ? P1_ROWS : P2_ROWS);
+          const int qrow = (b * a.Hq + hk * a.G) * a.W + it.rg * (PASS == 1 ? nq : P2_ROWS);
           mbar_arrive_expect_tx(&ts.qbar, (uint32_t)nq * 256u);
           for (int h = 0; h < 2; ++h)
             asm volatile(
@@ -317,16 +324,20 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
           if (T >= 2 && !tc_wait(&ts.tempty[buf], ((T >> 1) & 1) ^ 1, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kt = smem_u32(sK + s * T_KTILE), qt = smem_u32(sQ);
-          const uint32_t d = tbase + (uint32_t)(buf * ncols);
+          const uint32_t d = tbase + (uint32_t)(buf * bcols);
 #pragma unroll
           for (int kk8 = 0; kk8 < 8; ++kk8) {
             const int kb = kk8 >> 2, kk = kk8 & 3;
             const uint64_t kdesc = sdesc_k_sw128(kt + kb * (T_KTILE / 2) + kk * 32);
             const uint64_t qdesc = sdesc_k_sw128(qt + kb * nq * 128 + kk * 32);
-            if (PASS == 1)
+            if (PASS == 1) {
               tc_mma_bf16(d, qdesc, kdesc, idesc, kk8 > 0);
-            else
+              // rows 128-255 of the Q tile (16 KB further into each k-block) into the second half of the buffer
+              if (wide) tc_mma_bf16(d + T_KEYS, sdesc_k_sw128(qt + kb * nq * 128 + 128 * 128 + kk * 32), kdesc, idesc,
+                                    kk8 > 0);
+            } else {
               tc_mma_bf16(d, kdesc, qdesc, idesc, kk8 > 0);
+            }
           }
           tc_commit(&ts.empty[s]);
           tc_commit(&ts.tfull[buf]);
@@ -336,29 +347,34 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
   } else {
     // ----------------------------------------------------------- epilogue --
     // Two sets of four warps; set e drains TMEM buffer e, i.e. the tiles T of the
-    // CTA's stream with T % 2 == e.
+    // CTA's stream with T % 2 == e (wide pass 1: set e drains rows 128 e .. of
+    // every tile, from the half e of that tile's buffer).
     const int eset = (warp - 2) >> 2;                // 0 or 1
     const int quad = warp & 3;                       // TMEM lanes 32*quad .. +31
     const int r_loc = 32 * quad + lane;              // TMEM lane of this thread
     const int etid = (warp - 2) * 32 + lane;         // 0 .. 255 over both sets
     const uint32_t lane_addr = tbase + ((uint32_t)(32 * quad) << 16) + (uint32_t)(eset * ncols);
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * quad) << 16) + (uint32_t)(eset * T_KEYS);   // (wide)
     int T0 = 0, key = -1;                            // first tile of the item in the CTA's stream
     for (int ii = ib; ii < ie; ++ii) {
       const PassItem it = pass_item<PASS>(a, item_at<PASS>(ib, ie, ii));
       const int j032 = (int)it.j0;
       const int pair = it.pair;
       const int S32 = (int)pair_S(a, pair), L32 = max(S32 - a.W, 0);   // this row's prompt and prefix
-      const int row0 = it.rg * (PASS == 1 ? P1_ROWS : P2_ROWS);
-      const int tfirst = (T0 & 1) == eset ? 0 : 1;   // this set's first tile of the item
+      const int row0 = it.rg * (PASS == 1 ? nq : P2_ROWS);
+      const int tfirst = wide ? 0 : ((T0 & 1) == eset ? 0 : 1);   // this set's first tile of the item
+      const int tstep = wide ? 1 : 2;
       if (PASS == 1) {
-        const int r = row0 + r_loc;                  // query row in the group
+        const int r = row0 + (wide ? P1_ROWS * eset : 0) + r_loc;   // query row in the group
         const bool rvalid = r < a.R;
         const int lim = S32 - a.W + (rvalid ? (r % a.W) : 0);     // last key this row attends
         float m = neg_inf(), l = 0.f;
-        for (int t = tfirst; t < it.ntiles; t += 2) {
+        for (int t = tfirst; t < it.ntiles; t += tstep) {
           const int T = T0 + t;
+          const int bf = wide ? (T & 1) : eset;         // this tile's buffer
+          const uint32_t la = wide ? lane_base + (uint32_t)(bf * bcols) : lane_addr;
           // the warp gives up together: the TMEM loads below are warp-collective
-          if (!__all_sync(0xffffffffu, tc_wait(&ts.tfull[eset], (T >> 1) & 1, abort_flag, err))) break;
+          if (!__all_sync(0xffffffffu, tc_wait(&ts.tfull[bf], (T >> 1) & 1, abort_flag, err))) break;
           tc_fence_after();
           // online softmax over the tile's four 32-key chunks; the next chunk's
           // TMEM load is in flight while one is reduced (64 value registers)
@@ -366,12 +382,12 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
           const bool full_tile = jt + T_KEYS <= S32 - a.W;   // every row attends every key of the tile
           const int jmax = min(S32 - 1, lim) - jt;           // last attended column of the tile
           float va[32], vb[32];
-          tmem_ld32(lane_addr, va);
+          tmem_ld32(la, va);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float* cur = (c & 1) ? vb : va;
-            if (c < 3) tmem_ld32(lane_addr + 32 * (c + 1), (c & 1) ? va : vb);
+            if (c < 3) tmem_ld32(la + 32 * (c + 1), (c & 1) ? va : vb);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
             float mn;
@@ -415,16 +431,21 @@ __global__ void __launch_bounds__(T_NT, 1) snap_pass_kernel(const __grid_constan
             if (c < 3) tmem_wait_ld();
           }
           tc_fence_before();
-          mbar_arrive(&ts.tempty[eset]);
+          mbar_arrive(&ts.tempty[bf]);
         }
-        if (eset == 1) ts.part[r_loc] = make_float2(m, l);
-        asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
-        if (eset == 0) {
-          const float2 o = ts.part[r_loc];
-          const float mn = fmaxf(m, o.x);
-          const float ls =
-              (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (o.x == neg_inf() ? 0.f : o.y * exp2f(o.x - mn));
-          if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + it.chunk] = make_float2(mn, ls);
+        if (wide) {
+          if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + it.chunk] = make_float2(m, l);
+        } else {
+          // the two sets drained alternate tiles of the same rows: merge
+          if (eset == 1) ts.part[r_loc] = make_float2(m, l);
+          asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+          if (eset == 0) {
+            const float2 o = ts.part[r_loc];
+            const float mn = fmaxf(m, o.x);
+            const float ls =
+                (m == neg_inf() ? 0.f : l * exp2f(m - mn)) + (o.x == neg_inf() ? 0.f : o.y * exp2f(o.x - mn));
+            if (rvalid) a.stats[((size_t)pair * a.R + r) * a.nchunk1 + it.chunk] = make_float2(mn, ls);
+          }
         }
       } else {
         const int k = pair * a.RG2 + it.rg;
@@ -1309,6 +1330,7 @@ size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32
 }
 
 int snap_pass2_rows(int32_t G, int32_t W) { return std::min(P2_ROWS, (G * W + 31) & ~31); }
+int snap_pass1_rows(int32_t G, int32_t W) { return G * W > P1_ROWS ? 2 * P1_ROWS : P1_ROWS; }
 
 // CTAs of the cluster pool + select for prefix length L and half window h:
 // 1..max_nc when it applies (the separate pool + select takes longer prefixes
@@ -1350,6 +1372,8 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
   static int cl_max = 8;                          // largest cluster of the pool + select
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(snap_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(snap_pass_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(snap_pass_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T_SMEM);
     // (the window and keys of half width 31 plus the static select state pass the default 48 KB)
@@ -1395,7 +1419,8 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     p.G = a.G;
     p.W = W;
     p.R = a.G * W;
-    p.RG1 = (p.R + P1_ROWS - 1) / P1_ROWS;
+    p.p1rows = snap_pass1_rows(a.G, W);
+    p.RG1 = (p.R + p.p1rows - 1) / p.p1rows;
     p.RG2 = (p.R + P2_ROWS - 1) / P2_ROWS;
     p.nq2 = snap_pass2_rows(a.G, W);
     p.nchunk1 = (int)((a.S + P_CHUNK - 1) / P_CHUNK);
@@ -1411,7 +1436,8 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     p.nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
     // persistent grids: one CTA per SM (the ring and Q tile fill the shared memory)
     const int items1 = pairs * p.RG1 * p.nchunk1, items2 = pairs * p.RG2 * p.nchunk2;
-    cudaError_t e = launch_pdl(snap_pass_kernel<1>, dim3((unsigned)std::min(items1, snap_num_sms())), dim3(T_NT),
+    cudaError_t e = launch_pdl(p.p1rows > P1_ROWS ? snap_pass_kernel<1, true> : snap_pass_kernel<1>,
+                               dim3((unsigned)std::min(items1, snap_num_sms())), dim3(T_NT),
                                T_SMEM, st, *tmK, *tmQ1, p);
     if (e != cudaSuccess) return e;
     e = launch_pdl(snap_pass_kernel<2>, dim3((unsigned)std::min(items2, snap_num_sms())), dim3(T_NT), T_SMEM, st,
