@@ -722,6 +722,8 @@ def _snap_case(seed, B, Hq, Hkv, S, W, P, B1, n_sink=0, cap_extra=5, q_scale=1.0
     (1, 32, 8, 65000, 32, 63, 2000, 0),     # cluster of 8
     (1, 32, 8, 100000, 32, 63, 1500, 4),    # cluster of 13 where the GPU allows more than 8, else pool and select apart
     (1, 32, 8, 5000, 32, 65, 700, 0),       # pool 65: pool and select as separate kernels
+    (1, 48, 8, 2500, 32, 63, 300, 0),       # G * W = 192: pass 1 with 256 rows per CTA, 64 of them past the group
+    (2, 64, 8, 3000, 20, 63, 400, 2),       # W = 20, G * W = 160: the same with a window off 32, sinks
 ])
 def test_snap_evict_parity(B, Hq, Hkv, S, W, P, B1, sink):
     _snap_case(500 + S, B, Hq, Hkv, S, W, P, B1, sink)
