@@ -93,6 +93,24 @@ D4 = (1, 32, 8, 128)
     (lambda: rkv.rkv_hsa_decode_ragged(D4, 16, 16, 16, 100, None, 50, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_hsa_decode_ragged(D4, 16, 16, 16, 100, 16, 0, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
     (lambda: rkv.rkv_hsa_decode_ragged(D4, 16, 16, 16, 100, 16, 101, 16, 16, 16, 8, 4, 0.1, 16, stream=0), 1),
+    # stage 1 per request: per-row arrays required and 4-byte aligned, a keep count that fits every
+    # row's window and sinks; pages a power of two in [8, 128] that cover the longest prompt
+    (lambda: rkv.rkv_snap_evict_ragged(D4, 16, 32, 16, 16, 100, None, 100, 63, 0, 16, 50, 0.1, 16, 50, 16, 16, 50,
+                                       None, 256, 1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict_ragged(D4, 16, 32, 16, 16, 100, 16, 100, 63, 4, 16, 36, 0.1, 16, 50, 16, 16, 50,
+                                       None, 256, 1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict_ragged(D4, 16, 32, 16, 16, 100, 18, 100, 63, 0, 16, 50, 0.1, 16, 50, 16, 16, 50,
+                                       None, 256, 1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict_paged(D4, 16, 32, 16, 16, 8, 64, None, 2, 16, 100, 63, 0, 16, 50, 0.1, 16, 50,
+                                      16, 16, 50, None, 256, 1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict_paged(D4, 16, 32, 16, 16, 8, 48, 16, 4, 16, 100, 63, 0, 16, 50, 0.1, 16, 50,
+                                      16, 16, 50, None, 256, 1 << 30, stream=0), 2),
+    (lambda: rkv.rkv_snap_evict_paged(D4, 16, 32, 16, 16, 8, 256, 16, 1, 16, 100, 63, 0, 16, 50, 0.1, 16, 50,
+                                      16, 16, 50, None, 256, 1 << 30, stream=0), 2),
+    (lambda: rkv.rkv_snap_evict_paged(D4, 16, 32, 16, 16, 8, 64, 16, 1, 16, 100, 63, 0, 16, 50, 0.1, 16, 50,
+                                      16, 16, 50, None, 256, 1 << 30, stream=0), 1),
+    (lambda: rkv.rkv_snap_evict_paged(D4, 16, 32, 16, 16, 0, 64, 16, 2, 16, 100, 63, 0, 16, 50, 0.1, 16, 50,
+                                      16, 16, 50, None, 256, 1 << 30, stream=0), 1),
     (lambda: rkv.rkv_build_kt(D4, 16, 10, 20, None, 0, 16, 16, 4, stream=0), 1),
     (lambda: rkv.rkv_build_kt(D4, 16, 100, 100, None, 0, 16, 16, 6, stream=0), 1),
     (lambda: rkv.rkv_append_kv(D4, 16, 16, 16, 16, 100, 10, 11, None, 0, 16, 10, 16, stream=0), 1),
