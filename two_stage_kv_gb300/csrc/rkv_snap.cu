@@ -74,7 +74,7 @@ namespace {
 constexpr int T_KEYS = 128;                       // keys per tile
 constexpr int T_NST = 4;                          // smem ring depth (3 measured 1 % slower on the 32K layer)
 constexpr int T_NT = 320;                         // producer, MMA, two sets of 4 epilogue warps
-constexpr int P_CHUNK = 2048;                     // keys per CTA
+constexpr int P_CHUNK = 2048;                     // keys per work item (smaller when that leaves SMs idle)
 constexpr int P1_ROWS = 128;                      // query rows per pass-1 MMA (M); a CTA takes one or two
 constexpr int P2_ROWS = 256;                      // query rows per pass-2 CTA (MMA N, max)
 constexpr uint32_t T_KTILE = T_KEYS * 256;        // 32 KB: two 16 KB k-blocks
@@ -89,6 +89,7 @@ struct PassArgs {
   int32_t Hq, Hkv, G, W, R, RG1, RG2, nchunk1, nq2;
   int32_t p1rows;                  // query rows per pass-1 CTA: 128, or 256 for groups of more than 128 rows
   int32_t pairs, nchunk2;
+  int32_t chunk;                   // keys per work item: P_CHUNK, halved down to 2 tiles for small jobs
   float scale_log2;
   float2* stats;                   // [pairs][R][nchunk1]
   float* scores;                   // [pairs][RG2][L]
@@ -169,7 +170,7 @@ __device__ __forceinline__ int64_t pair_S(const PassArgs& a, int pair) {
   return a.S_rows ? min(max((int64_t)a.S_rows[pair / a.Hkv], (int64_t)1), a.S) : a.S;
 }
 
-// One work item = (pair, row group, key chunk of P_CHUNK keys).  The grid is
+// One work item = (pair, row group, key chunk of a.chunk keys).  The grid is
 // persistent: CTA c takes the contiguous items [c*n/grid, (c+1)*n/grid), so
 // the K stream, the MMAs and the epilogue run across item boundaries without
 // draining; the Q tile is reloaded only when (pair, row group) changes.
@@ -189,8 +190,8 @@ __device__ __forceinline__ PassItem pass_item(const PassArgs& a, int item) {
   // (a batch row shorter than the longest has empty items past its own length)
   const int64_t Sp = pair_S(a, it.pair);
   const int64_t kend = (PASS == 1) ? Sp : max(Sp - (int64_t)a.W, (int64_t)0);
-  it.j0 = (int64_t)it.chunk * P_CHUNK;
-  const int64_t j1 = min(kend, it.j0 + (int64_t)P_CHUNK);
+  it.j0 = (int64_t)it.chunk * a.chunk;
+  const int64_t j1 = min(kend, it.j0 + (int64_t)a.chunk);
   it.ntiles = j1 > it.j0 ? (int)((j1 - it.j0 + T_KEYS - 1) / T_KEYS) : 0;
   return it;
 }
@@ -1318,13 +1319,24 @@ int snap_num_sms() {
 
 }  // namespace
 
+// Keys per work item of the score passes: P_CHUNK, halved (down to two tiles)
+// while the pass-1 items would not cover the GPU's 152 SMs; a function of the
+// shape alone, so the workspace query and the launch agree on any device.
+int snap_chunk_keys(int64_t pairs, int64_t S, int64_t rg1) {
+  int c = P_CHUNK;
+  while (c > 2 * T_KEYS && pairs * rg1 * ((S + c - 1) / c) < 152) c >>= 1;
+  return c;
+}
+
 size_t snap_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t W) {
   const int64_t pairs = (int64_t)B * Hkv;
   const int G = Hq / Hkv;
   const int64_t R = (int64_t)G * W;
   const int64_t RG = (R + P2_ROWS - 1) / P2_ROWS;
   const int64_t L = std::max<int64_t>(S - W, 0);
-  const int64_t nchunk1 = (S + P_CHUNK - 1) / P_CHUNK;
+  const int64_t p1 = R > P1_ROWS ? 2 * P1_ROWS : P1_ROWS;
+  const int chunk = snap_chunk_keys(pairs, S, (R + p1 - 1) / p1);
+  const int64_t nchunk1 = (S + chunk - 1) / chunk;
   return al256((size_t)pairs * R * nchunk1 * sizeof(float2)) + al256((size_t)pairs * RG * L * sizeof(float)) +
          al256((size_t)pairs * L * sizeof(float));
 }
@@ -1423,7 +1435,8 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     p.RG1 = (p.R + p.p1rows - 1) / p.p1rows;
     p.RG2 = (p.R + P2_ROWS - 1) / P2_ROWS;
     p.nq2 = snap_pass2_rows(a.G, W);
-    p.nchunk1 = (int)((a.S + P_CHUNK - 1) / P_CHUNK);
+    p.chunk = snap_chunk_keys(pairs, a.S, p.RG1);
+    p.nchunk1 = (int)((a.S + p.chunk - 1) / p.chunk);
     p.scale_log2 = a.scale_log2;
     uint8_t* w = reinterpret_cast<uint8_t*>(a.ws);
     p.stats = reinterpret_cast<float2*>(w);
@@ -1433,7 +1446,7 @@ cudaError_t snap_launch(const SnapArgs& a, const CUtensorMap* tmK, const CUtenso
     float* pooled_log = reinterpret_cast<float*>(w);   // log2 pooled scores (separate pool + select)
 
     p.pairs = pairs;
-    p.nchunk2 = (int)((L + P_CHUNK - 1) / P_CHUNK);
+    p.nchunk2 = (int)((L + p.chunk - 1) / p.chunk);
     // persistent grids: one CTA per SM (the ring and Q tile fill the shared memory)
     const int items1 = pairs * p.RG1 * p.nchunk1, items2 = pairs * p.RG2 * p.nchunk2;
     cudaError_t e = launch_pdl(p.p1rows > P1_ROWS ? snap_pass_kernel<1, true> : snap_pass_kernel<1>,
