@@ -868,25 +868,27 @@ __global__ void __launch_bounds__(CL_NT) snap_pool_select_cl_kernel(const float*
       }
       cp_async_commit();
       cp_async_wait_all();
-    }
-    for (int u0 = RG == 1 ? Uloc : tid; u0 < Uloc; u0 += 8 * CL_NT) {
-      float v[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int j = p0 + u0 + t * CL_NT - h;
-        v[t] = (u0 + t * CL_NT < Uloc && j >= 0 && j < L) ? __ldg(sc + j) : neg_inf();
-      }
-      for (int r = 1; r < RG; ++r) {
+    } else {
+      // several row groups: their log2 sums are added up on the way
+      for (int u0 = tid; u0 < Uloc; u0 += 8 * CL_NT) {
+        float v[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int j = p0 + u0 + t * CL_NT - h;
-          if (u0 + t * CL_NT < Uloc && j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * Ls + j));
+          v[t] = (u0 + t * CL_NT < Uloc && j >= 0 && j < L) ? __ldg(sc + j) : neg_inf();
         }
-      }
+        for (int r = 1; r < RG; ++r) {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int u = u0 + t * CL_NT;
-        if (u < Uloc) xs[ps_pad(u)] = __float_as_uint(v[t]);
+          for (int t = 0; t < 8; ++t) {
+            const int j = p0 + u0 + t * CL_NT - h;
+            if (u0 + t * CL_NT < Uloc && j >= 0 && j < L) v[t] = log2_add(v[t], __ldg(sc + (size_t)r * Ls + j));
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int u = u0 + t * CL_NT;
+          if (u < Uloc) xs[ps_pad(u)] = __float_as_uint(v[t]);
+        }
       }
     }
   }
