@@ -93,14 +93,18 @@ def kernel_source_hash():
 
 def ncu_traffic_per_launch():
     """DRAM bytes per HSA launch from the committed ncu summary, if it was taken
-    on the current kernel source; otherwise None."""
+    on the current kernel source (else None): (cold, caches flushed by ncu;
+    warm, a launch of the graph loop with the caches as the loop leaves them)."""
     if not os.path.exists(PROFILE_SUMMARY):
-        return None
+        return None, None
     with open(PROFILE_SUMMARY) as f:
         d = json.load(f)
     if d.get("kernel_source_hash") != kernel_source_hash():
-        return None
-    return d.get("dram_bytes_per_launch")
+        return None, None
+    warm = d.get("warm_dram_bytes_read")
+    if warm is not None:
+        warm += d.get("warm_dram_bytes_write", 0)
+    return d.get("dram_bytes_per_launch"), warm
 
 
 class ClockSampler:
@@ -311,9 +315,12 @@ def run_ours(args, rank, world, local):
     bytes_avg = sum(hsa_bytes_per_launch(wl, B1, k2, B1 + s + 1) for s in range(wl.steps)) / wl.steps
     peak, peak_kind = peaks()
     achieved = bytes_avg / (hsa_avg_us * 1e-6) / 1e9
-    traffic = ncu_traffic_per_launch()
+    traffic, traffic_warm = ncu_traffic_per_launch()
     roofline = {"kernel": "hsa_decode_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                # (cold: caches flushed by ncu, all 2*D KT rows of a CTA's blocks prefetched from DRAM;
+                # warm: a launch inside the graph loop, the state the timed region runs in)
+                "traffic_warm": traffic_warm,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else
                 "fallback 6.8 TB/s", "bytes_per_launch": int(bytes_avg), "avg_launch_us": round(hsa_avg_us, 3),
                 "timing": "decode-phase events of the last timed pass / 64 launches (gaps included)",
