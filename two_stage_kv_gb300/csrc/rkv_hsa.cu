@@ -1153,11 +1153,11 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
       }
       const float mn0 = fmaxf(wm[0], m0), mn1 = fmaxf(wm[1], m1);
-      const float cr0 = (wm[0] == neg_inf()) ? 0.f : exp2f(wm[0] - mn0);
-      const float cr1 = (wm[1] == neg_inf()) ? 0.f : exp2f(wm[1] - mn1);
+      const float cr0 = (wm[0] == neg_inf()) ? 0.f : ex2_ftz(wm[0] - mn0);
+      const float cr1 = (wm[1] == neg_inf()) ? 0.f : ex2_ftz(wm[1] - mn1);
       float p[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) p[e] = (x[0][e] == neg_inf()) ? 0.f : exp2f(x[0][e] - ((e & 1) ? mn1 : mn0));
+      for (int e = 0; e < 4; ++e) p[e] = (x[0][e] == neg_inf()) ? 0.f : ex2_ftz(x[0][e] - ((e & 1) ? mn1 : mn0));
       float s0 = p[0] + p[2], s1 = p[1] + p[3];
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -1220,14 +1220,14 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
           for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][h]);
           const float mo = fs.mrun[h];
           mnew[ht][hh] = m;
-          corr[ht][hh] = (mo == neg_inf()) ? 0.f : exp2f(mo - m);
+          corr[ht][hh] = (mo == neg_inf()) ? 0.f : ex2_ftz(mo - m);
         }
       // --- probabilities, their head sums, and P^T fragments for every warp
   #pragma unroll
       for (int ht = 0; ht < NH; ++ht) {
         float p[4];
   #pragma unroll
-        for (int e = 0; e < 4; ++e) p[e] = (x[ht][e] == neg_inf()) ? 0.f : exp2f(x[ht][e] - mnew[ht][e & 1]);
+        for (int e = 0; e < 4; ++e) p[e] = (x[ht][e] == neg_inf()) ? 0.f : ex2_ftz(x[ht][e] - mnew[ht][e & 1]);
         float s0 = p[0] + p[2], s1 = p[1] + p[3];
   #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -1255,7 +1255,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
         float m = fs.mrun[tid];
   #pragma unroll
         for (int w = 0; w < NWARP; ++w) m = fmaxf(m, fs.wmaxh[w][tid]);
-        const float c = (fs.mrun[tid] == neg_inf()) ? 0.f : exp2f(fs.mrun[tid] - m);
+        const float c = (fs.mrun[tid] == neg_inf()) ? 0.f : ex2_ftz(fs.mrun[tid] - m);
         float l = fs.lrun[tid] * c;
   #pragma unroll
         for (int w = 0; w < NWARP; ++w) l += fs.wsumh[w][tid];
@@ -1351,7 +1351,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       }
 #pragma unroll
       for (int w = 0; w < NWARP; ++w) {
-        fw[w] = fw[w] == neg_inf() ? 0.f : exp2f(fw[w] - M);   // a warp with no token of head g weighs 0
+        fw[w] = fw[w] == neg_inf() ? 0.f : ex2_ftz(fw[w] - M);   // a warp with no token of head g weighs 0
         L = fmaf(fw[w], fs.wsumh[w][g], L);
       }
       const int owner = own_of(g), gl = slot_of(g);
@@ -1416,7 +1416,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       float A = 0.f, L = 0.f;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const float f = (mr[r] == neg_inf()) ? 0.f : exp2f(mr[r] - M);
+        const float f = (mr[r] == neg_inf()) ? 0.f : ex2_ftz(mr[r] - M);
         A = fmaf(f, vr[r], A);
         L = fmaf(f, lr[r], L);
       }
