@@ -1014,13 +1014,13 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       const int32_t* ib = MT ? a.idx + (size_t)pair * a.idx_cap : nullptr;
       for (int i = tid; i < rows * 16; i += NT) {
         const int r = i >> 4, ch = i & 15;
-        const int slot = r / blk;
+        const int slot = divb(r);
         const int t = sel[r0 + slot] * blk + (r - slot * blk);
         const uint32_t o = (uint32_t)(ch >> 3) * half + swz128(r, ch & 7);
         if (t < n_old) {
           // row of token t: MT candidate row, paged (page, head) slab row, or t itself
           const int64_t prow = MT ? min(max((int64_t)ib[t], (int64_t)0), a.cap - 1)
-                               : PG ? ((int64_t)bt_s[t / blk] * a.Hkv + hk) * blk + (t % blk) : (int64_t)t;
+                               : PG ? ((int64_t)bt_s[divb(t)] * a.Hkv + hk) * blk + (t - divb(t) * blk) : (int64_t)t;
           cp_async_16(smem_u32(tK) + o, kb + prow * HD + ch * 8);
           cp_async_16(smem_u32(tV) + o, vb + prow * HD + ch * 8);
         } else if (t == n_old && app) {
@@ -1043,7 +1043,7 @@ __global__ void __launch_bounds__(NT, 2) hsa_decode_kernel(const __grid_constant
       // candidate rows of this round, one bit per staged row
       bool e = false;
       if (tid < rows) {
-        const int slot = tid / blk;
+        const int slot = divb(tid);
         const int t = sel[r0 + slot] * blk + (tid - slot * blk);
         e = t < n_tot && (t >= a.n_prompt || ((__ldg(mrow + (t >> 5)) >> (t & 31)) & 1u) != 0);
       }
